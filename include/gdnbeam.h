@@ -1,0 +1,293 @@
+/*
+ * gdnbeam — large-beam Gated DeltaNet decoding with a shared context state,
+ * append-only transition records, an ancestry index and projection replay.
+ *
+ * Sources, named by page title:
+ *   OneLA   "OneLA: Scaling Linear-Attention Decoding to Large Beams in
+ *            Generative Recommendation" (review page)
+ *   RecoGEM "RecoGEM: A Serving System for Production-Scale Generative
+ *            Recommendation"
+ *
+ * Conventions for every call below.
+ *   - Pointers are DEVICE pointers owned by the caller unless marked (host).
+ *     The library never allocates device memory: the context carves all it
+ *     needs out of one caller-allocated workspace.
+ *   - Calls are asynchronous on the given stream. They return a status:
+ *     0 on success or a negative GDNBEAM_E* code. Argument errors are found
+ *     on the host before anything is launched. Errors found on the device
+ *     (an out-of-range token, parent or slot index; a non-finite score) set a
+ *     device error word, skip the offending access and are reported by
+ *     gdnbeam_status()/gdnbeam_device_status(); the device never traps.
+ *   - Storage type is fp32 (GDNBEAM_F32) or bf16 (GDNBEAM_BF16) for every
+ *     tensor marked "storage"; accumulation is always fp32.
+ *   - Per-beam tensors of one decode call are packed [R][W_t][...]: request
+ *     r's beam b is row r*W_t + b.
+ *   - Decode call t (0 <= t <= T-2) runs on the beams kept by selection t
+ *     and feeds selection t+1; selection 0 reads the prefill row. A beam's
+ *     slot at depth j is its ancestor's row index at decode call j.
+ */
+#ifndef GDNBEAM_H_
+#define GDNBEAM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gdnbeam_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+  GDNBEAM_OK = 0,
+  GDNBEAM_EINVAL = -1,       /* null pointer, size out of range, bad index argument */
+  GDNBEAM_EUNSUPPORTED = -2, /* shape or dtype this build does not handle */
+  GDNBEAM_EWORKSPACE = -3,   /* workspace or scratch smaller than required */
+  GDNBEAM_ESTATE = -4,       /* call out of order (step before prefill, t out of sequence) */
+  GDNBEAM_ECUDA = -5,        /* a CUDA runtime/driver call or a launch failed */
+  GDNBEAM_EDEVICE = -6,      /* the device error word was set */
+  GDNBEAM_ENOMEM = -7        /* host allocation of the context failed */
+};
+
+enum { GDNBEAM_F32 = 0, GDNBEAM_BF16 = 1 };
+
+/* Device error word bits (gdnbeam_device_status). */
+enum {
+  GDNBEAM_DERR_TOKEN = 1,     /* token id outside [0, V) */
+  GDNBEAM_DERR_PARENT = 2,    /* parent index outside [0, W_{t-1}) */
+  GDNBEAM_DERR_SLOT = 4,      /* ancestry slot outside its depth's beam count */
+  GDNBEAM_DERR_NONFINITE = 8, /* a score was NaN or infinite */
+  GDNBEAM_DERR_TIMEOUT = 16,  /* a bounded on-chip wait gave up */
+  GDNBEAM_DERR_SELECT = 32    /* selection bookkeeping inconsistency */
+};
+
+#define GDNBEAM_MAX_T 8        /* longest SID (selections) supported */
+
+/* Shape of one decode job. d_k, d_v in {16, 32, 64, 128}; 1 <= T <= GDNBEAM_MAX_T;
+ * V <= 16384; W_max <= 4096. residual = 0 requires layers = 1 and reads the
+ * codebook logits off concat_h(o) (OneLA §1.2 eq. 3 output); residual = 1 runs
+ * a residual stream with unit-gain RMSNorm (eps 1e-6) before each layer and
+ * before the codebook head, which requires H*d_v == d_model. */
+typedef struct gdnbeam_config {
+  int R;        /* requests decoded together */
+  int layers;   /* stacked GDN layers */
+  int H;        /* heads per layer */
+  int d_k;      /* key / query width per head */
+  int d_v;      /* value width per head */
+  int d_model;  /* embedding width */
+  int V;        /* codebook size (candidates per beam) */
+  int T;        /* SID length = number of selections */
+  int W_max;    /* largest beam count of any selection */
+  int L_max;    /* longest prompt gdnbeam_prefill_state accepts */
+  int dtype;    /* GDNBEAM_F32 or GDNBEAM_BF16 storage */
+  int residual; /* 0: single layer; 1: residual stream + RMSNorm glue */
+} gdnbeam_config;
+
+/* Weights, storage type, row-major, owned by the caller and kept alive for
+ * the life of the context.
+ *   E       [V][d_model]                      token embedding
+ *   W_proj  [layers][N_proj][d_model]         N_proj = 2*H*d_k + H*d_v + 2*H rows:
+ *             H*d_k query rows, H*d_k key rows, H*d_v value rows, then the H
+ *             decay-gate vectors w_alpha and the H write-gate vectors w_beta
+ *   W_o     [V][F]                            codebook head; F = H*d_v (single
+ *             layer) or d_model (residual) */
+typedef struct gdnbeam_weights {
+  const void* E;
+  const void* W_proj;
+  const void* W_o;
+} gdnbeam_weights;
+
+/* Optional fp32 copies of intermediate values before storage rounding, for
+ * parity checks. Any member may be NULL. Shapes for a call on n = R*W_t rows:
+ *   q, k [layers][n][H*d_k]; v, delta, o [layers][n][H*d_v];
+ *   alpha, beta [layers][n][H]; logits [n][V]. */
+typedef struct gdnbeam_dumps {
+  float* q;
+  float* k;
+  float* v;
+  float* alpha;
+  float* beta;
+  float* delta;
+  float* o;
+  float* logits;
+} gdnbeam_dumps;
+
+/* Memory accounting of a configuration (host only, no CUDA call). */
+typedef struct gdnbeam_footprint {
+  size_t sctx_bytes;          /* shared context states: R*layers*H*d_v*d_k (storage) */
+  size_t record_elements;     /* elements of one transition record: 1 + d_v + d_k (OneLA §2.2 eq. 5) */
+  size_t records_bytes;       /* all record slots: R*layers*H*(T-1)*W_max*(d_v + d_k) storage + alpha fp32 */
+  size_t ancestry_bytes;      /* ancestry index and token paths (int32) */
+  size_t fullstate_bytes;     /* one per-beam full state per beam: R*layers*H*W_max*d_v*d_k (storage) */
+  size_t workspace_bytes;     /* everything gdnbeam_create needs */
+} gdnbeam_footprint;
+
+typedef struct gdnbeam_ctx gdnbeam_ctx;
+
+/* ---------------------------------------------------------------------------
+ * Context-level calls (the decode loop)
+ * ------------------------------------------------------------------------- */
+
+/* Validates cfg and fills *out (host). Returns GDNBEAM_EINVAL/EUNSUPPORTED on
+ * a configuration this build rejects. */
+int gdnbeam_footprint_of(const gdnbeam_config* cfg, gdnbeam_footprint* out);
+
+/* Creates a context over a caller-allocated workspace of at least
+ * footprint.workspace_bytes, 256-byte aligned. The host-side context struct is
+ * the only thing the library allocates; weights and workspace stay owned by
+ * the caller. *out is set on success, NULL otherwise. */
+int gdnbeam_create(const gdnbeam_config* cfg, const gdnbeam_weights* w,
+                   void* workspace, size_t workspace_bytes, gdnbeam_ctx** out);
+void gdnbeam_destroy(gdnbeam_ctx* ctx);
+
+/* Prefill (OneLA §1.1, §2.1): runs the GDN recurrence (eq. 3) from S = 0 over
+ * every request's prompt, keeps S_ctx per (request, layer, head) in the
+ * workspace and writes the root row's logits and log-normaliser.
+ *   prompt      [R][L] int32 token ids, 1 <= L <= L_max
+ *   root_logits [R][V] storage
+ *   root_lse    [R] fp32, lse = log sum_v exp(z_v) */
+int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L,
+                          void* root_logits, float* root_lse, gdnbeam_stream_t stream);
+
+/* One decode call t on W_t beams per request (OneLA §2.3-2.5):
+ *   1. ancestry update (eq. 9) from parents (ignored at t = 0) and token paths;
+ *   2. projections of the beams' tokens -> q, k, v, alpha, beta; k and alpha
+ *      go straight into the depth-t record slot;
+ *   3. fused replay: u_q, u_k from S_ctx, folded along the ancestors' records
+ *      (eqs. 6-7), then delta_t and o_t (eq. 8); delta_t fills the record;
+ *   4. codebook logits and their log-normaliser.
+ *   parents [R][W_t] int32 rows of the previous call (t >= 1)
+ *   tokens  [R][W_t] int32 token ids chosen by the selection that made the beams
+ *   logits  [R*W_t][V] storage (out);  lse [R*W_t] fp32 (out)
+ *   dumps   optional (host struct of device pointers), may be NULL
+ * Calls must come in order t = 0, 1, ..., T-2 after a prefill; t = 0 may be
+ * issued again at any time to restart decoding from the same prefill. */
+int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents,
+                 const int32_t* tokens, void* logits, float* lse,
+                 const gdnbeam_dumps* dumps, gdnbeam_stream_t stream);
+
+/* Global top-W_next over the W_t x V candidates of every request (OneLA §1.1;
+ * RecoGEM §4.3 two-stage exact selection). Score of candidate (b, v):
+ *   s = fl32(cum'_b + fl32(z_bv - lse_b)),  cum'_b = fl32(cum_b + bias_b)
+ * in IEEE fp32 without contraction; order by s descending, then flat index
+ * b*V + v ascending. t = -1 selects from the prefill row (W_t must be 1).
+ *   logits [R*W_t][V] storage; lse [R*W_t]; cum [R*W_t] or NULL (= 0);
+ *   bias [R*W_t] or NULL; outputs parents, tokens [R][W_next] int32 and
+ *   cum_next [R][W_next] fp32, in selection order.
+ * Requires W_next <= min(W_max, W_t*V). */
+int gdnbeam_select(gdnbeam_ctx* ctx, int t, int W_t, int W_next, const void* logits,
+                   const float* lse, const float* cum, const float* bias,
+                   int32_t* parents, int32_t* tokens, float* cum_next,
+                   gdnbeam_stream_t stream);
+
+/* Final SID paths after the last selection: sid [R][W_final][T] int32. */
+int gdnbeam_get_paths(gdnbeam_ctx* ctx, int W_final, const int32_t* parents,
+                      const int32_t* tokens, int32_t* sid, gdnbeam_stream_t stream);
+
+/* Copies S_ctx, storage type [R][layers][H][d_v][d_k], into out. */
+int gdnbeam_read_sctx(gdnbeam_ctx* ctx, void* out, gdnbeam_stream_t stream);
+
+/* Marks every request's state as released: records stay where they are
+ * (nothing moves, OneLA §2.1/§2.4); a new prefill is required before the next
+ * step. Host only. */
+int gdnbeam_reset(gdnbeam_ctx* ctx);
+
+/* Synchronises the stream, then returns GDNBEAM_EDEVICE if the device error
+ * word is set (and clears it), GDNBEAM_ECUDA on a CUDA error, else 0. */
+int gdnbeam_status(gdnbeam_ctx* ctx, gdnbeam_stream_t stream);
+
+/* Reads and optionally clears the device error word of the current device
+ * (synchronous). Returns a GDNBEAM_DERR_* bit set, or a negative status. */
+int gdnbeam_device_status(int clear);
+
+/* Name of the kernel variant the context uses for each stage
+ * ("tc" = tcgen05 tensor cores, "simt" = CUDA cores), as a static string such
+ * as "proj=tc replay=tc logits=tc select=radix". */
+const char* gdnbeam_variant(const gdnbeam_ctx* ctx);
+
+const char* gdnbeam_strerror(int status);
+
+/* ---------------------------------------------------------------------------
+ * Tensor-level calls: each stage on explicit buffers (same kernels the
+ * context runs). cfg gives dims and dtype; only the fields named matter.
+ * ------------------------------------------------------------------------- */
+
+/* Projections for n rows of one layer (OneLA §1.2 eq. 3 inputs).
+ *   u [n][d_model] storage, W_proj [N_proj][d_model] storage (one layer);
+ *   q [n][H*d_k], k [n][H*d_k], v [n][H*d_v] storage; alpha, beta [n][H] fp32.
+ *   q and k are L2-normalised per head (eps 1e-6 inside the root);
+ *   alpha = exp(-softplus(w_alpha.u)), beta = sigmoid(w_beta.u).
+ * scratch: device buffer of gdnbeam_project_scratch_bytes(cfg, n) bytes
+ * (0 for the tensor-core path; may then be NULL). dumps: optional fp32 copies
+ * (layer 0 slots of gdnbeam_dumps). */
+size_t gdnbeam_project_scratch_bytes(const gdnbeam_config* cfg, int n);
+int gdnbeam_project(const gdnbeam_config* cfg, int n, const void* u, const void* W_proj,
+                    void* q, void* k, void* v, float* alpha, float* beta,
+                    void* scratch, size_t scratch_bytes, const gdnbeam_dumps* dumps,
+                    gdnbeam_stream_t stream);
+
+/* Records of one depth (OneLA §2.2 eq. 5), rows packed [R][W_j][H]. */
+typedef struct gdnbeam_records {
+  const void* k;       /* [R*W_j][H*d_k] storage */
+  const void* delta;   /* [R*W_j][H*d_v] storage */
+  const float* alpha;  /* [R*W_j][H] */
+  int W_j;             /* beams per request at that depth */
+} gdnbeam_records;
+
+/* Fused shared-context replay for one layer at decode call t (OneLA §2.3
+ * eqs. 6-8, §2.5): for every request r, beam b < W_t and head h,
+ *   u_q = S_ctx q_b, u_k = S_ctx k_b, folded over j < t with the record at
+ *   slot anc[r*W_t+b][j] of depth j; delta = beta (v - alpha u_k);
+ *   o = alpha u_q + delta (k_b . q_b).
+ *   sctx [R][H][d_v][d_k] storage (stride between requests: sctx_rstride elements)
+ *   q, k [R*W_t][H*d_k], v [R*W_t][H*d_v] storage; alpha, beta [R*W_t][H]
+ *   depth: host array of t record descriptors; anc [R*W_t][anc_stride] int32
+ *   delta_out, o_out [R*W_t][H*d_v] storage; x_inout optional fp32
+ *   [R*W_t][H*d_v] residual stream to which o is added (NULL: none).
+ *   dumps: optional fp32 delta / o (layer 0 slots). */
+int gdnbeam_replay(const gdnbeam_config* cfg, int t, int W_t, const void* sctx,
+                   long long sctx_rstride, const void* q, const void* k, const void* v,
+                   const float* alpha, const float* beta, const gdnbeam_records* depth,
+                   const int32_t* anc, int anc_stride, void* delta_out, void* o_out,
+                   float* x_inout, const gdnbeam_dumps* dumps, gdnbeam_stream_t stream);
+
+/* Codebook logits for n rows: z = W_o feat, lse = log sum exp z.
+ *   feat [n][F] storage; W_o [V][F]; z [n][V] storage; lse [n] fp32. */
+size_t gdnbeam_logits_scratch_bytes(const gdnbeam_config* cfg, int n);
+int gdnbeam_logits(const gdnbeam_config* cfg, int n, const void* feat, const void* W_o,
+                   void* z, float* lse, void* scratch, size_t scratch_bytes,
+                   const gdnbeam_dumps* dumps, gdnbeam_stream_t stream);
+
+/* Exact global top-W_next per request, as gdnbeam_select, on explicit
+ * scratch of gdnbeam_select_scratch_bytes(R, W_t, W_next, V) bytes. */
+size_t gdnbeam_select_scratch_bytes(int R, int W_t, int W_next, int V);
+int gdnbeam_select_topw(int R, int W_t, int W_next, int V, int dtype, const void* logits,
+                        const float* lse, const float* cum, const float* bias,
+                        int32_t* parents, int32_t* tokens, float* cum_next,
+                        void* scratch, size_t scratch_bytes, gdnbeam_stream_t stream);
+
+/* Ancestry-index update of OneLA §2.4 eq. 9 for decode call t:
+ *   anc_out[r*W_t+b][j] = anc_prev[r*W_prev+p][j] (j < t-1), anc_out[..][t-1] = p,
+ *   with p = parents[r*W_t+b]; sid_out[..][s] = sid_prev[..p..][s] (s < t),
+ *   sid_out[..][t] = tokens[r*W_t+b]. Row stride of anc and sid is T ints.
+ *   At t = 0 anc is untouched and sid_out[..][0] = tokens. */
+int gdnbeam_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int32_t* parents,
+                     const int32_t* tokens, const int32_t* anc_prev, const int32_t* sid_prev,
+                     int32_t* anc_out, int32_t* sid_out, gdnbeam_stream_t stream);
+
+/* Prefill recurrence over L tokens for every (request, head) from S = 0
+ * (OneLA §1.2 eq. 3).
+ *   q, k [R*L][H*d_k], v [R*L][H*d_v] storage; alpha, beta [R*L][H] fp32;
+ *   sctx_out [R][H][d_v][d_k] storage (request stride sctx_rstride elements);
+ *   o_last [R][H*d_v] storage output at the last position (or NULL);
+ *   x_inout optional fp32 [R*L][H*d_v]: o of every position is added to it. */
+int gdnbeam_prefill_scan(const gdnbeam_config* cfg, int L, const void* q, const void* k,
+                         const void* v, const float* alpha, const float* beta,
+                         void* sctx_out, long long sctx_rstride, void* o_last,
+                         float* x_inout, gdnbeam_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDNBEAM_H_ */

@@ -1,0 +1,562 @@
+// C ABI of the gdnbeam library: argument checks, workspace layout, call
+// sequencing, and the dispatch of each stage to its kernels.
+#include <new>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "launchers.h"
+
+using namespace gdnbeam;
+
+namespace {
+
+__device__ unsigned int g_dev_error_word;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {nullptr};
+
+unsigned* err_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = (unsigned*)p;
+  }
+  return g_err_ptr[dev];
+}
+
+inline size_t elem_size(int dtype) { return dtype == GDNBEAM_BF16 ? 2 : 4; }
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline int n_proj(const gdnbeam_config& c) { return 2 * c.H * c.d_k + c.H * c.d_v + 2 * c.H; }
+inline int feat_dim(const gdnbeam_config& c) { return c.residual ? c.d_model : c.H * c.d_v; }
+inline bool pow2_head(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+int validate(const gdnbeam_config* c) {
+  if (!c) return GDNBEAM_EINVAL;
+  if (c->R < 1 || c->layers < 1 || c->H < 1 || c->d_model < 1 || c->V < 2 || c->T < 1 ||
+      c->W_max < 1 || c->L_max < 1)
+    return GDNBEAM_EINVAL;
+  if (c->T > GDNBEAM_MAX_T || !pow2_head(c->d_k) || !pow2_head(c->d_v)) return GDNBEAM_EUNSUPPORTED;
+  if (c->dtype != GDNBEAM_F32 && c->dtype != GDNBEAM_BF16) return GDNBEAM_EUNSUPPORTED;
+  if (c->V > 16384 || c->W_max > 4096) return GDNBEAM_EUNSUPPORTED;
+  if (!c->residual && c->layers != 1) return GDNBEAM_EUNSUPPORTED;
+  if (c->residual && c->H * c->d_v != c->d_model) return GDNBEAM_EUNSUPPORTED;
+  if ((long long)c->W_max * c->V >= (1ll << 31)) return GDNBEAM_EUNSUPPORTED;
+  if ((long long)c->R * c->L_max >= (1ll << 31) || (long long)c->R * c->W_max * c->V >= (1ll << 40))
+    return GDNBEAM_EUNSUPPORTED;
+  return GDNBEAM_OK;
+}
+
+}  // namespace
+
+struct gdnbeam_ctx {
+  gdnbeam_config c;
+  gdnbeam_weights w;
+  char* ws;
+  size_t ws_bytes;
+  bool tc_gemm, tc_replay;
+  char variant[96];
+  // persistent state
+  void* sctx;        // [R][layers][H][d_v][d_k]
+  void* gtr_k;       // [layers][T-1][R*W_max][H*d_k]
+  void* gtr_delta;   // [layers][T-1][R*W_max][H*d_v]
+  float* gtr_alpha;  // [layers][T-1][R*W_max][H]
+  int32_t* anc[2];   // [R*W_max][T]
+  int32_t* sid[2];   // [R*W_max][T]
+  // transients of one decode call
+  void* u;      // [R*W_max][d_model]
+  float* x;     // [R*W_max][d_model] residual stream (residual only)
+  void* q;      // [R*W_max][H*d_k]
+  void* v;      // [R*W_max][H*d_v]
+  float* beta;  // [R*W_max][H]
+  void* o;      // [R*W_max][H*d_v]
+  void* sel;    // selection scratch
+  size_t sel_bytes;
+  void* gemm;   // GEMM scratch (fp32 raw outputs or logits partials)
+  size_t gemm_bytes;
+  // prefill buffers for R*L_max rows
+  void *pf_u, *pf_q, *pf_k, *pf_v, *pf_feat;
+  float *pf_x, *pf_alpha, *pf_beta;
+  // sequencing
+  int prefilled;
+  int last_step;
+  int W_hist[GDNBEAM_MAX_T];
+
+  size_t rec_rows() const { return (size_t)c.R * c.W_max; }
+  char* gk(int layer, int j) const {
+    return (char*)gtr_k + ((size_t)layer * (c.T - 1) + j) * rec_rows() * c.H * c.d_k * elem_size(c.dtype);
+  }
+  char* gd(int layer, int j) const {
+    return (char*)gtr_delta + ((size_t)layer * (c.T - 1) + j) * rec_rows() * c.H * c.d_v * elem_size(c.dtype);
+  }
+  float* ga(int layer, int j) const {
+    return gtr_alpha + ((size_t)layer * (c.T - 1) + j) * rec_rows() * c.H;
+  }
+};
+
+namespace {
+
+// Lays the workspace out from base (nullptr = dry run) and returns its size.
+size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
+             gdnbeam_footprint* fp) {
+  const size_t es = elem_size(c.dtype);
+  const size_t rows = (size_t)c.R * c.W_max;
+  const size_t pf_rows = (size_t)c.R * c.L_max;
+  const int depths = c.T > 1 ? c.T - 1 : 0;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    char* p = base ? base + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  size_t sctx_b = (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * es;
+  size_t gk_b = (size_t)c.layers * depths * rows * c.H * c.d_k * es;
+  size_t gd_b = (size_t)c.layers * depths * rows * c.H * c.d_v * es;
+  size_t ga_b = (size_t)c.layers * depths * rows * c.H * sizeof(float);
+  size_t anc_b = rows * c.T * sizeof(int32_t);
+  char* p_sctx = take(sctx_b);
+  char* p_gk = take(gk_b);
+  char* p_gd = take(gd_b);
+  char* p_ga = take(ga_b);
+  char* p_anc0 = take(anc_b);
+  char* p_anc1 = take(anc_b);
+  char* p_sid0 = take(anc_b);
+  char* p_sid1 = take(anc_b);
+  char* p_u = take(rows * c.d_model * es);
+  char* p_x = take(c.residual ? rows * c.d_model * sizeof(float) : 0);
+  char* p_q = take(rows * c.H * c.d_k * es);
+  char* p_v = take(rows * c.H * c.d_v * es);
+  char* p_beta = take(rows * c.H * sizeof(float));
+  char* p_o = take(rows * c.H * c.d_v * es);
+  // the widest selection reads W_max rows per request and keeps W_max beams
+  size_t sel_b = select_scratch_bytes(c.R, c.W_max, c.W_max, c.V);
+  char* p_sel = take(sel_b);
+  size_t gemm_b;
+  if (tc_gemm) {
+    gemm_b = tc_logits_scratch_bytes(c, (int)(rows > (size_t)c.R ? rows : c.R));
+  } else {
+    size_t a = rows * (size_t)n_proj(c) * 4, b = rows * (size_t)c.V * 4;
+    size_t p = pf_rows * (size_t)n_proj(c) * 4, r = (size_t)c.R * c.V * 4;
+    gemm_b = a > b ? a : b;
+    if (p > gemm_b) gemm_b = p;
+    if (r > gemm_b) gemm_b = r;
+  }
+  char* p_gemm = take(gemm_b);
+  char* p_pfu = take(pf_rows * c.d_model * es);
+  char* p_pfx = take(c.residual ? pf_rows * c.d_model * sizeof(float) : 0);
+  char* p_pfq = take(pf_rows * c.H * c.d_k * es);
+  char* p_pfk = take(pf_rows * c.H * c.d_k * es);
+  char* p_pfv = take(pf_rows * c.H * c.d_v * es);
+  char* p_pfa = take(pf_rows * c.H * sizeof(float));
+  char* p_pfb = take(pf_rows * c.H * sizeof(float));
+  char* p_pff = take((size_t)c.R * feat_dim(c) * es);
+  if (x) {
+    x->sctx = p_sctx; x->gtr_k = p_gk; x->gtr_delta = p_gd; x->gtr_alpha = (float*)p_ga;
+    x->anc[0] = (int32_t*)p_anc0; x->anc[1] = (int32_t*)p_anc1;
+    x->sid[0] = (int32_t*)p_sid0; x->sid[1] = (int32_t*)p_sid1;
+    x->u = p_u; x->x = (float*)p_x; x->q = p_q; x->v = p_v; x->beta = (float*)p_beta;
+    x->o = p_o; x->sel = p_sel; x->sel_bytes = sel_b; x->gemm = p_gemm; x->gemm_bytes = gemm_b;
+    x->pf_u = p_pfu; x->pf_x = (float*)p_pfx; x->pf_q = p_pfq; x->pf_k = p_pfk;
+    x->pf_v = p_pfv; x->pf_alpha = (float*)p_pfa; x->pf_beta = (float*)p_pfb; x->pf_feat = p_pff;
+  }
+  if (fp) {
+    fp->sctx_bytes = sctx_b;
+    fp->record_elements = 1 + (size_t)c.d_v + c.d_k;
+    fp->records_bytes = gk_b + gd_b + ga_b;
+    fp->ancestry_bytes = 4 * anc_b;
+    fp->fullstate_bytes = (size_t)c.R * c.layers * c.H * c.W_max * c.d_v * c.d_k * es;
+    fp->workspace_bytes = off;
+  }
+  return off;
+}
+
+int project_any(const gdnbeam_config& c, bool tc, int n, const void* u, const void* Wp, void* q,
+                void* k, void* v, float* alpha, float* beta, void* scratch, size_t scratch_bytes,
+                const gdnbeam_dumps* d, cudaStream_t s) {
+  if (tc) return launch_tc_project(c, n, u, Wp, q, k, v, alpha, beta, d, s);
+  const int Np = n_proj(c);
+  if (!scratch || scratch_bytes < (size_t)n * Np * 4) return GDNBEAM_EWORKSPACE;
+  int st = launch_simt_gemm_nt(c.dtype, n, Np, c.d_model, u, c.d_model, Wp, c.d_model,
+                               (float*)scratch, Np, s);
+  if (st) return st;
+  return launch_proj_epilogue(c, n, (const float*)scratch, q, k, v, alpha, beta, d, s);
+}
+
+int logits_any(const gdnbeam_config& c, bool tc, int n, const void* feat, const void* Wo,
+               void* z, float* lse, void* scratch, size_t scratch_bytes, const gdnbeam_dumps* d,
+               cudaStream_t s) {
+  if (tc) {
+    if (scratch_bytes < tc_logits_scratch_bytes(c, n)) return GDNBEAM_EWORKSPACE;
+    return launch_tc_logits(c, n, feat, Wo, z, lse, scratch, d, s);
+  }
+  const int F = feat_dim(c);
+  if (!scratch || scratch_bytes < (size_t)n * c.V * 4) return GDNBEAM_EWORKSPACE;
+  int st = launch_simt_gemm_nt(c.dtype, n, c.V, F, feat, F, Wo, F, (float*)scratch, c.V, s);
+  if (st) return st;
+  return launch_logits_rows(c.dtype, n, c.V, (const float*)scratch, z, lse,
+                            d ? d->logits : nullptr, s);
+}
+
+gdnbeam_dumps layer_dumps(const gdnbeam_dumps* d, const gdnbeam_config& c, int layer, size_t n) {
+  gdnbeam_dumps o{};
+  if (!d) return o;
+  auto sh = [&](float* p, size_t per) { return p ? p + (size_t)layer * n * per : nullptr; };
+  o.q = sh(d->q, (size_t)c.H * c.d_k);
+  o.k = sh(d->k, (size_t)c.H * c.d_k);
+  o.v = sh(d->v, (size_t)c.H * c.d_v);
+  o.alpha = sh(d->alpha, c.H);
+  o.beta = sh(d->beta, c.H);
+  o.delta = sh(d->delta, (size_t)c.H * c.d_v);
+  o.o = sh(d->o, (size_t)c.H * c.d_v);
+  o.logits = d->logits;
+  return o;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdnbeam_strerror(int st) {
+  switch (st) {
+    case GDNBEAM_OK: return "ok";
+    case GDNBEAM_EINVAL: return "invalid argument";
+    case GDNBEAM_EUNSUPPORTED: return "unsupported shape or dtype";
+    case GDNBEAM_EWORKSPACE: return "workspace or scratch too small";
+    case GDNBEAM_ESTATE: return "call out of sequence";
+    case GDNBEAM_ECUDA: return "CUDA error";
+    case GDNBEAM_EDEVICE: return "device-side error";
+    case GDNBEAM_ENOMEM: return "host allocation failed";
+    default: return "unknown status";
+  }
+}
+
+int gdnbeam_footprint_of(const gdnbeam_config* cfg, gdnbeam_footprint* out) {
+  int st = validate(cfg);
+  if (st) return st;
+  if (!out) return GDNBEAM_EINVAL;
+  carve(*cfg, tc_gemm_supported(*cfg), nullptr, nullptr, out);
+  return GDNBEAM_OK;
+}
+
+int gdnbeam_create(const gdnbeam_config* cfg, const gdnbeam_weights* w, void* workspace,
+                   size_t workspace_bytes, gdnbeam_ctx** out) {
+  if (!out) return GDNBEAM_EINVAL;
+  *out = nullptr;
+  int st = validate(cfg);
+  if (st) return st;
+  if (!w || !w->E || !w->W_proj || !w->W_o || !workspace) return GDNBEAM_EINVAL;
+  if (((uintptr_t)workspace & 255) != 0) return GDNBEAM_EINVAL;
+  const bool tc = tc_gemm_supported(*cfg);
+  if (workspace_bytes < carve(*cfg, tc, nullptr, nullptr, nullptr)) return GDNBEAM_EWORKSPACE;
+  gdnbeam_ctx* x = new (std::nothrow) gdnbeam_ctx();
+  if (!x) return GDNBEAM_ENOMEM;
+  x->c = *cfg;
+  x->w = *w;
+  x->ws = (char*)workspace;
+  x->ws_bytes = workspace_bytes;
+  x->tc_gemm = tc;
+  x->tc_replay = tc_replay_supported(cfg->dtype, cfg->d_k, cfg->d_v);
+  carve(*cfg, tc, (char*)workspace, x, nullptr);
+  snprintf(x->variant, sizeof(x->variant), "proj=%s replay=%s logits=%s select=radix2",
+           tc ? "tc" : "simt", x->tc_replay ? "tc" : "simt", tc ? "tc" : "simt");
+  x->prefilled = 0;
+  x->last_step = -1;
+  *out = x;
+  return GDNBEAM_OK;
+}
+
+void gdnbeam_destroy(gdnbeam_ctx* ctx) { delete ctx; }
+
+const char* gdnbeam_variant(const gdnbeam_ctx* ctx) { return ctx ? ctx->variant : ""; }
+
+int gdnbeam_reset(gdnbeam_ctx* ctx) {
+  if (!ctx) return GDNBEAM_EINVAL;
+  ctx->prefilled = 0;
+  ctx->last_step = -1;
+  return GDNBEAM_OK;
+}
+
+int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* root_logits,
+                          float* root_lse, gdnbeam_stream_t stream) {
+  if (!ctx || !prompt || !root_logits || !root_lse) return GDNBEAM_EINVAL;
+  const gdnbeam_config& c = ctx->c;
+  if (L < 1 || L > c.L_max) return GDNBEAM_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned* err = err_ptr();
+  const int n = c.R * L;
+  const size_t es = elem_size(c.dtype);
+  const int Np = n_proj(c);
+  const long long rstride = (long long)c.layers * c.H * c.d_v * c.d_k;
+  ctx->prefilled = 0;
+  int st = launch_gather_rows(c.dtype, n, c.d_model, prompt, c.V, ctx->w.E, ctx->pf_u,
+                              c.residual ? ctx->pf_x : nullptr, err, s);
+  if (st) return st;
+  for (int layer = 0; layer < c.layers; ++layer) {
+    if (c.residual) {
+      st = launch_rmsnorm_rows(c.dtype, n, c.d_model, ctx->pf_x, c.d_model, ctx->pf_u, s);
+      if (st) return st;
+    }
+    const char* Wp = (const char*)ctx->w.W_proj + (size_t)layer * Np * c.d_model * es;
+    st = project_any(c, ctx->tc_gemm, n, ctx->pf_u, Wp, ctx->pf_q, ctx->pf_k, ctx->pf_v,
+                     ctx->pf_alpha, ctx->pf_beta, ctx->gemm, ctx->gemm_bytes, nullptr, s);
+    if (st) return st;
+    char* sc = (char*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k * es;
+    st = launch_prefill_scan(c, L, ctx->pf_q, ctx->pf_k, ctx->pf_v, ctx->pf_alpha, ctx->pf_beta,
+                             sc, rstride, c.residual ? nullptr : ctx->pf_feat,
+                             c.residual ? ctx->pf_x : nullptr, s);
+    if (st) return st;
+  }
+  if (c.residual) {
+    st = launch_rmsnorm_rows(c.dtype, c.R, c.d_model, ctx->pf_x + (size_t)(L - 1) * c.d_model,
+                             (long long)L * c.d_model, ctx->pf_feat, s);
+    if (st) return st;
+  }
+  st = logits_any(c, ctx->tc_gemm, c.R, ctx->pf_feat, ctx->w.W_o, root_logits, root_lse,
+                  ctx->gemm, ctx->gemm_bytes, nullptr, s);
+  if (st) return st;
+  ctx->prefilled = 1;
+  ctx->last_step = -1;
+  return GDNBEAM_OK;
+}
+
+int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const int32_t* tokens,
+                 void* logits, float* lse, const gdnbeam_dumps* dumps, gdnbeam_stream_t stream) {
+  if (!ctx || !tokens || !logits || !lse) return GDNBEAM_EINVAL;
+  const gdnbeam_config& c = ctx->c;
+  if (t < 0 || t > c.T - 2 || W_t < 1 || W_t > c.W_max) return GDNBEAM_EINVAL;
+  if (t > 0 && !parents) return GDNBEAM_EINVAL;
+  if (!ctx->prefilled) return GDNBEAM_ESTATE;
+  if (t > 0 && ctx->last_step != t - 1) return GDNBEAM_ESTATE;
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned* err = err_ptr();
+  const int n = c.R * W_t;
+  const size_t es = elem_size(c.dtype);
+  const int Np = n_proj(c);
+  const int W_prev = t > 0 ? ctx->W_hist[t - 1] : 1;
+  const int cur = t & 1;
+  ctx->last_step = -2;  // invalid until this call succeeds
+  int st = launch_ancestry(c.R, t, c.T, c.V, W_prev, W_t, parents, tokens, ctx->anc[cur ^ 1],
+                           ctx->sid[cur ^ 1], ctx->anc[cur], ctx->sid[cur], err, s);
+  if (st) return st;
+  st = launch_gather_rows(c.dtype, n, c.d_model, tokens, c.V, ctx->w.E, ctx->u,
+                          c.residual ? ctx->x : nullptr, err, s);
+  if (st) return st;
+  for (int layer = 0; layer < c.layers; ++layer) {
+    if (c.residual) {
+      st = launch_rmsnorm_rows(c.dtype, n, c.d_model, ctx->x, c.d_model, ctx->u, s);
+      if (st) return st;
+    }
+    gdnbeam_dumps ld = layer_dumps(dumps, c, layer, n);
+    const char* Wp = (const char*)ctx->w.W_proj + (size_t)layer * Np * c.d_model * es;
+    st = project_any(c, ctx->tc_gemm, n, ctx->u, Wp, ctx->q, ctx->gk(layer, t), ctx->v,
+                     ctx->ga(layer, t), ctx->beta, ctx->gemm, ctx->gemm_bytes, &ld, s);
+    if (st) return st;
+    ReplayArgs a{};
+    a.R = c.R; a.H = c.H; a.d_k = c.d_k; a.d_v = c.d_v; a.t = t; a.W_t = W_t;
+    a.sctx = (const char*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k * es;
+    a.sctx_rstride = (long long)c.layers * c.H * c.d_v * c.d_k;
+    a.q = ctx->q; a.k = ctx->gk(layer, t); a.v = ctx->v;
+    a.alpha = ctx->ga(layer, t); a.beta = ctx->beta;
+    for (int j = 0; j < t; ++j) {
+      a.depth[j].k = ctx->gk(layer, j);
+      a.depth[j].delta = ctx->gd(layer, j);
+      a.depth[j].alpha = ctx->ga(layer, j);
+      a.depth[j].W_j = ctx->W_hist[j];
+    }
+    a.anc = ctx->anc[cur]; a.anc_stride = c.T;
+    a.delta_out = ctx->gd(layer, t); a.o_out = ctx->o;
+    a.x_inout = c.residual ? ctx->x : nullptr;
+    a.delta_dump = ld.delta; a.o_dump = ld.o;
+    a.err = err;
+    st = ctx->tc_replay ? launch_tc_replay(a, s) : launch_replay(c.dtype, a, s);
+    if (st) return st;
+  }
+  const void* feat = ctx->o;
+  if (c.residual) {
+    st = launch_rmsnorm_rows(c.dtype, n, c.d_model, ctx->x, c.d_model, ctx->u, s);
+    if (st) return st;
+    feat = ctx->u;
+  }
+  gdnbeam_dumps zd{};
+  if (dumps) zd.logits = dumps->logits;
+  st = logits_any(c, ctx->tc_gemm, n, feat, ctx->w.W_o, logits, lse, ctx->gemm, ctx->gemm_bytes,
+                  &zd, s);
+  if (st) return st;
+  ctx->W_hist[t] = W_t;
+  ctx->last_step = t;
+  return GDNBEAM_OK;
+}
+
+int gdnbeam_select(gdnbeam_ctx* ctx, int t, int W_t, int W_next, const void* logits,
+                   const float* lse, const float* cum, const float* bias, int32_t* parents,
+                   int32_t* tokens, float* cum_next, gdnbeam_stream_t stream) {
+  if (!ctx) return GDNBEAM_EINVAL;
+  const gdnbeam_config& c = ctx->c;
+  if (t < -1 || t > c.T - 2) return GDNBEAM_EINVAL;
+  if (t == -1 && W_t != 1) return GDNBEAM_EINVAL;
+  if (W_t < 1 || W_t > c.W_max || W_next < 1 || W_next > c.W_max) return GDNBEAM_EINVAL;
+  return gdnbeam_select_topw(c.R, W_t, W_next, c.V, c.dtype, logits, lse, cum, bias, parents,
+                             tokens, cum_next, ctx->sel, ctx->sel_bytes, stream);
+}
+
+int gdnbeam_get_paths(gdnbeam_ctx* ctx, int W_final, const int32_t* parents,
+                      const int32_t* tokens, int32_t* sid, gdnbeam_stream_t stream) {
+  if (!ctx || !tokens || !sid) return GDNBEAM_EINVAL;
+  const gdnbeam_config& c = ctx->c;
+  if (W_final < 1 || W_final > c.W_max) return GDNBEAM_EINVAL;
+  const int t = c.T - 1;
+  if (t > 0) {
+    if (!parents) return GDNBEAM_EINVAL;
+    if (ctx->last_step != c.T - 2) return GDNBEAM_ESTATE;
+  }
+  const int W_prev = t > 0 ? ctx->W_hist[t - 1] : 1;
+  const int prev = (t - 1) & 1;
+  return launch_ancestry(c.R, t, c.T, c.V, W_prev, W_final, parents, tokens, nullptr,
+                         t > 0 ? ctx->sid[prev] : nullptr, nullptr, sid, err_ptr(),
+                         (cudaStream_t)stream);
+}
+
+int gdnbeam_read_sctx(gdnbeam_ctx* ctx, void* out, gdnbeam_stream_t stream) {
+  if (!ctx || !out) return GDNBEAM_EINVAL;
+  if (!ctx->prefilled) return GDNBEAM_ESTATE;
+  const gdnbeam_config& c = ctx->c;
+  size_t bytes = (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * elem_size(c.dtype);
+  GDN_CUDA(cudaMemcpyAsync(out, ctx->sctx, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+  return GDNBEAM_OK;
+}
+
+int gdnbeam_device_status(int clear) {
+  unsigned* p = err_ptr();
+  if (!p) return GDNBEAM_ECUDA;
+  unsigned v = 0;
+  GDN_CUDA(cudaDeviceSynchronize());
+  GDN_CUDA(cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost));
+  if (clear && v) {
+    unsigned z = 0;
+    GDN_CUDA(cudaMemcpy(p, &z, sizeof(z), cudaMemcpyHostToDevice));
+  }
+  return (int)v;
+}
+
+int gdnbeam_status(gdnbeam_ctx* ctx, gdnbeam_stream_t stream) {
+  if (!ctx) return GDNBEAM_EINVAL;
+  GDN_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  GDN_CUDA(cudaGetLastError());
+  int v = gdnbeam_device_status(1);
+  if (v < 0) return v;
+  return v ? GDNBEAM_EDEVICE : GDNBEAM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-level calls
+// ---------------------------------------------------------------------------
+
+size_t gdnbeam_project_scratch_bytes(const gdnbeam_config* cfg, int n) {
+  if (validate(cfg) || n < 0) return 0;
+  if (tc_gemm_supported(*cfg)) return 0;
+  return (size_t)n * n_proj(*cfg) * 4;
+}
+
+int gdnbeam_project(const gdnbeam_config* cfg, int n, const void* u, const void* W_proj, void* q,
+                    void* k, void* v, float* alpha, float* beta, void* scratch,
+                    size_t scratch_bytes, const gdnbeam_dumps* dumps, gdnbeam_stream_t stream) {
+  int st = validate(cfg);
+  if (st) return st;
+  if (n < 0 || !u || !W_proj || !q || !k || !v || !alpha || !beta) return GDNBEAM_EINVAL;
+  if (n == 0) return GDNBEAM_OK;
+  return project_any(*cfg, tc_gemm_supported(*cfg), n, u, W_proj, q, k, v, alpha, beta, scratch,
+                     scratch_bytes, dumps, (cudaStream_t)stream);
+}
+
+int gdnbeam_replay(const gdnbeam_config* cfg, int t, int W_t, const void* sctx,
+                   long long sctx_rstride, const void* q, const void* k, const void* v,
+                   const float* alpha, const float* beta, const gdnbeam_records* depth,
+                   const int32_t* anc, int anc_stride, void* delta_out, void* o_out,
+                   float* x_inout, const gdnbeam_dumps* dumps, gdnbeam_stream_t stream) {
+  int st = validate(cfg);
+  if (st) return st;
+  const gdnbeam_config& c = *cfg;
+  if (t < 0 || t >= GDNBEAM_MAX_T || W_t < 1 || !sctx || !q || !k || !v || !alpha || !beta ||
+      !delta_out || !o_out)
+    return GDNBEAM_EINVAL;
+  if (t > 0 && (!depth || !anc || anc_stride < t)) return GDNBEAM_EINVAL;
+  ReplayArgs a{};
+  a.R = c.R; a.H = c.H; a.d_k = c.d_k; a.d_v = c.d_v; a.t = t; a.W_t = W_t;
+  a.sctx = sctx; a.sctx_rstride = sctx_rstride;
+  a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta;
+  for (int j = 0; j < t; ++j) {
+    if (!depth[j].k || !depth[j].delta || !depth[j].alpha || depth[j].W_j < 1) return GDNBEAM_EINVAL;
+    a.depth[j] = depth[j];
+  }
+  a.anc = anc; a.anc_stride = anc_stride;
+  a.delta_out = delta_out; a.o_out = o_out; a.x_inout = x_inout;
+  a.delta_dump = dumps ? dumps->delta : nullptr;
+  a.o_dump = dumps ? dumps->o : nullptr;
+  a.err = err_ptr();
+  if (tc_replay_supported(c.dtype, c.d_k, c.d_v)) return launch_tc_replay(a, (cudaStream_t)stream);
+  return launch_replay(c.dtype, a, (cudaStream_t)stream);
+}
+
+size_t gdnbeam_logits_scratch_bytes(const gdnbeam_config* cfg, int n) {
+  if (validate(cfg) || n < 0) return 0;
+  if (tc_gemm_supported(*cfg)) return tc_logits_scratch_bytes(*cfg, n);
+  return (size_t)n * cfg->V * 4;
+}
+
+int gdnbeam_logits(const gdnbeam_config* cfg, int n, const void* feat, const void* W_o, void* z,
+                   float* lse, void* scratch, size_t scratch_bytes, const gdnbeam_dumps* dumps,
+                   gdnbeam_stream_t stream) {
+  int st = validate(cfg);
+  if (st) return st;
+  if (n < 0 || !feat || !W_o || !z || !lse) return GDNBEAM_EINVAL;
+  if (n == 0) return GDNBEAM_OK;
+  return logits_any(*cfg, tc_gemm_supported(*cfg), n, feat, W_o, z, lse, scratch, scratch_bytes,
+                    dumps, (cudaStream_t)stream);
+}
+
+size_t gdnbeam_select_scratch_bytes(int R, int W_t, int W_next, int V) {
+  if (R < 1 || W_t < 1 || W_next < 1 || V < 1) return 0;
+  return select_scratch_bytes(R, W_t, W_next, V);
+}
+
+int gdnbeam_select_topw(int R, int W_t, int W_next, int V, int dtype, const void* logits,
+                        const float* lse, const float* cum, const float* bias, int32_t* parents,
+                        int32_t* tokens, float* cum_next, void* scratch, size_t scratch_bytes,
+                        gdnbeam_stream_t stream) {
+  if (R < 1 || W_t < 1 || W_next < 1 || V < 2 || !logits || !lse || !parents || !tokens ||
+      !cum_next || !scratch)
+    return GDNBEAM_EINVAL;
+  if (dtype != GDNBEAM_F32 && dtype != GDNBEAM_BF16) return GDNBEAM_EUNSUPPORTED;
+  if ((long long)W_t * V >= (1ll << 31) || (long long)W_next > (long long)W_t * V)
+    return GDNBEAM_EINVAL;
+  if (scratch_bytes < select_scratch_bytes(R, W_t, W_next, V)) return GDNBEAM_EWORKSPACE;
+  return launch_select(R, W_t, W_next, V, dtype, logits, lse, cum, bias, parents, tokens,
+                       cum_next, scratch, err_ptr(), (cudaStream_t)stream);
+}
+
+int gdnbeam_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int32_t* parents,
+                     const int32_t* tokens, const int32_t* anc_prev, const int32_t* sid_prev,
+                     int32_t* anc_out, int32_t* sid_out, gdnbeam_stream_t stream) {
+  if (R < 1 || t < 0 || t >= T || T > GDNBEAM_MAX_T || W_t < 1 || W_prev < 1 || !tokens ||
+      !sid_out)
+    return GDNBEAM_EINVAL;
+  if (t > 0 && (!parents || !sid_prev)) return GDNBEAM_EINVAL;
+  if (t > 1 && anc_out && !anc_prev) return GDNBEAM_EINVAL;
+  return launch_ancestry(R, t, T, V, W_prev, W_t, parents, tokens, anc_prev, sid_prev, anc_out,
+                         sid_out, err_ptr(), (cudaStream_t)stream);
+}
+
+int gdnbeam_prefill_scan(const gdnbeam_config* cfg, int L, const void* q, const void* k,
+                         const void* v, const float* alpha, const float* beta, void* sctx_out,
+                         long long sctx_rstride, void* o_last, float* x_inout,
+                         gdnbeam_stream_t stream) {
+  int st = validate(cfg);
+  if (st) return st;
+  if (L < 1 || !q || !k || !v || !alpha || !beta || !sctx_out) return GDNBEAM_EINVAL;
+  return launch_prefill_scan(*cfg, L, q, k, v, alpha, beta, sctx_out, sctx_rstride, o_last,
+                             x_inout, (cudaStream_t)stream);
+}
+
+}  // extern "C"

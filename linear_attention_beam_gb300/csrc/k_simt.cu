@@ -1,0 +1,251 @@
+// CUDA-core kernels for the shape-general path: embedding gather, RMSNorm,
+// a tiled fp32-accumulating GEMM, and the projection / logits epilogues.
+// These serve the fp32 storage runs and any shape the tensor-core kernels do
+// not cover; the bf16 d = 128 hot path uses the tcgen05 kernels instead.
+#include "common.cuh"
+#include "launchers.h"
+
+namespace gdnbeam {
+
+// ---------------------------------------------------------------------------
+// Embedding gather: u[m] = E[tok[m]]
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void gather_rows_kernel(int n, int d_model, const int32_t* __restrict__ tokens, int V,
+                                   const T* __restrict__ E, T* __restrict__ u,
+                                   float* __restrict__ x, unsigned* err) {
+  int m = blockIdx.x;
+  if (m >= n) return;
+  int tok = tokens[m];
+  bool ok = tok >= 0 && tok < V;
+  if (!ok && threadIdx.x == 0) raise_error(err, GDNBEAM_DERR_TOKEN);
+  const T* src = E + (size_t)(ok ? tok : 0) * d_model;
+  for (int c = threadIdx.x; c < d_model; c += blockDim.x) {
+    T val = ok ? src[c] : St<T>::from_f(0.0f);
+    u[(size_t)m * d_model + c] = val;
+    if (x) x[(size_t)m * d_model + c] = St<T>::to_f(val);
+  }
+}
+
+int launch_gather_rows(int dtype, int n, int d_model, const int32_t* tokens, int V,
+                       const void* E, void* u, float* x, unsigned* err, cudaStream_t s) {
+  if (n <= 0) return GDNBEAM_OK;
+  if (dtype == GDNBEAM_BF16)
+    gather_rows_kernel<__nv_bfloat16><<<n, 256, 0, s>>>(n, d_model, tokens, V,
+        (const __nv_bfloat16*)E, (__nv_bfloat16*)u, x, err);
+  else
+    gather_rows_kernel<float><<<n, 256, 0, s>>>(n, d_model, tokens, V, (const float*)E,
+                                                (float*)u, x, err);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm rows (unit gain, eps 1e-6): one warp per row
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void rmsnorm_rows_kernel(int n, int d, const float* __restrict__ x, long long xs,
+                                    T* __restrict__ u) {
+  int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int lane = threadIdx.x & 31;
+  if (warp >= n) return;
+  const float* row = x + (size_t)warp * xs;
+  float ss = 0.0f;
+  for (int c = lane; c < d; c += 32) ss += row[c] * row[c];
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  float inv = 1.0f / sqrtf(ss / (float)d + 1e-6f);
+  for (int c = lane; c < d; c += 32) stf(u + (size_t)warp * d + c, row[c] * inv);
+}
+
+int launch_rmsnorm_rows(int dtype, int n, int d, const float* x, long long xs, void* u,
+                        cudaStream_t s) {
+  if (n <= 0) return GDNBEAM_OK;
+  int blocks = (n + 7) / 8;
+  if (dtype == GDNBEAM_BF16)
+    rmsnorm_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(n, d, x, xs, (__nv_bfloat16*)u);
+  else
+    rmsnorm_rows_kernel<float><<<blocks, 256, 0, s>>>(n, d, x, xs, (float*)u);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// C = A . B^T on CUDA cores: 64x64 tile, 16-deep k slices, 4x4 per thread
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) simt_gemm_nt_kernel(int M, int N, int K,
+    const T* __restrict__ A, int lda, const T* __restrict__ B, int ldb, float* __restrict__ C,
+    int ldc) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+      int r = i >> 4, kk = i & 15;
+      int gk = k0 + kk;
+      int gm = m0 + r, gn = n0 + r;
+      As[kk][r] = (gm < M && gk < K) ? ldf(A + (size_t)gm * lda + gk) : 0.0f;
+      Bs[kk][r] = (gn < N && gk < K) ? ldf(B + (size_t)gn * ldb + gk) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int gm = m0 + ty * 4 + i;
+    if (gm >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int gn = n0 + tx * 4 + j;
+      if (gn < N) C[(size_t)gm * ldc + gn] = acc[i][j];
+    }
+  }
+}
+
+int launch_simt_gemm_nt(int dtype, int M, int N, int K, const void* A, int lda, const void* B,
+                        int ldb, float* C, int ldc, cudaStream_t s) {
+  if (M <= 0 || N <= 0) return GDNBEAM_OK;
+  dim3 grid((N + 63) / 64, (M + 63) / 64);
+  if (grid.y > 65535) return GDNBEAM_EUNSUPPORTED;
+  if (dtype == GDNBEAM_BF16)
+    simt_gemm_nt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(M, N, K, (const __nv_bfloat16*)A,
+        lda, (const __nv_bfloat16*)B, ldb, C, ldc);
+  else
+    simt_gemm_nt_kernel<float><<<grid, 256, 0, s>>>(M, N, K, (const float*)A, lda,
+                                                    (const float*)B, ldb, C, ldc);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Projection epilogue: one warp per (row, head)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void proj_epilogue_kernel(int n, int H, int dk, int dv, const float* __restrict__ P,
+                                     T* __restrict__ q, T* __restrict__ k, T* __restrict__ v,
+                                     float* __restrict__ alpha, float* __restrict__ beta,
+                                     gdnbeam_dumps dmp) {
+  int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  int lane = threadIdx.x & 31;
+  if (gw >= n * H) return;
+  int m = gw / H, h = gw % H;
+  const int Np = 2 * H * dk + H * dv + 2 * H;
+  const float* row = P + (size_t)m * Np;
+  const float* pq = row + h * dk;
+  const float* pk = row + H * dk + h * dk;
+  const float* pv = row + 2 * H * dk + h * dv;
+  float sq = 0.0f, sk = 0.0f;
+  for (int c = lane; c < dk; c += 32) { sq += pq[c] * pq[c]; sk += pk[c] * pk[c]; }
+  for (int o = 16; o > 0; o >>= 1) {
+    sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+  }
+  float iq = 1.0f / sqrtf(sq + 1e-6f), ik = 1.0f / sqrtf(sk + 1e-6f);
+  size_t oq = (size_t)m * H * dk + (size_t)h * dk, ov = (size_t)m * H * dv + (size_t)h * dv;
+  for (int c = lane; c < dk; c += 32) {
+    float qq = pq[c] * iq, kk = pk[c] * ik;
+    stf(q + oq + c, qq);
+    stf(k + oq + c, kk);
+    if (dmp.q) dmp.q[oq + c] = qq;
+    if (dmp.k) dmp.k[oq + c] = kk;
+  }
+  for (int c = lane; c < dv; c += 32) {
+    stf(v + ov + c, pv[c]);
+    if (dmp.v) dmp.v[ov + c] = pv[c];
+  }
+  if (lane == 0) {
+    float a = decay_gate(row[2 * H * dk + H * dv + h]);
+    float b = write_gate(row[2 * H * dk + H * dv + H + h]);
+    alpha[(size_t)m * H + h] = a;
+    beta[(size_t)m * H + h] = b;
+    if (dmp.alpha) dmp.alpha[(size_t)m * H + h] = a;
+    if (dmp.beta) dmp.beta[(size_t)m * H + h] = b;
+  }
+}
+
+int launch_proj_epilogue(const gdnbeam_config& c, int n, const float* P, void* q, void* k,
+                         void* v, float* alpha, float* beta, const gdnbeam_dumps* d,
+                         cudaStream_t s) {
+  if (n <= 0) return GDNBEAM_OK;
+  gdnbeam_dumps dm = d ? *d : gdnbeam_dumps{};
+  long long warps = (long long)n * c.H;
+  int blocks = (int)((warps + 7) / 8);
+  if (c.dtype == GDNBEAM_BF16)
+    proj_epilogue_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(n, c.H, c.d_k, c.d_v, P,
+        (__nv_bfloat16*)q, (__nv_bfloat16*)k, (__nv_bfloat16*)v, alpha, beta, dm);
+  else
+    proj_epilogue_kernel<float><<<blocks, 256, 0, s>>>(n, c.H, c.d_k, c.d_v, P, (float*)q,
+        (float*)k, (float*)v, alpha, beta, dm);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Logits rows: store z in the storage type and lse = max + log sum exp(z - max)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void logits_rows_kernel(int n, int V, const float* __restrict__ Z, T* __restrict__ z,
+                                   float* __restrict__ lse, float* __restrict__ zd) {
+  int m = blockIdx.x;
+  const float* row = Z + (size_t)m * V;
+  __shared__ float red[32];
+  float mx = -INFINITY;
+  for (int c = threadIdx.x; c < V; c += blockDim.x) mx = fmaxf(mx, row[c]);
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float w = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : -INFINITY;
+    for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
+    if (threadIdx.x == 0) red[0] = w;
+  }
+  __syncthreads();
+  mx = red[0];
+  __syncthreads();
+  float se = 0.0f;
+  for (int c = threadIdx.x; c < V; c += blockDim.x) {
+    float val = row[c];
+    se += expf(val - mx);
+    stf(z + (size_t)m * V + c, val);
+    if (zd) zd[(size_t)m * V + c] = val;
+  }
+  for (int o = 16; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = se;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+    lse[m] = mx + logf(tot);
+  }
+}
+
+int launch_logits_rows(int dtype, int n, int V, const float* Z, void* z, float* lse,
+                       float* z_dump, cudaStream_t s) {
+  if (n <= 0) return GDNBEAM_OK;
+  if (dtype == GDNBEAM_BF16)
+    logits_rows_kernel<__nv_bfloat16><<<n, 256, 0, s>>>(n, V, Z, (__nv_bfloat16*)z, lse, z_dump);
+  else
+    logits_rows_kernel<float><<<n, 256, 0, s>>>(n, V, Z, (float*)z, lse, z_dump);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
+}  // namespace gdnbeam

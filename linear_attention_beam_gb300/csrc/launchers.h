@@ -1,0 +1,81 @@
+// Host-side launchers of the gdnbeam kernels (internal to the library).
+// Each returns a GDNBEAM_* status; all take the device error word pointer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdnbeam.h"
+
+namespace gdnbeam {
+
+// ---- CUDA-core kernels (any supported shape, fp32 or bf16 storage) -------
+
+// u[m] = E[tokens[m]] (storage copy); if x != NULL also x[m] = fp32(E[...]).
+int launch_gather_rows(int dtype, int n, int d_model, const int32_t* tokens, int V,
+                       const void* E, void* u, float* x, unsigned* err, cudaStream_t s);
+
+// u[m] = x[m] / sqrt(mean(x[m]^2) + 1e-6), stored in the storage type.
+// Rows are x + m*x_stride (fp32) and u + m*d (storage).
+int launch_rmsnorm_rows(int dtype, int n, int d, const float* x, long long x_stride, void* u,
+                        cudaStream_t s);
+
+// C[M][N] (fp32, row stride ldc) = A[M][K] . B[N][K]^T, storage inputs.
+int launch_simt_gemm_nt(int dtype, int M, int N, int K, const void* A, int lda,
+                        const void* B, int ldb, float* C, int ldc, cudaStream_t s);
+
+// Raw projections P[n][N_proj] (fp32) -> q, k, v (storage), alpha, beta.
+int launch_proj_epilogue(const gdnbeam_config& c, int n, const float* P, void* q, void* k,
+                         void* v, float* alpha, float* beta, const gdnbeam_dumps* d,
+                         cudaStream_t s);
+
+// Raw logits Z[n][V] (fp32) -> z (storage), lse, optional fp32 dump.
+int launch_logits_rows(int dtype, int n, int V, const float* Z, void* z, float* lse,
+                       float* z_dump, cudaStream_t s);
+
+// ---- tcgen05 tensor-core GEMMs (bf16, d = 128, d_model % 64 == 0) --------
+
+bool tc_gemm_supported(const gdnbeam_config& c);
+int launch_tc_project(const gdnbeam_config& c, int n, const void* u, const void* W_proj,
+                      void* q, void* k, void* v, float* alpha, float* beta,
+                      const gdnbeam_dumps* d, cudaStream_t s);
+size_t tc_logits_scratch_bytes(const gdnbeam_config& c, int n);
+int launch_tc_logits(const gdnbeam_config& c, int n, const void* feat, const void* W_o,
+                     void* z, float* lse, void* scratch, const gdnbeam_dumps* d,
+                     cudaStream_t s);
+
+// ---- replay, prefill, selection, ancestry ---------------------------------
+
+struct ReplayArgs {
+  int R, H, d_k, d_v, t, W_t;
+  const void* sctx;
+  long long sctx_rstride;
+  const void *q, *k, *v;
+  const float *alpha, *beta;
+  gdnbeam_records depth[GDNBEAM_MAX_T];
+  const int32_t* anc;
+  int anc_stride;
+  void *delta_out, *o_out;
+  float* x_inout;
+  float *delta_dump, *o_dump;
+  unsigned* err;
+};
+int launch_replay(int dtype, const ReplayArgs& a, cudaStream_t s);
+bool tc_replay_supported(int dtype, int d_k, int d_v);
+int launch_tc_replay(const ReplayArgs& a, cudaStream_t s);
+
+int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const void* k,
+                        const void* v, const float* alpha, const float* beta, void* sctx,
+                        long long sctx_rstride, void* o_last, float* x_inout, cudaStream_t s);
+
+size_t select_scratch_bytes(int R, int W_t, int W_next, int V);
+int launch_select(int R, int W_t, int W_next, int V, int dtype, const void* logits,
+                  const float* lse, const float* cum, const float* bias, int32_t* parents,
+                  int32_t* tokens, float* cum_next, void* scratch, unsigned* err,
+                  cudaStream_t s);
+
+int launch_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int32_t* parents,
+                    const int32_t* tokens, const int32_t* anc_prev, const int32_t* sid_prev,
+                    int32_t* anc_out, int32_t* sid_out, unsigned* err, cudaStream_t s);
+
+}  // namespace gdnbeam

@@ -9,5 +9,5 @@ from .fullstate import (  # noqa: F401
     gdn_transition, state_from_records, step_from_records, prefill_scan,
     codebook_logits, log_normalizer, layer_feature, scores_f32, select_top,
     kept_scores_f32, ancestry_slots, token_paths, prefill, decode_request,
-    chain_decode, CallTrace, RequestTrace,
+    chain_decode, chain_trace, CallTrace, RequestTrace,
 )

@@ -358,26 +358,38 @@ def decode_request(wl, params, prompt: np.ndarray, bias: Optional[np.ndarray] = 
                         calls, sid)
 
 
-def chain_decode(wl, params, S_ctx: np.ndarray, path: Sequence[int]):
+def chain_trace(wl, params, S_ctx: np.ndarray, path: Sequence[int]) -> List[CallTrace]:
     """Decode one SID path sequentially (a single beam, no beam tree).
 
-    path: tokens fed at decode calls 0..len(path)-1. Returns per-call
-    (features [F], z [V], lse) lists.
+    path: tokens fed at decode calls 0..len(path)-1 (the beam's ancestors'
+    tokens, root first). Returns one single-row CallTrace per call. A beam's
+    values at call t depend only on S_ctx and its own path, so this gives the
+    FullState result for sampled beams of a large beam tree.
     """
     S = np.array(S_ctx, dtype=F64, copy=True)
-    feats, zs, lses = [], [], []
+    out: List[CallTrace] = []
     for tok in path:
+        tr = CallTrace(tokens=np.array([tok], dtype=np.int32))
         x = params.E[[tok]].astype(F64)
         feat_in = x
         for layer in range(wl.layers):
             u = rms_normalize(x) if wl.residual else x
             q, k, v, a, b = gdn_inputs(wl, params, layer, u)
-            S[layer], _, o = gdn_transition(S[layer], q[0], k[0], v[0], a[0], b[0])
+            S[layer], delta, o = gdn_transition(S[layer], q[0], k[0], v[0], a[0], b[0])
+            tr.q.append(q); tr.k.append(k); tr.v.append(v); tr.alpha.append(a); tr.beta.append(b)
+            tr.delta.append(delta[None]); tr.o.append(o[None])
             if wl.residual:
                 x = x + o.reshape(1, -1)
             else:
                 feat_in = o.reshape(1, -1)
-        f = layer_feature(wl, x if wl.residual else feat_in)[0]
-        z = codebook_logits(params, f[None, :])[0]
-        feats.append(f); zs.append(z); lses.append(float(log_normalizer(z[None, :])[0]))
-    return feats, zs, lses
+        tr.feat = layer_feature(wl, x if wl.residual else feat_in)
+        tr.z = codebook_logits(params, tr.feat)
+        tr.lse = log_normalizer(tr.z)
+        out.append(tr)
+    return out
+
+
+def chain_decode(wl, params, S_ctx: np.ndarray, path: Sequence[int]):
+    """Per-call (feature [F], z [V], lse) of one sequentially decoded path."""
+    tr = chain_trace(wl, params, S_ctx, path)
+    return ([c.feat[0] for c in tr], [c.z[0] for c in tr], [float(c.lse[0]) for c in tr])

@@ -1,0 +1,303 @@
+"""Each CUDA stage against the oracle on identical stored inputs, through the
+tensor-level C ABI. Shapes span several tiles and end in ragged tails."""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import synth
+import linear_attention_beam_gb300 as gb
+from gpu_util import (DEV, TOL_BF16, TOL_F32, cfg_for, device_status_clear, host, maxrel,
+                      store, tdt, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+U = 2.0 ** -8  # bf16 unit roundoff (storage rounding of a stored output)
+
+
+def _tol(wl):
+    return TOL_BF16 if wl.dtype == "bf16" else TOL_F32
+
+
+def _check_stored(g, o, wl, what):
+    """Stored output: within tol of max|o| plus the storage rounding of o."""
+    g = np.asarray(g, np.float64); o = np.asarray(o, np.float64)
+    extra = U * np.abs(o) if wl.dtype == "bf16" else 0.0
+    bound = _tol(wl) * np.abs(o).max() + extra
+    bad = np.abs(g - o) > bound
+    assert not bad.any(), f"{what}: {bad.sum()} elements out of bound, maxrel={maxrel(g, o):.3g}"
+
+
+def _unit_rows(rng, shape):
+    x = rng.standard_normal(shape)
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+# ------------------------------------------------------------------ selection
+
+def _select_case(rng, R, W_t, W_next, V, dtype, ties=True, bias=True):
+    z = rng.standard_normal((R, W_t, V)).astype(np.float32) * 2.0
+    if ties:
+        z[:, :, ::5] = z[:, :, :1]
+        if W_t > 1:
+            z[:, 1] = z[:, 0]
+    z = synth.to_storage(z, dtype)
+    lse = np.stack([oracle.log_normalizer(z[r]) for r in range(R)]).astype(np.float32)
+    cum = np.sort(rng.standard_normal((R, W_t)).astype(np.float32))[:, ::-1].copy()
+    if W_t > 2:
+        cum[:, 2] = cum[:, 1]
+    b = rng.standard_normal((R, W_t)).astype(np.float32) * 2.0 if bias else None
+    return z, lse, cum, b
+
+
+@pytest.mark.parametrize("R,W_t,W_next,V,dtype", [
+    (1, 1, 8, 16, "f32"), (3, 5, 7, 300, "bf16"), (2, 37, 64, 513, "bf16"),
+    (4, 64, 200, 100, "f32"), (2, 9, 45, 5, "bf16"), (1, 3, 1, 2, "f32")])
+def test_select_topw_bit_exact(R, W_t, W_next, V, dtype):
+    rng = np.random.default_rng(R * 1000 + W_t + V)
+    z, lse, cum, b = _select_case(rng, R, W_t, W_next, V, dtype)
+    lib = gb.load()
+    tz = to_dev(z.reshape(R * W_t, V), torch.bfloat16 if dtype == "bf16" else torch.float32)
+    scratch = torch.empty(lib.gdnbeam_select_scratch_bytes(R, W_t, W_next, V), dtype=torch.uint8, device=DEV)
+    for bias in (None, b):
+        par = torch.empty(R, W_next, dtype=torch.int32, device=DEV)
+        tok = torch.empty_like(par)
+        cn = torch.empty(R, W_next, dtype=torch.float32, device=DEV)
+        st = lib.gdnbeam_select_topw(R, W_t, W_next, V, gb.BF16 if dtype == "bf16" else gb.F32,
+                                     gb.ptr(tz), gb.ptr(to_dev(lse)), gb.ptr(to_dev(cum)),
+                                     gb.ptr(to_dev(bias) if bias is not None else None),
+                                     gb.ptr(par), gb.ptr(tok), gb.ptr(cn), gb.ptr(scratch),
+                                     scratch.numel(), None)
+        assert st == 0
+        assert device_status_clear() == 0
+        for r in range(R):
+            p, t, s = oracle.select_top(z[r], lse[r], cum[r], W_next, None if bias is None else bias[r])
+            np.testing.assert_array_equal(par[r].cpu().numpy(), p)
+            np.testing.assert_array_equal(tok[r].cpu().numpy(), t)
+            np.testing.assert_array_equal(cn[r].cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
+def test_select_topw_full_size_sampled():
+    # 64 requests x 512 beams x 8192 codes: the batched workload's selection
+    R, W, V = 64, 512, 8192
+    rng = np.random.default_rng(77)
+    z, lse, cum, _ = _select_case(rng, R, W, W, V, "bf16", bias=False)
+    lib = gb.load()
+    scratch = torch.empty(lib.gdnbeam_select_scratch_bytes(R, W, W, V), dtype=torch.uint8, device=DEV)
+    par = torch.empty(R, W, dtype=torch.int32, device=DEV)
+    tok = torch.empty_like(par)
+    cn = torch.empty(R, W, dtype=torch.float32, device=DEV)
+    assert lib.gdnbeam_select_topw(R, W, W, V, gb.BF16, gb.ptr(to_dev(z.reshape(R * W, V), torch.bfloat16)),
+                                   gb.ptr(to_dev(lse)), gb.ptr(to_dev(cum)), None, gb.ptr(par),
+                                   gb.ptr(tok), gb.ptr(cn), gb.ptr(scratch), scratch.numel(), None) == 0
+    assert device_status_clear() == 0
+    for r in (0, 29, 63):
+        p, t, s = oracle.select_top(z[r], lse[r], cum[r], W)
+        np.testing.assert_array_equal(par[r].cpu().numpy(), p)
+        np.testing.assert_array_equal(tok[r].cpu().numpy(), t)
+        np.testing.assert_array_equal(cn[r].cpu().numpy(), s)
+    # properties on every request: sorted keys, valid indices
+    c = cn.cpu().numpy()
+    assert np.all(np.diff(c, axis=1) <= 0)
+    assert par.min().item() >= 0 and par.max().item() < W and tok.max().item() < V
+
+
+# ------------------------------------------------------------------ ancestry
+
+def test_ancestry_op_matches_walk():
+    rng = np.random.default_rng(5)
+    T, R, V = 5, 3, 11
+    W = [4, 6, 3, 7, 5]
+    parents = [np.zeros((R, W[0]), np.int32)] + [rng.integers(0, W[s - 1], (R, W[s])).astype(np.int32) for s in range(1, T)]
+    tokens = [rng.integers(0, V, (R, W[s])).astype(np.int32) for s in range(T)]
+    lib = gb.load()
+    Wm = max(W)
+    anc = [torch.zeros(R * Wm, T, dtype=torch.int32, device=DEV) for _ in range(2)]
+    sid = [torch.zeros(R * Wm, T, dtype=torch.int32, device=DEV) for _ in range(2)]
+    for t in range(T):
+        cur, prev = anc[t & 1], anc[(t & 1) ^ 1]
+        st = lib.gdnbeam_ancestry(R, t, T, V, W[t - 1] if t else 1, W[t], gb.ptr(to_dev(parents[t], torch.int32)),
+                                  gb.ptr(to_dev(tokens[t], torch.int32)), gb.ptr(prev), gb.ptr(sid[(t & 1) ^ 1]),
+                                  gb.ptr(cur), gb.ptr(sid[t & 1]), None)
+        assert st == 0
+        for r in range(R):
+            exp = oracle.ancestry_slots([p[r] for p in parents], t)
+            got = cur[r * W[t]:(r + 1) * W[t], :t].cpu().numpy()
+            np.testing.assert_array_equal(got, exp)
+    for r in range(R):
+        exp = oracle.token_paths([p[r] for p in parents], [x[r] for x in tokens])
+        np.testing.assert_array_equal(sid[(T - 1) & 1][r * W[-1]:(r + 1) * W[-1]].cpu().numpy(), exp)
+    assert device_status_clear() == 0
+
+
+# ------------------------------------------------------------------ replay
+
+@pytest.mark.parametrize("dtype,d,H,R,W_t,t,resid", [
+    ("f32", 16, 1, 1, 8, 2, False), ("bf16", 128, 3, 2, 37, 2, False),
+    ("bf16", 64, 2, 3, 20, 3, True), ("f32", 128, 2, 2, 19, 1, False),
+    ("bf16", 128, 2, 2, 300, 0, False), ("bf16", 32, 1, 1, 5, 5, False)])
+def test_replay_op(dtype, d, H, R, W_t, t, resid):
+    wl = synth.tiny_workload(d=d, V=7, H=H, R=R, dtype=dtype)
+    rng = np.random.default_rng(d + H + W_t + t)
+    st_ = lambda a: store(a, wl)
+    S_ctx = st_(rng.standard_normal((R, H, d, d)) * 0.05)
+    Wj = [int(rng.integers(1, 40)) for _ in range(t)]
+    rec_k = [st_(_unit_rows(rng, (R, Wj[j], H, d))) for j in range(t)]
+    rec_d = [st_(rng.standard_normal((R, Wj[j], H, d)) * 0.5) for j in range(t)]
+    rec_a = [rng.uniform(0.2, 1.0, (R, Wj[j], H)).astype(np.float32).astype(np.float64) for j in range(t)]
+    q = st_(_unit_rows(rng, (R, W_t, H, d)))
+    k = st_(_unit_rows(rng, (R, W_t, H, d)))
+    v = st_(rng.standard_normal((R, W_t, H, d)))
+    al = rng.uniform(0.1, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
+    be = rng.uniform(0.0, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
+    anc = np.stack([rng.integers(0, Wj[j], (R, W_t)) for j in range(t)], -1).astype(np.int32) if t else np.zeros((R, W_t, 1), np.int32)
+    x0 = rng.standard_normal((R, W_t, H * d)) if resid else None
+
+    td = tdt(wl)
+    keep = []
+    recs = (gb.Records * max(t, 1))()
+    for j in range(t):
+        tk, tdl, ta = to_dev(rec_k[j].reshape(-1), td), to_dev(rec_d[j].reshape(-1), td), to_dev(rec_a[j].reshape(-1))
+        keep += [tk, tdl, ta]
+        recs[j] = gb.Records(gb.ptr(tk), gb.ptr(tdl), gb.ptr(ta), Wj[j])
+    n = R * W_t
+    d_out = torch.empty(n, H * d, dtype=td, device=DEV)
+    o_out = torch.empty_like(d_out)
+    d_dump = torch.zeros(n, H * d, device=DEV)
+    o_dump = torch.zeros_like(d_dump)
+    x_dev = to_dev(x0.reshape(n, H * d)) if resid else None
+    dm = gb.dumps(delta=d_dump, o=o_dump)
+    cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d, T=max(t + 1, 2))
+    lib = gb.load()
+    st = lib.gdnbeam_replay(C.byref(cfg), t, W_t, gb.ptr(to_dev(S_ctx.reshape(-1), td)), H * d * d,
+                            gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
+                            gb.ptr(to_dev(v.reshape(-1), td)), gb.ptr(to_dev(al.reshape(-1))),
+                            gb.ptr(to_dev(be.reshape(-1))), recs,
+                            gb.ptr(to_dev(anc.reshape(n, -1), torch.int32)), anc.shape[-1],
+                            gb.ptr(d_out), gb.ptr(o_out), gb.ptr(x_dev), C.byref(dm), None)
+    assert st == 0
+    assert device_status_clear() == 0
+    exp_d = np.zeros((R, W_t, H, d)); exp_o = np.zeros_like(exp_d)
+    for r in range(R):
+        for b in range(W_t):
+            for h in range(H):
+                chain = [(rec_a[j][r, anc[r, b, j], h], rec_d[j][r, anc[r, b, j], h], rec_k[j][r, anc[r, b, j], h]) for j in range(t)]
+                exp_d[r, b, h], exp_o[r, b, h] = oracle.step_from_records(
+                    S_ctx[r, h], chain, q[r, b, h], k[r, b, h], v[r, b, h], al[r, b, h], be[r, b, h])
+    tol = _tol(wl)
+    assert maxrel(host(d_dump).reshape(exp_d.shape), exp_d) <= tol
+    assert maxrel(host(o_dump).reshape(exp_o.shape), exp_o) <= tol
+    _check_stored(host(d_out).reshape(exp_d.shape), exp_d, wl, "delta")
+    _check_stored(host(o_out).reshape(exp_o.shape), exp_o, wl, "o")
+    if resid:
+        assert maxrel(host(x_dev).reshape(R, W_t, H * d), x0 + exp_o.reshape(R, W_t, H * d)) <= tol
+
+
+def test_replay_rejects_out_of_range_slot():
+    wl = synth.tiny_workload(d=16, V=7, H=1, R=1, dtype="f32")
+    lib = gb.load()
+    t, W_t, d = 1, 4, 16
+    z = lambda *s: torch.zeros(*s, device=DEV)
+    k1, d1, a1 = z(3 * d), z(3 * d), z(3)
+    recs = (gb.Records * 1)(gb.Records(gb.ptr(k1), gb.ptr(d1), gb.ptr(a1), 3))
+    anc = torch.tensor([[0], [1], [7], [2]], dtype=torch.int32, device=DEV)  # 7 >= W_j = 3
+    cfg = cfg_for(wl)
+    out = z(W_t * d)
+    st = lib.gdnbeam_replay(C.byref(cfg), t, W_t, gb.ptr(z(d * d)), d * d, gb.ptr(z(W_t * d)), gb.ptr(z(W_t * d)),
+                            gb.ptr(z(W_t * d)), gb.ptr(z(W_t)), gb.ptr(z(W_t)), recs, gb.ptr(anc), 1,
+                            gb.ptr(out), gb.ptr(z(W_t * d)), None, None, None)
+    assert st == 0
+    assert device_status_clear() & gb.DERR["slot"]
+    assert device_status_clear() == 0
+
+
+# ------------------------------------------------------------------ projections
+
+@pytest.mark.parametrize("dtype,d,H,d_model,n", [("f32", 16, 1, 16, 8), ("bf16", 32, 3, 96, 70),
+                                                 ("bf16", 128, 2, 256, 130), ("f32", 64, 2, 64, 33)])
+def test_project_op(dtype, d, H, d_model, n):
+    wl = synth.tiny_workload(d=d, V=9, H=H, d_model=d_model, dtype=dtype, seed=d + n)
+    p = synth.make_params(wl)
+    rng = np.random.default_rng(n)
+    u = store(rng.standard_normal((n, d_model)), wl)
+    q, k, v, a, b = oracle.gdn_inputs(wl, p, 0, u)
+    td = tdt(wl)
+    Wp = to_dev(np.concatenate([p.Wq[0], p.Wk[0], p.Wv[0], p.w_alpha[0], p.w_beta[0]]), td)
+    lib = gb.load()
+    cfg = cfg_for(wl)
+    outs = [torch.empty(n, H * d, dtype=td, device=DEV) for _ in range(3)]
+    al, be = torch.empty(n, H, device=DEV), torch.empty(n, H, device=DEV)
+    dq, dk, dv = (torch.zeros(n, H * d, device=DEV) for _ in range(3))
+    dm = gb.dumps(q=dq, k=dk, v=dv)
+    sb = lib.gdnbeam_project_scratch_bytes(C.byref(cfg), n)
+    scratch = torch.empty(max(sb, 1), dtype=torch.uint8, device=DEV)
+    st = lib.gdnbeam_project(C.byref(cfg), n, gb.ptr(to_dev(u, td)), gb.ptr(Wp), gb.ptr(outs[0]),
+                             gb.ptr(outs[1]), gb.ptr(outs[2]), gb.ptr(al), gb.ptr(be), gb.ptr(scratch),
+                             sb, C.byref(dm), None)
+    assert st == 0
+    tol = _tol(wl)
+    for got, dump, exp, nm in ((outs[0], dq, q, "q"), (outs[1], dk, k, "k"), (outs[2], dv, v, "v")):
+        assert maxrel(host(dump), exp.reshape(n, -1)) <= tol, nm
+        _check_stored(host(got), exp.reshape(n, -1), wl, nm)
+    assert maxrel(host(al), a) <= tol and maxrel(host(be), b) <= tol
+
+
+# ------------------------------------------------------------------ logits
+
+@pytest.mark.parametrize("dtype,F,V,n", [("f32", 16, 16, 8), ("bf16", 128, 300, 70), ("bf16", 256, 1000, 129)])
+def test_logits_op(dtype, F, V, n):
+    wl = synth.tiny_workload(d=F, V=V, H=1, d_model=F, dtype=dtype, seed=F + V)
+    p = synth.make_params(wl)
+    rng = np.random.default_rng(V)
+    feat = store(rng.standard_normal((n, F)), wl)
+    z = oracle.codebook_logits(p, feat)
+    lse = oracle.log_normalizer(z)
+    td = tdt(wl)
+    lib = gb.load()
+    cfg = cfg_for(wl)
+    zo = torch.empty(n, V, dtype=td, device=DEV)
+    lo = torch.empty(n, device=DEV)
+    zd = torch.zeros(n, V, device=DEV)
+    dm = gb.dumps(logits=zd)
+    sb = lib.gdnbeam_logits_scratch_bytes(C.byref(cfg), n)
+    scratch = torch.empty(max(sb, 1), dtype=torch.uint8, device=DEV)
+    assert lib.gdnbeam_logits(C.byref(cfg), n, gb.ptr(to_dev(feat, td)), gb.ptr(to_dev(p.Wo, td)),
+                              gb.ptr(zo), gb.ptr(lo), gb.ptr(scratch), sb, C.byref(dm), None) == 0
+    tol = _tol(wl)
+    assert maxrel(host(zd), z) <= tol
+    _check_stored(host(zo), z, wl, "z")
+    assert np.abs(host(lo) - lse).max() <= tol * np.abs(z).max()
+
+
+# ------------------------------------------------------------------ prefill
+
+@pytest.mark.parametrize("dtype,d,H,R,L,resid", [("f32", 16, 1, 1, 32, False), ("bf16", 32, 2, 2, 33, True),
+                                                 ("bf16", 128, 2, 2, 65, False)])
+def test_prefill_scan_op(dtype, d, H, R, L, resid):
+    wl = synth.tiny_workload(d=d, V=5, H=H, R=R, dtype=dtype)
+    rng = np.random.default_rng(L + d)
+    q = store(_unit_rows(rng, (R, L, H, d)), wl)
+    k = store(_unit_rows(rng, (R, L, H, d)), wl)
+    v = store(rng.standard_normal((R, L, H, d)), wl)
+    a = rng.uniform(0.3, 1.0, (R, L, H)).astype(np.float32).astype(np.float64)
+    b = rng.uniform(0.0, 1.0, (R, L, H)).astype(np.float32).astype(np.float64)
+    x0 = rng.standard_normal((R, L, H * d)) if resid else None
+    td = tdt(wl)
+    lib = gb.load()
+    cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d)
+    sc = torch.empty(R, H, d, d, dtype=td, device=DEV)
+    ol = torch.empty(R, H * d, dtype=td, device=DEV)
+    xd = to_dev(x0.reshape(R * L, H * d)) if resid else None
+    st = lib.gdnbeam_prefill_scan(C.byref(cfg), L, gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
+                                  gb.ptr(to_dev(v.reshape(-1), td)), gb.ptr(to_dev(a.reshape(-1))),
+                                  gb.ptr(to_dev(b.reshape(-1))), gb.ptr(sc), H * d * d, gb.ptr(ol), gb.ptr(xd), None)
+    assert st == 0
+    for r in range(R):
+        S, o = oracle.prefill_scan(q[r], k[r], v[r], a[r], b[r])
+        _check_stored(host(sc[r]), S, wl, "S_ctx")
+        _check_stored(host(ol[r]).reshape(H, d), o[-1], wl, "o_last")
+        if resid:
+            assert maxrel(host(xd).reshape(R, L, H * d)[r], x0[r] + o.reshape(L, H * d)) <= _tol(wl)
