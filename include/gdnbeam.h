@@ -114,7 +114,7 @@ typedef struct gdnbeam_dumps {
 
 /* Memory accounting of a configuration (host only, no CUDA call). */
 typedef struct gdnbeam_footprint {
-  size_t sctx_bytes;          /* shared context states: R*layers*H*d_v*d_k (storage) */
+  size_t sctx_bytes;          /* shared context states: R*layers*H*d_v*d_k fp32 */
   size_t record_elements;     /* elements of one transition record: 1 + d_v + d_k (OneLA §2.2 eq. 5) */
   size_t records_bytes;       /* all record slots: R*layers*H*(T-1)*W_max*(d_v + d_k) storage + alpha fp32 */
   size_t ancestry_bytes;      /* ancestry index and token paths (int32) */
@@ -184,8 +184,10 @@ int gdnbeam_select(gdnbeam_ctx* ctx, int t, int W_t, int W_next, const void* log
 int gdnbeam_get_paths(gdnbeam_ctx* ctx, int W_final, const int32_t* parents,
                       const int32_t* tokens, int32_t* sid, gdnbeam_stream_t stream);
 
-/* Copies S_ctx, storage type [R][layers][H][d_v][d_k], into out. */
-int gdnbeam_read_sctx(gdnbeam_ctx* ctx, void* out, gdnbeam_stream_t stream);
+/* Copies S_ctx, fp32 [R][layers][H][d_v][d_k], into out. S_ctx is kept in
+ * fp32 for every storage type: one copy per (request, layer, head) is shared
+ * by all beams, so its width is amortised over the beam width. */
+int gdnbeam_read_sctx(gdnbeam_ctx* ctx, float* out, gdnbeam_stream_t stream);
 
 /* Marks every request's state as released: records stay where they are
  * (nothing moves, OneLA §2.1/§2.4); a new prefill is required before the next
@@ -206,6 +208,32 @@ int gdnbeam_device_status(int clear);
 const char* gdnbeam_variant(const gdnbeam_ctx* ctx);
 
 const char* gdnbeam_strerror(int status);
+
+/* Stages a context times when timing is on (gdnbeam_stage_times). */
+enum {
+  GDNBEAM_STAGE_ANCESTRY = 0, /* eq. 9 update and token paths */
+  GDNBEAM_STAGE_EMBED = 1,    /* embedding gather, RMSNorm glue */
+  GDNBEAM_STAGE_PROJECT = 2,  /* q, k, v, alpha, beta projections */
+  GDNBEAM_STAGE_REPLAY = 3,   /* fused shared-context replay */
+  GDNBEAM_STAGE_LOGITS = 4,   /* codebook logits and log-normaliser */
+  GDNBEAM_STAGE_SELECT = 5,   /* two-stage top-W selection */
+  GDNBEAM_STAGE_PREFILL = 6,  /* prefill recurrence */
+  GDNBEAM_NSTAGES = 7
+};
+
+/* Turns per-stage timing on or off (host). While on, every stage the
+ * context launches is bracketed by two CUDA events on its stream; nothing
+ * else changes. Turning it on clears earlier records. */
+int gdnbeam_timing(gdnbeam_ctx* ctx, int enable);
+
+/* Synchronises the recorded events and writes, per stage, the summed
+ * milliseconds (ms[GDNBEAM_NSTAGES]) and the number of timed launches
+ * (count[GDNBEAM_NSTAGES], may be NULL); then clears the records. */
+int gdnbeam_stage_times(gdnbeam_ctx* ctx, float* ms, int* count);
+
+/* Kernel launches this library has issued in this process (all contexts and
+ * tensor-level calls); clear != 0 resets the counter after reading. */
+long long gdnbeam_launches(int clear);
 
 /* ---------------------------------------------------------------------------
  * Tensor-level calls: each stage on explicit buffers (same kernels the
@@ -239,13 +267,13 @@ typedef struct gdnbeam_records {
  *   u_q = S_ctx q_b, u_k = S_ctx k_b, folded over j < t with the record at
  *   slot anc[r*W_t+b][j] of depth j; delta = beta (v - alpha u_k);
  *   o = alpha u_q + delta (k_b . q_b).
- *   sctx [R][H][d_v][d_k] storage (stride between requests: sctx_rstride elements)
+ *   sctx [R][H][d_v][d_k] fp32 (stride between requests: sctx_rstride elements)
  *   q, k [R*W_t][H*d_k], v [R*W_t][H*d_v] storage; alpha, beta [R*W_t][H]
  *   depth: host array of t record descriptors; anc [R*W_t][anc_stride] int32
  *   delta_out, o_out [R*W_t][H*d_v] storage; x_inout optional fp32
  *   [R*W_t][H*d_v] residual stream to which o is added (NULL: none).
  *   dumps: optional fp32 delta / o (layer 0 slots). */
-int gdnbeam_replay(const gdnbeam_config* cfg, int t, int W_t, const void* sctx,
+int gdnbeam_replay(const gdnbeam_config* cfg, int t, int W_t, const float* sctx,
                    long long sctx_rstride, const void* q, const void* k, const void* v,
                    const float* alpha, const float* beta, const gdnbeam_records* depth,
                    const int32_t* anc, int anc_stride, void* delta_out, void* o_out,
@@ -278,12 +306,12 @@ int gdnbeam_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int3
 /* Prefill recurrence over L tokens for every (request, head) from S = 0
  * (OneLA §1.2 eq. 3).
  *   q, k [R*L][H*d_k], v [R*L][H*d_v] storage; alpha, beta [R*L][H] fp32;
- *   sctx_out [R][H][d_v][d_k] storage (request stride sctx_rstride elements);
+ *   sctx_out [R][H][d_v][d_k] fp32 (request stride sctx_rstride elements);
  *   o_last [R][H*d_v] storage output at the last position (or NULL);
  *   x_inout optional fp32 [R*L][H*d_v]: o of every position is added to it. */
 int gdnbeam_prefill_scan(const gdnbeam_config* cfg, int L, const void* q, const void* k,
                          const void* v, const float* alpha, const float* beta,
-                         void* sctx_out, long long sctx_rstride, void* o_last,
+                         float* sctx_out, long long sctx_rstride, void* o_last,
                          float* x_inout, gdnbeam_stream_t stream);
 
 #ifdef __cplusplus

@@ -23,6 +23,7 @@ __all__ = [
 
 F32, BF16 = 0, 1
 MAX_T = 8
+STAGES = ("ancestry", "embed", "project", "replay", "logits", "select", "prefill")
 
 OK, EINVAL, EUNSUPPORTED, EWORKSPACE, ESTATE, ECUDA, EDEVICE, ENOMEM = 0, -1, -2, -3, -4, -5, -6, -7
 DERR = {"token": 1, "parent": 2, "slot": 4, "nonfinite": 8, "timeout": 16, "select": 32}
@@ -76,6 +77,9 @@ _SIGS = {
     "gdnbeam_device_status": (_I, [_I]),
     "gdnbeam_variant": (C.c_char_p, [_P]),
     "gdnbeam_strerror": (C.c_char_p, [_I]),
+    "gdnbeam_timing": (_I, [_P, _I]),
+    "gdnbeam_stage_times": (_I, [_P, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
+    "gdnbeam_launches": (C.c_longlong, [_I]),
     "gdnbeam_project_scratch_bytes": (_SZ, [C.POINTER(Config), _I]),
     "gdnbeam_project": (_I, [C.POINTER(Config), _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                              C.POINTER(Dumps), _S]),

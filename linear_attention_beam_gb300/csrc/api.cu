@@ -1,13 +1,20 @@
 // C ABI of the gdnbeam library: argument checks, workspace layout, call
 // sequencing, and the dispatch of each stage to its kernels.
+#include <atomic>
 #include <new>
 #include <stdio.h>
 #include <string.h>
+#include <vector>
 
 #include "common.cuh"
 #include "launchers.h"
 
 using namespace gdnbeam;
+
+namespace gdnbeam {
+static std::atomic<long long> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace gdnbeam
 
 namespace {
 
@@ -83,6 +90,34 @@ struct gdnbeam_ctx {
   int prefilled;
   int last_step;
   int W_hist[GDNBEAM_MAX_T];
+  // per-stage timing
+  bool timing = false;
+  std::vector<cudaEvent_t> ev_pool;
+  std::vector<int> ev_stage;   // stage of each recorded pair
+  size_t ev_used = 0;          // pairs recorded since the last read
+
+  ~gdnbeam_ctx() {
+    for (cudaEvent_t e : ev_pool) cudaEventDestroy(e);
+  }
+  // Brackets one stage with events when timing is on; returns the pair index.
+  int tic(int stage, cudaStream_t s) {
+    if (!timing) return -1;
+    if (2 * (ev_used + 1) > ev_pool.size()) {
+      for (int i = 0; i < 2; ++i) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return -1;
+        ev_pool.push_back(e);
+      }
+    }
+    int idx = (int)ev_used++;
+    if ((int)ev_stage.size() <= idx) ev_stage.resize(idx + 1);
+    ev_stage[idx] = stage;
+    cudaEventRecord(ev_pool[2 * idx], s);
+    return idx;
+  }
+  void toc(int idx, cudaStream_t s) {
+    if (idx >= 0) cudaEventRecord(ev_pool[2 * idx + 1], s);
+  }
 
   size_t rec_rows() const { return (size_t)c.R * c.W_max; }
   char* gk(int layer, int j) const {
@@ -111,7 +146,9 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
     off += align256(bytes);
     return p;
   };
-  size_t sctx_b = (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * es;
+  // S_ctx is kept in fp32 whatever the storage type: it is read once per
+  // (request, head) tile and shared by every beam, so its width costs little.
+  size_t sctx_b = (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * sizeof(float);
   size_t gk_b = (size_t)c.layers * depths * rows * c.H * c.d_k * es;
   size_t gd_b = (size_t)c.layers * depths * rows * c.H * c.d_v * es;
   size_t ga_b = (size_t)c.layers * depths * rows * c.H * sizeof(float);
@@ -290,22 +327,30 @@ int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* 
   const int Np = n_proj(c);
   const long long rstride = (long long)c.layers * c.H * c.d_v * c.d_k;
   ctx->prefilled = 0;
+  int ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
   int st = launch_gather_rows(c.dtype, n, c.d_model, prompt, c.V, ctx->w.E, ctx->pf_u,
                               c.residual ? ctx->pf_x : nullptr, err, s);
+  ctx->toc(ev, s);
   if (st) return st;
   for (int layer = 0; layer < c.layers; ++layer) {
     if (c.residual) {
+      ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
       st = launch_rmsnorm_rows(c.dtype, n, c.d_model, ctx->pf_x, c.d_model, ctx->pf_u, s);
+      ctx->toc(ev, s);
       if (st) return st;
     }
     const char* Wp = (const char*)ctx->w.W_proj + (size_t)layer * Np * c.d_model * es;
+    ev = ctx->tic(GDNBEAM_STAGE_PROJECT, s);
     st = project_any(c, ctx->tc_gemm, n, ctx->pf_u, Wp, ctx->pf_q, ctx->pf_k, ctx->pf_v,
                      ctx->pf_alpha, ctx->pf_beta, ctx->gemm, ctx->gemm_bytes, nullptr, s);
+    ctx->toc(ev, s);
     if (st) return st;
-    char* sc = (char*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k * es;
+    float* sc = (float*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k;
+    ev = ctx->tic(GDNBEAM_STAGE_PREFILL, s);
     st = launch_prefill_scan(c, L, ctx->pf_q, ctx->pf_k, ctx->pf_v, ctx->pf_alpha, ctx->pf_beta,
                              sc, rstride, c.residual ? nullptr : ctx->pf_feat,
                              c.residual ? ctx->pf_x : nullptr, s);
+    ctx->toc(ev, s);
     if (st) return st;
   }
   if (c.residual) {
@@ -313,8 +358,10 @@ int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* 
                              (long long)L * c.d_model, ctx->pf_feat, s);
     if (st) return st;
   }
+  ev = ctx->tic(GDNBEAM_STAGE_LOGITS, s);
   st = logits_any(c, ctx->tc_gemm, c.R, ctx->pf_feat, ctx->w.W_o, root_logits, root_lse,
                   ctx->gemm, ctx->gemm_bytes, nullptr, s);
+  ctx->toc(ev, s);
   if (st) return st;
   ctx->prefilled = 1;
   ctx->last_step = -1;
@@ -337,25 +384,33 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
   const int W_prev = t > 0 ? ctx->W_hist[t - 1] : 1;
   const int cur = t & 1;
   ctx->last_step = -2;  // invalid until this call succeeds
+  int ev = ctx->tic(GDNBEAM_STAGE_ANCESTRY, s);
   int st = launch_ancestry(c.R, t, c.T, c.V, W_prev, W_t, parents, tokens, ctx->anc[cur ^ 1],
                            ctx->sid[cur ^ 1], ctx->anc[cur], ctx->sid[cur], err, s);
+  ctx->toc(ev, s);
   if (st) return st;
+  ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
   st = launch_gather_rows(c.dtype, n, c.d_model, tokens, c.V, ctx->w.E, ctx->u,
                           c.residual ? ctx->x : nullptr, err, s);
+  ctx->toc(ev, s);
   if (st) return st;
   for (int layer = 0; layer < c.layers; ++layer) {
     if (c.residual) {
+      ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
       st = launch_rmsnorm_rows(c.dtype, n, c.d_model, ctx->x, c.d_model, ctx->u, s);
+      ctx->toc(ev, s);
       if (st) return st;
     }
     gdnbeam_dumps ld = layer_dumps(dumps, c, layer, n);
     const char* Wp = (const char*)ctx->w.W_proj + (size_t)layer * Np * c.d_model * es;
+    ev = ctx->tic(GDNBEAM_STAGE_PROJECT, s);
     st = project_any(c, ctx->tc_gemm, n, ctx->u, Wp, ctx->q, ctx->gk(layer, t), ctx->v,
                      ctx->ga(layer, t), ctx->beta, ctx->gemm, ctx->gemm_bytes, &ld, s);
+    ctx->toc(ev, s);
     if (st) return st;
     ReplayArgs a{};
     a.R = c.R; a.H = c.H; a.d_k = c.d_k; a.d_v = c.d_v; a.t = t; a.W_t = W_t;
-    a.sctx = (const char*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k * es;
+    a.sctx = (const float*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k;
     a.sctx_rstride = (long long)c.layers * c.H * c.d_v * c.d_k;
     a.q = ctx->q; a.k = ctx->gk(layer, t); a.v = ctx->v;
     a.alpha = ctx->ga(layer, t); a.beta = ctx->beta;
@@ -370,19 +425,25 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
     a.x_inout = c.residual ? ctx->x : nullptr;
     a.delta_dump = ld.delta; a.o_dump = ld.o;
     a.err = err;
+    ev = ctx->tic(GDNBEAM_STAGE_REPLAY, s);
     st = ctx->tc_replay ? launch_tc_replay(a, s) : launch_replay(c.dtype, a, s);
+    ctx->toc(ev, s);
     if (st) return st;
   }
   const void* feat = ctx->o;
   if (c.residual) {
+    ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
     st = launch_rmsnorm_rows(c.dtype, n, c.d_model, ctx->x, c.d_model, ctx->u, s);
+    ctx->toc(ev, s);
     if (st) return st;
     feat = ctx->u;
   }
   gdnbeam_dumps zd{};
   if (dumps) zd.logits = dumps->logits;
+  ev = ctx->tic(GDNBEAM_STAGE_LOGITS, s);
   st = logits_any(c, ctx->tc_gemm, n, feat, ctx->w.W_o, logits, lse, ctx->gemm, ctx->gemm_bytes,
                   &zd, s);
+  ctx->toc(ev, s);
   if (st) return st;
   ctx->W_hist[t] = W_t;
   ctx->last_step = t;
@@ -397,8 +458,11 @@ int gdnbeam_select(gdnbeam_ctx* ctx, int t, int W_t, int W_next, const void* log
   if (t < -1 || t > c.T - 2) return GDNBEAM_EINVAL;
   if (t == -1 && W_t != 1) return GDNBEAM_EINVAL;
   if (W_t < 1 || W_t > c.W_max || W_next < 1 || W_next > c.W_max) return GDNBEAM_EINVAL;
-  return gdnbeam_select_topw(c.R, W_t, W_next, c.V, c.dtype, logits, lse, cum, bias, parents,
-                             tokens, cum_next, ctx->sel, ctx->sel_bytes, stream);
+  int ev = ctx->tic(GDNBEAM_STAGE_SELECT, (cudaStream_t)stream);
+  int st = gdnbeam_select_topw(c.R, W_t, W_next, c.V, c.dtype, logits, lse, cum, bias, parents,
+                               tokens, cum_next, ctx->sel, ctx->sel_bytes, stream);
+  ctx->toc(ev, (cudaStream_t)stream);
+  return st;
 }
 
 int gdnbeam_get_paths(gdnbeam_ctx* ctx, int W_final, const int32_t* parents,
@@ -418,11 +482,39 @@ int gdnbeam_get_paths(gdnbeam_ctx* ctx, int W_final, const int32_t* parents,
                          (cudaStream_t)stream);
 }
 
-int gdnbeam_read_sctx(gdnbeam_ctx* ctx, void* out, gdnbeam_stream_t stream) {
+int gdnbeam_timing(gdnbeam_ctx* ctx, int enable) {
+  if (!ctx) return GDNBEAM_EINVAL;
+  ctx->timing = enable != 0;
+  ctx->ev_used = 0;
+  return GDNBEAM_OK;
+}
+
+int gdnbeam_stage_times(gdnbeam_ctx* ctx, float* ms, int* count) {
+  if (!ctx || !ms) return GDNBEAM_EINVAL;
+  for (int i = 0; i < GDNBEAM_NSTAGES; ++i) {
+    ms[i] = 0.0f;
+    if (count) count[i] = 0;
+  }
+  for (size_t i = 0; i < ctx->ev_used; ++i) {
+    GDN_CUDA(cudaEventSynchronize(ctx->ev_pool[2 * i + 1]));
+    float t = 0.0f;
+    GDN_CUDA(cudaEventElapsedTime(&t, ctx->ev_pool[2 * i], ctx->ev_pool[2 * i + 1]));
+    ms[ctx->ev_stage[i]] += t;
+    if (count) count[ctx->ev_stage[i]] += 1;
+  }
+  ctx->ev_used = 0;
+  return GDNBEAM_OK;
+}
+
+long long gdnbeam_launches(int clear) {
+  return clear ? g_launches.exchange(0) : g_launches.load();
+}
+
+int gdnbeam_read_sctx(gdnbeam_ctx* ctx, float* out, gdnbeam_stream_t stream) {
   if (!ctx || !out) return GDNBEAM_EINVAL;
   if (!ctx->prefilled) return GDNBEAM_ESTATE;
   const gdnbeam_config& c = ctx->c;
-  size_t bytes = (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * elem_size(c.dtype);
+  size_t bytes = (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * sizeof(float);
   GDN_CUDA(cudaMemcpyAsync(out, ctx->sctx, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
   return GDNBEAM_OK;
 }
@@ -470,7 +562,7 @@ int gdnbeam_project(const gdnbeam_config* cfg, int n, const void* u, const void*
                      scratch_bytes, dumps, (cudaStream_t)stream);
 }
 
-int gdnbeam_replay(const gdnbeam_config* cfg, int t, int W_t, const void* sctx,
+int gdnbeam_replay(const gdnbeam_config* cfg, int t, int W_t, const float* sctx,
                    long long sctx_rstride, const void* q, const void* k, const void* v,
                    const float* alpha, const float* beta, const gdnbeam_records* depth,
                    const int32_t* anc, int anc_stride, void* delta_out, void* o_out,
@@ -549,7 +641,7 @@ int gdnbeam_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int3
 }
 
 int gdnbeam_prefill_scan(const gdnbeam_config* cfg, int L, const void* q, const void* k,
-                         const void* v, const float* alpha, const float* beta, void* sctx_out,
+                         const void* v, const float* alpha, const float* beta, float* sctx_out,
                          long long sctx_rstride, void* o_last, float* x_inout,
                          gdnbeam_stream_t stream) {
   int st = validate(cfg);

@@ -55,9 +55,15 @@ __device__ __forceinline__ float from_orderable(uint32_t o) {
 
 }  // namespace gdnbeam
 
-// Host-side launch checking.
+namespace gdnbeam {
+// Counts kernel launches issued by the library (defined in api.cu).
+void note_launch();
+}  // namespace gdnbeam
+
+// Host-side launch checking; every kernel launch is followed by this.
 #define GDN_LAUNCH_CHECK()                                 \
   do {                                                     \
+    gdnbeam::note_launch();                                \
     cudaError_t e_ = cudaGetLastError();                   \
     if (e_ != cudaSuccess) return GDNBEAM_ECUDA;           \
   } while (0)

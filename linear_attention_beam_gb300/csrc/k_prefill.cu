@@ -16,7 +16,7 @@ template <typename T, int DK>
 __global__ void __launch_bounds__(128) prefill_scan_kernel(
     int L, int H, int dv, const T* __restrict__ q, const T* __restrict__ k,
     const T* __restrict__ v, const float* __restrict__ alpha, const float* __restrict__ beta,
-    T* __restrict__ sctx, long long rstride, T* __restrict__ o_last, float* __restrict__ x) {
+    float* __restrict__ sctx, long long rstride, T* __restrict__ o_last, float* __restrict__ x) {
   const int r = blockIdx.x / H, h = blockIdx.x % H;
   const int i = threadIdx.x;
   __shared__ float kb[2][DK], qb[2][DK], gb[2][2];
@@ -69,21 +69,21 @@ __global__ void __launch_bounds__(128) prefill_scan_kernel(
     __syncthreads();
   }
   if (i < dv) {
-    T* out = sctx + (size_t)r * rstride + ((size_t)h * dv + i) * DK;
+    float* out = sctx + (size_t)r * rstride + ((size_t)h * dv + i) * DK;
 #pragma unroll
-    for (int c = 0; c < DK; ++c) stf(out + c, S[c]);
+    for (int c = 0; c < DK; ++c) out[c] = S[c];
   }
 }
 
 template <typename T>
 int dispatch_dk(const gdnbeam_config& c, int L, const void* q, const void* k, const void* v,
-                const float* alpha, const float* beta, void* sctx, long long rs, void* o_last,
+                const float* alpha, const float* beta, float* sctx, long long rs, void* o_last,
                 float* x, cudaStream_t s) {
   dim3 grid(c.R * c.H);
   const int threads = 128;
 #define GDN_SCAN(DK)                                                                         \
   prefill_scan_kernel<T, DK><<<grid, threads, 0, s>>>(L, c.H, c.d_v, (const T*)q,           \
-      (const T*)k, (const T*)v, alpha, beta, (T*)sctx, rs, (T*)o_last, x)
+      (const T*)k, (const T*)v, alpha, beta, sctx, rs, (T*)o_last, x)
   switch (c.d_k) {
     case 16: GDN_SCAN(16); break;
     case 32: GDN_SCAN(32); break;
@@ -99,7 +99,7 @@ int dispatch_dk(const gdnbeam_config& c, int L, const void* q, const void* k, co
 }  // namespace
 
 int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const void* k,
-                        const void* v, const float* alpha, const float* beta, void* sctx,
+                        const void* v, const float* alpha, const float* beta, float* sctx,
                         long long rs, void* o_last, float* x, cudaStream_t s) {
   if (L <= 0) return GDNBEAM_EINVAL;
   if (c.d_v > 128) return GDNBEAM_EUNSUPPORTED;

@@ -91,12 +91,12 @@ __global__ void __launch_bounds__(kThreads) replay_simt_kernel(ReplayArgs a) {
   float uq[kBeams], uk[kBeams];
 #pragma unroll
   for (int b = 0; b < kBeams; ++b) { uq[b] = 0.0f; uk[b] = 0.0f; }
-  const T* S = (const T*)a.sctx + (size_t)r * a.sctx_rstride + (size_t)h * dv * dk;
+  const float* S = a.sctx + (size_t)r * a.sctx_rstride + (size_t)h * dv * dk;
   for (int c0 = 0; c0 < dk; c0 += kChunk) {
     __syncthreads();
     for (int i = tid; i < dv * kChunk; i += kThreads) {
       int row = i / kChunk, c = i % kChunk;
-      sc[row * (kChunk + 1) + c] = (c0 + c < dk) ? ldf(S + (size_t)row * dk + c0 + c) : 0.0f;
+      sc[row * (kChunk + 1) + c] = (c0 + c < dk) ? S[(size_t)row * dk + c0 + c] : 0.0f;
     }
     __syncthreads();
     if (tid < dv) {

@@ -48,7 +48,7 @@ int launch_tc_logits(const gdnbeam_config& c, int n, const void* feat, const voi
 
 struct ReplayArgs {
   int R, H, d_k, d_v, t, W_t;
-  const void* sctx;
+  const float* sctx;  // fp32 [R][H][d_v][d_k], request stride sctx_rstride
   long long sctx_rstride;
   const void *q, *k, *v;
   const float *alpha, *beta;
@@ -65,7 +65,7 @@ bool tc_replay_supported(int dtype, int d_k, int d_v);
 int launch_tc_replay(const ReplayArgs& a, cudaStream_t s);
 
 int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const void* k,
-                        const void* v, const float* alpha, const float* beta, void* sctx,
+                        const void* v, const float* alpha, const float* beta, float* sctx,
                         long long sctx_rstride, void* o_last, float* x_inout, cudaStream_t s);
 
 size_t select_scratch_bytes(int R, int W_t, int W_next, int V);

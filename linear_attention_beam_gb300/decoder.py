@@ -140,7 +140,7 @@ class BeamDecoder:
 
     def read_sctx(self) -> torch.Tensor:
         c = self.cfg
-        out = torch.empty(c.R, c.layers, c.H, c.d_v, c.d_k, dtype=self.tdtype, device=self.device)
+        out = torch.empty(c.R, c.layers, c.H, c.d_v, c.d_k, dtype=torch.float32, device=self.device)
         check(self.lib.gdnbeam_read_sctx(self.ctx, ptr(out), None), "read_sctx")
         return out
 

@@ -295,15 +295,17 @@ def prefill(wl, params, prompt: np.ndarray):
 
 
 def decode_request(wl, params, prompt: np.ndarray, bias: Optional[np.ndarray] = None,
-                   forced=None) -> RequestTrace:
+                   forced=None, context=None) -> RequestTrace:
     """Large-beam FullState decode of one request.
 
     bias: [T-1, W_max] per-parent bias for this request, or None.
     forced: optional (parents, tokens) lists indexed by selection; when given,
     the beam tree follows them instead of the oracle's own selections (both
     sides then run on the same lineage). Scores kept are still the oracle's.
+    context: optional (S_ctx, root feature) from an earlier prefill() of the
+    same prompt, to skip recomputing it.
     """
-    S_ctx, root_feat = prefill(wl, params, prompt)
+    S_ctx, root_feat = context if context is not None else prefill(wl, params, prompt)
     root_z = codebook_logits(params, root_feat[None, :])[0]
     root_lse = float(log_normalizer(root_z[None, :])[0])
 

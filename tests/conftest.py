@@ -11,3 +11,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long CPU-side oracle work")
+
+
+@pytest.fixture(autouse=True)
+def _release_device_temporaries():
+    yield
+    mod = sys.modules.get("gpu_util")
+    if mod is not None:
+        mod.release()

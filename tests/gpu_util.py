@@ -23,8 +23,22 @@ def maxrel(g, o) -> float:
     return float(np.abs(g - o).max() / den) if den > 0 else float(np.abs(g - o).max())
 
 
+# Device tensors made by to_dev stay referenced until the test ends, so a
+# pointer handed to the library is never freed (and reused) before the
+# asynchronous kernel that reads it has run.
+_LIVE = []
+
+
 def to_dev(a, dtype=torch.float32):
-    return torch.as_tensor(np.ascontiguousarray(a)).to(DEV, dtype=dtype)
+    t = torch.as_tensor(np.ascontiguousarray(a)).to(DEV, dtype=dtype)
+    _LIVE.append(t)
+    return t
+
+
+def release():
+    if _LIVE:
+        torch.cuda.synchronize()
+        _LIVE.clear()
 
 
 def dt(wl):

@@ -143,7 +143,7 @@ def test_replay_op(dtype, d, H, R, W_t, t, resid):
     wl = synth.tiny_workload(d=d, V=7, H=H, R=R, dtype=dtype)
     rng = np.random.default_rng(d + H + W_t + t)
     st_ = lambda a: store(a, wl)
-    S_ctx = st_(rng.standard_normal((R, H, d, d)) * 0.05)
+    S_ctx = (rng.standard_normal((R, H, d, d)) * 0.05).astype(np.float32).astype(np.float64)
     Wj = [int(rng.integers(1, 40)) for _ in range(t)]
     rec_k = [st_(_unit_rows(rng, (R, Wj[j], H, d))) for j in range(t)]
     rec_d = [st_(rng.standard_normal((R, Wj[j], H, d)) * 0.5) for j in range(t)]
@@ -172,7 +172,7 @@ def test_replay_op(dtype, d, H, R, W_t, t, resid):
     dm = gb.dumps(delta=d_dump, o=o_dump)
     cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d, T=max(t + 1, 2))
     lib = gb.load()
-    st = lib.gdnbeam_replay(C.byref(cfg), t, W_t, gb.ptr(to_dev(S_ctx.reshape(-1), td)), H * d * d,
+    st = lib.gdnbeam_replay(C.byref(cfg), t, W_t, gb.ptr(to_dev(S_ctx.reshape(-1))), H * d * d,
                             gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
                             gb.ptr(to_dev(v.reshape(-1), td)), gb.ptr(to_dev(al.reshape(-1))),
                             gb.ptr(to_dev(be.reshape(-1))), recs,
@@ -249,7 +249,8 @@ def test_project_op(dtype, d, H, d_model, n):
 
 @pytest.mark.parametrize("dtype,F,V,n", [("f32", 16, 16, 8), ("bf16", 128, 300, 70), ("bf16", 256, 1000, 129)])
 def test_logits_op(dtype, F, V, n):
-    wl = synth.tiny_workload(d=F, V=V, H=1, d_model=F, dtype=dtype, seed=F + V)
+    d = min(F, 128)
+    wl = synth.tiny_workload(d=d, V=V, H=F // d, d_model=F, dtype=dtype, seed=F + V)
     p = synth.make_params(wl)
     rng = np.random.default_rng(V)
     feat = store(rng.standard_normal((n, F)), wl)
@@ -288,7 +289,7 @@ def test_prefill_scan_op(dtype, d, H, R, L, resid):
     td = tdt(wl)
     lib = gb.load()
     cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d)
-    sc = torch.empty(R, H, d, d, dtype=td, device=DEV)
+    sc = torch.empty(R, H, d, d, dtype=torch.float32, device=DEV)
     ol = torch.empty(R, H * d, dtype=td, device=DEV)
     xd = to_dev(x0.reshape(R * L, H * d)) if resid else None
     st = lib.gdnbeam_prefill_scan(C.byref(cfg), L, gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
@@ -297,7 +298,7 @@ def test_prefill_scan_op(dtype, d, H, R, L, resid):
     assert st == 0
     for r in range(R):
         S, o = oracle.prefill_scan(q[r], k[r], v[r], a[r], b[r])
-        _check_stored(host(sc[r]), S, wl, "S_ctx")
+        assert maxrel(host(sc[r]), S) <= _tol(wl), "S_ctx"
         _check_stored(host(ol[r]).reshape(H, d), o[-1], wl, "o_last")
         if resid:
             assert maxrel(host(xd).reshape(R, L, H * d)[r], x0[r] + o.reshape(L, H * d)) <= _tol(wl)
