@@ -1,19 +1,447 @@
-// tcgen05 tensor-core GEMMs (placeholder until the kernels land).
+// tcgen05 tensor-core GEMMs for the two dense contractions of a decode call:
+//   * projections  P = U . W_proj^T  (q, k, v, decay and write gates), with
+//     the per-head L2 normalisation of q and k and the gate functions fused
+//     into the epilogue (OneLA §1.2 eq. 3 inputs);
+//   * codebook logits Z = F . W_o^T, with the bf16 store of z and per-tile
+//     (max, sum exp) partials of the row log-normaliser fused in.
+//
+// One persistent CTA per SM, 192 threads in three roles:
+//   warp 0      one thread issues TMA tile loads (A 128x64, B 256x64 bf16,
+//               128-byte swizzle) into a 4-stage shared-memory ring;
+//   warp 1      owns the TMEM allocation (2 x 256 fp32 columns) and one thread
+//               issues tcgen05.mma (M=128, N=256, K=16) into the accumulator
+//               of the current tile, committing each stage back to the
+//               producer and each finished tile to the epilogue;
+//   warps 2-5   read the accumulator rows out of TMEM (lane = tile row) and
+//               run the fused epilogue while the next tile accumulates into
+//               the other TMEM buffer.
+// Every mbarrier wait is bounded in time; on a time-out the kernel raises
+// GDNBEAM_DERR_TIMEOUT, all roles leave their loops, in-flight copies and
+// MMAs are drained (again with a bound) and TMEM is freed.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "launchers.h"
+#include "tc_ptx.cuh"
 
 namespace gdnbeam {
 
-bool tc_gemm_supported(const gdnbeam_config&) { return false; }
-int launch_tc_project(const gdnbeam_config&, int, const void*, const void*, void*, void*, void*,
-                      float*, float*, const gdnbeam_dumps*, cudaStream_t) {
-  return GDNBEAM_EUNSUPPORTED;
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kNumBars = 2 * STAGES + 4 + 1;
+constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + 1024 + kNumBars * 8 + 16;
+
+enum { EPI_LOGITS = 0, EPI_PROJ = 1 };
+
+struct EpiArgs {
+  int M, N, K;
+  unsigned* err;
+  // logits
+  __nv_bfloat16* z;
+  float* z_dump;
+  float2* part;  // [M][n_tiles] (max, sum exp(z - max))
+  // projections
+  int H;
+  __nv_bfloat16 *q, *k, *v;
+  float *alpha, *beta;
+  float *dq, *dk, *dv, *da, *db;
+};
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[w * 8 + 2 * j], v[w * 8 + 2 * j + 1]);
+      p[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    d4[w] = make_uint4(p[0], p[1], p[2], p[3]);
+  }
 }
-size_t tc_logits_scratch_bytes(const gdnbeam_config&, int) { return 0; }
-int launch_tc_logits(const gdnbeam_config&, int, const void*, const void*, void*, float*, void*,
-                     const gdnbeam_dumps*, cudaStream_t) {
-  return GDNBEAM_EUNSUPPORTED;
+
+__device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32]) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) d4[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
 }
+
+// Logits epilogue for one tile row: bf16 z, optional fp32 dump, and the
+// row's (max, sum exp) over this tile's columns.
+__device__ __forceinline__ void epi_logits(const EpiArgs& ea, uint32_t taddr, int m, int n0,
+                                           int n_tile, int n_tiles) {
+  float run_max = -INFINITY, run_sum = 0.0f;
+  const bool row_ok = m < ea.M;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tc::tmem_ld32(taddr + c * 32, v);
+    const int n = n0 + c * 32;
+    if (!row_ok || n >= ea.N) continue;
+    const size_t off = (size_t)m * ea.N + n;
+    if (n + 32 <= ea.N) {
+      store_bf16x32(ea.z + off, v);
+      if (ea.z_dump) store_f32x32(ea.z_dump + off, v);
+    } else {
+      for (int j = 0; j < 32 && n + j < ea.N; ++j) {
+        ea.z[off + j] = __float2bfloat16_rn(v[j]);
+        if (ea.z_dump) ea.z_dump[off + j] = v[j];
+      }
+    }
+    const int cnt = min(32, ea.N - n);
+    float cm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < cnt) cm = fmaxf(cm, v[j]);
+    const float nm = fmaxf(run_max, cm);
+    float s = run_sum * expf(run_max - nm);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < cnt) s += expf(v[j] - nm);
+    run_sum = s;
+    run_max = nm;
+  }
+  if (row_ok) ea.part[(size_t)m * n_tiles + n_tile] = make_float2(run_max, run_sum);
+}
+
+// Projection epilogue for one tile row; head width 128, tile of two heads.
+__device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int m, int n0) {
+  const int H = ea.H, D = 128;
+  const bool row_ok = m < ea.M;
+  const int q_end = H * D, k_end = 2 * H * D, v_end = 3 * H * D;
+#pragma unroll 1
+  for (int g = 0; g < BN / D; ++g) {
+    const int col0 = n0 + g * D;
+    if (col0 >= ea.N) break;
+    const uint32_t ta = taddr + g * D;
+    if (col0 < k_end) {
+      const bool is_q = col0 < q_end;
+      const int head = (is_q ? col0 : col0 - q_end) / D;
+      float ss = 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::tmem_ld32(ta + c * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+      }
+      const float inv = 1.0f / sqrtf(ss + 1e-6f);
+      __nv_bfloat16* dst = is_q ? ea.q : ea.k;
+      float* dmp = is_q ? ea.dq : ea.dk;
+      const size_t off = (size_t)m * H * D + (size_t)head * D;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::tmem_ld32(ta + c * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= inv;
+        if (row_ok) {
+          store_bf16x32(dst + off + c * 32, v);
+          if (dmp) store_f32x32(dmp + off + c * 32, v);
+        }
+      }
+    } else if (col0 < v_end) {
+      const int head = (col0 - k_end) / D;
+      const size_t off = (size_t)m * H * D + (size_t)head * D;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::tmem_ld32(ta + c * 32, v);
+        if (row_ok) {
+          store_bf16x32(ea.v + off + c * 32, v);
+          if (ea.dv) store_f32x32(ea.dv + off + c * 32, v);
+        }
+      }
+    } else {
+      // gate columns: H decay-gate logits, then H write-gate logits
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tc::tmem_ld32(ta + c * 32, v);
+        if (!row_ok) continue;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int idx = c * 32 + j;
+          if (idx < H) {
+            const float a = decay_gate(v[j]);
+            ea.alpha[(size_t)m * H + idx] = a;
+            if (ea.da) ea.da[(size_t)m * H + idx] = a;
+          } else if (idx < 2 * H) {
+            const float b = write_gate(v[j]);
+            ea.beta[(size_t)m * H + idx - H] = b;
+            if (ea.db) ea.db[(size_t)m * H + idx - H] = b;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   EpiArgs ea) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + kNumBars * 8);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto sA = [&](int s) { return base + (uint32_t)s * STAGE_BYTES; };
+  auto sB = [&](int s) { return base + (uint32_t)s * STAGE_BYTES + A_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = (ea.M + BM - 1) / BM, n_tiles = (ea.N + BN - 1) / BN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int k_blocks = (ea.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(full(s), 1);
+      tc::mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(tfull(a), 1);
+      tc::mbar_init(tempty(a), 4);
+    }
+    tc::mbar_init(drain_bar, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch(&tmA);
+    tc::tma_prefetch(&tmB);
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued_phase[STAGES];
+      bool issued[STAGES];
+      for (int i = 0; i < STAGES; ++i) issued[i] = false;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!tc::mbar_wait(empty(s), ph ^ 1u, abort, ea.err)) { ok = false; break; }
+          tc::mbar_arrive_expect_tx(full(s), STAGE_BYTES);
+          tc::tma_load_2d(sA(s), &tmA, kb * BK, m0, full(s));
+          tc::tma_load_2d(sB(s), &tmB, kb * BK, n0, full(s));
+          issued[s] = true;
+          issued_phase[s] = ph;
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      // every copy this thread started has landed before the CTA can exit
+      for (int i = 0; i < STAGES; ++i)
+        if (issued[i]) tc::mbar_wait_drain(full(i), issued_phase[i]);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      int i = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++i) {
+        const int acc = i & 1;
+        const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+        if (!tc::mbar_wait(tempty(acc), aph ^ 1u, abort, ea.err)) break;
+        tc::fence_after_sync();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!tc::mbar_wait(full(s), ph, abort, ea.err)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint64_t ad = tc::sw128_desc(sA(s)), bd = tc::sw128_desc(sB(s));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0);
+          tc::mma_commit(empty(s));
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (ok) tc::mma_commit(tfull(acc));
+      }
+      // every MMA this thread issued has finished before TMEM is released
+      tc::mma_commit(drain_bar);
+      tc::mbar_wait_drain(drain_bar, 0);
+    }
+  } else {
+    const int lane_grp = warp & 3;  // TMEM lanes 32*lane_grp .. +31
+    const int row = lane_grp * 32 + lane;
+    int i = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++i) {
+      const int acc = i & 1;
+      const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+      const bool got = tc::mbar_wait(tfull(acc), aph, abort, ea.err);
+      __syncwarp();  // the TMEM loads below are warp-collective
+      if (!got) break;
+      tc::fence_after_sync();
+      const int m_tile = tile / n_tiles, n_tile = tile % n_tiles;
+      const uint32_t taddr = tmem_base + ((uint32_t)(lane_grp * 32) << 16) + (uint32_t)(acc * BN);
+      if (EPI == EPI_LOGITS)
+        epi_logits(ea, taddr, m_tile * BM + row, n_tile * BN, n_tile, n_tiles);
+      else
+        epi_proj(ea, taddr, m_tile * BM + row, n_tile * BN);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tempty(acc));
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// lse = M + log sum_i s_i exp(m_i - M) over a row's tile partials.
+__global__ void lse_reduce_kernel(int n, int n_tiles, const float2* __restrict__ part,
+                                  float* __restrict__ lse) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= n) return;
+  const float2* p = part + (size_t)row * n_tiles;
+  float mx = -INFINITY;
+  for (int i = lane; i < n_tiles; i += 32) mx = fmaxf(mx, p[i].x);
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float s = 0.0f;
+  for (int i = lane; i < n_tiles; i += 32) s += p[i].y * expf(p[i].x - mx);
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) lse[row] = mx + logf(s);
+}
+
+// ---- host side ---------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows][cols] as a 2-D tensor map with a box of
+// 64 columns x box_rows rows and 128-byte swizzling.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  if (((uintptr_t)ptr & 15) != 0 || (cols * 2) % 16 != 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return sms[dev];
+}
+
+template <int EPI>
+int launch_gemm(const void* A, const void* B, const EpiArgs& ea, cudaStream_t s) {
+  if (ea.M <= 0) return GDNBEAM_OK;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, ea.M, ea.K, BM) || !make_map(&tb, B, ea.N, ea.K, BN)) return GDNBEAM_ECUDA;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[EPI]) {
+    GDN_CUDA(cudaFuncSetAttribute(tc_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kSmemBytes));
+    attr_set[EPI] = true;
+  }
+  const int tiles = ((ea.M + BM - 1) / BM) * ((ea.N + BN - 1) / BN);
+  int grid = num_sms();
+  if (grid <= 0) return GDNBEAM_ECUDA;
+  if (grid > tiles) grid = tiles;
+  tc_gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, ea);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
+}  // namespace
+
+bool tc_gemm_supported(const gdnbeam_config& c) {
+  const int F = c.residual ? c.d_model : c.H * c.d_v;
+  return c.dtype == GDNBEAM_BF16 && c.d_k == 128 && c.d_v == 128 && c.d_model % BK == 0 &&
+         F % BK == 0 && c.V % 8 == 0 && 2 * c.H <= 128;
+}
+
+int launch_tc_project(const gdnbeam_config& c, int n, const void* u, const void* W_proj, void* q,
+                      void* k, void* v, float* alpha, float* beta, const gdnbeam_dumps* d,
+                      cudaStream_t s) {
+  EpiArgs ea{};
+  ea.M = n;
+  ea.N = 2 * c.H * c.d_k + c.H * c.d_v + 2 * c.H;
+  ea.K = c.d_model;
+  ea.H = c.H;
+  ea.q = (__nv_bfloat16*)q;
+  ea.k = (__nv_bfloat16*)k;
+  ea.v = (__nv_bfloat16*)v;
+  ea.alpha = alpha;
+  ea.beta = beta;
+  if (d) {
+    ea.dq = d->q; ea.dk = d->k; ea.dv = d->v; ea.da = d->alpha; ea.db = d->beta;
+  }
+  return launch_gemm<EPI_PROJ>(u, W_proj, ea, s);
+}
+
+size_t tc_logits_scratch_bytes(const gdnbeam_config& c, int n) {
+  return (size_t)n * ((c.V + BN - 1) / BN) * sizeof(float2);
+}
+
+int launch_tc_logits(const gdnbeam_config& c, int n, const void* feat, const void* W_o, void* z,
+                     float* lse, void* scratch, const gdnbeam_dumps* d, cudaStream_t s) {
+  EpiArgs ea{};
+  ea.M = n;
+  ea.N = c.V;
+  ea.K = c.residual ? c.d_model : c.H * c.d_v;
+  ea.z = (__nv_bfloat16*)z;
+  ea.z_dump = d ? d->logits : nullptr;
+  ea.part = (float2*)scratch;
+  int st = launch_gemm<EPI_LOGITS>(feat, W_o, ea, s);
+  if (st) return st;
+  const int n_tiles = (c.V + BN - 1) / BN;
+  lse_reduce_kernel<<<(n + 7) / 8, 256, 0, s>>>(n, n_tiles, (const float2*)scratch, lse);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
 bool tc_replay_supported(int, int, int) { return false; }
 int launch_tc_replay(const ReplayArgs&, cudaStream_t) { return GDNBEAM_EUNSUPPORTED; }
 

@@ -146,3 +146,13 @@ def test_select_topw_argument_checks():
 def test_strerror():
     lib = gb.load()
     assert lib.gdnbeam_strerror(gb.ESTATE).decode() == "call out of sequence"
+
+
+def test_hot_path_uses_tensor_core_kernels():
+    lib, h, _ = make_ctx(synth.BATCHED)
+    v = lib.gdnbeam_variant(h).decode()
+    assert "proj=tc" in v and "logits=tc" in v, v
+    lib.gdnbeam_destroy(h)
+    lib, h, _ = make_ctx(synth.TINY)
+    assert "proj=simt" in lib.gdnbeam_variant(h).decode()
+    lib.gdnbeam_destroy(h)

@@ -302,3 +302,17 @@ def test_prefill_scan_op(dtype, d, H, R, L, resid):
         _check_stored(host(ol[r]).reshape(H, d), o[-1], wl, "o_last")
         if resid:
             assert maxrel(host(xd).reshape(R, L, H * d)[r], x0[r] + o.reshape(L, H * d)) <= _tol(wl)
+
+
+# ------------------------------------------------------------------ tensor-core GEMMs
+
+@pytest.mark.parametrize("H,d_model,n", [(16, 2048, 300), (8, 1024, 129), (2, 256, 1), (16, 2048, 1024)])
+def test_project_op_tensor_cores(H, d_model, n):
+    # bf16, head width 128: the tcgen05 projection GEMM (ragged row tails,
+    # the gate columns in a partly filled last tile)
+    test_project_op("bf16", 128, H, d_model, n)
+
+
+@pytest.mark.parametrize("F,V,n", [(2048, 8192, 300), (1024, 4096, 129), (256, 1000, 1), (2048, 8192, 512)])
+def test_logits_op_tensor_cores(F, V, n):
+    test_logits_op("bf16", F, V, n)
