@@ -81,8 +81,12 @@ struct gdnbeam_ctx {
   void* o;      // [R*W_max][H*d_v]
   void* sel;    // selection scratch
   size_t sel_bytes;
-  void* gemm;   // GEMM scratch (fp32 raw outputs or logits partials)
+  void* gemm;   // CUDA-core GEMM scratch (fp32 raw outputs)
   size_t gemm_bytes;
+  float2* tstats;  // [R*W_max][ceil(V/256)]: per (row, 256-code tile) max logit and
+                   // sum of exp(z - max), left by the logits stage
+  const void* last_logits;  // logits buffer the last logits stage wrote
+  int last_rows;
   // prefill buffers for R*L_max rows
   void *pf_u, *pf_q, *pf_k, *pf_v, *pf_feat;
   float *pf_x, *pf_alpha, *pf_beta;
@@ -172,7 +176,7 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
   char* p_sel = take(sel_b);
   size_t gemm_b;
   if (tc_gemm) {
-    gemm_b = tc_logits_scratch_bytes(c, (int)(rows > (size_t)c.R ? rows : c.R));
+    gemm_b = 0;  // the tensor-core GEMMs need no scratch; logits partials go to tstats
   } else {
     size_t a = rows * (size_t)n_proj(c) * 4, b = rows * (size_t)c.V * 4;
     size_t p = pf_rows * (size_t)n_proj(c) * 4, r = (size_t)c.R * c.V * 4;
@@ -181,6 +185,8 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
     if (r > gemm_b) gemm_b = r;
   }
   char* p_gemm = take(gemm_b);
+  const int n_hint_tiles = (c.V + kHintTile - 1) / kHintTile;
+  char* p_tst = take((rows > (size_t)c.R ? rows : (size_t)c.R) * n_hint_tiles * sizeof(float2));
   char* p_pfu = take(pf_rows * c.d_model * es);
   char* p_pfx = take(c.residual ? pf_rows * c.d_model * sizeof(float) : 0);
   char* p_pfq = take(pf_rows * c.H * c.d_k * es);
@@ -195,6 +201,7 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
     x->sid[0] = (int32_t*)p_sid0; x->sid[1] = (int32_t*)p_sid1;
     x->u = p_u; x->x = (float*)p_x; x->q = p_q; x->v = p_v; x->beta = (float*)p_beta;
     x->o = p_o; x->sel = p_sel; x->sel_bytes = sel_b; x->gemm = p_gemm; x->gemm_bytes = gemm_b;
+    x->tstats = (float2*)p_tst; x->last_logits = nullptr; x->last_rows = 0;
     x->pf_u = p_pfu; x->pf_x = (float*)p_pfx; x->pf_q = p_pfq; x->pf_k = p_pfk;
     x->pf_v = p_pfv; x->pf_alpha = (float*)p_pfa; x->pf_beta = (float*)p_pfb; x->pf_feat = p_pff;
   }
@@ -221,19 +228,24 @@ int project_any(const gdnbeam_config& c, bool tc, int n, const void* u, const vo
   return launch_proj_epilogue(c, n, (const float*)scratch, q, k, v, alpha, beta, d, s);
 }
 
+// Logits for n rows. tstats (may be NULL on the CUDA-core path) receives the
+// per (row, 256-code tile) maximum and sum of exp; the tensor-core path
+// needs it as its partial buffer.
 int logits_any(const gdnbeam_config& c, bool tc, int n, const void* feat, const void* Wo,
-               void* z, float* lse, void* scratch, size_t scratch_bytes, const gdnbeam_dumps* d,
-               cudaStream_t s) {
+               void* z, float* lse, void* scratch, size_t scratch_bytes, float2* tstats,
+               const gdnbeam_dumps* d, cudaStream_t s) {
   if (tc) {
-    if (scratch_bytes < tc_logits_scratch_bytes(c, n)) return GDNBEAM_EWORKSPACE;
-    return launch_tc_logits(c, n, feat, Wo, z, lse, scratch, d, s);
+    if (!tstats) return GDNBEAM_EWORKSPACE;
+    return launch_tc_logits(c, n, feat, Wo, z, lse, tstats, d, s);
   }
   const int F = feat_dim(c);
   if (!scratch || scratch_bytes < (size_t)n * c.V * 4) return GDNBEAM_EWORKSPACE;
   int st = launch_simt_gemm_nt(c.dtype, n, c.V, F, feat, F, Wo, F, (float*)scratch, c.V, s);
   if (st) return st;
-  return launch_logits_rows(c.dtype, n, c.V, (const float*)scratch, z, lse,
-                            d ? d->logits : nullptr, s);
+  st = launch_logits_rows(c.dtype, n, c.V, (const float*)scratch, z, lse,
+                          d ? d->logits : nullptr, s);
+  if (st || !tstats) return st;
+  return launch_tile_max(c.dtype, n, c.V, z, tstats, s);
 }
 
 gdnbeam_dumps layer_dumps(const gdnbeam_dumps* d, const gdnbeam_config& c, int layer, size_t n) {
@@ -360,7 +372,9 @@ int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* 
   }
   ev = ctx->tic(GDNBEAM_STAGE_LOGITS, s);
   st = logits_any(c, ctx->tc_gemm, c.R, ctx->pf_feat, ctx->w.W_o, root_logits, root_lse,
-                  ctx->gemm, ctx->gemm_bytes, nullptr, s);
+                  ctx->gemm, ctx->gemm_bytes, ctx->tstats, nullptr, s);
+  ctx->last_logits = root_logits;
+  ctx->last_rows = c.R;
   ctx->toc(ev, s);
   if (st) return st;
   ctx->prefilled = 1;
@@ -442,7 +456,9 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
   if (dumps) zd.logits = dumps->logits;
   ev = ctx->tic(GDNBEAM_STAGE_LOGITS, s);
   st = logits_any(c, ctx->tc_gemm, n, feat, ctx->w.W_o, logits, lse, ctx->gemm, ctx->gemm_bytes,
-                  &zd, s);
+                  ctx->tstats, &zd, s);
+  ctx->last_logits = logits;
+  ctx->last_rows = n;
   ctx->toc(ev, s);
   if (st) return st;
   ctx->W_hist[t] = W_t;
@@ -458,9 +474,15 @@ int gdnbeam_select(gdnbeam_ctx* ctx, int t, int W_t, int W_next, const void* log
   if (t < -1 || t > c.T - 2) return GDNBEAM_EINVAL;
   if (t == -1 && W_t != 1) return GDNBEAM_EINVAL;
   if (W_t < 1 || W_t > c.W_max || W_next < 1 || W_next > c.W_max) return GDNBEAM_EINVAL;
+  if (!logits || !lse || !parents || !tokens || !cum_next) return GDNBEAM_EINVAL;
+  if ((long long)W_next > (long long)W_t * c.V) return GDNBEAM_EINVAL;
+  // The tile maxima the logits stage left behind bound the selection when
+  // these are the logits it wrote; the result is exact either way.
+  const float2* hint =
+      (logits == ctx->last_logits && ctx->last_rows == c.R * W_t) ? ctx->tstats : nullptr;
   int ev = ctx->tic(GDNBEAM_STAGE_SELECT, (cudaStream_t)stream);
-  int st = gdnbeam_select_topw(c.R, W_t, W_next, c.V, c.dtype, logits, lse, cum, bias, parents,
-                               tokens, cum_next, ctx->sel, ctx->sel_bytes, stream);
+  int st = launch_select(c.R, W_t, W_next, c.V, c.dtype, logits, lse, cum, bias, hint, parents,
+                         tokens, cum_next, ctx->sel, err_ptr(), (cudaStream_t)stream);
   ctx->toc(ev, (cudaStream_t)stream);
   return st;
 }
@@ -604,8 +626,10 @@ int gdnbeam_logits(const gdnbeam_config* cfg, int n, const void* feat, const voi
   if (st) return st;
   if (n < 0 || !feat || !W_o || !z || !lse) return GDNBEAM_EINVAL;
   if (n == 0) return GDNBEAM_OK;
-  return logits_any(*cfg, tc_gemm_supported(*cfg), n, feat, W_o, z, lse, scratch, scratch_bytes,
-                    dumps, (cudaStream_t)stream);
+  const bool tc = tc_gemm_supported(*cfg);
+  if (tc && scratch_bytes < tc_logits_scratch_bytes(*cfg, n)) return GDNBEAM_EWORKSPACE;
+  return logits_any(*cfg, tc, n, feat, W_o, z, lse, scratch, scratch_bytes,
+                    tc ? (float2*)scratch : nullptr, dumps, (cudaStream_t)stream);
 }
 
 size_t gdnbeam_select_scratch_bytes(int R, int W_t, int W_next, int V) {
@@ -624,7 +648,7 @@ int gdnbeam_select_topw(int R, int W_t, int W_next, int V, int dtype, const void
   if ((long long)W_t * V >= (1ll << 31) || (long long)W_next > (long long)W_t * V)
     return GDNBEAM_EINVAL;
   if (scratch_bytes < select_scratch_bytes(R, W_t, W_next, V)) return GDNBEAM_EWORKSPACE;
-  return launch_select(R, W_t, W_next, V, dtype, logits, lse, cum, bias, parents, tokens,
+  return launch_select(R, W_t, W_next, V, dtype, logits, lse, cum, bias, nullptr, parents, tokens,
                        cum_next, scratch, err_ptr(), (cudaStream_t)stream);
 }
 

@@ -1,17 +1,25 @@
 // Exact global top-W beam selection and the ancestry-index update.
 //
 // Selection (OneLA §1.1: all live beams expand over the codebook and one
-// global top-k keeps the survivors) runs in the two exact stages of RecoGEM
-// §4.3: a per-row precut keeps each beam row's local top-K (K = min(W_next,
-// V)), then a request-level selection picks the W_next winners among the
-// precut survivors. A candidate dropped by the precut is beaten by K
-// candidates of its own row, so it cannot be among the final K.
+// global top-k keeps the survivors) orders candidate (b, v) of a request by
+//   s = fl32(cum'_b + fl32(z_bv - lse_b)),  cum'_b = fl32(cum_b + bias_b),
+// descending, ties to the lower flat index b*V + v. Every candidate carries
+// one 64-bit key: the orderable image of s in the high word and
+// (2^32 - 1 - flat) in the low word, so larger keys rank first and keys are
+// unique within a request.
 //
-// Every candidate carries one 64-bit key: the orderable image of its fp32
-// score in the high word and (2^32 - 1 - flat index) in the low word, so the
-// largest keys are the highest scores with ties going to the lower flat
-// index b*V + v. Keys are unique within a request; both stages find the
-// K-th largest key by MSB-first 8-bit radix passes.
+// Fast path (one read of the logits):
+//   bound   per request, the scores of one real candidate per (row, 256-code
+//           tile) — the tile maximum, which the logits GEMM already produces
+//           for the log-normaliser — and the W-th largest of them, tau;
+//   filter  every candidate with s >= tau is appended to the request's buffer;
+//   final   exact top-W of the buffer by radix search on the keys, sorted.
+// If the buffer holds at least W candidates, every candidate left out scores
+// below the W-th largest kept one, so the result is exact whatever tau was.
+// Otherwise (or if the buffer overflows) the request falls back to the two
+// exact stages of RecoGEM §4.3: a per-row precut to the local top-K
+// (K = min(W, V)), then a request-level selection among the survivors; a
+// candidate the precut drops is beaten by K candidates of its own row.
 //
 // Ancestry (OneLA §2.4 eq. 9): each child copies its parent's slot list and
 // appends the parent's row as the slot of the previous depth.
@@ -22,28 +30,62 @@ namespace gdnbeam {
 
 namespace {
 
+constexpr int kTile = 256;           // codes per hint tile (the logits GEMM tile width)
+constexpr int kBoundThreads = 1024;
+constexpr int kFilterThreads = 256;
+constexpr int kFinalThreads = 1024;
+constexpr int kFinalSmemKeys = 16384; // candidates a final block keeps on chip
 constexpr int kRowThreads = 512;
 constexpr int kReqThreads = 1024;
 constexpr int kMaxSort = 4096;
 
-__device__ __forceinline__ uint64_t make_key(float s, uint32_t flat) {
-  return ((uint64_t)orderable(s) << 32) | (uint64_t)(0xFFFFFFFFu - flat);
+__device__ __forceinline__ uint64_t make_key(uint32_t ord, uint32_t flat) {
+  return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - flat);
 }
 
-// Block-wide radix search for the K-th largest of n keys read through get().
-// Returns (prefix, mask): the K largest keys are exactly those with
-// (key & mask) >= prefix. Needs hist[256] and two shared words.
-template <typename Get>
-__device__ void radix_kth(int n, unsigned K, Get get, unsigned* hist, unsigned* sh,
-                          uint64_t& prefix_out, uint64_t& mask_out) {
-  uint64_t prefix = 0, mask = 0;
+__device__ __forceinline__ float score(float cp, float zv, float l) {
+  return __fadd_rn(cp, __fsub_rn(zv, l));
+}
+
+// Unpacks one 16-byte load into VEC stored values, as floats.
+template <typename T, int VEC> struct Unpack;
+template <> struct Unpack<__nv_bfloat16, 8> {
+  static __device__ __forceinline__ void run(const uint4& r, float (&f)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+};
+template <> struct Unpack<float, 4> {
+  static __device__ __forceinline__ void run(const uint4& r, float (&f)[4]) {
+    f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+  }
+};
+
+__device__ __forceinline__ float cum_prime(const float* cum, const float* bias, size_t row) {
+  float cp = cum ? cum[row] : 0.0f;
+  if (bias) cp = __fadd_rn(cp, bias[row]);
+  return cp;
+}
+
+// Block-wide MSB-first radix search for the K-th largest of n keys read
+// through get(). Returns prefix such that the keys >= prefix are the K
+// largest (with ties at the K-th value all included when keys repeat).
+// Needs hist[256] and sh[3] in shared memory.
+template <typename Key, typename Get>
+__device__ Key radix_kth(int n, unsigned K, Get get, unsigned* hist, unsigned* sh) {
+  Key prefix = 0, mask = 0;
   unsigned remaining = K;
-  for (int shift = 56; shift >= 0; shift -= 8) {
+  for (int shift = 8 * (int)sizeof(Key) - 8; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      uint64_t key = get(i);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 0xFF], 1u);
+      Key key = get(i);
+      if ((key & mask) == prefix) atomicAdd(&hist[(unsigned)(key >> shift) & 0xFFu], 1u);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -55,100 +97,30 @@ __device__ void radix_kth(int n, unsigned K, Get get, unsigned* hist, unsigned* 
       }
       sh[0] = (unsigned)d;
       sh[1] = remaining - above;
-      sh[2] = (hist[d] == remaining - above) ? 1u : 0u;  // whole bucket is taken
+      sh[2] = (hist[d] == remaining - above) ? 1u : 0u;  // the whole bucket is taken
     }
     __syncthreads();
-    prefix |= (uint64_t)sh[0] << shift;
-    mask |= (uint64_t)0xFF << shift;
+    prefix |= (Key)sh[0] << shift;
+    mask |= (Key)0xFF << shift;
     remaining = sh[1];
     const bool done = sh[2] != 0;
     __syncthreads();
     if (done) break;
   }
-  prefix_out = prefix;
-  mask_out = mask;
+  return prefix;
 }
 
-// Stage 1: per beam row, the local top-K keys (unordered) -> cand[row][K].
-template <typename T>
-__global__ void __launch_bounds__(kRowThreads) select_rowcut_kernel(
-    int W_t, int V, int K, const T* __restrict__ logits, const float* __restrict__ lse,
-    const float* __restrict__ cum, const float* __restrict__ bias, uint64_t* __restrict__ cand,
-    unsigned* err) {
-  extern __shared__ uint64_t keys[];  // [V]
-  __shared__ unsigned hist[256];
-  __shared__ unsigned sh[4];
-  const int row = blockIdx.x;
-  const int b = row % W_t;
-  const float l = lse[row];
-  float cp = cum ? cum[row] : 0.0f;
-  if (bias) cp = __fadd_rn(cp, bias[row]);
-  const T* zr = logits + (size_t)row * V;
-  bool bad = false;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    float s = __fadd_rn(cp, __fsub_rn(ldf(zr + v), l));
-    if (!isfinite(s)) bad = true;
-    keys[v] = make_key(s, (uint32_t)b * (uint32_t)V + (uint32_t)v);
-  }
-  if (bad) raise_error(err, GDNBEAM_DERR_NONFINITE);
-  if (threadIdx.x == 0) sh[3] = 0;
-  __syncthreads();
-  uint64_t* out = cand + (size_t)row * K;
-  if (K >= V) {
-    for (int v = threadIdx.x; v < V; v += blockDim.x) out[v] = keys[v];
-    return;
-  }
-  uint64_t prefix, mask;
-  radix_kth(V, (unsigned)K, [&](int i) { return keys[i]; }, hist, sh, prefix, mask);
-  for (int v = threadIdx.x; v < V; v += blockDim.x) {
-    uint64_t key = keys[v];
-    if ((key & mask) >= prefix) {
-      unsigned idx = atomicAdd(&sh[3], 1u);
-      if (idx < (unsigned)K) out[idx] = key;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && sh[3] != (unsigned)K) raise_error(err, GDNBEAM_DERR_SELECT);
-}
-
-// Stage 2: per request, the W_next largest of its W_t*K precut keys, sorted.
-__global__ void __launch_bounds__(kReqThreads) select_request_kernel(
-    int W_t, int K, int W_next, int V, const uint64_t* __restrict__ cand,
-    int32_t* __restrict__ parents, int32_t* __restrict__ tokens, float* __restrict__ cum_next,
-    unsigned* err) {
-  __shared__ unsigned hist[256];
-  __shared__ unsigned sh[4];
-  __shared__ uint64_t win[kMaxSort];
-  const int r = blockIdx.x;
-  const int n = W_t * K;
-  const uint64_t* c = cand + (size_t)r * n;
-  uint64_t prefix = 0, mask = 0;
-  if (W_next < n) {
-    radix_kth(n, (unsigned)W_next, [&](int i) { return c[i]; }, hist, sh, prefix, mask);
-  }
-  int P = 1;
-  while (P < W_next) P <<= 1;
-  for (int i = threadIdx.x; i < P; i += blockDim.x) win[i] = 0;
-  if (threadIdx.x == 0) sh[3] = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    uint64_t key = c[i];
-    if ((key & mask) >= prefix) {
-      unsigned idx = atomicAdd(&sh[3], 1u);
-      if (idx < (unsigned)W_next) win[idx] = key;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && sh[3] != (unsigned)W_next) raise_error(err, GDNBEAM_DERR_SELECT);
-  // bitonic sort, descending
+// Sorts win[0..P) descending (P a power of two) and writes the first W_next.
+__device__ void sort_and_emit(uint64_t* win, int P, int W_next, int V, int32_t* parents,
+                              int32_t* tokens, float* cum_next) {
   for (int size = 2; size <= P; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int i = threadIdx.x; i < P; i += blockDim.x) {
         int j = i ^ stride;
         if (j > i) {
           bool desc = (i & size) == 0;
-          uint64_t a = win[i], bb = win[j];
-          if (desc ? (a < bb) : (a > bb)) { win[i] = bb; win[j] = a; }
+          uint64_t a = win[i], b = win[j];
+          if (desc ? (a < b) : (a > b)) { win[i] = b; win[j] = a; }
         }
       }
       __syncthreads();
@@ -157,11 +129,280 @@ __global__ void __launch_bounds__(kReqThreads) select_request_kernel(
   for (int i = threadIdx.x; i < W_next; i += blockDim.x) {
     uint64_t key = win[i];
     uint32_t flat = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFu);
-    size_t o = (size_t)r * W_next + i;
-    parents[o] = (int32_t)(flat / (uint32_t)V);
-    tokens[o] = (int32_t)(flat % (uint32_t)V);
-    cum_next[o] = from_orderable((uint32_t)(key >> 32));
+    parents[i] = (int32_t)(flat / (uint32_t)V);
+    tokens[i] = (int32_t)(flat % (uint32_t)V);
+    cum_next[i] = from_orderable((uint32_t)(key >> 32));
   }
+}
+
+struct SelScratch {
+  int* count;       // [R] candidates appended by the filter
+  uint32_t* thr;    // [R] orderable score bound
+  int* fb_flag;     // [R] request needs the fallback
+  int* fb_any;      // [1]
+  uint64_t* cand;   // [R][cap]
+  uint64_t* pre;    // [R*W_t][K] fallback precut keys
+  float2* hint;     // [R*W_t][n_tiles] tile maxima computed here when not supplied
+  int cap;
+};
+
+size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int cap_of(int W_t, int W_next, int V) {
+  long long cap = 16LL * W_next;
+  if (cap < V) cap = V;
+  if (cap > (long long)W_t * V) cap = (long long)W_t * V;
+  return (int)cap;
+}
+
+SelScratch carve_sel(void* base, int R, int W_t, int W_next, int V, size_t* total) {
+  SelScratch s{};
+  const int K = W_next < V ? W_next : V;
+  const int n_tiles = (V + kTile - 1) / kTile;
+  s.cap = cap_of(W_t, W_next, V);
+  char* p = (char*)base;
+  size_t off = 0;
+  auto take = [&](size_t b) { char* q = p ? p + off : nullptr; off += a256(b); return q; };
+  s.count = (int*)take((size_t)R * 4);
+  s.thr = (uint32_t*)take((size_t)R * 4);
+  s.fb_flag = (int*)take((size_t)R * 4);
+  s.fb_any = (int*)take(16);
+  s.cand = (uint64_t*)take((size_t)R * s.cap * 8);
+  s.pre = (uint64_t*)take((size_t)R * W_t * K * 8);
+  s.hint = (float2*)take((size_t)R * W_t * n_tiles * sizeof(float2));
+  if (total) *total = off;
+  return s;
+}
+
+// ---- hint pre-pass: the maximum stored logit of every (row, 256-code tile)
+template <typename T>
+__global__ void tile_max_kernel(int n, int V, int n_tiles, const T* __restrict__ z,
+                                float2* __restrict__ hint) {
+  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= (long long)n * n_tiles) return;
+  const int row = (int)(w / n_tiles), tile = (int)(w % n_tiles);
+  const T* zr = z + (size_t)row * V + (size_t)tile * kTile;
+  const int cnt = min(kTile, V - tile * kTile);
+  float mx = -INFINITY;
+  for (int c = lane; c < cnt; c += 32) mx = fmaxf(mx, ldf(zr + c));
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) hint[w] = make_float2(mx, 0.0f);
+}
+
+// ---- bound: the W_next-th largest hint score of each request
+template <typename T>
+__global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
+    int W_t, int V, int n_tiles, int W_next, const float2* __restrict__ hint,
+    const float* __restrict__ lse, const float* __restrict__ cum, const float* __restrict__ bias,
+    SelScratch ss, int smem_keys) {
+  extern __shared__ uint32_t hkeys[];
+  __shared__ unsigned hist[256];
+  __shared__ unsigned sh[3];
+  const int r = blockIdx.x;
+  const int n_h = W_t * n_tiles;
+  if (threadIdx.x == 0) {
+    ss.count[r] = 0;
+    if (r == 0) *ss.fb_any = 0;
+  }
+  if (W_next > n_h) {  // too few hints for a bound: keep every candidate
+    if (threadIdx.x == 0) ss.thr[r] = 0u;
+    return;
+  }
+  auto key_of = [&](int i) -> uint32_t {
+    const int b = i / n_tiles;
+    const size_t row = (size_t)r * W_t + b;
+    const float zm = hint[row * n_tiles + (i % n_tiles)].x;
+    const float zs = St<T>::to_f(St<T>::from_f(zm));  // stored value of the tile's top element
+    return orderable(score(cum_prime(cum, bias, row), zs, lse[row]));
+  };
+  uint32_t t;
+  if (n_h <= smem_keys) {
+    for (int i = threadIdx.x; i < n_h; i += blockDim.x) hkeys[i] = key_of(i);
+    __syncthreads();
+    t = radix_kth<uint32_t>(n_h, (unsigned)W_next, [&](int i) { return hkeys[i]; }, hist, sh);
+  } else {
+    t = radix_kth<uint32_t>(n_h, (unsigned)W_next, key_of, hist, sh);
+  }
+  if (threadIdx.x == 0) ss.thr[r] = t;
+}
+
+// ---- filter: append every candidate whose score reaches the bound
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
+    int W_t, int V, const T* __restrict__ z, const float* __restrict__ lse,
+    const float* __restrict__ cum, const float* __restrict__ bias, SelScratch ss, unsigned* err) {
+  const int row = blockIdx.x;
+  const int r = row / W_t, b = row % W_t;
+  const float l = lse[row];
+  const float cp = cum_prime(cum, bias, row);
+  const uint32_t thr = ss.thr[r];
+  const T* zr = z + (size_t)row * V;
+  const int lane = threadIdx.x & 31;
+  const uint32_t flat0 = (uint32_t)b * (uint32_t)V;
+  uint64_t* out = ss.cand + (size_t)r * ss.cap;
+  bool bad = false;
+  for (int v0 = 0; v0 < V; v0 += kFilterThreads * VEC) {
+    const int v = v0 + threadIdx.x * VEC;
+    float vals[VEC];
+    if constexpr (VEC > 1) {
+      if (v < V) {
+        Unpack<T, VEC>::run(__ldg(reinterpret_cast<const uint4*>(zr + v)), vals);
+      } else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) vals[j] = -INFINITY;
+      }
+    } else {
+      vals[0] = (v < V) ? ldf(zr + v) : -INFINITY;
+    }
+    unsigned hits = 0;
+    uint32_t ords[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+      const float s = score(cp, vals[j], l);
+      if (v + j < V) {
+        if (!isfinite(s)) bad = true;
+        ords[j] = orderable(s);
+        if (ords[j] >= thr) hits |= 1u << j;
+      }
+    }
+    const int mine = __popc(hits);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total) {
+      int base = 0;
+      if (lane == 31) base = atomicAdd(ss.count + r, total);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int idx = base + incl - mine;
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) {
+        if (hits & (1u << j)) {
+          if (idx < ss.cap) out[idx] = make_key(ords[j], flat0 + (uint32_t)(v + j));
+          ++idx;
+        }
+      }
+    }
+  }
+  if (bad) raise_error(err, GDNBEAM_DERR_NONFINITE);
+}
+
+// ---- final: exact top-W_next of the filtered candidates, sorted
+__global__ void __launch_bounds__(kFinalThreads) select_final_kernel(
+    int V, int W_next, SelScratch ss, int32_t* __restrict__ parents, int32_t* __restrict__ tokens,
+    float* __restrict__ cum_next) {
+  extern __shared__ uint64_t keys[];  // [kFinalSmemKeys]
+  __shared__ unsigned hist[256];
+  __shared__ unsigned sh[4];
+  __shared__ uint64_t win[kMaxSort];
+  const int r = blockIdx.x;
+  const int n_c = ss.count[r];
+  if (n_c < W_next || n_c > ss.cap) {
+    if (threadIdx.x == 0) {
+      ss.fb_flag[r] = 1;
+      atomicOr(ss.fb_any, 1);
+    }
+    return;
+  }
+  if (threadIdx.x == 0) ss.fb_flag[r] = 0;
+  const uint64_t* c = ss.cand + (size_t)r * ss.cap;
+  const bool on_chip = n_c <= kFinalSmemKeys;
+  if (on_chip) {
+    for (int i = threadIdx.x; i < n_c; i += blockDim.x) keys[i] = c[i];
+    __syncthreads();
+  }
+  auto get = [&](int i) { return on_chip ? keys[i] : c[i]; };
+  uint64_t prefix = 0;
+  if (W_next < n_c) prefix = radix_kth<uint64_t>(n_c, (unsigned)W_next, get, hist, sh);
+  int P = 1;
+  while (P < W_next) P <<= 1;
+  for (int i = threadIdx.x; i < P; i += blockDim.x) win[i] = 0;
+  if (threadIdx.x == 0) sh[3] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_c; i += blockDim.x) {
+    uint64_t key = get(i);
+    if (key >= prefix) {
+      unsigned idx = atomicAdd(&sh[3], 1u);
+      if (idx < (unsigned)W_next) win[idx] = key;
+    }
+  }
+  __syncthreads();
+  const size_t o = (size_t)r * W_next;
+  sort_and_emit(win, P, W_next, V, parents + o, tokens + o, cum_next + o);
+}
+
+// ---- fallback stage 1: per-row local top-K (rows of flagged requests only)
+template <typename T>
+__global__ void __launch_bounds__(kRowThreads) select_rowcut_kernel(
+    int n_rows, int W_t, int V, int K, const T* __restrict__ logits, const float* __restrict__ lse,
+    const float* __restrict__ cum, const float* __restrict__ bias, SelScratch ss, unsigned* err) {
+  extern __shared__ uint64_t rkeys[];  // [V]
+  __shared__ unsigned hist[256];
+  __shared__ unsigned sh[4];
+  if (*(volatile int*)ss.fb_any == 0) return;
+  for (int row = blockIdx.x; row < n_rows; row += gridDim.x) {
+    if (!ss.fb_flag[row / W_t]) continue;
+    const int b = row % W_t;
+    const float l = lse[row];
+    const float cp = cum_prime(cum, bias, row);
+    const T* zr = logits + (size_t)row * V;
+    __syncthreads();
+    for (int v = threadIdx.x; v < V; v += blockDim.x)
+      rkeys[v] = make_key(orderable(score(cp, ldf(zr + v), l)), (uint32_t)b * (uint32_t)V + (uint32_t)v);
+    if (threadIdx.x == 0) sh[3] = 0;
+    __syncthreads();
+    uint64_t* out = ss.pre + (size_t)row * K;
+    if (K >= V) {
+      for (int v = threadIdx.x; v < V; v += blockDim.x) out[v] = rkeys[v];
+      continue;
+    }
+    const uint64_t prefix = radix_kth<uint64_t>(V, (unsigned)K, [&](int i) { return rkeys[i]; }, hist, sh);
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      uint64_t key = rkeys[v];
+      if (key >= prefix) {
+        unsigned idx = atomicAdd(&sh[3], 1u);
+        if (idx < (unsigned)K) out[idx] = key;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && sh[3] != (unsigned)K) raise_error(err, GDNBEAM_DERR_SELECT);
+  }
+}
+
+// ---- fallback stage 2: request-level top-W_next among the precut keys
+__global__ void __launch_bounds__(kReqThreads) select_request_kernel(
+    int W_t, int K, int W_next, int V, SelScratch ss, int32_t* __restrict__ parents,
+    int32_t* __restrict__ tokens, float* __restrict__ cum_next, unsigned* err) {
+  __shared__ unsigned hist[256];
+  __shared__ unsigned sh[4];
+  __shared__ uint64_t win[kMaxSort];
+  const int r = blockIdx.x;
+  if (!ss.fb_flag[r]) return;
+  const int n = W_t * K;
+  const uint64_t* c = ss.pre + (size_t)r * n;
+  auto get = [&](int i) { return c[i]; };
+  uint64_t prefix = 0;
+  if (W_next < n) prefix = radix_kth<uint64_t>(n, (unsigned)W_next, get, hist, sh);
+  int P = 1;
+  while (P < W_next) P <<= 1;
+  for (int i = threadIdx.x; i < P; i += blockDim.x) win[i] = 0;
+  if (threadIdx.x == 0) sh[3] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    uint64_t key = c[i];
+    if (key >= prefix) {
+      unsigned idx = atomicAdd(&sh[3], 1u);
+      if (idx < (unsigned)W_next) win[idx] = key;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && sh[3] != (unsigned)W_next) raise_error(err, GDNBEAM_DERR_SELECT);
+  const size_t o = (size_t)r * W_next;
+  sort_and_emit(win, P, W_next, V, parents + o, tokens + o, cum_next + o);
 }
 
 __global__ void ancestry_kernel(int R, int t, int T, int V, int W_prev, int W_t,
@@ -198,34 +439,95 @@ __global__ void ancestry_kernel(int R, int t, int T, int V, int W_prev, int W_t,
   so[t] = tok;
 }
 
+int sm_count() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
+  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return sms[dev] > 0 ? sms[dev] : 132;
+}
+
+template <typename T>
+int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, const float* cum,
+               const float* bias, const float2* hint, int32_t* parents, int32_t* tokens,
+               float* cum_next, void* scratch, unsigned* err, cudaStream_t s) {
+  const int K = W_next < V ? W_next : V;
+  const int n = R * W_t;
+  const int n_tiles = (V + kTile - 1) / kTile;
+  SelScratch ss = carve_sel(scratch, R, W_t, W_next, V, nullptr);
+  if (!hint) {
+    const long long warps = (long long)n * n_tiles;
+    tile_max_kernel<T><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(n, V, n_tiles, z, ss.hint);
+    GDN_LAUNCH_CHECK();
+    hint = ss.hint;
+  }
+  // bound
+  const int n_h = W_t * n_tiles;
+  const int bound_keys = n_h <= 49152 ? n_h : 0;
+  const size_t bound_smem = (size_t)bound_keys * 4;
+  GDN_CUDA(cudaFuncSetAttribute(select_bound_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(bound_smem > 0 ? bound_smem : 4)));
+  select_bound_kernel<T><<<R, kBoundThreads, bound_smem, s>>>(W_t, V, n_tiles, W_next, hint, lse,
+                                                              cum, bias, ss, bound_keys);
+  GDN_LAUNCH_CHECK();
+  // filter
+  constexpr int VEC = 16 / sizeof(T);
+  const bool vec_ok = (V % VEC) == 0 && ((uintptr_t)z & 15) == 0;
+  if (vec_ok)
+    select_filter_kernel<T, VEC><<<n, kFilterThreads, 0, s>>>(W_t, V, z, lse, cum, bias, ss, err);
+  else
+    select_filter_kernel<T, 1><<<n, kFilterThreads, 0, s>>>(W_t, V, z, lse, cum, bias, ss, err);
+  GDN_LAUNCH_CHECK();
+  // final
+  const size_t fin_smem = (size_t)kFinalSmemKeys * 8;
+  GDN_CUDA(cudaFuncSetAttribute(select_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)fin_smem));
+  select_final_kernel<<<R, kFinalThreads, fin_smem, s>>>(V, W_next, ss, parents, tokens, cum_next);
+  GDN_LAUNCH_CHECK();
+  // exact fallback for requests whose buffer was short or overflowed
+  const size_t row_smem = (size_t)V * 8;
+  GDN_CUDA(cudaFuncSetAttribute(select_rowcut_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)row_smem));
+  const int rc_grid = n < 4 * sm_count() ? n : 4 * sm_count();
+  select_rowcut_kernel<T><<<rc_grid, kRowThreads, row_smem, s>>>(n, W_t, V, K, z, lse, cum, bias,
+                                                                 ss, err);
+  GDN_LAUNCH_CHECK();
+  select_request_kernel<<<R, kReqThreads, 0, s>>>(W_t, K, W_next, V, ss, parents, tokens, cum_next,
+                                                  err);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
 }  // namespace
 
 size_t select_scratch_bytes(int R, int W_t, int W_next, int V) {
-  int K = W_next < V ? W_next : V;
-  return (size_t)R * W_t * K * sizeof(uint64_t);
+  size_t total = 0;
+  carve_sel(nullptr, R, W_t, W_next, V, &total);
+  return total;
 }
 
 int launch_select(int R, int W_t, int W_next, int V, int dtype, const void* logits,
-                  const float* lse, const float* cum, const float* bias, int32_t* parents,
-                  int32_t* tokens, float* cum_next, void* scratch, unsigned* err, cudaStream_t s) {
+                  const float* lse, const float* cum, const float* bias, const float2* hint,
+                  int32_t* parents, int32_t* tokens, float* cum_next, void* scratch,
+                  unsigned* err, cudaStream_t s) {
   if (W_next > kMaxSort || V > 16384) return GDNBEAM_EUNSUPPORTED;
-  const int K = W_next < V ? W_next : V;
-  uint64_t* cand = (uint64_t*)scratch;
-  size_t smem = (size_t)V * sizeof(uint64_t);
-  if (dtype == GDNBEAM_BF16) {
-    auto kern = select_rowcut_kernel<__nv_bfloat16>;
-    GDN_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    kern<<<R * W_t, kRowThreads, smem, s>>>(W_t, V, K, (const __nv_bfloat16*)logits, lse, cum,
-                                            bias, cand, err);
-  } else {
-    auto kern = select_rowcut_kernel<float>;
-    GDN_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    kern<<<R * W_t, kRowThreads, smem, s>>>(W_t, V, K, (const float*)logits, lse, cum, bias,
-                                            cand, err);
-  }
-  GDN_LAUNCH_CHECK();
-  select_request_kernel<<<R, kReqThreads, 0, s>>>(W_t, K, W_next, V, cand, parents, tokens,
-                                                  cum_next, err);
+  if (dtype == GDNBEAM_BF16)
+    return run_select<__nv_bfloat16>(R, W_t, W_next, V, (const __nv_bfloat16*)logits, lse, cum,
+                                     bias, hint, parents, tokens, cum_next, scratch, err, s);
+  return run_select<float>(R, W_t, W_next, V, (const float*)logits, lse, cum, bias, hint, parents,
+                           tokens, cum_next, scratch, err, s);
+}
+
+int launch_tile_max(int dtype, int n, int V, const void* z, float2* hint, cudaStream_t s) {
+  const int n_tiles = (V + kTile - 1) / kTile;
+  const long long warps = (long long)n * n_tiles;
+  if (warps == 0) return GDNBEAM_OK;
+  if (dtype == GDNBEAM_BF16)
+    tile_max_kernel<__nv_bfloat16><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
+        n, V, n_tiles, (const __nv_bfloat16*)z, hint);
+  else
+    tile_max_kernel<float><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(n, V, n_tiles,
+                                                                      (const float*)z, hint);
   GDN_LAUNCH_CHECK();
   return GDNBEAM_OK;
 }

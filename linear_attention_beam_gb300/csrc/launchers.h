@@ -68,11 +68,16 @@ int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const voi
                         const void* v, const float* alpha, const float* beta, float* sctx,
                         long long sctx_rstride, void* o_last, float* x_inout, cudaStream_t s);
 
+// Selection scratch and launch. hint (may be NULL): per (row, 256-code tile)
+// the maximum logit in .x, as the logits stages leave it; NULL computes it.
 size_t select_scratch_bytes(int R, int W_t, int W_next, int V);
 int launch_select(int R, int W_t, int W_next, int V, int dtype, const void* logits,
-                  const float* lse, const float* cum, const float* bias, int32_t* parents,
-                  int32_t* tokens, float* cum_next, void* scratch, unsigned* err,
-                  cudaStream_t s);
+                  const float* lse, const float* cum, const float* bias, const float2* hint,
+                  int32_t* parents, int32_t* tokens, float* cum_next, void* scratch,
+                  unsigned* err, cudaStream_t s);
+// Per (row, 256-code tile) maximum of stored logits into hint[row][tile].x.
+int launch_tile_max(int dtype, int n, int V, const void* z, float2* hint, cudaStream_t s);
+constexpr int kHintTile = 256;
 
 int launch_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int32_t* parents,
                     const int32_t* tokens, const int32_t* anc_prev, const int32_t* sid_prev,

@@ -136,7 +136,7 @@ def test_call_sequence_is_enforced_on_the_host():
 def test_select_topw_argument_checks():
     lib = gb.load()
     sb = lib.gdnbeam_select_scratch_bytes(2, 4, 3, 10)
-    assert sb == 2 * 4 * 3 * 8
+    assert sb >= 2 * 4 * 3 * 8  # at least the per-row precut keys of the exact fallback
     a = FAKE_WS
     assert lib.gdnbeam_select_topw(2, 4, 3, 10, gb.BF16, a, a, None, None, a, a, a, a, sb - 1, None) == gb.EWORKSPACE
     assert lib.gdnbeam_select_topw(2, 1, 11, 10, gb.BF16, a, a, None, None, a, a, a, a, 10 ** 9, None) == gb.EINVAL

@@ -316,3 +316,27 @@ def test_project_op_tensor_cores(H, d_model, n):
 @pytest.mark.parametrize("F,V,n", [(2048, 8192, 300), (1024, 4096, 129), (256, 1000, 1), (2048, 8192, 512)])
 def test_logits_op_tensor_cores(F, V, n):
     test_logits_op("bf16", F, V, n)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_select_massive_ties_take_the_exact_fallback(dtype):
+    # every candidate ties: the bound keeps all of them, the buffer overflows
+    # and the two-stage exact path must still give the lowest flat indices
+    R, W_t, W_next, V = 2, 64, 5, 100
+    z = np.zeros((R, W_t, V), np.float32)
+    lse = np.zeros((R, W_t), np.float32)
+    cum = np.zeros((R, W_t), np.float32)
+    lib = gb.load()
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    scratch = torch.empty(lib.gdnbeam_select_scratch_bytes(R, W_t, W_next, V), dtype=torch.uint8, device=DEV)
+    par = torch.empty(R, W_next, dtype=torch.int32, device=DEV)
+    tok = torch.empty_like(par)
+    cn = torch.empty(R, W_next, device=DEV)
+    tz, tl, tc_ = to_dev(z.reshape(R * W_t, V), td), to_dev(lse), to_dev(cum)
+    assert lib.gdnbeam_select_topw(R, W_t, W_next, V, gb.BF16 if dtype == "bf16" else gb.F32, gb.ptr(tz),
+                                   gb.ptr(tl), gb.ptr(tc_), None, gb.ptr(par), gb.ptr(tok), gb.ptr(cn),
+                                   gb.ptr(scratch), scratch.numel(), None) == 0
+    assert device_status_clear() == 0
+    for r in range(R):
+        np.testing.assert_array_equal(par[r].cpu().numpy(), [0] * 5)
+        np.testing.assert_array_equal(tok[r].cpu().numpy(), [0, 1, 2, 3, 4])
