@@ -442,7 +442,5 @@ int launch_tc_logits(const gdnbeam_config& c, int n, const void* feat, const voi
   return GDNBEAM_OK;
 }
 
-bool tc_replay_supported(int, int, int) { return false; }
-int launch_tc_replay(const ReplayArgs&, cudaStream_t) { return GDNBEAM_EUNSUPPORTED; }
 
 }  // namespace gdnbeam

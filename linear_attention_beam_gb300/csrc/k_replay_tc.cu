@@ -1,0 +1,432 @@
+// Fused shared-context replay on tcgen05 tensor cores (bf16, d_k = d_v = 128).
+//
+// OneLA §2.5: one block per (request, head) loads that head's S_ctx once and
+// reuses it for every beam tile; per tile it forms the two projections of
+// §2.3 eqs. 6-7 from S_ctx, folds the ancestors' records (alpha_j, delta_j,
+// k_j) into them, evaluates eq. 8 and writes only delta_t (the new record)
+// and o_t. No per-beam d_v x d_k state exists anywhere.
+//
+// Mapping to sm_103a:
+//   * S_ctx is fp32 in memory; the block splits it into bf16 hi + lo halves
+//     in shared memory (128-byte swizzled, K-major), the A operand (M = 128
+//     value rows) of two MMAs per K step, so the contraction keeps ~16
+//     mantissa bits of S_ctx.
+//   * Beams go in tiles of 32. Per tile one producer warp stages by TMA the
+//     32 queries and 32 keys as the B operand (N = 64: q rows then k rows),
+//     the 32 value rows, and with 256-byte bulk copies each beam's ancestor
+//     records delta_j and k_j, found through the ancestry index; stages are
+//     double-buffered on mbarriers.
+//   * One thread issues tcgen05.mma into a double-buffered TMEM accumulator:
+//     column b holds u_q of beam b, column 32 + b its u_k, lane = value row.
+//   * Four epilogue warps (thread = value row i) compute the replay scalars
+//     k_j.q_t, k_j.k_t and k_t.q_t, fold the records, apply eq. 8, and write
+//     delta_t and o_t into shared tiles that TMA stores to memory.
+// Every wait is bounded in time (GDNBEAM_DERR_TIMEOUT on expiry).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launchers.h"
+#include "tc_ptx.cuh"
+
+namespace gdnbeam {
+
+namespace {
+
+constexpr int D = 128;            // head width (d_k = d_v)
+constexpr int NB = 32;            // beams per tile
+constexpr int kThreads = 192;
+constexpr int kMaxDepth = 6;      // replay depths this kernel stages
+constexpr int A_BYTES = 2 * D * D;          // one bf16 half of S_ctx: 32 KiB
+constexpr int B_BYTES = 2 * NB * D * 2;     // q and k rows: 16 KiB
+constexpr int V_BYTES = NB * D * 2;         // value rows: 8 KiB
+constexpr int REC_BYTES = 2 * NB * D * 2;   // delta_j and k_j rows of one depth: 16 KiB
+constexpr int OUT_BYTES = 2 * NB * D * 2;   // delta_t and o_t tiles: 16 KiB
+constexpr int kMaxStages = 3;
+
+struct TcReplayParams {
+  int R, H, t, W_t, n_tiles, stages, stage_bytes;
+  const float* sctx;
+  long long sctx_rstride;
+  const float *alpha, *beta;
+  const __nv_bfloat16* rec_k[kMaxDepth];
+  const __nv_bfloat16* rec_d[kMaxDepth];
+  const float* rec_a[kMaxDepth];
+  int W_j[kMaxDepth];
+  const int32_t* anc;
+  int anc_stride;
+  float* x_inout;
+  float *delta_dump, *o_dump;
+  unsigned* err;
+};
+
+// Byte offset of element (row, col) of a [rows][64] bf16 block in the
+// 128-byte swizzled layout TMA writes (16-byte chunks XOR row mod 8).
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+  return (uint32_t)row * 128u + ((uint32_t)(((col >> 3) ^ (row & 7)) & 7) << 4) +
+         (uint32_t)(col & 7) * 2u;
+}
+
+__device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    replay_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_oo, TcReplayParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
+  __shared__ float s_cq[NB][kMaxDepth], s_ck[NB][kMaxDepth], s_aj[NB][kMaxDepth];
+  __shared__ int s_slot[NB][kMaxDepth];
+  __shared__ float s_kq[NB], s_al[NB], s_be[NB];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA_hi = base, sA_lo = base + A_BYTES;
+  const uint32_t sStage0 = base + 2 * A_BYTES;
+  const uint32_t sOut0 = sStage0 + (uint32_t)(p.stages * p.stage_bytes);
+  uint8_t* gStage0 = gbase + 2 * A_BYTES;
+  uint8_t* gOut0 = gStage0 + p.stages * p.stage_bytes;
+  auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
+  auto full = [&](int s) { return bar(s); };
+  auto empty = [&](int s) { return bar(kMaxStages + s); };
+  auto tfull = [&](int a) { return bar(2 * kMaxStages + a); };
+  auto tempty = [&](int a) { return bar(2 * kMaxStages + 2 + a); };
+  const uint32_t drain_bar = bar(2 * kMaxStages + 4);
+  volatile int* abort = &s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x / p.H, h = blockIdx.x % p.H;
+  const int t = p.t;
+
+  // ---- S_ctx of this (request, head) -> bf16 hi / lo A operands
+  {
+    const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * D * D;
+    for (int u = threadIdx.x; u < D * (D / 8); u += kThreads) {
+      const int row = u >> 4, chunk = u & 15;  // 16 chunks of 8 columns per row
+      const float4 x0 = *reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8);
+      const float4 x1 = *reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8 + 4);
+      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat16 h0 = __float2bfloat16_rn(xs[2 * e]), h1 = __float2bfloat16_rn(xs[2 * e + 1]);
+        __nv_bfloat16 l0 = __float2bfloat16_rn(xs[2 * e] - __bfloat162float(h0));
+        __nv_bfloat16 l1 = __float2bfloat16_rn(xs[2 * e + 1] - __bfloat162float(h1));
+        hi[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        lo[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+      const int kb = chunk >> 3, col = (chunk & 7) * 8;
+      const uint32_t off = (uint32_t)kb * (D * 128) + sw128_off(row, col);
+      *reinterpret_cast<uint4*>(gbase + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(gbase + A_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    tc::fence_proxy_async_smem();
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      tc::mbar_init(full(s), 1);
+      tc::mbar_init(empty(s), 2);  // released by the MMA commit and by the epilogue
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(tfull(a), 1);
+      tc::mbar_init(tempty(a), 4);
+    }
+    tc::mbar_init(drain_bar, 1);
+    s_abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch(&tm_q); tc::tma_prefetch(&tm_k); tc::tma_prefetch(&tm_v);
+    tc::tma_prefetch(&tm_do); tc::tma_prefetch(&tm_oo);
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&s_tmem), 128);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = s_tmem;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    bool issued[kMaxStages] = {false, false, false};
+    uint32_t issued_ph[kMaxStages] = {0, 0, 0};
+    for (int i = 0; i < p.n_tiles; ++i) {
+      const int s = i % p.stages;
+      const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+      int ok = 0;
+      if (lane == 0) ok = tc::mbar_wait(empty(s), ph ^ 1u, abort, p.err) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // the whole warp stops together
+      const int b0 = i * NB;
+      const int nb = min(NB, p.W_t - b0);
+      const uint32_t st = sStage0 + (uint32_t)(s * p.stage_bytes);
+      if (lane == 0) {
+        tc::mbar_arrive_expect_tx(full(s), (uint32_t)(B_BYTES + V_BYTES + t * nb * 2 * D * 2));
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint32_t bk = st + kb * (2 * NB * 128);
+          tc::tma_load_3d(bk, &tm_q, h * D + kb * 64, b0, r, full(s));
+          tc::tma_load_3d(bk + NB * 128, &tm_k, h * D + kb * 64, b0, r, full(s));
+          tc::tma_load_3d(st + B_BYTES + kb * (NB * 128), &tm_v, h * D + kb * 64, b0, r, full(s));
+        }
+      }
+      __syncwarp();
+      if (lane < nb) {
+        const size_t row = (size_t)r * p.W_t + b0 + lane;
+        for (int j = 0; j < t; ++j) {
+          int slot = p.anc[row * p.anc_stride + j];
+          if (slot < 0 || slot >= p.W_j[j]) slot = 0;  // flagged by the epilogue
+          const size_t rec = ((size_t)r * p.W_j[j] + slot) * p.H + h;
+          const uint32_t dst = st + B_BYTES + V_BYTES + j * REC_BYTES + lane * (D * 2);
+          tc::bulk_load(dst, p.rec_d[j] + rec * D, D * 2, full(s));
+          tc::bulk_load(dst + NB * D * 2, p.rec_k[j] + rec * D, D * 2, full(s));
+        }
+      }
+      if (lane == 0) { issued[s] = true; issued_ph[s] = ph; }
+    }
+    if (lane == 0)
+      for (int s = 0; s < p.stages; ++s)
+        if (issued[s]) tc::mbar_wait_drain(full(s), issued_ph[s]);
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(D, 2 * NB);
+      for (int i = 0; i < p.n_tiles; ++i) {
+        const int s = i % p.stages;
+        const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+        const int acc = i & 1;
+        const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+        if (!tc::mbar_wait(full(s), ph, abort, p.err)) break;
+        if (!tc::mbar_wait(tempty(acc), aph ^ 1u, abort, p.err)) break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem_base + (uint32_t)(acc * 2 * NB);
+        const uint32_t st = sStage0 + (uint32_t)(s * p.stage_bytes);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint64_t ahi = tc::sw128_desc(sA_hi + kb * (D * 128));
+          const uint64_t alo = tc::sw128_desc(sA_lo + kb * (D * 128));
+          const uint64_t bd = tc::sw128_desc(st + kb * (2 * NB * 128));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            tc::mma_bf16(d, ahi + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0);
+            tc::mma_bf16(d, alo + 2u * kk, bd + 2u * kk, idesc, 1u);
+          }
+        }
+        tc::mma_commit(empty(s));
+        tc::mma_commit(tfull(acc));
+      }
+      tc::mma_commit(drain_bar);
+      tc::mbar_wait_drain(drain_bar, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int ew = warp - 2;                 // 0..3
+    const int ep = threadIdx.x - 64;         // 0..127
+    const int i_row = (warp & 3) * 32 + lane;  // value row = TMEM lane
+    bool dead = false;
+    for (int i = 0; i < p.n_tiles; ++i) {
+      const int s = i % p.stages;
+      const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+      const int acc = i & 1;
+      const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+      const int ob = i & 1;
+      const int b0 = i * NB;
+      const int nb = min(NB, p.W_t - b0);
+      // A failed wait marks the warp dead: it then skips all work but keeps
+      // taking part in the named barriers, so no other epilogue warp waits
+      // on it forever.
+      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait(full(s), ph, abort, p.err));
+      const uint8_t* gst = gStage0 + s * p.stage_bytes;
+      if (ep == 0) tc::bulk_wait_read<1>();  // out buffer ob is free again
+      // per-beam gates and ancestor slots
+      if (!dead && ew == 0 && lane < nb) {
+        const size_t row = (size_t)r * p.W_t + b0 + lane;
+        s_al[lane] = p.alpha[row * p.H + h];
+        s_be[lane] = p.beta[row * p.H + h];
+        for (int j = 0; j < t; ++j) {
+          int slot = p.anc[row * p.anc_stride + j];
+          if (slot < 0 || slot >= p.W_j[j]) {
+            raise_error(p.err, GDNBEAM_DERR_SLOT);
+            slot = -1;
+          }
+          s_slot[lane][j] = slot;
+          s_aj[lane][j] = slot >= 0 ? p.rec_a[j][((size_t)r * p.W_j[j] + slot) * p.H + h] : 0.0f;
+        }
+      }
+      // replay scalars: k_j.q_t, k_j.k_t (eqs. 6-7) and k_t.q_t (eq. 8)
+      for (int b = ew; b < (dead ? 0 : nb); b += 4) {
+        const int c = lane * 4;  // 4 key columns per lane
+        const int kb = c >> 6, cc = c & 63;
+        const uint8_t* bk = gst + kb * (2 * NB * 128);
+        const uint2 qw = *reinterpret_cast<const uint2*>(bk + sw128_off(b, cc));
+        const uint2 kw = *reinterpret_cast<const uint2*>(bk + sw128_off(NB + b, cc));
+        const float q4[4] = {bf(qw.x & 0xFFFF), bf(qw.x >> 16), bf(qw.y & 0xFFFF), bf(qw.y >> 16)};
+        const float k4[4] = {bf(kw.x & 0xFFFF), bf(kw.x >> 16), bf(kw.y & 0xFFFF), bf(kw.y >> 16)};
+        float kq = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kq = fmaf(k4[e], q4[e], kq);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+        if (lane == 0) s_kq[b] = kq;
+        for (int j = 0; j < t; ++j) {
+          const uint8_t* kr = gst + B_BYTES + V_BYTES + j * REC_BYTES + NB * D * 2 + b * (D * 2);
+          const uint2 rw = *reinterpret_cast<const uint2*>(kr + c * 2);
+          const float r4[4] = {bf(rw.x & 0xFFFF), bf(rw.x >> 16), bf(rw.y & 0xFFFF), bf(rw.y >> 16)};
+          float cq = 0.f, ck = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            cq = fmaf(r4[e], q4[e], cq);
+            ck = fmaf(r4[e], k4[e], ck);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            cq += __shfl_xor_sync(0xffffffffu, cq, o);
+            ck += __shfl_xor_sync(0xffffffffu, ck, o);
+          }
+          if (lane == 0) { s_cq[b][j] = cq; s_ck[b][j] = ck; }
+        }
+      }
+      tc::named_sync(1, 128);
+      // u_q, u_k of every beam for this thread's value row
+      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait(tfull(acc), aph, abort, p.err));
+      float uq[NB], uk[NB];
+      if (!dead) {
+        tc::fence_after_sync();
+        const uint32_t ta = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(acc * 2 * NB);
+        tc::tmem_ld32(ta, uq);
+        tc::tmem_ld32(ta + NB, uk);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tempty(acc));
+      }
+      // fold the records and apply eq. 8
+      const int half = i_row >> 6, col = i_row & 63;
+      const uint8_t* vt = gst + B_BYTES + half * (NB * 128) + col * 2;
+      uint8_t* od = gOut0 + ob * OUT_BYTES + half * (NB * 128) + col * 2;
+      uint8_t* oo = od + NB * D * 2;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (!dead && b < nb) {
+          float u_q = uq[b], u_k = uk[b];
+          for (int j = 0; j < t; ++j) {
+            if (s_slot[b][j] < 0) continue;
+            const float a = s_aj[b][j];
+            const float dj = bf(*reinterpret_cast<const uint16_t*>(
+                gst + B_BYTES + V_BYTES + j * REC_BYTES + b * (D * 2) + i_row * 2));
+            u_q = a * u_q + dj * s_cq[b][j];
+            u_k = a * u_k + dj * s_ck[b][j];
+          }
+          const float al = s_al[b], be = s_be[b];
+          const float vv = bf(*reinterpret_cast<const uint16_t*>(vt + b * 128));
+          const float delta = be * (vv - al * u_k);
+          const float o = al * u_q + delta * s_kq[b];
+          *reinterpret_cast<__nv_bfloat16*>(od + b * 128) = __float2bfloat16_rn(delta);
+          *reinterpret_cast<__nv_bfloat16*>(oo + b * 128) = __float2bfloat16_rn(o);
+          const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row;
+          if (p.delta_dump) p.delta_dump[goff] = delta;
+          if (p.o_dump) p.o_dump[goff] = o;
+          if (p.x_inout) p.x_inout[goff] += o;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::named_sync(1, 128);
+      if (ep == 0 && !dead) {
+        tc::mbar_arrive(empty(s));  // value rows and records of stage s are consumed
+        const uint32_t so = sOut0 + (uint32_t)(ob * OUT_BYTES);
+        for (int hf = 0; hf < 2; ++hf) {
+          tc::tma_store_3d(&tm_do, h * D + hf * 64, b0, r, so + hf * (NB * 128));
+          tc::tma_store_3d(&tm_oo, h * D + hf * 64, b0, r, so + NB * D * 2 + hf * (NB * 128));
+        }
+        tc::bulk_commit();
+      }
+    }
+    if (ep == 0) tc::bulk_wait_all();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, 128);
+  }
+}
+
+// ---- host side -----------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+// [R][W_t][H*128] bf16 as a 3-D map with a 64-column x 32-row x 1 box.
+bool beam_map(CUtensorMap* map, const void* ptr, int R, int W_t, int H, bool swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || ((uintptr_t)ptr & 15) != 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)H * D, (cuuint64_t)W_t, (cuuint64_t)R};
+  cuuint64_t strides[2] = {(cuuint64_t)H * D * 2, (cuuint64_t)W_t * H * D * 2};
+  cuuint32_t box[3] = {64, NB, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_replay_supported(int dtype, int d_k, int d_v) {
+  return dtype == GDNBEAM_BF16 && d_k == D && d_v == D;
+}
+
+int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
+  if (a.W_t <= 0) return GDNBEAM_OK;
+  if (a.t > kMaxDepth || a.d_k != D || a.d_v != D) return launch_replay(GDNBEAM_BF16, a, s);
+  TcReplayParams p{};
+  p.R = a.R; p.H = a.H; p.t = a.t; p.W_t = a.W_t;
+  p.n_tiles = (a.W_t + NB - 1) / NB;
+  p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES;
+  const int static_bytes = 8 * 1024;
+  const int budget = 227 * 1024 - static_bytes - 1024 - 2 * A_BYTES - 2 * OUT_BYTES;
+  p.stages = budget / p.stage_bytes;
+  if (p.stages > kMaxStages) p.stages = kMaxStages;
+  if (p.stages < 1) return launch_replay(GDNBEAM_BF16, a, s);
+  p.sctx = a.sctx; p.sctx_rstride = a.sctx_rstride;
+  p.alpha = a.alpha; p.beta = a.beta;
+  for (int j = 0; j < a.t; ++j) {
+    p.rec_k[j] = (const __nv_bfloat16*)a.depth[j].k;
+    p.rec_d[j] = (const __nv_bfloat16*)a.depth[j].delta;
+    p.rec_a[j] = a.depth[j].alpha;
+    p.W_j[j] = a.depth[j].W_j;
+    if (((uintptr_t)p.rec_k[j] & 15) || ((uintptr_t)p.rec_d[j] & 15)) return GDNBEAM_EINVAL;
+  }
+  p.anc = a.anc; p.anc_stride = a.anc_stride;
+  p.x_inout = a.x_inout; p.delta_dump = a.delta_dump; p.o_dump = a.o_dump; p.err = a.err;
+  if (((uintptr_t)a.sctx & 15) || (a.sctx_rstride % 4) != 0) return GDNBEAM_EINVAL;
+  CUtensorMap mq, mk, mv, md, mo;
+  if (!beam_map(&mq, a.q, a.R, a.W_t, a.H, true) || !beam_map(&mk, a.k, a.R, a.W_t, a.H, true) ||
+      !beam_map(&mv, a.v, a.R, a.W_t, a.H, false) ||
+      !beam_map(&md, a.delta_out, a.R, a.W_t, a.H, false) ||
+      !beam_map(&mo, a.o_out, a.R, a.W_t, a.H, false))
+    return GDNBEAM_ECUDA;
+  const size_t dyn = 1024 + 2 * A_BYTES + (size_t)p.stages * p.stage_bytes + 2 * OUT_BYTES;
+  GDN_CUDA(cudaFuncSetAttribute(replay_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)dyn));
+  replay_tc_kernel<<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, mv, md, mo, p);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
+}  // namespace gdnbeam

@@ -138,7 +138,10 @@ def test_ancestry_op_matches_walk():
 @pytest.mark.parametrize("dtype,d,H,R,W_t,t,resid", [
     ("f32", 16, 1, 1, 8, 2, False), ("bf16", 128, 3, 2, 37, 2, False),
     ("bf16", 64, 2, 3, 20, 3, True), ("f32", 128, 2, 2, 19, 1, False),
-    ("bf16", 128, 2, 2, 300, 0, False), ("bf16", 32, 1, 1, 5, 5, False)])
+    ("bf16", 128, 2, 2, 300, 0, False), ("bf16", 32, 1, 1, 5, 5, False),
+    ("bf16", 128, 4, 3, 64, 3, False), ("bf16", 128, 1, 1, 1, 1, False),
+    ("bf16", 128, 2, 1, 96, 5, False), ("bf16", 128, 2, 2, 40, 1, True),
+    ("bf16", 128, 3, 2, 512, 2, False)])
 def test_replay_op(dtype, d, H, R, W_t, t, resid):
     wl = synth.tiny_workload(d=d, V=7, H=H, R=R, dtype=dtype)
     rng = np.random.default_rng(d + H + W_t + t)
@@ -196,19 +199,25 @@ def test_replay_op(dtype, d, H, R, W_t, t, resid):
         assert maxrel(host(x_dev).reshape(R, W_t, H * d), x0 + exp_o.reshape(R, W_t, H * d)) <= tol
 
 
-def test_replay_rejects_out_of_range_slot():
-    wl = synth.tiny_workload(d=16, V=7, H=1, R=1, dtype="f32")
+@pytest.mark.parametrize("dtype,d", [("f32", 16), ("bf16", 128)])
+def test_replay_rejects_out_of_range_slot(dtype, d):
+    wl = synth.tiny_workload(d=d, V=7, H=1, R=1, dtype=dtype)
     lib = gb.load()
-    t, W_t, d = 1, 4, 16
-    z = lambda *s: torch.zeros(*s, device=DEV)
-    k1, d1, a1 = z(3 * d), z(3 * d), z(3)
+    t, W_t = 1, 4
+    td = tdt(wl)
+    keep = []
+    def z(*s, dt=torch.float32):
+        x = torch.zeros(*s, device=DEV, dtype=dt)
+        keep.append(x)
+        return x
+    k1, d1, a1 = z(3 * d, dt=td), z(3 * d, dt=td), z(3)
     recs = (gb.Records * 1)(gb.Records(gb.ptr(k1), gb.ptr(d1), gb.ptr(a1), 3))
     anc = torch.tensor([[0], [1], [7], [2]], dtype=torch.int32, device=DEV)  # 7 >= W_j = 3
     cfg = cfg_for(wl)
-    out = z(W_t * d)
-    st = lib.gdnbeam_replay(C.byref(cfg), t, W_t, gb.ptr(z(d * d)), d * d, gb.ptr(z(W_t * d)), gb.ptr(z(W_t * d)),
-                            gb.ptr(z(W_t * d)), gb.ptr(z(W_t)), gb.ptr(z(W_t)), recs, gb.ptr(anc), 1,
-                            gb.ptr(out), gb.ptr(z(W_t * d)), None, None, None)
+    st = lib.gdnbeam_replay(C.byref(cfg), t, W_t, gb.ptr(z(d * d)), d * d, gb.ptr(z(W_t * d, dt=td)),
+                            gb.ptr(z(W_t * d, dt=td)), gb.ptr(z(W_t * d, dt=td)), gb.ptr(z(W_t)), gb.ptr(z(W_t)),
+                            recs, gb.ptr(anc), 1, gb.ptr(z(W_t * d, dt=td)), gb.ptr(z(W_t * d, dt=td)), None,
+                            None, None)
     assert st == 0
     assert device_status_clear() & gb.DERR["slot"]
     assert device_status_clear() == 0
