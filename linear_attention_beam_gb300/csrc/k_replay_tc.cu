@@ -34,12 +34,15 @@ namespace {
 
 constexpr int D = 128;            // head width (d_k = d_v)
 constexpr int NB = 32;            // beams per tile
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;      // two per SM sub-partition; each owns 16 beams of a tile
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kMaxDepth = 6;      // replay depths this kernel stages
 constexpr int A_BYTES = 2 * D * D;          // one bf16 half of S_ctx: 32 KiB
 constexpr int B_BYTES = 2 * NB * D * 2;     // q and k rows: 16 KiB
 constexpr int V_BYTES = NB * D * 2;         // value rows: 8 KiB
 constexpr int REC_BYTES = 2 * NB * D * 2;   // delta_j and k_j rows of one depth: 16 KiB
+constexpr int META_BYTES = 1024;            // per-beam gates and ancestors' decays
 constexpr int OUT_BYTES = 2 * NB * D * 2;   // delta_t and o_t tiles: 16 KiB
 constexpr int kMaxStages = 3;
 
@@ -66,7 +69,7 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
          (uint32_t)(col & 7) * 2u;
 }
 
-__device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+__device__ __forceinline__ float bf(uint32_t x16) { return __uint_as_float(x16 << 16); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     replay_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -75,9 +78,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_oo, TcReplayParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
-  __shared__ float s_cq[NB][kMaxDepth], s_ck[NB][kMaxDepth], s_aj[NB][kMaxDepth];
-  __shared__ int s_slot[NB][kMaxDepth];
-  __shared__ float s_kq[NB], s_al[NB], s_be[NB];
+  __shared__ float4 s_beam[NB];             // (alpha_t, beta_t, k_t.q_t, -)
+  __shared__ float4 s_rec[NB][kMaxDepth];   // (alpha_j, k_j.q_t, k_j.k_t, -)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -100,14 +102,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x / p.H, h = blockIdx.x % p.H;
   const int t = p.t;
+  const int meta_off = B_BYTES + V_BYTES + t * REC_BYTES;  // within a stage
 
   // ---- S_ctx of this (request, head) -> bf16 hi / lo A operands
   {
     const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * D * D;
+#pragma unroll 2
     for (int u = threadIdx.x; u < D * (D / 8); u += kThreads) {
       const int row = u >> 4, chunk = u & 15;  // 16 chunks of 8 columns per row
-      const float4 x0 = *reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8);
-      const float4 x1 = *reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8 + 4);
+      const float4 x0 = __ldg(reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8));
+      const float4 x1 = __ldg(reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8 + 4));
       const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       uint32_t hi[4], lo[4];
 #pragma unroll
@@ -127,12 +131,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      tc::mbar_init(full(s), 1);
+      tc::mbar_init(full(s), 32);  // every producer lane arrives after its stores and copies
       tc::mbar_init(empty(s), 2);  // released by the MMA commit and by the epilogue
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull(a), 1);
-      tc::mbar_init(tempty(a), 4);
+      tc::mbar_init(tempty(a), kEpiWarps);
     }
     tc::mbar_init(drain_bar, 1);
     s_abort = 0;
@@ -156,13 +160,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = i % p.stages;
       const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
       int ok = 0;
-      if (lane == 0) ok = tc::mbar_wait(empty(s), ph ^ 1u, abort, p.err) ? 1 : 0;
+      if (lane == 0) ok = tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // the whole warp stops together
       const int b0 = i * NB;
       const int nb = min(NB, p.W_t - b0);
       const uint32_t st = sStage0 + (uint32_t)(s * p.stage_bytes);
+      uint8_t* gst = gStage0 + s * p.stage_bytes;
       if (lane == 0) {
-        tc::mbar_arrive_expect_tx(full(s), (uint32_t)(B_BYTES + V_BYTES + t * nb * 2 * D * 2));
+        tc::mbar_expect_tx(full(s), (uint32_t)(B_BYTES + V_BYTES + t * nb * 2 * D * 2));
         for (int kb = 0; kb < 2; ++kb) {
           const uint32_t bk = st + kb * (2 * NB * 128);
           tc::tma_load_3d(bk, &tm_q, h * D + kb * 64, b0, r, full(s));
@@ -173,15 +178,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane < nb) {
         const size_t row = (size_t)r * p.W_t + b0 + lane;
+        float2* albe = reinterpret_cast<float2*>(gst + meta_off);
+        float* aj = reinterpret_cast<float*>(gst + meta_off + NB * 8);
+        albe[lane] = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
         for (int j = 0; j < t; ++j) {
           int slot = p.anc[row * p.anc_stride + j];
-          if (slot < 0 || slot >= p.W_j[j]) slot = 0;  // flagged by the epilogue
+          float a = -1.0f;  // marks a slot outside its depth: the record is skipped
+          if (slot < 0 || slot >= p.W_j[j]) {
+            raise_error(p.err, GDNBEAM_DERR_SLOT);
+            slot = 0;
+          } else {
+            a = p.rec_a[j][((size_t)r * p.W_j[j] + slot) * p.H + h];
+          }
+          aj[lane * kMaxDepth + j] = a;
           const size_t rec = ((size_t)r * p.W_j[j] + slot) * p.H + h;
           const uint32_t dst = st + B_BYTES + V_BYTES + j * REC_BYTES + lane * (D * 2);
           tc::bulk_load(dst, p.rec_d[j] + rec * D, D * 2, full(s));
           tc::bulk_load(dst + NB * D * 2, p.rec_k[j] + rec * D, D * 2, full(s));
         }
       }
+      tc::mbar_arrive(full(s));  // releases this lane's stage stores
       if (lane == 0) { issued[s] = true; issued_ph[s] = ph; }
     }
     if (lane == 0)
@@ -196,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
         const int acc = i & 1;
         const uint32_t aph = (uint32_t)(i >> 1) & 1u;
-        if (!tc::mbar_wait(full(s), ph, abort, p.err)) break;
-        if (!tc::mbar_wait(tempty(acc), aph ^ 1u, abort, p.err)) break;
+        if (!tc::mbar_wait_sleep(full(s), ph, abort, p.err)) break;
+        if (!tc::mbar_wait_sleep(tempty(acc), aph ^ 1u, abort, p.err)) break;
         tc::fence_after_sync();
         const uint32_t d = tmem_base + (uint32_t)(acc * 2 * NB);
         const uint32_t st = sStage0 + (uint32_t)(s * p.stage_bytes);
@@ -220,9 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;                 // 0..3
-    const int ep = threadIdx.x - 64;         // 0..127
+    const int ew = warp - 2;                   // 0..7
+    const int ep = threadIdx.x - 64;           // 0..255
+    const int hb = ew >> 2;                    // which 16 beams of a tile this warp folds
     const int i_row = (warp & 3) * 32 + lane;  // value row = TMEM lane
+    const int half = i_row >> 6, col = i_row & 63;
     bool dead = false;
     for (int i = 0; i < p.n_tiles; ++i) {
       const int s = i % p.stages;
@@ -235,26 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A failed wait marks the warp dead: it then skips all work but keeps
       // taking part in the named barriers, so no other epilogue warp waits
       // on it forever.
-      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait(full(s), ph, abort, p.err));
+      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(full(s), ph, abort, p.err));
       const uint8_t* gst = gStage0 + s * p.stage_bytes;
       if (ep == 0) tc::bulk_wait_read<1>();  // out buffer ob is free again
-      // per-beam gates and ancestor slots
-      if (!dead && ew == 0 && lane < nb) {
-        const size_t row = (size_t)r * p.W_t + b0 + lane;
-        s_al[lane] = p.alpha[row * p.H + h];
-        s_be[lane] = p.beta[row * p.H + h];
-        for (int j = 0; j < t; ++j) {
-          int slot = p.anc[row * p.anc_stride + j];
-          if (slot < 0 || slot >= p.W_j[j]) {
-            raise_error(p.err, GDNBEAM_DERR_SLOT);
-            slot = -1;
-          }
-          s_slot[lane][j] = slot;
-          s_aj[lane][j] = slot >= 0 ? p.rec_a[j][((size_t)r * p.W_j[j] + slot) * p.H + h] : 0.0f;
-        }
-      }
       // replay scalars: k_j.q_t, k_j.k_t (eqs. 6-7) and k_t.q_t (eq. 8)
-      for (int b = ew; b < (dead ? 0 : nb); b += 4) {
+      const float2* albe = reinterpret_cast<const float2*>(gst + meta_off);
+      const float* ajs = reinterpret_cast<const float*>(gst + meta_off + NB * 8);
+      for (int b = ew; b < (dead ? 0 : nb); b += kEpiWarps) {
         const int c = lane * 4;  // 4 key columns per lane
         const int kb = c >> 6, cc = c & 63;
         const uint8_t* bk = gst + kb * (2 * NB * 128);
@@ -267,7 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) kq = fmaf(k4[e], q4[e], kq);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
-        if (lane == 0) s_kq[b] = kq;
+        if (lane == 0) {
+          const float2 ab = albe[b];
+          s_beam[b] = make_float4(ab.x, ab.y, kq, 0.f);
+        }
         for (int j = 0; j < t; ++j) {
           const uint8_t* kr = gst + B_BYTES + V_BYTES + j * REC_BYTES + NB * D * 2 + b * (D * 2);
           const uint2 rw = *reinterpret_cast<const uint2*>(kr + c * 2);
@@ -283,53 +291,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             cq += __shfl_xor_sync(0xffffffffu, cq, o);
             ck += __shfl_xor_sync(0xffffffffu, ck, o);
           }
-          if (lane == 0) { s_cq[b][j] = cq; s_ck[b][j] = ck; }
+          if (lane == 0) {
+            const float a = ajs[b * kMaxDepth + j];
+            // a skipped record leaves both projections unchanged
+            s_rec[b][j] = a >= 0.f ? make_float4(a, cq, ck, 0.f) : make_float4(1.f, 0.f, 0.f, 0.f);
+          }
         }
       }
-      tc::named_sync(1, 128);
-      // u_q, u_k of every beam for this thread's value row
-      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait(tfull(acc), aph, abort, p.err));
-      float uq[NB], uk[NB];
+      tc::named_sync(1, kEpiThreads);
+      // u_q, u_k of this warp's 16 beams for this thread's value row; fold
+      // the records and apply eq. 8
+      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(tfull(acc), aph, abort, p.err));
+      tc::fence_after_sync();
+      const uint32_t ta = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(acc * 2 * NB);
+      const uint8_t* vt = gst + B_BYTES + half * (NB * 128) + col * 2;
+      const uint8_t* rd = gst + B_BYTES + V_BYTES + i_row * 2;
+      uint8_t* od = gOut0 + ob * OUT_BYTES + half * (NB * 128) + col * 2;
+      uint8_t* oo = od + NB * D * 2;
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        const int bb = hb * 16 + g * 4;
+        float uq4[4], uk4[4];
+        tc::tmem_ld4(ta + bb, uq4);
+        tc::tmem_ld4(ta + NB + bb, uk4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int b = bb + e;
+          if (!dead && b < nb) {
+            float u_q = uq4[e], u_k = uk4[e];
+            for (int j = 0; j < t; ++j) {
+              const float4 rc = s_rec[b][j];
+              const float dj = bf(*reinterpret_cast<const uint16_t*>(rd + j * REC_BYTES + b * (D * 2)));
+              u_q = fmaf(rc.x, u_q, dj * rc.y);
+              u_k = fmaf(rc.x, u_k, dj * rc.z);
+            }
+            const float4 bm = s_beam[b];
+            const float vv = bf(*reinterpret_cast<const uint16_t*>(vt + b * 128));
+            const float delta = bm.y * (vv - bm.x * u_k);
+            const float o = fmaf(bm.x, u_q, delta * bm.z);
+            *reinterpret_cast<__nv_bfloat16*>(od + b * 128) = __float2bfloat16_rn(delta);
+            *reinterpret_cast<__nv_bfloat16*>(oo + b * 128) = __float2bfloat16_rn(o);
+            if (p.delta_dump || p.o_dump || p.x_inout) {
+              const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row;
+              if (p.delta_dump) p.delta_dump[goff] = delta;
+              if (p.o_dump) p.o_dump[goff] = o;
+              if (p.x_inout) p.x_inout[goff] += o;
+            }
+          }
+        }
+      }
       if (!dead) {
-        tc::fence_after_sync();
-        const uint32_t ta = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(acc * 2 * NB);
-        tc::tmem_ld32(ta, uq);
-        tc::tmem_ld32(ta + NB, uk);
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tempty(acc));
       }
-      // fold the records and apply eq. 8
-      const int half = i_row >> 6, col = i_row & 63;
-      const uint8_t* vt = gst + B_BYTES + half * (NB * 128) + col * 2;
-      uint8_t* od = gOut0 + ob * OUT_BYTES + half * (NB * 128) + col * 2;
-      uint8_t* oo = od + NB * D * 2;
-#pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        if (!dead && b < nb) {
-          float u_q = uq[b], u_k = uk[b];
-          for (int j = 0; j < t; ++j) {
-            if (s_slot[b][j] < 0) continue;
-            const float a = s_aj[b][j];
-            const float dj = bf(*reinterpret_cast<const uint16_t*>(
-                gst + B_BYTES + V_BYTES + j * REC_BYTES + b * (D * 2) + i_row * 2));
-            u_q = a * u_q + dj * s_cq[b][j];
-            u_k = a * u_k + dj * s_ck[b][j];
-          }
-          const float al = s_al[b], be = s_be[b];
-          const float vv = bf(*reinterpret_cast<const uint16_t*>(vt + b * 128));
-          const float delta = be * (vv - al * u_k);
-          const float o = al * u_q + delta * s_kq[b];
-          *reinterpret_cast<__nv_bfloat16*>(od + b * 128) = __float2bfloat16_rn(delta);
-          *reinterpret_cast<__nv_bfloat16*>(oo + b * 128) = __float2bfloat16_rn(o);
-          const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row;
-          if (p.delta_dump) p.delta_dump[goff] = delta;
-          if (p.o_dump) p.o_dump[goff] = o;
-          if (p.x_inout) p.x_inout[goff] += o;
-        }
-      }
       tc::fence_proxy_async_smem();
-      tc::named_sync(1, 128);
+      tc::named_sync(1, kEpiThreads);
       if (ep == 0 && !dead) {
         tc::mbar_arrive(empty(s));  // value rows and records of stage s are consumed
         const uint32_t so = sOut0 + (uint32_t)(ob * OUT_BYTES);
@@ -397,7 +414,7 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
   TcReplayParams p{};
   p.R = a.R; p.H = a.H; p.t = a.t; p.W_t = a.W_t;
   p.n_tiles = (a.W_t + NB - 1) / NB;
-  p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES;
+  p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES + META_BYTES;
   const int static_bytes = 8 * 1024;
   const int budget = 227 * 1024 - static_bytes - 1024 - 2 * A_BYTES - 2 * OUT_BYTES;
   p.stages = budget / p.stage_bytes;
