@@ -34,16 +34,18 @@ namespace {
 
 constexpr int D = 128;            // head width (d_k = d_v)
 constexpr int NB = 32;            // beams per tile
-constexpr int kEpiWarps = 8;      // two per SM sub-partition; each owns 16 beams of a tile
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kScalWarps = 4;     // replay scalars, 8 beams each
+constexpr int kFoldWarps = 8;     // record fold + eq. 8, a 16-beam x 32-row block each
+constexpr int kThreads = 32 * (2 + kScalWarps + kFoldWarps);
 constexpr int kMaxDepth = 6;      // replay depths this kernel stages
 constexpr int A_BYTES = 2 * D * D;          // one bf16 half of S_ctx: 32 KiB
 constexpr int B_BYTES = 2 * NB * D * 2;     // q and k rows: 16 KiB
 constexpr int V_BYTES = NB * D * 2;         // value rows: 8 KiB
 constexpr int REC_BYTES = 2 * NB * D * 2;   // delta_j and k_j rows of one depth: 16 KiB
 constexpr int META_BYTES = 1024;            // per-beam gates and ancestors' decays
-constexpr int OUT_BYTES = 2 * NB * D * 2;   // delta_t and o_t tiles: 16 KiB
+constexpr int SCAL_BYTES = 4096;            // per-beam scalars for the fold
+constexpr int SUB_BYTES = 2 * 16 * 32 * 2;  // one fold warp's delta and o block: 2 KiB
+constexpr int OUT_BYTES = kFoldWarps * 2 * SUB_BYTES;  // double-buffered: 32 KiB
 constexpr int kMaxStages = 3;
 
 struct TcReplayParams {
@@ -71,15 +73,18 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
 
 __device__ __forceinline__ float bf(uint32_t x16) { return __uint_as_float(x16 << 16); }
 
+// Stage layout: [B: q rows | k rows, per 64-column block][V][REC per depth:
+// delta rows | k rows][META: (alpha_t, beta_t) per beam, alpha_j per beam and
+// depth][SCAL: (alpha_t, beta_t, k_t.q_t) per beam, (alpha_j, k_j.q_t, k_j.k_t)
+// per beam and depth].
+template <int TD>  // replay depth t of this call
 __global__ void __launch_bounds__(kThreads, 1)
     replay_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_oo, TcReplayParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 5];
-  __shared__ float4 s_beam[NB];             // (alpha_t, beta_t, k_t.q_t, -)
-  __shared__ float4 s_rec[NB][kMaxDepth];   // (alpha_j, k_j.q_t, k_j.k_t, -)
+  __shared__ __align__(8) uint64_t bars[3 * kMaxStages + 5];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -94,15 +99,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
   auto full = [&](int s) { return bar(s); };
   auto empty = [&](int s) { return bar(kMaxStages + s); };
-  auto tfull = [&](int a) { return bar(2 * kMaxStages + a); };
-  auto tempty = [&](int a) { return bar(2 * kMaxStages + 2 + a); };
-  const uint32_t drain_bar = bar(2 * kMaxStages + 4);
+  auto scal = [&](int s) { return bar(2 * kMaxStages + s); };
+  auto tfull = [&](int a) { return bar(3 * kMaxStages + a); };
+  auto tempty = [&](int a) { return bar(3 * kMaxStages + 2 + a); };
+  const uint32_t drain_bar = bar(3 * kMaxStages + 4);
   volatile int* abort = &s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x / p.H, h = blockIdx.x % p.H;
-  const int t = p.t;
-  const int meta_off = B_BYTES + V_BYTES + t * REC_BYTES;  // within a stage
+  constexpr int t = TD;
+  const int rec_off = B_BYTES + V_BYTES;
+  const int meta_off = rec_off + t * REC_BYTES;
+  const int scal_off = meta_off + META_BYTES;
 
   // ---- S_ctx of this (request, head) -> bf16 hi / lo A operands
   {
@@ -131,12 +139,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      tc::mbar_init(full(s), 32);  // every producer lane arrives after its stores and copies
-      tc::mbar_init(empty(s), 2);  // released by the MMA commit and by the epilogue
+      tc::mbar_init(full(s), 32);   // every producer lane arrives after its stores and copies
+      tc::mbar_init(empty(s), 1 + kScalWarps + kFoldWarps);  // MMA commit + readers
+      tc::mbar_init(scal(s), kScalWarps);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull(a), 1);
-      tc::mbar_init(tempty(a), kEpiWarps);
+      tc::mbar_init(tempty(a), kFoldWarps);
     }
     tc::mbar_init(drain_bar, 1);
     s_abort = 0;
@@ -159,11 +168,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < p.n_tiles; ++i) {
       const int s = i % p.stages;
       const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+      const int b0 = i * NB;
+      const int nb = min(NB, p.W_t - b0);
+      // ancestors' slots and gates of this tile, fetched before the stage frees
+      int slot[TD > 0 ? TD : 1];
+      float a_j[TD > 0 ? TD : 1];
+      float al = 0.f, be = 0.f;
+      if (lane < nb) {
+        const size_t row = (size_t)r * p.W_t + b0 + lane;
+        al = p.alpha[row * p.H + h];
+        be = p.beta[row * p.H + h];
+#pragma unroll
+        for (int j = 0; j < t; ++j) {
+          int sl = p.anc[row * p.anc_stride + j];
+          a_j[j] = -1.0f;  // marks a slot outside its depth: the record is skipped
+          if (sl < 0 || sl >= p.W_j[j]) {
+            raise_error(p.err, GDNBEAM_DERR_SLOT);
+            sl = 0;
+          } else {
+            a_j[j] = p.rec_a[j][((size_t)r * p.W_j[j] + sl) * p.H + h];
+          }
+          slot[j] = sl;
+        }
+      }
       int ok = 0;
       if (lane == 0) ok = tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // the whole warp stops together
-      const int b0 = i * NB;
-      const int nb = min(NB, p.W_t - b0);
       const uint32_t st = sStage0 + (uint32_t)(s * p.stage_bytes);
       uint8_t* gst = gStage0 + s * p.stage_bytes;
       if (lane == 0) {
@@ -177,22 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane < nb) {
-        const size_t row = (size_t)r * p.W_t + b0 + lane;
         float2* albe = reinterpret_cast<float2*>(gst + meta_off);
-        float* aj = reinterpret_cast<float*>(gst + meta_off + NB * 8);
-        albe[lane] = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
+        float* ajs = reinterpret_cast<float*>(gst + meta_off + NB * 8);
+        albe[lane] = make_float2(al, be);
+#pragma unroll
         for (int j = 0; j < t; ++j) {
-          int slot = p.anc[row * p.anc_stride + j];
-          float a = -1.0f;  // marks a slot outside its depth: the record is skipped
-          if (slot < 0 || slot >= p.W_j[j]) {
-            raise_error(p.err, GDNBEAM_DERR_SLOT);
-            slot = 0;
-          } else {
-            a = p.rec_a[j][((size_t)r * p.W_j[j] + slot) * p.H + h];
-          }
-          aj[lane * kMaxDepth + j] = a;
-          const size_t rec = ((size_t)r * p.W_j[j] + slot) * p.H + h;
-          const uint32_t dst = st + B_BYTES + V_BYTES + j * REC_BYTES + lane * (D * 2);
+          ajs[lane * kMaxDepth + j] = a_j[j];
+          const size_t rec = ((size_t)r * p.W_j[j] + slot[j]) * p.H + h;
+          const uint32_t dst = st + rec_off + j * REC_BYTES + lane * (D * 2);
           tc::bulk_load(dst, p.rec_d[j] + rec * D, D * 2, full(s));
           tc::bulk_load(dst + NB * D * 2, p.rec_k[j] + rec * D, D * 2, full(s));
         }
@@ -234,14 +256,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(drain_bar);
       tc::mbar_wait_drain(drain_bar, 0);
     }
+  } else if (warp < 2 + kScalWarps) {
+    // ---------------------------------------------------------------- replay scalars
+    // k_j.q_t, k_j.k_t (eqs. 6-7) and k_t.q_t (eq. 8) for 8 beams of each
+    // tile; lane l holds key columns 4l..4l+3.
+    const int sw = warp - 2;
+    const int c = lane * 4, kb = c >> 6, cc = c & 63;
+    for (int i = 0; i < p.n_tiles; ++i) {
+      const int s = i % p.stages;
+      const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+      const int nb = min(NB, p.W_t - i * NB);
+      int ok = 0;
+      if (lane == 0) ok = tc::mbar_wait_sleep(full(s), ph, abort, p.err) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const uint8_t* gst = gStage0 + s * p.stage_bytes;
+      const uint8_t* bk = gst + kb * (2 * NB * 128);
+      const float2* albe = reinterpret_cast<const float2*>(gst + meta_off);
+      const float* ajs = reinterpret_cast<const float*>(gst + meta_off + NB * 8);
+      float4* s_beam = reinterpret_cast<float4*>(const_cast<uint8_t*>(gst) + scal_off);
+      float4* s_rec = s_beam + NB;
+#pragma unroll 1
+      for (int bb = sw * 8; bb < sw * 8 + 8; bb += 2) {
+        // two beams at a time: load, multiply, then reduce all sums together
+        float part[2][1 + 2 * TD];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int b = min(bb + e, NB - 1);
+          const uint2 qw = *reinterpret_cast<const uint2*>(bk + sw128_off(b, cc));
+          const uint2 kw = *reinterpret_cast<const uint2*>(bk + sw128_off(NB + b, cc));
+          const float q4[4] = {bf(qw.x & 0xFFFF), bf(qw.x >> 16), bf(qw.y & 0xFFFF), bf(qw.y >> 16)};
+          const float k4[4] = {bf(kw.x & 0xFFFF), bf(kw.x >> 16), bf(kw.y & 0xFFFF), bf(kw.y >> 16)};
+          float kq = 0.f;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) kq = fmaf(k4[x], q4[x], kq);
+          part[e][0] = kq;
+#pragma unroll
+          for (int j = 0; j < t; ++j) {
+            float cq = 0.f, ck = 0.f;
+            const uint8_t* kr = gst + rec_off + j * REC_BYTES + NB * D * 2 + b * (D * 2);
+            const uint2 rw = *reinterpret_cast<const uint2*>(kr + c * 2);
+            const float r4[4] = {bf(rw.x & 0xFFFF), bf(rw.x >> 16), bf(rw.y & 0xFFFF), bf(rw.y >> 16)};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              cq = fmaf(r4[x], q4[x], cq);
+              ck = fmaf(r4[x], k4[x], ck);
+            }
+            part[e][1 + 2 * j] = cq;
+            part[e][2 + 2 * j] = ck;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int x = 0; x < 1 + 2 * TD; ++x)
+              part[e][x] += __shfl_xor_sync(0xffffffffu, part[e][x], o);
+        if (lane == 0) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int b = bb + e;
+            if (b >= nb) continue;
+            const float2 ab = albe[b];
+            s_beam[b] = make_float4(ab.x, ab.y, part[e][0], 0.f);
+#pragma unroll
+            for (int j = 0; j < t; ++j) {
+              const float a = ajs[b * kMaxDepth + j];
+              // a skipped record leaves both projections unchanged
+              s_rec[b * kMaxDepth + j] = a >= 0.f ? make_float4(a, part[e][1 + 2 * j], part[e][2 + 2 * j], 0.f)
+                                                  : make_float4(1.f, 0.f, 0.f, 0.f);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(scal(s));   // releases the scalars to the fold warps
+        tc::mbar_arrive(empty(s));  // this warp is done reading the stage
+      }
+    }
   } else {
-    // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;                   // 0..7
-    const int ep = threadIdx.x - 64;           // 0..255
-    const int hb = ew >> 2;                    // which 16 beams of a tile this warp folds
-    const int i_row = (warp & 3) * 32 + lane;  // value row = TMEM lane
+    // ---------------------------------------------------------------- fold + eq. 8
+    const int fw = warp - 2 - kScalWarps;        // 0..7
+    const int lg = warp & 3;                     // TMEM lane group
+    const int hb = fw >> 2;                      // beams hb*16 .. hb*16+15 of a tile
+    const int i_row = lg * 32 + lane;            // value row = TMEM lane
     const int half = i_row >> 6, col = i_row & 63;
-    bool dead = false;
     for (int i = 0; i < p.n_tiles; ++i) {
       const int s = i % p.stages;
       const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
@@ -250,114 +350,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ob = i & 1;
       const int b0 = i * NB;
       const int nb = min(NB, p.W_t - b0);
-      // A failed wait marks the warp dead: it then skips all work but keeps
-      // taking part in the named barriers, so no other epilogue warp waits
-      // on it forever.
-      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(full(s), ph, abort, p.err));
-      const uint8_t* gst = gStage0 + s * p.stage_bytes;
-      if (ep == 0) tc::bulk_wait_read<1>();  // out buffer ob is free again
-      // replay scalars: k_j.q_t, k_j.k_t (eqs. 6-7) and k_t.q_t (eq. 8)
-      const float2* albe = reinterpret_cast<const float2*>(gst + meta_off);
-      const float* ajs = reinterpret_cast<const float*>(gst + meta_off + NB * 8);
-      for (int b = ew; b < (dead ? 0 : nb); b += kEpiWarps) {
-        const int c = lane * 4;  // 4 key columns per lane
-        const int kb = c >> 6, cc = c & 63;
-        const uint8_t* bk = gst + kb * (2 * NB * 128);
-        const uint2 qw = *reinterpret_cast<const uint2*>(bk + sw128_off(b, cc));
-        const uint2 kw = *reinterpret_cast<const uint2*>(bk + sw128_off(NB + b, cc));
-        const float q4[4] = {bf(qw.x & 0xFFFF), bf(qw.x >> 16), bf(qw.y & 0xFFFF), bf(qw.y >> 16)};
-        const float k4[4] = {bf(kw.x & 0xFFFF), bf(kw.x >> 16), bf(kw.y & 0xFFFF), bf(kw.y >> 16)};
-        float kq = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) kq = fmaf(k4[e], q4[e], kq);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
-        if (lane == 0) {
-          const float2 ab = albe[b];
-          s_beam[b] = make_float4(ab.x, ab.y, kq, 0.f);
-        }
-        for (int j = 0; j < t; ++j) {
-          const uint8_t* kr = gst + B_BYTES + V_BYTES + j * REC_BYTES + NB * D * 2 + b * (D * 2);
-          const uint2 rw = *reinterpret_cast<const uint2*>(kr + c * 2);
-          const float r4[4] = {bf(rw.x & 0xFFFF), bf(rw.x >> 16), bf(rw.y & 0xFFFF), bf(rw.y >> 16)};
-          float cq = 0.f, ck = 0.f;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            cq = fmaf(r4[e], q4[e], cq);
-            ck = fmaf(r4[e], k4[e], ck);
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            cq += __shfl_xor_sync(0xffffffffu, cq, o);
-            ck += __shfl_xor_sync(0xffffffffu, ck, o);
-          }
-          if (lane == 0) {
-            const float a = ajs[b * kMaxDepth + j];
-            // a skipped record leaves both projections unchanged
-            s_rec[b][j] = a >= 0.f ? make_float4(a, cq, ck, 0.f) : make_float4(1.f, 0.f, 0.f, 0.f);
-          }
-        }
+      int ok = 0;
+      if (lane == 0) {
+        ok = tc::mbar_wait_sleep(full(s), ph, abort, p.err) &&
+             tc::mbar_wait_sleep(scal(s), ph, abort, p.err) &&
+             tc::mbar_wait_sleep(tfull(acc), aph, abort, p.err);
+        tc::bulk_wait_read<1>();  // this warp's out block ob is free again
       }
-      tc::named_sync(1, kEpiThreads);
-      // u_q, u_k of this warp's 16 beams for this thread's value row; fold
-      // the records and apply eq. 8
-      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(tfull(acc), aph, abort, p.err));
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       tc::fence_after_sync();
-      const uint32_t ta = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(acc * 2 * NB);
+      const uint8_t* gst = gStage0 + s * p.stage_bytes;
+      const float4* s_beam = reinterpret_cast<const float4*>(gst + scal_off);
+      const float4* s_rec = s_beam + NB;
+      const uint32_t ta = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * 2 * NB + hb * 16);
+      uint32_t uq[16], uk[16];
+      tc::tmem_ld16_nowait(ta, uq);
+      tc::tmem_ld16_nowait(ta + NB, uk);
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tempty(acc));
       const uint8_t* vt = gst + B_BYTES + half * (NB * 128) + col * 2;
-      const uint8_t* rd = gst + B_BYTES + V_BYTES + i_row * 2;
-      uint8_t* od = gOut0 + ob * OUT_BYTES + half * (NB * 128) + col * 2;
-      uint8_t* oo = od + NB * D * 2;
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        const int bb = hb * 16 + g * 4;
-        float uq4[4], uk4[4];
-        tc::tmem_ld4(ta + bb, uq4);
-        tc::tmem_ld4(ta + NB + bb, uk4);
+      const uint8_t* rd = gst + rec_off + i_row * 2;
+      uint8_t* sub = gOut0 + (fw * 2 + ob) * SUB_BYTES;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int b = bb + e;
-          if (!dead && b < nb) {
-            float u_q = uq4[e], u_k = uk4[e];
-            for (int j = 0; j < t; ++j) {
-              const float4 rc = s_rec[b][j];
-              const float dj = bf(*reinterpret_cast<const uint16_t*>(rd + j * REC_BYTES + b * (D * 2)));
-              u_q = fmaf(rc.x, u_q, dj * rc.y);
-              u_k = fmaf(rc.x, u_k, dj * rc.z);
-            }
-            const float4 bm = s_beam[b];
-            const float vv = bf(*reinterpret_cast<const uint16_t*>(vt + b * 128));
-            const float delta = bm.y * (vv - bm.x * u_k);
-            const float o = fmaf(bm.x, u_q, delta * bm.z);
-            *reinterpret_cast<__nv_bfloat16*>(od + b * 128) = __float2bfloat16_rn(delta);
-            *reinterpret_cast<__nv_bfloat16*>(oo + b * 128) = __float2bfloat16_rn(o);
-            if (p.delta_dump || p.o_dump || p.x_inout) {
-              const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row;
-              if (p.delta_dump) p.delta_dump[goff] = delta;
-              if (p.o_dump) p.o_dump[goff] = o;
-              if (p.x_inout) p.x_inout[goff] += o;
-            }
+      for (int e = 0; e < 16; ++e) {
+        const int b = hb * 16 + e;
+        if (b < nb) {
+          float u_q = __uint_as_float(uq[e]), u_k = __uint_as_float(uk[e]);
+#pragma unroll
+          for (int j = 0; j < t; ++j) {
+            const float4 rc = s_rec[b * kMaxDepth + j];
+            const float dj = bf(*reinterpret_cast<const uint16_t*>(rd + j * REC_BYTES + b * (D * 2)));
+            u_q = fmaf(rc.x, u_q, dj * rc.y);
+            u_k = fmaf(rc.x, u_k, dj * rc.z);
+          }
+          const float4 bm = s_beam[b];
+          const float vv = bf(*reinterpret_cast<const uint16_t*>(vt + b * 128));
+          const float delta = bm.y * (vv - bm.x * u_k);
+          const float o = fmaf(bm.x, u_q, delta * bm.z);
+          reinterpret_cast<__nv_bfloat16*>(sub)[e * 32 + lane] = __float2bfloat16_rn(delta);
+          reinterpret_cast<__nv_bfloat16*>(sub + SUB_BYTES / 2)[e * 32 + lane] = __float2bfloat16_rn(o);
+          if (p.delta_dump || p.o_dump || p.x_inout) {
+            const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row;
+            if (p.delta_dump) p.delta_dump[goff] = delta;
+            if (p.o_dump) p.o_dump[goff] = o;
+            if (p.x_inout) p.x_inout[goff] += o;
           }
         }
-      }
-      if (!dead) {
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tempty(acc));
       }
       tc::fence_proxy_async_smem();
-      tc::named_sync(1, kEpiThreads);
-      if (ep == 0 && !dead) {
-        tc::mbar_arrive(empty(s));  // value rows and records of stage s are consumed
-        const uint32_t so = sOut0 + (uint32_t)(ob * OUT_BYTES);
-        for (int hf = 0; hf < 2; ++hf) {
-          tc::tma_store_3d(&tm_do, h * D + hf * 64, b0, r, so + hf * (NB * 128));
-          tc::tma_store_3d(&tm_oo, h * D + hf * 64, b0, r, so + NB * D * 2 + hf * (NB * 128));
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(empty(s));  // this warp is done reading the stage
+        if (hb * 16 < nb) {
+          const uint32_t so = sOut0 + (uint32_t)((fw * 2 + ob) * SUB_BYTES);
+          tc::tma_store_3d(&tm_do, h * D + lg * 32, b0 + hb * 16, r, so);
+          tc::tma_store_3d(&tm_oo, h * D + lg * 32, b0 + hb * 16, r, so + SUB_BYTES / 2);
         }
         tc::bulk_commit();
       }
     }
-    if (ep == 0) tc::bulk_wait_all();
+    if (lane == 0) tc::bulk_wait_all();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -388,13 +442,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [R][W_t][H*128] bf16 as a 3-D map with a 64-column x 32-row x 1 box.
-bool beam_map(CUtensorMap* map, const void* ptr, int R, int W_t, int H, bool swizzle) {
+// [R][W_t][H*128] bf16 as a 3-D map with a box_cols x box_rows x 1 box.
+bool beam_map(CUtensorMap* map, const void* ptr, int R, int W_t, int H, bool swizzle,
+              int box_cols = 64, int box_rows = NB) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || ((uintptr_t)ptr & 15) != 0) return false;
   cuuint64_t dims[3] = {(cuuint64_t)H * D, (cuuint64_t)W_t, (cuuint64_t)R};
   cuuint64_t strides[2] = {(cuuint64_t)H * D * 2, (cuuint64_t)W_t * H * D * 2};
-  cuuint32_t box[3] = {64, NB, 1};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -414,9 +469,9 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
   TcReplayParams p{};
   p.R = a.R; p.H = a.H; p.t = a.t; p.W_t = a.W_t;
   p.n_tiles = (a.W_t + NB - 1) / NB;
-  p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES + META_BYTES;
-  const int static_bytes = 8 * 1024;
-  const int budget = 227 * 1024 - static_bytes - 1024 - 2 * A_BYTES - 2 * OUT_BYTES;
+  p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES + META_BYTES + SCAL_BYTES;
+  const int static_bytes = 1024;
+  const int budget = 227 * 1024 - static_bytes - 1024 - 2 * A_BYTES - OUT_BYTES;
   p.stages = budget / p.stage_bytes;
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 1) return launch_replay(GDNBEAM_BF16, a, s);
@@ -435,13 +490,22 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv, md, mo;
   if (!beam_map(&mq, a.q, a.R, a.W_t, a.H, true) || !beam_map(&mk, a.k, a.R, a.W_t, a.H, true) ||
       !beam_map(&mv, a.v, a.R, a.W_t, a.H, false) ||
-      !beam_map(&md, a.delta_out, a.R, a.W_t, a.H, false) ||
-      !beam_map(&mo, a.o_out, a.R, a.W_t, a.H, false))
+      !beam_map(&md, a.delta_out, a.R, a.W_t, a.H, false, 32, 16) ||
+      !beam_map(&mo, a.o_out, a.R, a.W_t, a.H, false, 32, 16))
     return GDNBEAM_ECUDA;
-  const size_t dyn = 1024 + 2 * A_BYTES + (size_t)p.stages * p.stage_bytes + 2 * OUT_BYTES;
-  GDN_CUDA(cudaFuncSetAttribute(replay_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)dyn));
-  replay_tc_kernel<<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, mv, md, mo, p);
+  const size_t dyn = 1024 + 2 * A_BYTES + (size_t)p.stages * p.stage_bytes + OUT_BYTES;
+  switch (a.t) {
+#define GDN_REPLAY_TC(TD_)                                                                   \
+  case TD_:                                                                                  \
+    GDN_CUDA(cudaFuncSetAttribute(replay_tc_kernel<TD_>,                                     \
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));   \
+    replay_tc_kernel<TD_><<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, mv, md, mo, p);           \
+    break;
+    GDN_REPLAY_TC(0) GDN_REPLAY_TC(1) GDN_REPLAY_TC(2) GDN_REPLAY_TC(3) GDN_REPLAY_TC(4)
+    GDN_REPLAY_TC(5) GDN_REPLAY_TC(6)
+#undef GDN_REPLAY_TC
+    default: return launch_replay(GDNBEAM_BF16, a, s);
+  }
   GDN_LAUNCH_CHECK();
   return GDNBEAM_OK;
 }
