@@ -34,31 +34,29 @@ namespace {
 
 constexpr int D = 128;            // head width (d_k = d_v)
 constexpr int NB = 32;            // beams per tile
-constexpr int kScalWarps = 4;     // replay scalars, 8 beams each
-constexpr int kFoldWarps = 8;     // record fold + eq. 8, a 16-beam x 32-row block each
-constexpr int kThreads = 32 * (2 + kScalWarps + kFoldWarps);
+constexpr int kEpiWarps = 8;      // two per SM sub-partition; each folds 16 beams of a tile
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kMaxDepth = 6;      // replay depths this kernel stages
 constexpr int A_BYTES = 2 * D * D;          // one bf16 half of S_ctx: 32 KiB
 constexpr int B_BYTES = 2 * NB * D * 2;     // q and k rows: 16 KiB
-constexpr int V_BYTES = NB * D * 2;         // value rows: 8 KiB
 constexpr int REC_BYTES = 2 * NB * D * 2;   // delta_j and k_j rows of one depth: 16 KiB
 constexpr int META_BYTES = 1024;            // per-beam gates and ancestors' decays
-constexpr int SCAL_BYTES = 4096;            // per-beam scalars for the fold
-constexpr int SUB_BYTES = 2 * 16 * 32 * 2;  // one fold warp's delta and o block: 2 KiB
-constexpr int OUT_BYTES = kFoldWarps * 2 * SUB_BYTES;  // double-buffered: 32 KiB
-constexpr int kMaxStages = 3;
+constexpr int kMaxStages = 4;
 
 struct TcReplayParams {
   int R, H, t, W_t, n_tiles, stages, stage_bytes;
   const float* sctx;
   long long sctx_rstride;
   const float *alpha, *beta;
+  const __nv_bfloat16* v;
   const __nv_bfloat16* rec_k[kMaxDepth];
   const __nv_bfloat16* rec_d[kMaxDepth];
   const float* rec_a[kMaxDepth];
   int W_j[kMaxDepth];
   const int32_t* anc;
   int anc_stride;
+  __nv_bfloat16 *delta_out, *o_out;
   float* x_inout;
   float *delta_dump, *o_dump;
   unsigned* err;
@@ -73,18 +71,18 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
 
 __device__ __forceinline__ float bf(uint32_t x16) { return __uint_as_float(x16 << 16); }
 
-// Stage layout: [B: q rows | k rows, per 64-column block][V][REC per depth:
+// Stage layout: [B: q rows | k rows, per 64-column block][REC per depth:
 // delta rows | k rows][META: (alpha_t, beta_t) per beam, alpha_j per beam and
-// depth][SCAL: (alpha_t, beta_t, k_t.q_t) per beam, (alpha_j, k_j.q_t, k_j.k_t)
-// per beam and depth].
+// depth (negative for a slot outside its depth)].
 template <int TD>  // replay depth t of this call
 __global__ void __launch_bounds__(kThreads, 1)
     replay_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_do,
-                     const __grid_constant__ CUtensorMap tm_oo, TcReplayParams p) {
+                     TcReplayParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[3 * kMaxStages + 5];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 6];
+  // replay scalars of two tiles (the fold reads one while the next is computed)
+  __shared__ float4 s_beam[2][NB];                              // (alpha_t, beta_t, k_t.q_t, -)
+  __shared__ float4 s_rec[2][NB][TD > 0 ? TD : 1];              // (alpha_j, k_j.q_t, k_j.k_t, -)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -93,67 +91,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA_hi = base, sA_lo = base + A_BYTES;
   const uint32_t sStage0 = base + 2 * A_BYTES;
-  const uint32_t sOut0 = sStage0 + (uint32_t)(p.stages * p.stage_bytes);
   uint8_t* gStage0 = gbase + 2 * A_BYTES;
-  uint8_t* gOut0 = gStage0 + p.stages * p.stage_bytes;
   auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
   auto full = [&](int s) { return bar(s); };
   auto empty = [&](int s) { return bar(kMaxStages + s); };
-  auto scal = [&](int s) { return bar(2 * kMaxStages + s); };
-  auto tfull = [&](int a) { return bar(3 * kMaxStages + a); };
-  auto tempty = [&](int a) { return bar(3 * kMaxStages + 2 + a); };
-  const uint32_t drain_bar = bar(3 * kMaxStages + 4);
+  auto tfull = [&](int a) { return bar(2 * kMaxStages + a); };
+  auto tempty = [&](int a) { return bar(2 * kMaxStages + 2 + a); };
+  const uint32_t a_ready = bar(2 * kMaxStages + 4);
+  const uint32_t drain_bar = bar(2 * kMaxStages + 5);
   volatile int* abort = &s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x / p.H, h = blockIdx.x % p.H;
   constexpr int t = TD;
-  const int rec_off = B_BYTES + V_BYTES;
+  const int rec_off = B_BYTES;
   const int meta_off = rec_off + t * REC_BYTES;
-  const int scal_off = meta_off + META_BYTES;
 
-  // ---- S_ctx of this (request, head) -> bf16 hi / lo A operands
-  {
-    const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * D * D;
-#pragma unroll 2
-    for (int u = threadIdx.x; u < D * (D / 8); u += kThreads) {
-      const int row = u >> 4, chunk = u & 15;  // 16 chunks of 8 columns per row
-      const float4 x0 = __ldg(reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8));
-      const float4 x1 = __ldg(reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8 + 4));
-      const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat16 h0 = __float2bfloat16_rn(xs[2 * e]), h1 = __float2bfloat16_rn(xs[2 * e + 1]);
-        __nv_bfloat16 l0 = __float2bfloat16_rn(xs[2 * e] - __bfloat162float(h0));
-        __nv_bfloat16 l1 = __float2bfloat16_rn(xs[2 * e + 1] - __bfloat162float(h1));
-        hi[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        lo[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-      }
-      const int kb = chunk >> 3, col = (chunk & 7) * 8;
-      const uint32_t off = (uint32_t)kb * (D * 128) + sw128_off(row, col);
-      *reinterpret_cast<uint4*>(gbase + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(gbase + A_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    tc::fence_proxy_async_smem();
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      tc::mbar_init(full(s), 32);   // every producer lane arrives after its stores and copies
-      tc::mbar_init(empty(s), 1 + kScalWarps + kFoldWarps);  // MMA commit + readers
-      tc::mbar_init(scal(s), kScalWarps);
+      tc::mbar_init(full(s), 32);  // every producer lane arrives after its stores and copies
+      tc::mbar_init(empty(s), 2);  // released by the MMA commit and by the epilogue
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull(a), 1);
-      tc::mbar_init(tempty(a), kFoldWarps);
+      tc::mbar_init(tempty(a), kEpiWarps);
     }
+    tc::mbar_init(a_ready, kEpiWarps);
     tc::mbar_init(drain_bar, 1);
     s_abort = 0;
     tc::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tc::tma_prefetch(&tm_q); tc::tma_prefetch(&tm_k); tc::tma_prefetch(&tm_v);
-    tc::tma_prefetch(&tm_do); tc::tma_prefetch(&tm_oo);
+    tc::tma_prefetch(&tm_q); tc::tma_prefetch(&tm_k);
   }
   if (warp == 1) tc::tmem_alloc(tc::smem_u32(&s_tmem), 128);
   tc::fence_before_sync();
@@ -163,14 +132,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    bool issued[kMaxStages] = {false, false, false};
-    uint32_t issued_ph[kMaxStages] = {0, 0, 0};
+    bool issued[kMaxStages] = {false, false, false, false};
+    uint32_t issued_ph[kMaxStages] = {0, 0, 0, 0};
     for (int i = 0; i < p.n_tiles; ++i) {
       const int s = i % p.stages;
       const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
       const int b0 = i * NB;
       const int nb = min(NB, p.W_t - b0);
-      // ancestors' slots and gates of this tile, fetched before the stage frees
+      // this tile's gates and ancestor slots, fetched before the stage frees
       int slot[TD > 0 ? TD : 1];
       float a_j[TD > 0 ? TD : 1];
       float al = 0.f, be = 0.f;
@@ -197,12 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st = sStage0 + (uint32_t)(s * p.stage_bytes);
       uint8_t* gst = gStage0 + s * p.stage_bytes;
       if (lane == 0) {
-        tc::mbar_expect_tx(full(s), (uint32_t)(B_BYTES + V_BYTES + t * nb * 2 * D * 2));
+        tc::mbar_expect_tx(full(s), (uint32_t)(B_BYTES + t * nb * 2 * D * 2));
         for (int kb = 0; kb < 2; ++kb) {
           const uint32_t bk = st + kb * (2 * NB * 128);
           tc::tma_load_3d(bk, &tm_q, h * D + kb * 64, b0, r, full(s));
           tc::tma_load_3d(bk + NB * 128, &tm_k, h * D + kb * 64, b0, r, full(s));
-          tc::tma_load_3d(st + B_BYTES + kb * (NB * 128), &tm_v, h * D + kb * 64, b0, r, full(s));
         }
       }
       __syncwarp();
@@ -229,7 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(D, 2 * NB);
-      for (int i = 0; i < p.n_tiles; ++i) {
+      bool ok = tc::mbar_wait_sleep(a_ready, 0, abort, p.err);
+      for (int i = 0; ok && i < p.n_tiles; ++i) {
         const int s = i % p.stages;
         const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
         const int acc = i & 1;
@@ -256,162 +225,191 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(drain_bar);
       tc::mbar_wait_drain(drain_bar, 0);
     }
-  } else if (warp < 2 + kScalWarps) {
-    // ---------------------------------------------------------------- replay scalars
-    // k_j.q_t, k_j.k_t (eqs. 6-7) and k_t.q_t (eq. 8) for 8 beams of each
-    // tile; lane l holds key columns 4l..4l+3.
-    const int sw = warp - 2;
-    const int c = lane * 4, kb = c >> 6, cc = c & 63;
-    for (int i = 0; i < p.n_tiles; ++i) {
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int ew = warp - 2;                   // 0..7
+    const int ep = threadIdx.x - 64;           // 0..255
+    const int hb = ew >> 2;                    // which 16 beams of a tile this warp folds
+    const int lg = warp & 3;                   // TMEM lane group
+    const int i_row = lg * 32 + lane;          // value row = TMEM lane
+
+    // S_ctx of this (request, head) -> bf16 hi / lo A operands, while the
+    // producer already streams the first tiles
+    {
+      const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * D * D;
+      constexpr int kUnits = D * (D / 8) / kEpiThreads;  // 8 row-chunks per thread
+      float4 xv[kUnits][2];
+#pragma unroll
+      for (int k = 0; k < kUnits; ++k) {
+        const int u = ep + k * kEpiThreads, row = u >> 4, chunk = u & 15;
+        xv[k][0] = __ldg(reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8));
+        xv[k][1] = __ldg(reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8 + 4));
+      }
+#pragma unroll
+      for (int k = 0; k < kUnits; ++k) {
+        const int u = ep + k * kEpiThreads, row = u >> 4, chunk = u & 15;
+        const float xs[8] = {xv[k][0].x, xv[k][0].y, xv[k][0].z, xv[k][0].w,
+                             xv[k][1].x, xv[k][1].y, xv[k][1].z, xv[k][1].w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat16 h0 = __float2bfloat16_rn(xs[2 * e]), h1 = __float2bfloat16_rn(xs[2 * e + 1]);
+          __nv_bfloat16 l0 = __float2bfloat16_rn(xs[2 * e] - __bfloat162float(h0));
+          __nv_bfloat16 l1 = __float2bfloat16_rn(xs[2 * e + 1] - __bfloat162float(h1));
+          hi[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+          lo[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+        }
+        const int kb = chunk >> 3, col = (chunk & 7) * 8;
+        const uint32_t off = (uint32_t)kb * (D * 128) + sw128_off(row, col);
+        *reinterpret_cast<uint4*>(gbase + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(gbase + A_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(a_ready);
+    }
+
+    // replay scalars k_j.q_t, k_j.k_t (eqs. 6-7) and k_t.q_t (eq. 8) of tile
+    // i into buffer i & 1; warp ew takes beams ew, ew + 8, ew + 16, ew + 24
+    auto scalars = [&](int i) -> bool {
       const int s = i % p.stages;
       const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
       const int nb = min(NB, p.W_t - i * NB);
-      int ok = 0;
-      if (lane == 0) ok = tc::mbar_wait_sleep(full(s), ph, abort, p.err) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (__any_sync(0xffffffffu, !tc::mbar_wait_sleep(full(s), ph, abort, p.err))) return false;
       const uint8_t* gst = gStage0 + s * p.stage_bytes;
-      const uint8_t* bk = gst + kb * (2 * NB * 128);
       const float2* albe = reinterpret_cast<const float2*>(gst + meta_off);
       const float* ajs = reinterpret_cast<const float*>(gst + meta_off + NB * 8);
-      float4* s_beam = reinterpret_cast<float4*>(const_cast<uint8_t*>(gst) + scal_off);
-      float4* s_rec = s_beam + NB;
-#pragma unroll 1
-      for (int bb = sw * 8; bb < sw * 8 + 8; bb += 2) {
-        // two beams at a time: load, multiply, then reduce all sums together
-        float part[2][1 + 2 * TD];
+      const int c = lane * 4, kb = c >> 6, cc = c & 63;
+      const uint8_t* bk = gst + kb * (2 * NB * 128);
+      float part[4][1 + 2 * TD];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int b = min(bb + e, NB - 1);
-          const uint2 qw = *reinterpret_cast<const uint2*>(bk + sw128_off(b, cc));
-          const uint2 kw = *reinterpret_cast<const uint2*>(bk + sw128_off(NB + b, cc));
-          const float q4[4] = {bf(qw.x & 0xFFFF), bf(qw.x >> 16), bf(qw.y & 0xFFFF), bf(qw.y >> 16)};
-          const float k4[4] = {bf(kw.x & 0xFFFF), bf(kw.x >> 16), bf(kw.y & 0xFFFF), bf(kw.y >> 16)};
-          float kq = 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const int b = ew + 8 * e;
+        const uint2 qw = *reinterpret_cast<const uint2*>(bk + sw128_off(b, cc));
+        const uint2 kw = *reinterpret_cast<const uint2*>(bk + sw128_off(NB + b, cc));
+        const float q4[4] = {bf(qw.x & 0xFFFF), bf(qw.x >> 16), bf(qw.y & 0xFFFF), bf(qw.y >> 16)};
+        const float k4[4] = {bf(kw.x & 0xFFFF), bf(kw.x >> 16), bf(kw.y & 0xFFFF), bf(kw.y >> 16)};
+        float kq = 0.f;
 #pragma unroll
-          for (int x = 0; x < 4; ++x) kq = fmaf(k4[x], q4[x], kq);
-          part[e][0] = kq;
+        for (int x = 0; x < 4; ++x) kq = fmaf(k4[x], q4[x], kq);
+        part[e][0] = kq;
+#pragma unroll
+        for (int j = 0; j < t; ++j) {
+          const uint8_t* kr = gst + rec_off + j * REC_BYTES + NB * D * 2 + b * (D * 2);
+          const uint2 rw = *reinterpret_cast<const uint2*>(kr + c * 2);
+          const float r4[4] = {bf(rw.x & 0xFFFF), bf(rw.x >> 16), bf(rw.y & 0xFFFF), bf(rw.y >> 16)};
+          float cq = 0.f, ck = 0.f;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            cq = fmaf(r4[x], q4[x], cq);
+            ck = fmaf(r4[x], k4[x], ck);
+          }
+          part[e][1 + 2 * j] = cq;
+          part[e][2 + 2 * j] = ck;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int x = 0; x < 1 + 2 * TD; ++x)
+            part[e][x] += __shfl_xor_sync(0xffffffffu, part[e][x], o);
+      if (lane == 0) {
+        const int sb = i & 1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int b = ew + 8 * e;
+          if (b >= nb) continue;
+          const float2 ab = albe[b];
+          s_beam[sb][b] = make_float4(ab.x, ab.y, part[e][0], 0.f);
 #pragma unroll
           for (int j = 0; j < t; ++j) {
-            float cq = 0.f, ck = 0.f;
-            const uint8_t* kr = gst + rec_off + j * REC_BYTES + NB * D * 2 + b * (D * 2);
-            const uint2 rw = *reinterpret_cast<const uint2*>(kr + c * 2);
-            const float r4[4] = {bf(rw.x & 0xFFFF), bf(rw.x >> 16), bf(rw.y & 0xFFFF), bf(rw.y >> 16)};
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              cq = fmaf(r4[x], q4[x], cq);
-              ck = fmaf(r4[x], k4[x], ck);
-            }
-            part[e][1 + 2 * j] = cq;
-            part[e][2 + 2 * j] = ck;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-#pragma unroll
-            for (int x = 0; x < 1 + 2 * TD; ++x)
-              part[e][x] += __shfl_xor_sync(0xffffffffu, part[e][x], o);
-        if (lane == 0) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int b = bb + e;
-            if (b >= nb) continue;
-            const float2 ab = albe[b];
-            s_beam[b] = make_float4(ab.x, ab.y, part[e][0], 0.f);
-#pragma unroll
-            for (int j = 0; j < t; ++j) {
-              const float a = ajs[b * kMaxDepth + j];
-              // a skipped record leaves both projections unchanged
-              s_rec[b * kMaxDepth + j] = a >= 0.f ? make_float4(a, part[e][1 + 2 * j], part[e][2 + 2 * j], 0.f)
-                                                  : make_float4(1.f, 0.f, 0.f, 0.f);
-            }
+            const float a = ajs[b * kMaxDepth + j];
+            // a skipped record leaves both projections unchanged
+            s_rec[sb][b][j] = a >= 0.f ? make_float4(a, part[e][1 + 2 * j], part[e][2 + 2 * j], 0.f)
+                                       : make_float4(1.f, 0.f, 0.f, 0.f);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(scal(s));   // releases the scalars to the fold warps
-        tc::mbar_arrive(empty(s));  // this warp is done reading the stage
-      }
-    }
-  } else {
-    // ---------------------------------------------------------------- fold + eq. 8
-    const int fw = warp - 2 - kScalWarps;        // 0..7
-    const int lg = warp & 3;                     // TMEM lane group
-    const int hb = fw >> 2;                      // beams hb*16 .. hb*16+15 of a tile
-    const int i_row = lg * 32 + lane;            // value row = TMEM lane
-    const int half = i_row >> 6, col = i_row & 63;
-    for (int i = 0; i < p.n_tiles; ++i) {
-      const int s = i % p.stages;
-      const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
-      const int acc = i & 1;
-      const uint32_t aph = (uint32_t)(i >> 1) & 1u;
-      const int ob = i & 1;
-      const int b0 = i * NB;
-      const int nb = min(NB, p.W_t - b0);
-      int ok = 0;
-      if (lane == 0) {
-        ok = tc::mbar_wait_sleep(full(s), ph, abort, p.err) &&
-             tc::mbar_wait_sleep(scal(s), ph, abort, p.err) &&
-             tc::mbar_wait_sleep(tfull(acc), aph, abort, p.err);
-        tc::bulk_wait_read<1>();  // this warp's out block ob is free again
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      tc::fence_after_sync();
-      const uint8_t* gst = gStage0 + s * p.stage_bytes;
-      const float4* s_beam = reinterpret_cast<const float4*>(gst + scal_off);
-      const float4* s_rec = s_beam + NB;
-      const uint32_t ta = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * 2 * NB + hb * 16);
-      uint32_t uq[16], uk[16];
-      tc::tmem_ld16_nowait(ta, uq);
-      tc::tmem_ld16_nowait(ta + NB, uk);
-      tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tempty(acc));
-      const uint8_t* vt = gst + B_BYTES + half * (NB * 128) + col * 2;
-      const uint8_t* rd = gst + rec_off + i_row * 2;
-      uint8_t* sub = gOut0 + (fw * 2 + ob) * SUB_BYTES;
+      return true;
+    };
+
+    // this thread's value entries of its 16 beams of tile i, loaded one tile
+    // ahead so the fold never waits on them
+    auto load_values = [&](int i, uint16_t (&vr)[16]) {
+      const int b0 = i * NB, nb = min(NB, p.W_t - b0);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int b = hb * 16 + e;
-        if (b < nb) {
-          float u_q = __uint_as_float(uq[e]), u_k = __uint_as_float(uk[e]);
+        vr[e] = b < nb ? __ldg(reinterpret_cast<const uint16_t*>(
+                             p.v + (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row))
+                       : (uint16_t)0;
+      }
+    };
+    uint16_t vraw[16];
+    if (p.n_tiles > 0) load_values(0, vraw);
+
+    // A failed wait marks the epilogue dead: it then skips all work but keeps
+    // taking part in the named barriers, so no epilogue warp waits forever.
+    bool dead = p.n_tiles > 0 ? !scalars(0) : false;
+    tc::named_sync(1, kEpiThreads);
+    for (int i = 0; i < p.n_tiles; ++i) {
+      const int s = i % p.stages;
+      const int acc = i & 1;
+      const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+      const int sb = i & 1;
+      const int b0 = i * NB;
+      const int nb = min(NB, p.W_t - b0);
+      uint16_t vnext[16];
+      if (i + 1 < p.n_tiles) load_values(i + 1, vnext);
+      if (!dead && i + 1 < p.n_tiles) dead = !scalars(i + 1);
+      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(tfull(acc), aph, abort, p.err));
+      if (!dead) {
+        tc::fence_after_sync();
+        const uint8_t* gst = gStage0 + s * p.stage_bytes;
+        const uint32_t ta = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * 2 * NB + hb * 16);
+        uint32_t uq[16], uk[16];
+        tc::tmem_ld16_nowait(ta, uq);
+        tc::tmem_ld16_nowait(ta + NB, uk);
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tempty(acc));
+        const uint8_t* rd = gst + rec_off + i_row * 2;
 #pragma unroll
-          for (int j = 0; j < t; ++j) {
-            const float4 rc = s_rec[b * kMaxDepth + j];
-            const float dj = bf(*reinterpret_cast<const uint16_t*>(rd + j * REC_BYTES + b * (D * 2)));
-            u_q = fmaf(rc.x, u_q, dj * rc.y);
-            u_k = fmaf(rc.x, u_k, dj * rc.z);
-          }
-          const float4 bm = s_beam[b];
-          const float vv = bf(*reinterpret_cast<const uint16_t*>(vt + b * 128));
-          const float delta = bm.y * (vv - bm.x * u_k);
-          const float o = fmaf(bm.x, u_q, delta * bm.z);
-          reinterpret_cast<__nv_bfloat16*>(sub)[e * 32 + lane] = __float2bfloat16_rn(delta);
-          reinterpret_cast<__nv_bfloat16*>(sub + SUB_BYTES / 2)[e * 32 + lane] = __float2bfloat16_rn(o);
-          if (p.delta_dump || p.o_dump || p.x_inout) {
+        for (int e = 0; e < 16; ++e) {
+          const int b = hb * 16 + e;
+          if (b < nb) {
+            float u_q = __uint_as_float(uq[e]), u_k = __uint_as_float(uk[e]);
+#pragma unroll
+            for (int j = 0; j < t; ++j) {
+              const float4 rc = s_rec[sb][b][j];
+              const float dj = bf(*reinterpret_cast<const uint16_t*>(rd + j * REC_BYTES + b * (D * 2)));
+              u_q = fmaf(rc.x, u_q, dj * rc.y);
+              u_k = fmaf(rc.x, u_k, dj * rc.z);
+            }
+            const float4 bm = s_beam[sb][b];
+            const float vv = bf(vraw[e]);
+            const float delta = bm.y * (vv - bm.x * u_k);
+            const float o = fmaf(bm.x, u_q, delta * bm.z);
             const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row;
+            p.delta_out[goff] = __float2bfloat16_rn(delta);
+            p.o_out[goff] = __float2bfloat16_rn(o);
             if (p.delta_dump) p.delta_dump[goff] = delta;
             if (p.o_dump) p.o_dump[goff] = o;
             if (p.x_inout) p.x_inout[goff] += o;
           }
         }
       }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(empty(s));  // this warp is done reading the stage
-        if (hb * 16 < nb) {
-          const uint32_t so = sOut0 + (uint32_t)((fw * 2 + ob) * SUB_BYTES);
-          tc::tma_store_3d(&tm_do, h * D + lg * 32, b0 + hb * 16, r, so);
-          tc::tma_store_3d(&tm_oo, h * D + lg * 32, b0 + hb * 16, r, so + SUB_BYTES / 2);
-        }
-        tc::bulk_commit();
+      // every epilogue warp is done with stage s and with scalar buffer sb
+      tc::named_sync(1, kEpiThreads);
+      if (ep == 0 && !dead) tc::mbar_arrive(empty(s));
+      if (i + 1 < p.n_tiles) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) vraw[e] = vnext[e];
       }
     }
-    if (lane == 0) tc::bulk_wait_all();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -469,14 +467,15 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
   TcReplayParams p{};
   p.R = a.R; p.H = a.H; p.t = a.t; p.W_t = a.W_t;
   p.n_tiles = (a.W_t + NB - 1) / NB;
-  p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES + META_BYTES + SCAL_BYTES;
-  const int static_bytes = 1024;
-  const int budget = 227 * 1024 - static_bytes - 1024 - 2 * A_BYTES - OUT_BYTES;
+  p.stage_bytes = B_BYTES + a.t * REC_BYTES + META_BYTES;
+  const int static_bytes = 8 * 1024;  // scalar buffers and barriers
+  const int budget = 227 * 1024 - static_bytes - 1024 - 2 * A_BYTES;
   p.stages = budget / p.stage_bytes;
   if (p.stages > kMaxStages) p.stages = kMaxStages;
-  if (p.stages < 1) return launch_replay(GDNBEAM_BF16, a, s);
+  if (p.stages < 2) return launch_replay(GDNBEAM_BF16, a, s);
   p.sctx = a.sctx; p.sctx_rstride = a.sctx_rstride;
   p.alpha = a.alpha; p.beta = a.beta;
+  p.v = (const __nv_bfloat16*)a.v;
   for (int j = 0; j < a.t; ++j) {
     p.rec_k[j] = (const __nv_bfloat16*)a.depth[j].k;
     p.rec_d[j] = (const __nv_bfloat16*)a.depth[j].delta;
@@ -485,21 +484,19 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
     if (((uintptr_t)p.rec_k[j] & 15) || ((uintptr_t)p.rec_d[j] & 15)) return GDNBEAM_EINVAL;
   }
   p.anc = a.anc; p.anc_stride = a.anc_stride;
+  p.delta_out = (__nv_bfloat16*)a.delta_out; p.o_out = (__nv_bfloat16*)a.o_out;
   p.x_inout = a.x_inout; p.delta_dump = a.delta_dump; p.o_dump = a.o_dump; p.err = a.err;
   if (((uintptr_t)a.sctx & 15) || (a.sctx_rstride % 4) != 0) return GDNBEAM_EINVAL;
-  CUtensorMap mq, mk, mv, md, mo;
-  if (!beam_map(&mq, a.q, a.R, a.W_t, a.H, true) || !beam_map(&mk, a.k, a.R, a.W_t, a.H, true) ||
-      !beam_map(&mv, a.v, a.R, a.W_t, a.H, false) ||
-      !beam_map(&md, a.delta_out, a.R, a.W_t, a.H, false, 32, 16) ||
-      !beam_map(&mo, a.o_out, a.R, a.W_t, a.H, false, 32, 16))
+  CUtensorMap mq, mk;
+  if (!beam_map(&mq, a.q, a.R, a.W_t, a.H, true) || !beam_map(&mk, a.k, a.R, a.W_t, a.H, true))
     return GDNBEAM_ECUDA;
-  const size_t dyn = 1024 + 2 * A_BYTES + (size_t)p.stages * p.stage_bytes + OUT_BYTES;
+  const size_t dyn = 1024 + 2 * A_BYTES + (size_t)p.stages * p.stage_bytes;
   switch (a.t) {
 #define GDN_REPLAY_TC(TD_)                                                                   \
   case TD_:                                                                                  \
     GDN_CUDA(cudaFuncSetAttribute(replay_tc_kernel<TD_>,                                     \
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));   \
-    replay_tc_kernel<TD_><<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, mv, md, mo, p);           \
+    replay_tc_kernel<TD_><<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, p);                       \
     break;
     GDN_REPLAY_TC(0) GDN_REPLAY_TC(1) GDN_REPLAY_TC(2) GDN_REPLAY_TC(3) GDN_REPLAY_TC(4)
     GDN_REPLAY_TC(5) GDN_REPLAY_TC(6)
