@@ -294,6 +294,29 @@ int gdnbeam_select_topw(int R, int W_t, int W_next, int V, int dtype, const void
                         int32_t* parents, int32_t* tokens, float* cum_next,
                         void* scratch, size_t scratch_bytes, gdnbeam_stream_t stream);
 
+/* The same selection as gdnbeam_select_topw for callers that cannot allocate
+ * device memory: a plugin that its host framework calls with only its input
+ * and output tensors, or a process whose device memory another allocator has
+ * fully reserved, has no way to pass the scratch buffer that call needs. This
+ * variant takes no scratch and allocates nothing; it uses a fixed area of
+ * gdnbeam_select_noalloc_max_bytes() bytes (16 MiB) that the library keeps on
+ * every device where it is loaded, until the process exits. (The pages have no
+ * counterpart: this is a deployment convenience, not part of the method.)
+ *   - Selections whose scratch (gdnbeam_select_scratch_bytes) exceeds that
+ *     size are refused with GDNBEAM_EWORKSPACE before anything is launched.
+ *   - The first call on each device looks up the area's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the one area, and its contents persist between calls;
+ *     every call resets the counters it relies on before use. Calls whose
+ *     work overlaps on the GPU (other streams, other host threads) race on
+ *     the area: order them on one stream or synchronise between them.
+ * Arguments, outputs and errors are those of gdnbeam_select_topw. */
+size_t gdnbeam_select_noalloc_max_bytes(void);
+int gdnbeam_select_topw_noalloc(int R, int W_t, int W_next, int V, int dtype, const void* logits,
+                                const float* lse, const float* cum, const float* bias,
+                                int32_t* parents, int32_t* tokens, float* cum_next,
+                                gdnbeam_stream_t stream);
+
 /* Ancestry-index update of OneLA §2.4 eq. 9 for decode call t:
  *   anc_out[r*W_t+b][j] = anc_prev[r*W_prev+p][j] (j < t-1), anc_out[..][t-1] = p,
  *   with p = parents[r*W_t+b]; sid_out[..][s] = sid_prev[..p..][s] (s < t),

@@ -89,6 +89,8 @@ _SIGS = {
     "gdnbeam_logits": (_I, [C.POINTER(Config), _I, _P, _P, _P, _P, _P, _SZ, C.POINTER(Dumps), _S]),
     "gdnbeam_select_scratch_bytes": (_SZ, [_I, _I, _I, _I]),
     "gdnbeam_select_topw": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _S]),
+    "gdnbeam_select_noalloc_max_bytes": (_SZ, []),
+    "gdnbeam_select_topw_noalloc": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _S]),
     "gdnbeam_ancestry": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S]),
     "gdnbeam_prefill_scan": (_I, [C.POINTER(Config), _I, _P, _P, _P, _P, _P, _P, _LL, _P, _P, _S]),
 }

@@ -58,6 +58,8 @@ int validate(const gdnbeam_config* c) {
 
 }  // namespace
 
+unsigned* gdnbeam::error_word() { return err_ptr(); }
+
 struct gdnbeam_ctx {
   gdnbeam_config c;
   gdnbeam_weights w;

@@ -79,6 +79,9 @@ int launch_select(int R, int W_t, int W_next, int V, int dtype, const void* logi
 int launch_tile_max(int dtype, int n, int V, const void* z, float2* hint, cudaStream_t s);
 constexpr int kHintTile = 256;
 
+// Device error word of the current device (defined with the C ABI).
+unsigned* error_word();
+
 int launch_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int32_t* parents,
                     const int32_t* tokens, const int32_t* anc_prev, const int32_t* sid_prev,
                     int32_t* anc_out, int32_t* sid_out, unsigned* err, cudaStream_t s);
