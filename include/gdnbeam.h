@@ -81,6 +81,10 @@ typedef struct gdnbeam_config {
   int L_max;    /* longest prompt gdnbeam_prefill_state accepts */
   int dtype;    /* GDNBEAM_F32 or GDNBEAM_BF16 storage */
   int residual; /* 0: single layer; 1: residual stream + RMSNorm glue */
+  int state_path; /* 0: shared context + records + projection replay (OneLA);
+                     1: FullState baseline, one d_v x d_k state per beam copied
+                        on reorder (OneLA §3 "Controlled FullState"): same
+                        pipeline, only the state path swapped */
 } gdnbeam_config;
 
 /* Weights, storage type, row-major, owned by the caller and kept alive for

@@ -51,6 +51,7 @@ int validate(const gdnbeam_config* c) {
   if (!c->residual && c->layers != 1) return GDNBEAM_EUNSUPPORTED;
   if (c->residual && c->H * c->d_v != c->d_model) return GDNBEAM_EUNSUPPORTED;
   if ((long long)c->W_max * c->V >= (1ll << 31)) return GDNBEAM_EUNSUPPORTED;
+  if (c->state_path != 0 && c->state_path != 1) return GDNBEAM_EUNSUPPORTED;
   if ((long long)c->R * c->L_max >= (1ll << 31) || (long long)c->R * c->W_max * c->V >= (1ll << 40))
     return GDNBEAM_EUNSUPPORTED;
   return GDNBEAM_OK;
@@ -89,6 +90,7 @@ struct gdnbeam_ctx {
                    // sum of exp(z - max), left by the logits stage
   const void* last_logits;  // logits buffer the last logits stage wrote
   int last_rows;
+  void* states[2];  // FullState baseline: [R*W_max][layers][H][d_v][d_k] per buffer
   // prefill buffers for R*L_max rows
   void *pf_u, *pf_q, *pf_k, *pf_v, *pf_feat;
   float *pf_x, *pf_alpha, *pf_beta;
@@ -189,6 +191,9 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
   char* p_gemm = take(gemm_b);
   const int n_hint_tiles = (c.V + kHintTile - 1) / kHintTile;
   char* p_tst = take((rows > (size_t)c.R ? rows : (size_t)c.R) * n_hint_tiles * sizeof(float2));
+  const size_t st_b = c.state_path ? rows * c.layers * c.H * c.d_v * c.d_k * es : 0;
+  char* p_st0 = take(st_b);
+  char* p_st1 = take(st_b);
   char* p_pfu = take(pf_rows * c.d_model * es);
   char* p_pfx = take(c.residual ? pf_rows * c.d_model * sizeof(float) : 0);
   char* p_pfq = take(pf_rows * c.H * c.d_k * es);
@@ -204,6 +209,7 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
     x->u = p_u; x->x = (float*)p_x; x->q = p_q; x->v = p_v; x->beta = (float*)p_beta;
     x->o = p_o; x->sel = p_sel; x->sel_bytes = sel_b; x->gemm = p_gemm; x->gemm_bytes = gemm_b;
     x->tstats = (float2*)p_tst; x->last_logits = nullptr; x->last_rows = 0;
+    x->states[0] = p_st0; x->states[1] = p_st1;
     x->pf_u = p_pfu; x->pf_x = (float*)p_pfx; x->pf_q = p_pfq; x->pf_k = p_pfk;
     x->pf_v = p_pfv; x->pf_alpha = (float*)p_pfa; x->pf_beta = (float*)p_pfb; x->pf_feat = p_pff;
   }
@@ -310,8 +316,12 @@ int gdnbeam_create(const gdnbeam_config* cfg, const gdnbeam_weights* w, void* wo
   x->tc_gemm = tc;
   x->tc_replay = tc_replay_supported(cfg->dtype, cfg->d_k, cfg->d_v);
   carve(*cfg, tc, (char*)workspace, x, nullptr);
-  snprintf(x->variant, sizeof(x->variant), "proj=%s replay=%s logits=%s select=radix2",
-           tc ? "tc" : "simt", x->tc_replay ? "tc" : "simt", tc ? "tc" : "simt");
+  if (cfg->state_path)
+    snprintf(x->variant, sizeof(x->variant), "proj=%s state=fullstate logits=%s select=bound",
+             tc ? "tc" : "simt", tc ? "tc" : "simt");
+  else
+    snprintf(x->variant, sizeof(x->variant), "proj=%s replay=%s logits=%s select=bound",
+             tc ? "tc" : "simt", x->tc_replay ? "tc" : "simt", tc ? "tc" : "simt");
   x->prefilled = 0;
   x->last_step = -1;
   *out = x;
@@ -442,7 +452,20 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
     a.delta_dump = ld.delta; a.o_dump = ld.o;
     a.err = err;
     ev = ctx->tic(GDNBEAM_STAGE_REPLAY, s);
-    st = ctx->tc_replay ? launch_tc_replay(a, s) : launch_replay(c.dtype, a, s);
+    if (c.state_path) {
+      FullStateArgs f{};
+      f.R = c.R; f.H = c.H; f.d_k = c.d_k; f.d_v = c.d_v; f.t = t; f.W_t = W_t;
+      f.W_prev = W_prev; f.layers = c.layers; f.layer = layer;
+      f.sctx = a.sctx; f.sctx_rstride = a.sctx_rstride;
+      f.states_prev = ctx->states[cur ^ 1]; f.states_cur = ctx->states[cur];
+      f.parents = parents;
+      f.q = a.q; f.k = a.k; f.v = a.v; f.alpha = a.alpha; f.beta = a.beta;
+      f.delta_out = a.delta_out; f.o_out = a.o_out; f.x_inout = a.x_inout;
+      f.delta_dump = a.delta_dump; f.o_dump = a.o_dump; f.err = err;
+      st = launch_fullstate(c.dtype, f, s);
+    } else {
+      st = ctx->tc_replay ? launch_tc_replay(a, s) : launch_replay(c.dtype, a, s);
+    }
     ctx->toc(ev, s);
     if (st) return st;
   }

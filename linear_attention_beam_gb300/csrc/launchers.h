@@ -64,6 +64,23 @@ int launch_replay(int dtype, const ReplayArgs& a, cudaStream_t s);
 bool tc_replay_supported(int dtype, int d_k, int d_v);
 int launch_tc_replay(const ReplayArgs& a, cudaStream_t s);
 
+// FullState baseline step for one layer (one d_v x d_k state per beam).
+struct FullStateArgs {
+  int R, H, d_k, d_v, t, W_t, W_prev, layers, layer;
+  const float* sctx;           // fp32 [R][...], request stride sctx_rstride (t = 0 parents)
+  long long sctx_rstride;
+  const void* states_prev;     // storage [R*W_prev][layers][H][d_v][d_k]
+  void* states_cur;            // storage [R*W_t][layers][H][d_v][d_k]
+  const int32_t* parents;      // [R*W_t] rows of the previous call (t >= 1)
+  const void *q, *k, *v;
+  const float *alpha, *beta;
+  void *delta_out, *o_out;
+  float* x_inout;
+  float *delta_dump, *o_dump;
+  unsigned* err;
+};
+int launch_fullstate(int dtype, const FullStateArgs& a, cudaStream_t s);
+
 int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const void* k,
                         const void* v, const float* alpha, const float* beta, float* sctx,
                         long long sctx_rstride, void* o_last, float* x_inout, cudaStream_t s);

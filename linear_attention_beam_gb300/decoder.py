@@ -50,10 +50,11 @@ class DecodeResult:
 class BeamDecoder:
     def __init__(self, *, R: int, layers: int, H: int, d_k: int, d_v: int, d_model: int, V: int,
                  T: int, W_max: int, L_max: int, dtype: int, residual: bool,
-                 weights: Dict[str, torch.Tensor], device="cuda"):
+                 weights: Dict[str, torch.Tensor], device="cuda", state_path: int = 0):
         self.lib = load()
         self.cfg = Config(R=R, layers=layers, H=H, d_k=d_k, d_v=d_v, d_model=d_model, V=V, T=T,
-                          W_max=W_max, L_max=L_max, dtype=dtype, residual=int(residual))
+                          W_max=W_max, L_max=L_max, dtype=dtype, residual=int(residual),
+                          state_path=int(state_path))
         self.device = torch.device(device)
         self.dtype = dtype
         self.tdtype = TORCH_DTYPE[dtype]
@@ -77,11 +78,13 @@ class BeamDecoder:
         self.sid = torch.empty(R_, W, T, dtype=torch.int32, device=dev)
 
     @classmethod
-    def for_workload(cls, wl, weights, L_max: Optional[int] = None, device="cuda"):
+    def for_workload(cls, wl, weights, L_max: Optional[int] = None, device="cuda",
+                     state_path: int = 0):
+        """state_path 0: shared context + records + replay; 1: FullState baseline."""
         return cls(R=wl.R, layers=wl.layers, H=wl.H, d_k=wl.d_k, d_v=wl.d_v, d_model=wl.d_model,
                    V=wl.V, T=wl.T, W_max=wl.W_max, L_max=L_max or wl.L,
                    dtype=BF16 if wl.dtype == "bf16" else F32, residual=wl.residual,
-                   weights=weights, device=device)
+                   weights=weights, device=device, state_path=state_path)
 
     def __del__(self):
         try:

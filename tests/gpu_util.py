@@ -59,10 +59,10 @@ def host(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy()
 
 
-def decoder_for(wl, params, L_max=None):
+def decoder_for(wl, params, L_max=None, state_path=0):
     w = pack_weights(params.E, params.Wq, params.Wk, params.Wv, params.w_alpha, params.w_beta,
                      params.Wo, dt(wl), DEV)
-    return BeamDecoder.for_workload(wl, w, L_max=L_max)
+    return BeamDecoder.for_workload(wl, w, L_max=L_max, state_path=state_path)
 
 
 def cfg_for(wl, **over) -> gb.Config:

@@ -73,13 +73,16 @@ SMALL = {
 }
 
 
+@pytest.mark.parametrize("state_path", [0, 1], ids=["replay", "fullstate"])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_decode_forced_on_oracle_lineage(name):
+def test_decode_forced_on_oracle_lineage(name, state_path):
+    # state_path 1 is the FullState baseline (per-beam states copied on
+    # reorder): the same comparisons hold for it
     wl = SMALL[name]
     p = synth.make_params(wl)
     prompt = synth.make_prompt(wl)
     tr = oracle.decode_request(wl, p, prompt[0])
-    dec = decoder_for(wl, p)
+    dec = decoder_for(wl, p, state_path=state_path)
     dec.prefill(_i32(prompt))
     sctx = host(dec.read_sctx())[0]
     e = maxrel(sctx, tr.S_ctx); _record(name, "sctx", e)
