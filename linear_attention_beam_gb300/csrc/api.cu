@@ -91,6 +91,7 @@ struct gdnbeam_ctx {
   const void* last_logits;  // logits buffer the last logits stage wrote
   int last_rows;
   void* states[2];  // FullState baseline: [R*W_max][layers][H][d_v][d_k] per buffer
+  void* sctx_store; // FullState baseline: S_ctx in the storage type (t = 0 parent)
   // prefill buffers for R*L_max rows
   void *pf_u, *pf_q, *pf_k, *pf_v, *pf_feat;
   float *pf_x, *pf_alpha, *pf_beta;
@@ -194,6 +195,7 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
   const size_t st_b = c.state_path ? rows * c.layers * c.H * c.d_v * c.d_k * es : 0;
   char* p_st0 = take(st_b);
   char* p_st1 = take(st_b);
+  char* p_sst = take(c.state_path ? (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * es : 0);
   char* p_pfu = take(pf_rows * c.d_model * es);
   char* p_pfx = take(c.residual ? pf_rows * c.d_model * sizeof(float) : 0);
   char* p_pfq = take(pf_rows * c.H * c.d_k * es);
@@ -209,7 +211,7 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
     x->u = p_u; x->x = (float*)p_x; x->q = p_q; x->v = p_v; x->beta = (float*)p_beta;
     x->o = p_o; x->sel = p_sel; x->sel_bytes = sel_b; x->gemm = p_gemm; x->gemm_bytes = gemm_b;
     x->tstats = (float2*)p_tst; x->last_logits = nullptr; x->last_rows = 0;
-    x->states[0] = p_st0; x->states[1] = p_st1;
+    x->states[0] = p_st0; x->states[1] = p_st1; x->sctx_store = p_sst;
     x->pf_u = p_pfu; x->pf_x = (float*)p_pfx; x->pf_q = p_pfq; x->pf_k = p_pfk;
     x->pf_v = p_pfv; x->pf_alpha = (float*)p_pfa; x->pf_beta = (float*)p_pfb; x->pf_feat = p_pff;
   }
@@ -377,6 +379,11 @@ int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* 
     ctx->toc(ev, s);
     if (st) return st;
   }
+  if (c.state_path) {  // the FullState path keeps every state in the storage type
+    st = launch_to_storage(c.dtype, (size_t)c.R * c.layers * c.H * c.d_v * c.d_k,
+                           (const float*)ctx->sctx, ctx->sctx_store, s);
+    if (st) return st;
+  }
   if (c.residual) {
     st = launch_rmsnorm_rows(c.dtype, c.R, c.d_model, ctx->pf_x + (size_t)(L - 1) * c.d_model,
                              (long long)L * c.d_model, ctx->pf_feat, s);
@@ -456,7 +463,8 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
       FullStateArgs f{};
       f.R = c.R; f.H = c.H; f.d_k = c.d_k; f.d_v = c.d_v; f.t = t; f.W_t = W_t;
       f.W_prev = W_prev; f.layers = c.layers; f.layer = layer;
-      f.sctx = a.sctx; f.sctx_rstride = a.sctx_rstride;
+      f.sctx_store = (const char*)ctx->sctx_store + (size_t)layer * c.H * c.d_v * c.d_k * es;
+      f.sctx_rstride = a.sctx_rstride;
       f.states_prev = ctx->states[cur ^ 1]; f.states_cur = ctx->states[cur];
       f.parents = parents;
       f.q = a.q; f.k = a.k; f.v = a.v; f.alpha = a.alpha; f.beta = a.beta;

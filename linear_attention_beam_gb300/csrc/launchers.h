@@ -67,8 +67,8 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s);
 // FullState baseline step for one layer (one d_v x d_k state per beam).
 struct FullStateArgs {
   int R, H, d_k, d_v, t, W_t, W_prev, layers, layer;
-  const float* sctx;           // fp32 [R][...], request stride sctx_rstride (t = 0 parents)
-  long long sctx_rstride;
+  const void* sctx_store;      // storage copy of S_ctx [R][...] (the t = 0 parent)
+  long long sctx_rstride;      // request stride of sctx_store, elements
   const void* states_prev;     // storage [R*W_prev][layers][H][d_v][d_k]
   void* states_cur;            // storage [R*W_t][layers][H][d_v][d_k]
   const int32_t* parents;      // [R*W_t] rows of the previous call (t >= 1)
@@ -80,6 +80,8 @@ struct FullStateArgs {
   unsigned* err;
 };
 int launch_fullstate(int dtype, const FullStateArgs& a, cudaStream_t s);
+// dst[i] = storage(src[i]) for n elements (S_ctx copy for the FullState path).
+int launch_to_storage(int dtype, size_t n, const float* src, void* dst, cudaStream_t s);
 
 int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const void* k,
                         const void* v, const float* alpha, const float* beta, float* sctx,

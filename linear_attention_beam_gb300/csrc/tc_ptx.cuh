@@ -264,6 +264,13 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Contiguous shared -> global copy of `bytes` (multiple of 16, both ends
+// 16-byte aligned) in the current bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"((uint64_t)dst),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both ends
 // 16-byte aligned), completing on an mbarrier's transaction count.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
