@@ -66,6 +66,29 @@ template <> struct Unpack<float, 4> {
   }
 };
 
+// Order-preserving integer keys of stored logits (larger value, larger key;
+// NaN patterns sort beyond the infinities).
+template <typename T> struct SKey;
+template <> struct SKey<__nv_bfloat16> {
+  static constexpr uint32_t kNegInf = 0x007Fu, kPosInf = 0xFF80u;
+  static __device__ __forceinline__ uint32_t of_bits(uint32_t b) {
+    return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+  }
+  static __device__ __forceinline__ float value(uint32_t k) {
+    const uint32_t b = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+    return __uint_as_float(b << 16);
+  }
+};
+template <> struct SKey<float> {
+  static constexpr uint32_t kNegInf = 0x007FFFFFu, kPosInf = 0xFF800000u;
+  static __device__ __forceinline__ uint32_t of_bits(uint32_t b) {
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  static __device__ __forceinline__ float value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+  }
+};
+
 __device__ __forceinline__ float cum_prime(const float* cum, const float* bias, size_t row) {
   float cp = cum ? cum[row] : 0.0f;
   if (bias) cp = __fadd_rn(cp, bias[row]);
@@ -143,6 +166,8 @@ struct SelScratch {
   uint64_t* cand;   // [R][cap]
   uint64_t* pre;    // [R*W_t][K] fallback precut keys
   float2* hint;     // [R*W_t][n_tiles] tile maxima computed here when not supplied
+  uint32_t* zcut;   // [R*W_t] per row: storage key of the smallest logit whose score
+                    // reaches the bound (scores are monotone in the stored logit)
   int cap;
 };
 
@@ -170,6 +195,7 @@ SelScratch carve_sel(void* base, int R, int W_t, int W_next, int V, size_t* tota
   s.cand = (uint64_t*)take((size_t)R * s.cap * 8);
   s.pre = (uint64_t*)take((size_t)R * W_t * K * 8);
   s.hint = (float2*)take((size_t)R * W_t * n_tiles * sizeof(float2));
+  s.zcut = (uint32_t*)take((size_t)R * W_t * 4);
   if (total) *total = off;
   return s;
 }
@@ -207,6 +233,7 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
   }
   if (W_next > n_h) {  // too few hints for a bound: keep every candidate
     if (threadIdx.x == 0) ss.thr[r] = 0u;
+    for (int b = threadIdx.x; b < W_t; b += blockDim.x) ss.zcut[(size_t)r * W_t + b] = 0u;
     return;
   }
   auto key_of = [&](int i) -> uint32_t {
@@ -225,56 +252,101 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
     t = radix_kth<uint32_t>(n_h, (unsigned)W_next, key_of, hist, sh);
   }
   if (threadIdx.x == 0) ss.thr[r] = t;
+  // per row, the smallest stored logit whose score reaches t (bisection over
+  // the storage keys; the score is monotone in the logit)
+  for (int b = threadIdx.x; b < W_t; b += blockDim.x) {
+    const size_t row = (size_t)r * W_t + b;
+    const float cp = cum_prime(cum, bias, row), l = lse[row];
+    uint32_t lo = SKey<T>::kNegInf, hi = SKey<T>::kPosInf + 1u;  // hi: none reaches t
+    while (lo < hi) {
+      const uint32_t mid = lo + ((hi - lo) >> 1);
+      if (orderable(score(cp, SKey<T>::value(mid), l)) >= t) hi = mid; else lo = mid + 1u;
+    }
+    ss.zcut[row] = lo;
+  }
 }
 
 // ---- filter: append every candidate whose score reaches the bound
+// A candidate qualifies when its stored logit's key reaches the row's cutoff
+// key (an integer compare; two bf16 keys per 32-bit word with SIMD compares);
+// scores are evaluated only for the rare hits. Each thread keeps U 16-byte
+// loads in flight; a warp votes before it scans for append slots.
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
     int W_t, int V, const T* __restrict__ z, const float* __restrict__ lse,
     const float* __restrict__ cum, const float* __restrict__ bias, SelScratch ss, unsigned* err) {
+  constexpr int U = VEC > 1 ? 4 : 1;
+  constexpr int WORDS = VEC > 1 ? 4 : 1;  // 32-bit words per 16-byte load
   const int row = blockIdx.x;
   const int r = row / W_t, b = row % W_t;
-  const float l = lse[row];
-  const float cp = cum_prime(cum, bias, row);
-  const uint32_t thr = ss.thr[r];
+  const uint32_t cut = ss.zcut[row];
   const T* zr = z + (size_t)row * V;
   const int lane = threadIdx.x & 31;
   const uint32_t flat0 = (uint32_t)b * (uint32_t)V;
   uint64_t* out = ss.cand + (size_t)r * ss.cap;
   bool bad = false;
-  for (int v0 = 0; v0 < V; v0 += kFilterThreads * VEC) {
-    const int v = v0 + threadIdx.x * VEC;
-    float vals[VEC];
-    if constexpr (VEC > 1) {
-      if (v < V) {
-        Unpack<T, VEC>::run(__ldg(reinterpret_cast<const uint4*>(zr + v)), vals);
+  float cp = 0.f, l = 0.f;
+  bool have_row = false;
+  for (int v00 = 0; v00 < V; v00 += kFilterThreads * VEC * U) {
+    uint32_t w[U][WORDS];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v00 + (u * kFilterThreads + threadIdx.x) * VEC;
+      if constexpr (VEC > 1) {
+        if (v < V) {
+          const uint4 x = __ldg(reinterpret_cast<const uint4*>(zr + v));
+          w[u][0] = x.x; w[u][1] = x.y; w[u][2] = x.z; w[u][3] = x.w;
+        } else {
+          w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0u;  // never tested (v >= V)
+        }
       } else {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) vals[j] = -INFINITY;
-      }
-    } else {
-      vals[0] = (v < V) ? ldf(zr + v) : -INFINITY;
-    }
-    unsigned hits = 0;
-    uint32_t ords[VEC];
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) {
-      const float s = score(cp, vals[j], l);
-      if (v + j < V) {
-        if (!isfinite(s)) bad = true;
-        ords[j] = orderable(s);
-        if (ords[j] >= thr) hits |= 1u << j;
+        w[u][0] = (v < V) ? (uint32_t)(sizeof(T) == 2
+                                           ? (uint32_t)__bfloat16_as_ushort(*(const __nv_bfloat16*)(zr + v))
+                                           : __float_as_uint(*(const float*)(zr + v)))
+                          : 0u;
       }
     }
-    const int mine = __popc(hits);
-    int incl = mine;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (total) {
+    for (int u = 0; u < U; ++u) {
+      const int v = v00 + (u * kFilterThreads + threadIdx.x) * VEC;
+      unsigned hits = 0;
+      if (v < V) {
+        if constexpr (sizeof(T) == 2 && VEC > 1) {
+          const uint32_t cut2 = cut | (cut << 16);
+#pragma unroll
+          for (int q = 0; q < WORDS; ++q) {
+            const uint32_t x = w[u][q];
+            const uint32_t sgn = (x >> 15) & 0x00010001u;
+            const uint32_t key = x ^ (0x80008000u | (sgn * 0x7FFFu));  // two storage keys
+            const uint32_t ge = __vcmpgeu2(key, cut2);
+            hits |= ((ge & 1u) | ((ge >> 15) & 2u)) << (2 * q);
+            bad |= __vcmpeq2(x & 0x7F807F80u, 0x7F807F80u) != 0u;  // Inf or NaN
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            const uint32_t bits = sizeof(T) == 2 ? ((w[u][j >> 1] >> (16 * (j & 1))) & 0xFFFFu) : w[u][j];
+            if (v + j < V) {
+              if (SKey<T>::of_bits(bits) >= cut) hits |= 1u << j;
+              bad |= sizeof(T) == 2 ? ((bits & 0x7F80u) == 0x7F80u) : ((bits & 0x7F800000u) == 0x7F800000u);
+            }
+          }
+        }
+      }
+      if (!__any_sync(0xffffffffu, hits != 0)) continue;
+      if (!have_row) {
+        cp = cum_prime(cum, bias, row);
+        l = lse[row];
+        have_row = true;
+      }
+      const int mine = __popc(hits);
+      int incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
       int base = 0;
       if (lane == 31) base = atomicAdd(ss.count + r, total);
       base = __shfl_sync(0xffffffffu, base, 31);
@@ -282,12 +354,16 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
 #pragma unroll
       for (int j = 0; j < VEC; ++j) {
         if (hits & (1u << j)) {
-          if (idx < ss.cap) out[idx] = make_key(ords[j], flat0 + (uint32_t)(v + j));
+          const uint32_t bits = sizeof(T) == 2 ? ((w[u][j >> 1] >> (16 * (j & 1))) & 0xFFFFu) : w[u][j];
+          const float zv = sizeof(T) == 2 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
+          const uint32_t o = orderable(score(cp, zv, l));
+          if (idx < ss.cap) out[idx] = make_key(o, flat0 + (uint32_t)(v + j));
           ++idx;
         }
       }
     }
   }
+  if (!isfinite(lse[row]) || !isfinite(cum_prime(cum, bias, row))) bad = true;
   if (bad) raise_error(err, GDNBEAM_DERR_NONFINITE);
 }
 
