@@ -1,28 +1,34 @@
 // Fused shared-context replay on tcgen05 tensor cores (bf16, d_k = d_v = 128).
 //
-// OneLA §2.5: one block per (request, head) loads that head's S_ctx once and
-// reuses it for every beam tile; per tile it forms the two projections of
-// §2.3 eqs. 6-7 from S_ctx, folds the ancestors' records (alpha_j, delta_j,
-// k_j) into them, evaluates eq. 8 and writes only delta_t (the new record)
-// and o_t. No per-beam d_v x d_k state exists anywhere.
+// OneLA §2.5: one block per (request, head) holds that head's S_ctx for the
+// whole call and reuses it for every beam tile; per tile it forms the two
+// projections of §2.3 eqs. 6-7 from S_ctx, folds the ancestors' records
+// (alpha_j, delta_j, k_j) into them, evaluates eq. 8 and writes only delta_t
+// (the new record) and o_t. No per-beam d_v x d_k state exists anywhere.
 //
 // Mapping to sm_103a:
-//   * S_ctx is fp32 in memory; the block splits it into bf16 hi + lo halves
-//     in shared memory (128-byte swizzled, K-major), the A operand (M = 128
-//     value rows) of two MMAs per K step, so the contraction keeps ~16
-//     mantissa bits of S_ctx.
-//   * Beams go in tiles of 32. Per tile one producer warp stages by TMA the
-//     32 queries and 32 keys as the B operand (N = 64: q rows then k rows),
-//     the 32 value rows, and with 256-byte bulk copies each beam's ancestor
-//     records delta_j and k_j, found through the ancestry index; stages are
-//     double-buffered on mbarriers.
+//   * S_ctx (fp32 in memory) is split into bf16 hi + lo halves and kept in
+//     tensor memory as the A operand (M = 128 value rows) of two MMAs per K
+//     step, so the contraction keeps ~16 mantissa bits of S_ctx and shared
+//     memory is left to the beam pipeline.
+//   * Beams go in tiles of 32. A producer warp stages per tile, by TMA, the
+//     32 queries and keys (the B operand, N = 64: q rows then k rows, 128-byte
+//     swizzled) and the 32 value rows; two more warps gather each beam's
+//     ancestor records delta_j and k_j, four rows per request (small TMA
+//     requests are issued at a per-warp rate, so the work is spread). Stages
+//     sit on an mbarrier ring several tiles deep.
+//   * Gates, ancestor slots and ancestor decays of all the block's beams are
+//     read once into a shared table at block start, so no global load sits on
+//     the per-tile path.
 //   * One thread issues tcgen05.mma into a double-buffered TMEM accumulator:
 //     column b holds u_q of beam b, column 32 + b its u_k, lane = value row.
-//   * Four epilogue warps (thread = value row i) compute the replay scalars
-//     k_j.q_t, k_j.k_t and k_t.q_t, fold the records, apply eq. 8, and write
-//     delta_t and o_t into shared tiles that TMA stores to memory.
+//   * Eight epilogue warps (thread = value row; two warps per TMEM lane
+//     group, 16 beams each) compute the replay scalars k_j.q_t, k_j.k_t and
+//     k_t.q_t one tile ahead, fold the records, apply eq. 8 and write delta_t
+//     and o_t into a double-buffered shared tile that TMA stores to memory.
 // Every wait is bounded in time (GDNBEAM_DERR_TIMEOUT on expiry).
 #include <cuda.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "launchers.h"
@@ -34,29 +40,34 @@ namespace {
 
 constexpr int D = 128;            // head width (d_k = d_v)
 constexpr int NB = 32;            // beams per tile
-constexpr int kEpiWarps = 8;      // two per SM sub-partition; each folds 16 beams of a tile
+constexpr int kEpiWarps = 8;      // two per TMEM lane group; each folds 16 beams of a tile
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kThreads = 64 + kEpiThreads + 64;  // producer, MMA, epilogue, two record loaders
 constexpr int kMaxDepth = 6;      // replay depths this kernel stages
-constexpr int A_BYTES = 2 * D * D;          // one bf16 half of S_ctx: 32 KiB
 constexpr int B_BYTES = 2 * NB * D * 2;     // q and k rows: 16 KiB
+constexpr int V_BYTES = NB * D * 2;         // v rows: 8 KiB
 constexpr int REC_BYTES = 2 * NB * D * 2;   // delta_j and k_j rows of one depth: 16 KiB
-constexpr int META_BYTES = 1024;            // per-beam gates and ancestors' decays
-constexpr int kMaxStages = 4;
+constexpr int OUT_BYTES = 2 * NB * D * 2;   // delta_t and o_t rows of one tile: 16 KiB
+constexpr int OUT_WARP = 2 * 16 * 32 * 2;   // one warp's [16 beams][32 rows] of delta_t and o_t
+constexpr int kMaxStages = 6;
+// TMEM columns: two accumulators of 2 * NB, then S_ctx hi and lo (D / 2 each)
+constexpr uint32_t kColAHi = 4 * NB, kColALo = 4 * NB + D / 2, kTmemCols = 256;
+
+// Ancestor records of each depth as 2-D maps [R * W_j * H rows][128] with a
+// one-row, 64-column box, read four rows at a time.
+struct RecMaps {
+  CUtensorMap d[kMaxDepth], k[kMaxDepth];
+};
 
 struct TcReplayParams {
   int R, H, t, W_t, n_tiles, stages, stage_bytes;
   const float* sctx;
   long long sctx_rstride;
   const float *alpha, *beta;
-  const __nv_bfloat16* v;
-  const __nv_bfloat16* rec_k[kMaxDepth];
-  const __nv_bfloat16* rec_d[kMaxDepth];
   const float* rec_a[kMaxDepth];
   int W_j[kMaxDepth];
   const int32_t* anc;
   int anc_stride;
-  __nv_bfloat16 *delta_out, *o_out;
   float* x_inout;
   float *delta_dump, *o_dump;
   unsigned* err;
@@ -71,45 +82,61 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
 
 __device__ __forceinline__ float bf(uint32_t x16) { return __uint_as_float(x16 << 16); }
 
-// Stage layout: [B: q rows | k rows, per 64-column block][REC per depth:
-// delta rows | k rows][META: (alpha_t, beta_t) per beam, alpha_j per beam and
-// depth (negative for a slot outside its depth)].
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+// Dynamic shared memory (1024-byte aligned base):
+//   stages x [B: q rows | k rows per 64-column block (swizzled)]
+//            [V: value rows, two [32][64] boxes]
+//            [REC per depth: delta_j rows | k_j rows, each as two [32][64] halves]
+//   table: (alpha_t, beta_t) per beam, then per beam and depth the ancestor
+//          slot and its decay (negative for a slot outside its depth).
 template <int TD>  // replay depth t of this call
 __global__ void __launch_bounds__(kThreads, 1)
     replay_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_d,
+                     const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ RecMaps rm,
                      TcReplayParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 6];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 7];
   // replay scalars of two tiles (the fold reads one while the next is computed)
-  __shared__ float4 s_beam[2][NB];                              // (alpha_t, beta_t, k_t.q_t, -)
-  __shared__ float4 s_rec[2][NB][TD > 0 ? TD : 1];              // (alpha_j, k_j.q_t, k_j.k_t, -)
+  // per beam (beta_t, K0, Q0, k_t.q_t) and per ancestor record (K_j, Q_j): the
+  // fold written out, delta_t = beta_t v + K0 u_k + sum_j K_j delta_j and
+  // o_t = Q0 u_q + sum_j Q_j delta_j + (k_t.q_t) delta_t
+  __shared__ float4 s_beam[2][NB];
+  __shared__ float2 s_rec[2][NB][TD > 0 ? TD : 1];
+  // delta_t and o_t of two tiles, per epilogue warp a [16 beams][32 rows] box of each
+  __shared__ __align__(1024) uint8_t s_out[2][OUT_BYTES];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
+  constexpr int t = TD;
   const uint32_t raw = tc::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sA_hi = base, sA_lo = base + A_BYTES;
-  const uint32_t sStage0 = base + 2 * A_BYTES;
-  uint8_t* gStage0 = gbase + 2 * A_BYTES;
+  float2* tab_ab = reinterpret_cast<float2*>(gbase + p.stages * p.stage_bytes);
+  int* tab_slot = reinterpret_cast<int*>(tab_ab + p.W_t);
+  float* tab_aj = reinterpret_cast<float*>(tab_slot + p.W_t * t);
   auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
   auto full = [&](int s) { return bar(s); };
   auto empty = [&](int s) { return bar(kMaxStages + s); };
   auto tfull = [&](int a) { return bar(2 * kMaxStages + a); };
   auto tempty = [&](int a) { return bar(2 * kMaxStages + 2 + a); };
   const uint32_t a_ready = bar(2 * kMaxStages + 4);
-  const uint32_t drain_bar = bar(2 * kMaxStages + 5);
+  const uint32_t tab_ready = bar(2 * kMaxStages + 5);
+  const uint32_t drain_bar = bar(2 * kMaxStages + 6);
   volatile int* abort = &s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x / p.H, h = blockIdx.x % p.H;
-  constexpr int t = TD;
-  const int rec_off = B_BYTES;
-  const int meta_off = rec_off + t * REC_BYTES;
+  constexpr int v_off = B_BYTES;
+  constexpr int rec_off = B_BYTES + V_BYTES;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      tc::mbar_init(full(s), 32);  // every producer lane arrives after its stores and copies
+      tc::mbar_init(full(s), TD > 0 ? 3 : 1);  // the producer and the record loaders
       tc::mbar_init(empty(s), 2);  // released by the MMA commit and by the epilogue
     }
     for (int a = 0; a < 2; ++a) {
@@ -117,14 +144,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(tempty(a), kEpiWarps);
     }
     tc::mbar_init(a_ready, kEpiWarps);
+    tc::mbar_init(tab_ready, kEpiWarps);
     tc::mbar_init(drain_bar, 1);
     s_abort = 0;
     tc::fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tc::tma_prefetch(&tm_q); tc::tma_prefetch(&tm_k);
+    tc::tma_prefetch(&tm_q); tc::tma_prefetch(&tm_k); tc::tma_prefetch(&tm_v);
+    tc::tma_prefetch(&tm_d); tc::tma_prefetch(&tm_o);
   }
-  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&s_tmem), 128);
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&s_tmem), kTmemCols);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -132,67 +161,76 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    bool issued[kMaxStages] = {false, false, false, false};
-    uint32_t issued_ph[kMaxStages] = {0, 0, 0, 0};
-    for (int i = 0; i < p.n_tiles; ++i) {
-      const int s = i % p.stages;
-      const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
-      const int b0 = i * NB;
-      const int nb = min(NB, p.W_t - b0);
-      // this tile's gates and ancestor slots, fetched before the stage frees
-      int slot[TD > 0 ? TD : 1];
-      float a_j[TD > 0 ? TD : 1];
-      float al = 0.f, be = 0.f;
-      if (lane < nb) {
-        const size_t row = (size_t)r * p.W_t + b0 + lane;
-        al = p.alpha[row * p.H + h];
-        be = p.beta[row * p.H + h];
-#pragma unroll
-        for (int j = 0; j < t; ++j) {
-          int sl = p.anc[row * p.anc_stride + j];
-          a_j[j] = -1.0f;  // marks a slot outside its depth: the record is skipped
-          if (sl < 0 || sl >= p.W_j[j]) {
-            raise_error(p.err, GDNBEAM_DERR_SLOT);
-            sl = 0;
-          } else {
-            a_j[j] = p.rec_a[j][((size_t)r * p.W_j[j] + sl) * p.H + h];
-          }
-          slot[j] = sl;
-        }
-      }
-      int ok = 0;
-      if (lane == 0) ok = tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // the whole warp stops together
-      const uint32_t st = sStage0 + (uint32_t)(s * p.stage_bytes);
-      uint8_t* gst = gStage0 + s * p.stage_bytes;
-      if (lane == 0) {
-        tc::mbar_expect_tx(full(s), (uint32_t)(B_BYTES + t * nb * 2 * D * 2));
+    // q, k and v boxes of every tile (lane 0)
+    bool issued[kMaxStages] = {};
+    uint32_t issued_ph[kMaxStages] = {};
+    if (lane == 0) {
+      for (int i = 0; i < p.n_tiles; ++i) {
+        const int s = i % p.stages;
+        const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+        if (!tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err)) break;
+        const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
+        const int b0 = i * NB;
+        tc::mbar_arrive_expect_tx(full(s), (uint32_t)(B_BYTES + V_BYTES));
         for (int kb = 0; kb < 2; ++kb) {
           const uint32_t bk = st + kb * (2 * NB * 128);
           tc::tma_load_3d(bk, &tm_q, h * D + kb * 64, b0, r, full(s));
           tc::tma_load_3d(bk + NB * 128, &tm_k, h * D + kb * 64, b0, r, full(s));
+          tc::tma_load_3d(st + v_off + kb * (NB * 128), &tm_v, h * D + kb * 64, b0, r, full(s));
         }
+        issued[s] = true;
+        issued_ph[s] = ph;
       }
-      __syncwarp();
-      if (lane < nb) {
-        float2* albe = reinterpret_cast<float2*>(gst + meta_off);
-        float* ajs = reinterpret_cast<float*>(gst + meta_off + NB * 8);
-        albe[lane] = make_float2(al, be);
-#pragma unroll
-        for (int j = 0; j < t; ++j) {
-          ajs[lane * kMaxDepth + j] = a_j[j];
-          const size_t rec = ((size_t)r * p.W_j[j] + slot[j]) * p.H + h;
-          const uint32_t dst = st + rec_off + j * REC_BYTES + lane * (D * 2);
-          tc::bulk_load(dst, p.rec_d[j] + rec * D, D * 2, full(s));
-          tc::bulk_load(dst + NB * D * 2, p.rec_k[j] + rec * D, D * 2, full(s));
-        }
-      }
-      tc::mbar_arrive(full(s));  // releases this lane's stage stores
-      if (lane == 0) { issued[s] = true; issued_ph[s] = ph; }
-    }
-    if (lane == 0)
       for (int s = 0; s < p.stages; ++s)
         if (issued[s]) tc::mbar_wait_drain(full(s), issued_ph[s]);
+    }
+  } else if (warp >= 2 + kEpiWarps) {
+    // ---------------------------------------------------------------- records
+    // warp kind (0: delta_j, 1: k_j) gathers its record rows of every tile,
+    // four beams and one 64-column half per request; beams past the tile's
+    // end repeat a valid row
+    if (t > 0) {
+      const int kind = warp - (2 + kEpiWarps);
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait_sleep(tab_ready, 0, abort, p.err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      bool issued[kMaxStages] = {};
+      uint32_t issued_ph[kMaxStages] = {};
+      for (int i = 0; ok && i < p.n_tiles; ++i) {
+        const int s = i % p.stages;
+        const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+        if (lane == 0) ok = tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // the whole warp stops together
+        const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
+        const int b0 = i * NB;
+        const int nb = min(NB, p.W_t - b0);
+        if (lane == 0) tc::mbar_expect_tx(full(s), (uint32_t)(t * NB * D * 2));
+        __syncwarp();
+        for (int req = lane; req < 16 * t; req += 32) {
+          const int j = req >> 4, half = (req >> 3) & 1, g = req & 7;
+          int y[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int b = 4 * g + u;
+            const int sl = b < nb ? tab_slot[(b0 + b) * t + j] : 0;
+            y[u] = (r * p.W_j[j] + sl) * p.H + h;
+          }
+          const uint32_t dst = st + rec_off + (uint32_t)(j * REC_BYTES + kind * (NB * D * 2) +
+                                                         half * (NB * 128) + g * (4 * 128));
+          tc::tma_gather4(dst, kind == 0 ? &rm.d[j] : &rm.k[j], half * 64, y[0], y[1], y[2], y[3],
+                          full(s));
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tc::mbar_arrive(full(s));
+          issued[s] = true;
+          issued_ph[s] = ph;
+        }
+      }
+      if (lane == 0)
+        for (int s = 0; s < p.stages; ++s)
+          if (issued[s]) tc::mbar_wait_drain(full(s), issued_ph[s]);
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -207,16 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tc::mbar_wait_sleep(tempty(acc), aph ^ 1u, abort, p.err)) break;
         tc::fence_after_sync();
         const uint32_t d = tmem_base + (uint32_t)(acc * 2 * NB);
-        const uint32_t st = sStage0 + (uint32_t)(s * p.stage_bytes);
+        const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          const uint64_t ahi = tc::sw128_desc(sA_hi + kb * (D * 128));
-          const uint64_t alo = tc::sw128_desc(sA_lo + kb * (D * 128));
           const uint64_t bd = tc::sw128_desc(st + kb * (2 * NB * 128));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            tc::mma_bf16(d, ahi + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0);
-            tc::mma_bf16(d, alo + 2u * kk, bd + 2u * kk, idesc, 1u);
+            const uint32_t col = (uint32_t)(kb * 32 + kk * 8);  // 16 K elements = 8 columns
+            tc::mma_bf16_ts(d, tmem_base + kColAHi + col, bd + 2u * kk, idesc, (kb | kk) != 0);
+            tc::mma_bf16_ts(d, tmem_base + kColALo + col, bd + 2u * kk, idesc, 1u);
           }
         }
         tc::mma_commit(empty(s));
@@ -229,126 +266,142 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- epilogue
     const int ew = warp - 2;                   // 0..7
     const int ep = threadIdx.x - 64;           // 0..255
-    const int hb = ew >> 2;                    // which 16 beams of a tile this warp folds
+    const int hb = ew >> 2;                    // which half of a tile (beams) / of K this warp takes
     const int lg = warp & 3;                   // TMEM lane group
     const int i_row = lg * 32 + lane;          // value row = TMEM lane
+    const uint32_t lane_base = tmem_base + ((uint32_t)(lg * 32) << 16);
 
-    // S_ctx of this (request, head) -> bf16 hi / lo A operands, while the
-    // producer already streams the first tiles
-    {
-      const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * D * D;
-      constexpr int kUnits = D * (D / 8) / kEpiThreads;  // 8 row-chunks per thread
-      float4 xv[kUnits][2];
+    // the block's table: gates, ancestor slots and decays of every beam
+    for (int b = ep; b < p.W_t; b += kEpiThreads) {
+      const size_t row = (size_t)r * p.W_t + b;
+      tab_ab[b] = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
 #pragma unroll
-      for (int k = 0; k < kUnits; ++k) {
-        const int u = ep + k * kEpiThreads, row = u >> 4, chunk = u & 15;
-        xv[k][0] = __ldg(reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8));
-        xv[k][1] = __ldg(reinterpret_cast<const float4*>(S + (size_t)row * D + chunk * 8 + 4));
-      }
-#pragma unroll
-      for (int k = 0; k < kUnits; ++k) {
-        const int u = ep + k * kEpiThreads, row = u >> 4, chunk = u & 15;
-        const float xs[8] = {xv[k][0].x, xv[k][0].y, xv[k][0].z, xv[k][0].w,
-                             xv[k][1].x, xv[k][1].y, xv[k][1].z, xv[k][1].w};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          __nv_bfloat16 h0 = __float2bfloat16_rn(xs[2 * e]), h1 = __float2bfloat16_rn(xs[2 * e + 1]);
-          __nv_bfloat16 l0 = __float2bfloat16_rn(xs[2 * e] - __bfloat162float(h0));
-          __nv_bfloat16 l1 = __float2bfloat16_rn(xs[2 * e + 1] - __bfloat162float(h1));
-          hi[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-          lo[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      for (int j = 0; j < t; ++j) {
+        int sl = p.anc[row * p.anc_stride + j];
+        float a = -1.0f;  // marks a slot outside its depth: the record is skipped
+        if (sl < 0 || sl >= p.W_j[j]) {
+          raise_error(p.err, GDNBEAM_DERR_SLOT);
+          sl = 0;
+        } else {
+          a = p.rec_a[j][((size_t)r * p.W_j[j] + sl) * p.H + h];
         }
-        const int kb = chunk >> 3, col = (chunk & 7) * 8;
-        const uint32_t off = (uint32_t)kb * (D * 128) + sw128_off(row, col);
-        *reinterpret_cast<uint4*>(gbase + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(gbase + A_BYTES + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        tab_slot[b * t + j] = sl;
+        tab_aj[b * t + j] = a;
       }
-      tc::fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(tab_ready);
+
+    // S_ctx row i_row, K half hb -> bf16 hi / lo words in TMEM
+    {
+      const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * D * D +
+                       (size_t)i_row * D + hb * 64;
+      float4 x[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) x[c] = __ldg(reinterpret_cast<const float4*>(S) + c);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 v4 = x[half * 8 + c];
+          const float xs[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float a0 = xs[2 * e], a1 = xs[2 * e + 1];
+            const float h0 = __bfloat162float(__float2bfloat16_rn(a0));
+            const float h1 = __bfloat162float(__float2bfloat16_rn(a1));
+            hi[2 * c + e] = pack_bf16(h0, h1);
+            lo[2 * c + e] = pack_bf16(a0 - h0, a1 - h1);
+          }
+        }
+        const uint32_t col = (uint32_t)(hb * 32 + half * 16);
+        tc::tmem_st16(lane_base + kColAHi + col, hi);
+        tc::tmem_st16(lane_base + kColALo + col, lo);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(a_ready);
     }
+    // the scalar pass below reads the whole table
+    tc::named_sync(1, kEpiThreads);
 
     // replay scalars k_j.q_t, k_j.k_t (eqs. 6-7) and k_t.q_t (eq. 8) of tile
-    // i into buffer i & 1; warp ew takes beams ew, ew + 8, ew + 16, ew + 24
+    // i into buffer i & 1: eight lanes per beam, 16 dimensions each; warp ew
+    // takes beams 4 ew .. 4 ew + 3
     auto scalars = [&](int i) -> bool {
       const int s = i % p.stages;
       const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
-      const int nb = min(NB, p.W_t - i * NB);
+      const int b0 = i * NB;
+      const int nb = min(NB, p.W_t - b0);
       if (__any_sync(0xffffffffu, !tc::mbar_wait_sleep(full(s), ph, abort, p.err))) return false;
-      const uint8_t* gst = gStage0 + s * p.stage_bytes;
-      const float2* albe = reinterpret_cast<const float2*>(gst + meta_off);
-      const float* ajs = reinterpret_cast<const float*>(gst + meta_off + NB * 8);
-      const int c = lane * 4, kb = c >> 6, cc = c & 63;
+      const uint8_t* gst = gbase + s * p.stage_bytes;
+      const int bl = ew * 4 + (lane >> 3);
+      const int c0 = (lane & 7) * 16, kb = c0 >> 6, cc = c0 & 63;
       const uint8_t* bk = gst + kb * (2 * NB * 128);
-      float part[4][1 + 2 * TD];
+      float q16[16], k16[16];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int b = ew + 8 * e;
-        const uint2 qw = *reinterpret_cast<const uint2*>(bk + sw128_off(b, cc));
-        const uint2 kw = *reinterpret_cast<const uint2*>(bk + sw128_off(NB + b, cc));
-        const float q4[4] = {bf(qw.x & 0xFFFF), bf(qw.x >> 16), bf(qw.y & 0xFFFF), bf(qw.y >> 16)};
-        const float k4[4] = {bf(kw.x & 0xFFFF), bf(kw.x >> 16), bf(kw.y & 0xFFFF), bf(kw.y >> 16)};
-        float kq = 0.f;
-#pragma unroll
-        for (int x = 0; x < 4; ++x) kq = fmaf(k4[x], q4[x], kq);
-        part[e][0] = kq;
-#pragma unroll
-        for (int j = 0; j < t; ++j) {
-          const uint8_t* kr = gst + rec_off + j * REC_BYTES + NB * D * 2 + b * (D * 2);
-          const uint2 rw = *reinterpret_cast<const uint2*>(kr + c * 2);
-          const float r4[4] = {bf(rw.x & 0xFFFF), bf(rw.x >> 16), bf(rw.y & 0xFFFF), bf(rw.y >> 16)};
-          float cq = 0.f, ck = 0.f;
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            cq = fmaf(r4[x], q4[x], cq);
-            ck = fmaf(r4[x], k4[x], ck);
-          }
-          part[e][1 + 2 * j] = cq;
-          part[e][2 + 2 * j] = ck;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-#pragma unroll
-          for (int x = 0; x < 1 + 2 * TD; ++x)
-            part[e][x] += __shfl_xor_sync(0xffffffffu, part[e][x], o);
-      if (lane == 0) {
-        const int sb = i & 1;
+      for (int u = 0; u < 2; ++u) {
+        const uint4 qw = *reinterpret_cast<const uint4*>(bk + sw128_off(bl, cc + 8 * u));
+        const uint4 kw = *reinterpret_cast<const uint4*>(bk + sw128_off(NB + bl, cc + 8 * u));
+        const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, ka[4] = {kw.x, kw.y, kw.z, kw.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int b = ew + 8 * e;
-          if (b >= nb) continue;
-          const float2 ab = albe[b];
-          s_beam[sb][b] = make_float4(ab.x, ab.y, part[e][0], 0.f);
+          q16[8 * u + 2 * e] = bf(qa[e] & 0xFFFFu); q16[8 * u + 2 * e + 1] = bf(qa[e] >> 16);
+          k16[8 * u + 2 * e] = bf(ka[e] & 0xFFFFu); k16[8 * u + 2 * e + 1] = bf(ka[e] >> 16);
+        }
+      }
+      float part[1 + 2 * TD];
+      float kq0 = 0.f, kq1 = 0.f;
 #pragma unroll
-          for (int j = 0; j < t; ++j) {
-            const float a = ajs[b * kMaxDepth + j];
-            // a skipped record leaves both projections unchanged
-            s_rec[sb][b][j] = a >= 0.f ? make_float4(a, part[e][1 + 2 * j], part[e][2 + 2 * j], 0.f)
-                                       : make_float4(1.f, 0.f, 0.f, 0.f);
+      for (int x = 0; x < 16; x += 2) {
+        kq0 = fmaf(k16[x], q16[x], kq0);
+        kq1 = fmaf(k16[x + 1], q16[x + 1], kq1);
+      }
+      part[0] = kq0 + kq1;
+#pragma unroll
+      for (int j = 0; j < t; ++j) {
+        const uint8_t* kr = gst + rec_off + j * REC_BYTES + NB * D * 2 + kb * (NB * 128) + bl * 128 + cc * 2;
+        float cq0 = 0.f, ck0 = 0.f, cq1 = 0.f, ck1 = 0.f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint4 rw = *reinterpret_cast<const uint4*>(kr + 16 * u);
+          const uint32_t ra[4] = {rw.x, rw.y, rw.z, rw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float r0 = bf(ra[e] & 0xFFFFu), r1 = bf(ra[e] >> 16);
+            cq0 = fmaf(r0, q16[8 * u + 2 * e], cq0); cq1 = fmaf(r1, q16[8 * u + 2 * e + 1], cq1);
+            ck0 = fmaf(r0, k16[8 * u + 2 * e], ck0); ck1 = fmaf(r1, k16[8 * u + 2 * e + 1], ck1);
           }
         }
+        part[1 + 2 * j] = cq0 + cq1;
+        part[2 + 2 * j] = ck0 + ck1;
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1)
+#pragma unroll
+        for (int x = 0; x < 1 + 2 * TD; ++x) part[x] += __shfl_xor_sync(0xffffffffu, part[x], o);
+      if ((lane & 7) == 0 && bl < nb) {
+        // The fold u <- alpha_j u + delta_j c_j over j = 0 .. t-1 (eqs. 6-7)
+        // leaves u = (prod_j alpha_j) u_ctx + sum_j (c_j prod_{m > j} alpha_m)
+        // delta_j; eq. 8 is linear in both projections.
+        const int sb = i & 1;
+        const float2 ab = tab_ab[b0 + bl];  // (alpha_t, beta_t)
+        float tail = 1.f;                   // prod_{m > j} alpha_m
+#pragma unroll
+        for (int j = t - 1; j >= 0; --j) {
+          const float a = tab_aj[(b0 + bl) * t + j];
+          const bool use = a >= 0.f;  // a skipped record leaves both projections unchanged
+          const float wq = use ? part[1 + 2 * j] * tail : 0.f;
+          const float wk = use ? part[2 + 2 * j] * tail : 0.f;
+          s_rec[sb][bl][j] = make_float2(-ab.y * ab.x * wk, ab.x * wq);
+          if (use) tail *= a;
+        }
+        s_beam[sb][bl] = make_float4(ab.y, -ab.y * ab.x * tail, ab.x * tail, part[0]);
       }
       return true;
     };
-
-    // this thread's value entries of its 16 beams of tile i, loaded one tile
-    // ahead so the fold never waits on them
-    auto load_values = [&](int i, uint16_t (&vr)[16]) {
-      const int b0 = i * NB, nb = min(NB, p.W_t - b0);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int b = hb * 16 + e;
-        vr[e] = b < nb ? __ldg(reinterpret_cast<const uint16_t*>(
-                             p.v + (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row))
-                       : (uint16_t)0;
-      }
-    };
-    uint16_t vraw[16];
-    if (p.n_tiles > 0) load_values(0, vraw);
 
     // A failed wait marks the epilogue dead: it then skips all work but keeps
     // taking part in the named barriers, so no epilogue warp waits forever.
@@ -361,14 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sb = i & 1;
       const int b0 = i * NB;
       const int nb = min(NB, p.W_t - b0);
-      uint16_t vnext[16];
-      if (i + 1 < p.n_tiles) load_values(i + 1, vnext);
       if (!dead && i + 1 < p.n_tiles) dead = !scalars(i + 1);
       if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(tfull(acc), aph, abort, p.err));
       if (!dead) {
         tc::fence_after_sync();
-        const uint8_t* gst = gStage0 + s * p.stage_bytes;
-        const uint32_t ta = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * 2 * NB + hb * 16);
+        const uint8_t* gst = gbase + s * p.stage_bytes;
+        const uint32_t ta = lane_base + (uint32_t)(acc * 2 * NB + hb * 16);
         uint32_t uq[16], uk[16];
         tc::tmem_ld16_nowait(ta, uq);
         tc::tmem_ld16_nowait(ta + NB, uk);
@@ -376,46 +427,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tempty(acc));
-        const uint8_t* rd = gst + rec_off + i_row * 2;
+        const uint8_t* rd = gst + rec_off + (i_row >> 6) * (NB * 128) + (i_row & 63) * 2;
+        const uint8_t* vs = gst + v_off + (i_row >> 6) * (NB * 128) + (i_row & 63) * 2;
+        uint8_t* os = &s_out[sb][(hb * 4 + lg) * OUT_WARP] + lane * 2;
+        // every beam of the half tile is computed; rows past the last beam
+        // are never stored (the tile store clips them). The loop touches
+        // shared memory only, so its loads overlap freely.
+        float dl[16], ov[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int b = hb * 16 + e;
-          if (b < nb) {
-            float u_q = __uint_as_float(uq[e]), u_k = __uint_as_float(uk[e]);
+          const float4 bm = s_beam[sb][b];
+          const float vv = bf(*reinterpret_cast<const uint16_t*>(vs + b * 128));
+          float delta = fmaf(bm.y, __uint_as_float(uk[e]), bm.x * vv);
+          float o = bm.z * __uint_as_float(uq[e]);
 #pragma unroll
-            for (int j = 0; j < t; ++j) {
-              const float4 rc = s_rec[sb][b][j];
-              const float dj = bf(*reinterpret_cast<const uint16_t*>(rd + j * REC_BYTES + b * (D * 2)));
-              u_q = fmaf(rc.x, u_q, dj * rc.y);
-              u_k = fmaf(rc.x, u_k, dj * rc.z);
+          for (int j = 0; j < t; ++j) {
+            const float2 rc = s_rec[sb][b][j];
+            const float dj = bf(*reinterpret_cast<const uint16_t*>(rd + j * REC_BYTES + b * 128));
+            delta = fmaf(rc.x, dj, delta);
+            o = fmaf(rc.y, dj, o);
+          }
+          o = fmaf(bm.w, delta, o);
+          *reinterpret_cast<__nv_bfloat16*>(os + e * 64) = __float2bfloat16_rn(delta);
+          *reinterpret_cast<__nv_bfloat16*>(os + OUT_WARP / 2 + e * 64) = __float2bfloat16_rn(o);
+          dl[e] = delta;
+          ov[e] = o;
+        }
+        if (p.delta_dump || p.o_dump || p.x_inout) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int b = hb * 16 + e;
+            if (b < nb) {
+              const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row;
+              if (p.delta_dump) p.delta_dump[goff] = dl[e];
+              if (p.o_dump) p.o_dump[goff] = ov[e];
+              if (p.x_inout) p.x_inout[goff] += ov[e];
             }
-            const float4 bm = s_beam[sb][b];
-            const float vv = bf(vraw[e]);
-            const float delta = bm.y * (vv - bm.x * u_k);
-            const float o = fmaf(bm.x, u_q, delta * bm.z);
-            const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row;
-            p.delta_out[goff] = __float2bfloat16_rn(delta);
-            p.o_out[goff] = __float2bfloat16_rn(o);
-            if (p.delta_dump) p.delta_dump[goff] = delta;
-            if (p.o_dump) p.o_dump[goff] = o;
-            if (p.x_inout) p.x_inout[goff] += o;
           }
         }
+        // this warp's boxes go out by TMA; the store of two tiles ago has
+        // read the other buffer before the next tile writes it
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (hb * 16 < nb) {
+            const uint32_t ob = tc::smem_u32(&s_out[sb][(hb * 4 + lg) * OUT_WARP]);
+            tc::tma_store_3d(&tm_d, h * D + lg * 32, b0 + hb * 16, r, ob);
+            tc::tma_store_3d(&tm_o, h * D + lg * 32, b0 + hb * 16, r, ob + OUT_WARP / 2);
+          }
+          tc::bulk_commit();
+          tc::bulk_wait_read<1>();
+        }
+        __syncwarp();
       }
-      // every epilogue warp is done with stage s and with scalar buffer sb
+      // every epilogue warp is done with stage s and scalar buffer sb
       tc::named_sync(1, kEpiThreads);
       if (ep == 0 && !dead) tc::mbar_arrive(empty(s));
-      if (i + 1 < p.n_tiles) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) vraw[e] = vnext[e];
-      }
     }
+    if (lane == 0) tc::bulk_wait_all();
   }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem_base, 128);
+    tc::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -455,6 +531,19 @@ bool beam_map(CUtensorMap* map, const void* ptr, int R, int W_t, int H, bool swi
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows][128] bf16 (one record per row) as a 2-D map with a one-row, 64-column box.
+bool rows_map(CUtensorMap* map, const void* ptr, long long rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || ((uintptr_t)ptr & 15) != 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool tc_replay_supported(int dtype, int d_k, int d_v) {
@@ -467,36 +556,42 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
   TcReplayParams p{};
   p.R = a.R; p.H = a.H; p.t = a.t; p.W_t = a.W_t;
   p.n_tiles = (a.W_t + NB - 1) / NB;
-  p.stage_bytes = B_BYTES + a.t * REC_BYTES + META_BYTES;
-  const int static_bytes = 8 * 1024;  // scalar buffers and barriers
-  const int budget = 227 * 1024 - static_bytes - 1024 - 2 * A_BYTES;
-  p.stages = budget / p.stage_bytes;
+  p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES;
+  const size_t table = (size_t)a.W_t * (8 + 8 * a.t);
+  const int static_bytes = 2 * OUT_BYTES + 10 * 1024;  // output tiles, scalar buffers, barriers
+  const long long budget = 227LL * 1024 - static_bytes - 1024 - (long long)table;
+  p.stages = budget > 0 ? (int)(budget / p.stage_bytes) : 0;
   if (p.stages > kMaxStages) p.stages = kMaxStages;
   if (p.stages < 2) return launch_replay(GDNBEAM_BF16, a, s);
   p.sctx = a.sctx; p.sctx_rstride = a.sctx_rstride;
   p.alpha = a.alpha; p.beta = a.beta;
-  p.v = (const __nv_bfloat16*)a.v;
+  RecMaps rm;
+  memset(&rm, 0, sizeof(rm));
   for (int j = 0; j < a.t; ++j) {
-    p.rec_k[j] = (const __nv_bfloat16*)a.depth[j].k;
-    p.rec_d[j] = (const __nv_bfloat16*)a.depth[j].delta;
     p.rec_a[j] = a.depth[j].alpha;
     p.W_j[j] = a.depth[j].W_j;
-    if (((uintptr_t)p.rec_k[j] & 15) || ((uintptr_t)p.rec_d[j] & 15)) return GDNBEAM_EINVAL;
+    if (((uintptr_t)a.depth[j].k & 15) || ((uintptr_t)a.depth[j].delta & 15)) return GDNBEAM_EINVAL;
+    const long long rows = (long long)a.R * a.depth[j].W_j * a.H;
+    if (rows > 0x7FFFFFFFLL) return launch_replay(GDNBEAM_BF16, a, s);
+    if (!rows_map(&rm.d[j], a.depth[j].delta, rows) || !rows_map(&rm.k[j], a.depth[j].k, rows))
+      return GDNBEAM_ECUDA;
   }
   p.anc = a.anc; p.anc_stride = a.anc_stride;
-  p.delta_out = (__nv_bfloat16*)a.delta_out; p.o_out = (__nv_bfloat16*)a.o_out;
   p.x_inout = a.x_inout; p.delta_dump = a.delta_dump; p.o_dump = a.o_dump; p.err = a.err;
   if (((uintptr_t)a.sctx & 15) || (a.sctx_rstride % 4) != 0) return GDNBEAM_EINVAL;
-  CUtensorMap mq, mk;
-  if (!beam_map(&mq, a.q, a.R, a.W_t, a.H, true) || !beam_map(&mk, a.k, a.R, a.W_t, a.H, true))
+  CUtensorMap mq, mk, mv, md, mo;
+  if (!beam_map(&mq, a.q, a.R, a.W_t, a.H, true) || !beam_map(&mk, a.k, a.R, a.W_t, a.H, true) ||
+      !beam_map(&mv, a.v, a.R, a.W_t, a.H, false) ||
+      !beam_map(&md, a.delta_out, a.R, a.W_t, a.H, false, 32, 16) ||
+      !beam_map(&mo, a.o_out, a.R, a.W_t, a.H, false, 32, 16))
     return GDNBEAM_ECUDA;
-  const size_t dyn = 1024 + 2 * A_BYTES + (size_t)p.stages * p.stage_bytes;
+  const size_t dyn = 1024 + (size_t)p.stages * p.stage_bytes + table;
   switch (a.t) {
 #define GDN_REPLAY_TC(TD_)                                                                   \
   case TD_:                                                                                  \
     GDN_CUDA(cudaFuncSetAttribute(replay_tc_kernel<TD_>,                                     \
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));   \
-    replay_tc_kernel<TD_><<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, p);                       \
+    replay_tc_kernel<TD_><<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, mv, md, mo, rm, p);       \
     break;
     GDN_REPLAY_TC(0) GDN_REPLAY_TC(1) GDN_REPLAY_TC(2) GDN_REPLAY_TC(3) GDN_REPLAY_TC(4)
     GDN_REPLAY_TC(5) GDN_REPLAY_TC(6)

@@ -141,7 +141,7 @@ def test_ancestry_op_matches_walk():
     ("bf16", 128, 2, 2, 300, 0, False), ("bf16", 32, 1, 1, 5, 5, False),
     ("bf16", 128, 4, 3, 64, 3, False), ("bf16", 128, 1, 1, 1, 1, False),
     ("bf16", 128, 2, 1, 96, 5, False), ("bf16", 128, 2, 2, 40, 1, True),
-    ("bf16", 128, 3, 2, 512, 2, False)])
+    ("bf16", 128, 3, 2, 512, 2, False), ("bf16", 128, 2, 2, 70, 4, False)])
 def test_replay_op(dtype, d, H, R, W_t, t, resid):
     wl = synth.tiny_workload(d=d, V=7, H=H, R=R, dtype=dtype)
     rng = np.random.default_rng(d + H + W_t + t)
