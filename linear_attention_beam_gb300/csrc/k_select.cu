@@ -111,16 +111,42 @@ __device__ Key radix_kth(int n, unsigned K, Get get, unsigned* hist, unsigned* s
       if ((key & mask) == prefix) atomicAdd(&hist[(unsigned)(key >> shift) & 0xFFu], 1u);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned above = 0;
-      int d = 255;
-      for (; d > 0; --d) {
-        if (above + hist[d] >= remaining) break;
-        above += hist[d];
+    if (threadIdx.x < 32) {
+      // The highest bucket d >= 1 whose count from the top reaches
+      // `remaining` (bucket 0 when none does): lane l scans buckets
+      // 255 - 8l down to 248 - 8l after a warp scan of the lane totals.
+      const int l = threadIdx.x;
+      unsigned cnt[8], tot = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        cnt[k] = hist[255 - 8 * l - k];
+        tot += cnt[k];
       }
-      sh[0] = (unsigned)d;
-      sh[1] = remaining - above;
-      sh[2] = (hist[d] == remaining - above) ? 1u : 0u;  // the whole bucket is taken
+      unsigned incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (l >= o) incl += y;
+      }
+      const unsigned excl = incl - tot;
+      const unsigned hit = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
+      const int target = hit ? __ffs(hit) - 1 : 31;
+      if (l == target) {
+        unsigned above = excl;
+        int d = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int bin = 255 - 8 * l - k;
+          if (bin == 0 || above + cnt[k] >= remaining) {
+            d = bin;
+            break;
+          }
+          above += cnt[k];
+        }
+        sh[0] = (unsigned)d;
+        sh[1] = remaining - above;
+        sh[2] = (hist[d] == remaining - above) ? 1u : 0u;  // the whole bucket is taken
+      }
     }
     __syncthreads();
     prefix |= (Key)sh[0] << shift;
@@ -284,9 +310,9 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
   const int lane = threadIdx.x & 31;
   const uint32_t flat0 = (uint32_t)b * (uint32_t)V;
   uint64_t* out = ss.cand + (size_t)r * ss.cap;
+  // the row's scalars are read up front, beside the logits
+  const float cp = cum_prime(cum, bias, row), l = lse[row];
   bool bad = false;
-  float cp = 0.f, l = 0.f;
-  bool have_row = false;
   for (int v00 = 0; v00 < V; v00 += kFilterThreads * VEC * U) {
     uint32_t w[U][WORDS];
 #pragma unroll
@@ -334,11 +360,6 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
         }
       }
       if (!__any_sync(0xffffffffu, hits != 0)) continue;
-      if (!have_row) {
-        cp = cum_prime(cum, bias, row);
-        l = lse[row];
-        have_row = true;
-      }
       const int mine = __popc(hits);
       int incl = mine;
 #pragma unroll
@@ -363,7 +384,7 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
       }
     }
   }
-  if (!isfinite(lse[row]) || !isfinite(cum_prime(cum, bias, row))) bad = true;
+  if (!isfinite(l) || !isfinite(cp)) bad = true;
   if (bad) raise_error(err, GDNBEAM_DERR_NONFINITE);
 }
 
@@ -515,14 +536,6 @@ __global__ void ancestry_kernel(int R, int t, int T, int V, int W_prev, int W_t,
   so[t] = tok;
 }
 
-int sm_count() {
-  static int sms[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
-  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  return sms[dev] > 0 ? sms[dev] : 132;
-}
-
 template <typename T>
 int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, const float* cum,
                const float* bias, const float2* hint, int32_t* parents, int32_t* tokens,
@@ -575,6 +588,14 @@ int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, 
 }
 
 }  // namespace
+
+int sm_count() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
+  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return sms[dev] > 0 ? sms[dev] : 132;
+}
 
 size_t select_scratch_bytes(int R, int W_t, int W_next, int V) {
   size_t total = 0;

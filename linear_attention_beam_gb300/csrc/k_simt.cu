@@ -27,9 +27,53 @@ __global__ void gather_rows_kernel(int n, int d_model, const int32_t* __restrict
   }
 }
 
+// Same, 16 bytes per thread: chunk c of the output is row c / cpr, piece
+// c % cpr (cpr 16-byte pieces per row).
+template <typename T>
+__global__ void gather_rows_vec_kernel(long long chunks, int cpr, const int32_t* __restrict__ tokens,
+                                       int V, const uint4* __restrict__ E, uint4* __restrict__ u,
+                                       float4* __restrict__ x, unsigned* err) {
+  constexpr int EPC = 16 / (int)sizeof(T);
+  for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < chunks;
+       c += (long long)gridDim.x * blockDim.x) {
+    const long long m = c / cpr;
+    const int piece = (int)(c - m * cpr);
+    const int tok = __ldg(tokens + m);
+    const bool ok = tok >= 0 && tok < V;
+    if (!ok && piece == 0) raise_error(err, GDNBEAM_DERR_TOKEN);
+    const uint4 val = ok ? __ldg(E + (size_t)tok * cpr + piece) : make_uint4(0u, 0u, 0u, 0u);
+    u[c] = val;
+    if (x) {
+      const T* e = reinterpret_cast<const T*>(&val);
+      float f[EPC];
+#pragma unroll
+      for (int i = 0; i < EPC; ++i) f[i] = St<T>::to_f(e[i]);
+#pragma unroll
+      for (int i = 0; i < EPC / 4; ++i)
+        x[c * (EPC / 4) + i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+    }
+  }
+}
+
 int launch_gather_rows(int dtype, int n, int d_model, const int32_t* tokens, int V,
                        const void* E, void* u, float* x, unsigned* err, cudaStream_t s) {
   if (n <= 0) return GDNBEAM_OK;
+  const int esz = dtype == GDNBEAM_BF16 ? 2 : 4;
+  if ((d_model * esz) % 16 == 0 && ((uintptr_t)E & 15) == 0 && ((uintptr_t)u & 15) == 0 &&
+      ((uintptr_t)x & 15) == 0) {
+    const int cpr = d_model * esz / 16;
+    const long long chunks = (long long)n * cpr;
+    const long long want = (chunks + 255) / 256;
+    const int blocks = (int)(want < 16 * sm_count() ? want : 16 * sm_count());
+    if (dtype == GDNBEAM_BF16)
+      gather_rows_vec_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+          chunks, cpr, tokens, V, (const uint4*)E, (uint4*)u, (float4*)x, err);
+    else
+      gather_rows_vec_kernel<float><<<blocks, 256, 0, s>>>(chunks, cpr, tokens, V, (const uint4*)E,
+                                                           (uint4*)u, (float4*)x, err);
+    GDN_LAUNCH_CHECK();
+    return GDNBEAM_OK;
+  }
   if (dtype == GDNBEAM_BF16)
     gather_rows_kernel<__nv_bfloat16><<<n, 256, 0, s>>>(n, d_model, tokens, V,
         (const __nv_bfloat16*)E, (__nv_bfloat16*)u, x, err);

@@ -46,6 +46,9 @@ int launch_tc_logits(const gdnbeam_config& c, int n, const void* feat, const voi
 
 // ---- replay, prefill, selection, ancestry ---------------------------------
 
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
 struct ReplayArgs {
   int R, H, d_k, d_v, t, W_t;
   const float* sctx;  // fp32 [R][H][d_v][d_k], request stride sctx_rstride
