@@ -56,7 +56,10 @@ enum {
   GDNBEAM_DERR_TOKEN = 1,     /* token id outside [0, V) */
   GDNBEAM_DERR_PARENT = 2,    /* parent index outside [0, W_{t-1}) */
   GDNBEAM_DERR_SLOT = 4,      /* ancestry slot outside its depth's beam count */
-  GDNBEAM_DERR_NONFINITE = 8, /* a score was NaN or infinite */
+  GDNBEAM_DERR_NONFINITE = 8, /* a NaN or infinite logit, lse or cumulative score reached
+                               * selection (when the logits stage's tile maxima are
+                               * reused, a NaN or +inf logit shows through its row's
+                               * lse; a -inf logit then scores -inf unflagged) */
   GDNBEAM_DERR_TIMEOUT = 16,  /* a bounded on-chip wait gave up */
   GDNBEAM_DERR_SELECT = 32    /* selection bookkeeping inconsistency */
 };

@@ -26,6 +26,8 @@ MAX_T = 8
 STAGES = ("ancestry", "embed", "project", "replay", "logits", "select", "prefill")
 
 OK, EINVAL, EUNSUPPORTED, EWORKSPACE, ESTATE, ECUDA, EDEVICE, ENOMEM = 0, -1, -2, -3, -4, -5, -6, -7
+# device error word bits (gdnbeam_device_status)
+DERR_TOKEN, DERR_PARENT, DERR_SLOT, DERR_NONFINITE, DERR_TIMEOUT, DERR_SELECT = 1, 2, 4, 8, 16, 32
 DERR = {"token": 1, "parent": 2, "slot": 4, "nonfinite": 8, "timeout": 16, "select": 32}
 
 

@@ -255,7 +255,7 @@ int logits_any(const gdnbeam_config& c, bool tc, int n, const void* feat, const 
   st = launch_logits_rows(c.dtype, n, c.V, (const float*)scratch, z, lse,
                           d ? d->logits : nullptr, s);
   if (st || !tstats) return st;
-  return launch_tile_max(c.dtype, n, c.V, z, tstats, s);
+  return launch_tile_max(c.dtype, n, c.V, z, tstats, error_word(), s);
 }
 
 gdnbeam_dumps layer_dumps(const gdnbeam_dumps* d, const gdnbeam_config& c, int layer, size_t n) {

@@ -229,7 +229,7 @@ SelScratch carve_sel(void* base, int R, int W_t, int W_next, int V, size_t* tota
 // ---- hint pre-pass: the maximum stored logit of every (row, 256-code tile)
 template <typename T>
 __global__ void tile_max_kernel(int n, int V, int n_tiles, const T* __restrict__ z,
-                                float2* __restrict__ hint) {
+                                float2* __restrict__ hint, unsigned* err) {
   const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= (long long)n * n_tiles) return;
@@ -237,9 +237,15 @@ __global__ void tile_max_kernel(int n, int V, int n_tiles, const T* __restrict__
   const T* zr = z + (size_t)row * V + (size_t)tile * kTile;
   const int cnt = min(kTile, V - tile * kTile);
   float mx = -INFINITY;
-  for (int c = lane; c < cnt; c += 32) mx = fmaxf(mx, ldf(zr + c));
+  bool bad = false;
+  for (int c = lane; c < cnt; c += 32) {
+    const float zv = ldf(zr + c);
+    bad |= !isfinite(zv);
+    mx = fmaxf(mx, zv);
+  }
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane == 0) hint[w] = make_float2(mx, 0.0f);
+  if (bad) raise_error(err, GDNBEAM_DERR_NONFINITE);
 }
 
 // ---- bound: the W_next-th largest hint score of each request
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
   }
   if (W_next > n_h) {  // too few hints for a bound: keep every candidate
     if (threadIdx.x == 0) ss.thr[r] = 0u;
-    for (int b = threadIdx.x; b < W_t; b += blockDim.x) ss.zcut[(size_t)r * W_t + b] = 0u;
+    for (int b = threadIdx.x; b < W_t; b += blockDim.x) ss.zcut[(size_t)r * W_t + b] = SKey<T>::kNegInf;
     return;
   }
   auto key_of = [&](int i) -> uint32_t {
@@ -293,10 +299,13 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
 }
 
 // ---- filter: append every candidate whose score reaches the bound
-// A candidate qualifies when its stored logit's key reaches the row's cutoff
-// key (an integer compare; two bf16 keys per 32-bit word with SIMD compares);
-// scores are evaluated only for the rare hits. Each thread keeps U 16-byte
-// loads in flight; a warp votes before it scans for append slots.
+// A candidate qualifies when its stored logit reaches the row's cutoff value
+// (the logit whose storage key is the cutoff key: for non-NaN logits the two
+// orders agree, -0 and +0 scoring alike). bf16 logits are compared two at a
+// time with packed compares; scores are evaluated only for the rare hits.
+// Each thread keeps U 16-byte loads in flight; a warp votes before it scans
+// for append slots. Non-finite logits show in the row's lse (NaN or +inf
+// logits make it non-finite), which is checked here.
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
     int W_t, int V, const T* __restrict__ z, const float* __restrict__ lse,
@@ -305,14 +314,19 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
   constexpr int WORDS = VEC > 1 ? 4 : 1;  // 32-bit words per 16-byte load
   const int row = blockIdx.x;
   const int r = row / W_t, b = row % W_t;
-  const uint32_t cut = ss.zcut[row];
+  const float thr = SKey<T>::value(ss.zcut[row]);  // NaN when no logit qualifies
+  const __nv_bfloat16 thr_b = __float2bfloat16_rn(thr);  // exact: thr is a storage value
+  const __nv_bfloat162 thr2 = __halves2bfloat162(thr_b, thr_b);
   const T* zr = z + (size_t)row * V;
   const int lane = threadIdx.x & 31;
   const uint32_t flat0 = (uint32_t)b * (uint32_t)V;
   uint64_t* out = ss.cand + (size_t)r * ss.cap;
   // the row's scalars are read up front, beside the logits
   const float cp = cum_prime(cum, bias, row), l = lse[row];
-  bool bad = false;
+  auto zval = [&](const uint32_t* wu, int j) {
+    return sizeof(T) == 2 ? __uint_as_float(((wu[j >> 1] >> (16 * (j & 1))) & 0xFFFFu) << 16)
+                          : __uint_as_float(wu[j]);
+  };
   for (int v00 = 0; v00 < V; v00 += kFilterThreads * VEC * U) {
     uint32_t w[U][WORDS];
 #pragma unroll
@@ -335,31 +349,29 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int v = v00 + (u * kFilterThreads + threadIdx.x) * VEC;
-      unsigned hits = 0;
+      bool any = false;
       if (v < V) {
         if constexpr (sizeof(T) == 2 && VEC > 1) {
-          const uint32_t cut2 = cut | (cut << 16);
+          uint32_t m = 0;
 #pragma unroll
           for (int q = 0; q < WORDS; ++q) {
-            const uint32_t x = w[u][q];
-            const uint32_t sgn = (x >> 15) & 0x00010001u;
-            const uint32_t key = x ^ (0x80008000u | (sgn * 0x7FFFu));  // two storage keys
-            const uint32_t ge = __vcmpgeu2(key, cut2);
-            hits |= ((ge & 1u) | ((ge >> 15) & 2u)) << (2 * q);
-            bad |= __vcmpeq2(x & 0x7F807F80u, 0x7F807F80u) != 0u;  // Inf or NaN
+            __nv_bfloat162 x2;
+            *reinterpret_cast<uint32_t*>(&x2) = w[u][q];
+            m |= __hge2_mask(x2, thr2);
           }
+          any = m != 0;
         } else {
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) {
-            const uint32_t bits = sizeof(T) == 2 ? ((w[u][j >> 1] >> (16 * (j & 1))) & 0xFFFFu) : w[u][j];
-            if (v + j < V) {
-              if (SKey<T>::of_bits(bits) >= cut) hits |= 1u << j;
-              bad |= sizeof(T) == 2 ? ((bits & 0x7F80u) == 0x7F80u) : ((bits & 0x7F800000u) == 0x7F800000u);
-            }
-          }
+          for (int j = 0; j < VEC; ++j) any |= (v + j < V) && zval(w[u], j) >= thr;
         }
       }
-      if (!__any_sync(0xffffffffu, hits != 0)) continue;
+      if (!__any_sync(0xffffffffu, any)) continue;
+      unsigned hits = 0;
+      if (any) {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+          if (v + j < V && zval(w[u], j) >= thr) hits |= 1u << j;
+      }
       const int mine = __popc(hits);
       int incl = mine;
 #pragma unroll
@@ -375,15 +387,14 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
 #pragma unroll
       for (int j = 0; j < VEC; ++j) {
         if (hits & (1u << j)) {
-          const uint32_t bits = sizeof(T) == 2 ? ((w[u][j >> 1] >> (16 * (j & 1))) & 0xFFFFu) : w[u][j];
-          const float zv = sizeof(T) == 2 ? __uint_as_float(bits << 16) : __uint_as_float(bits);
-          const uint32_t o = orderable(score(cp, zv, l));
+          const uint32_t o = orderable(score(cp, zval(w[u], j), l));
           if (idx < ss.cap) out[idx] = make_key(o, flat0 + (uint32_t)(v + j));
           ++idx;
         }
       }
     }
   }
+  bool bad = false;
   if (!isfinite(l) || !isfinite(cp)) bad = true;
   if (bad) raise_error(err, GDNBEAM_DERR_NONFINITE);
 }
@@ -546,7 +557,7 @@ int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, 
   SelScratch ss = carve_sel(scratch, R, W_t, W_next, V, nullptr);
   if (!hint) {
     const long long warps = (long long)n * n_tiles;
-    tile_max_kernel<T><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(n, V, n_tiles, z, ss.hint);
+    tile_max_kernel<T><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(n, V, n_tiles, z, ss.hint, err);
     GDN_LAUNCH_CHECK();
     hint = ss.hint;
   }
@@ -615,16 +626,17 @@ int launch_select(int R, int W_t, int W_next, int V, int dtype, const void* logi
                            tokens, cum_next, scratch, err, s);
 }
 
-int launch_tile_max(int dtype, int n, int V, const void* z, float2* hint, cudaStream_t s) {
+int launch_tile_max(int dtype, int n, int V, const void* z, float2* hint, unsigned* err,
+                    cudaStream_t s) {
   const int n_tiles = (V + kTile - 1) / kTile;
   const long long warps = (long long)n * n_tiles;
   if (warps == 0) return GDNBEAM_OK;
   if (dtype == GDNBEAM_BF16)
     tile_max_kernel<__nv_bfloat16><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
-        n, V, n_tiles, (const __nv_bfloat16*)z, hint);
+        n, V, n_tiles, (const __nv_bfloat16*)z, hint, err);
   else
     tile_max_kernel<float><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(n, V, n_tiles,
-                                                                      (const float*)z, hint);
+                                                                      (const float*)z, hint, err);
   GDN_LAUNCH_CHECK();
   return GDNBEAM_OK;
 }

@@ -98,7 +98,8 @@ int launch_select(int R, int W_t, int W_next, int V, int dtype, const void* logi
                   int32_t* parents, int32_t* tokens, float* cum_next, void* scratch,
                   unsigned* err, cudaStream_t s);
 // Per (row, 256-code tile) maximum of stored logits into hint[row][tile].x.
-int launch_tile_max(int dtype, int n, int V, const void* z, float2* hint, cudaStream_t s);
+int launch_tile_max(int dtype, int n, int V, const void* z, float2* hint, unsigned* err,
+                    cudaStream_t s);
 constexpr int kHintTile = 256;
 
 // Device error word of the current device (defined with the C ABI).

@@ -31,6 +31,15 @@ def test_library_exports_every_declared_function():
     assert set(names) <= set(gb._SIGS)
 
 
+def test_binding_constants_match_the_header():
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    vals = {k: int(v) for k, v in re.findall(r"\b(GDNBEAM_[A-Z0-9_]+)\s*=\s*(-?\d+)", src)}
+    for name in ("OK", "EINVAL", "EUNSUPPORTED", "EWORKSPACE", "ESTATE", "ECUDA", "EDEVICE", "ENOMEM",
+                 "F32", "BF16", "DERR_TOKEN", "DERR_PARENT", "DERR_SLOT", "DERR_NONFINITE",
+                 "DERR_TIMEOUT", "DERR_SELECT"):
+        assert vals["GDNBEAM_" + name] == getattr(gb, name), name
+
+
 def cfg(wl, **kw):
     d = dict(R=wl.R, layers=wl.layers, H=wl.H, d_k=wl.d_k, d_v=wl.d_v, d_model=wl.d_model, V=wl.V,
              T=wl.T, W_max=wl.W_max, L_max=wl.L, dtype=gb.BF16 if wl.dtype == "bf16" else gb.F32,

@@ -349,3 +349,33 @@ def test_select_massive_ties_take_the_exact_fallback(dtype):
     for r in range(R):
         np.testing.assert_array_equal(par[r].cpu().numpy(), [0] * 5)
         np.testing.assert_array_equal(tok[r].cpu().numpy(), [0, 1, 2, 3, 4])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("bad", ["nan_logit", "inf_logit", "nan_lse"])
+def test_select_flags_non_finite_inputs(dtype, bad):
+    # a NaN or +inf logit (tile maxima computed by the selection itself) or a
+    # non-finite lse sets GDNBEAM_DERR_NONFINITE; the call still returns
+    R, W_t, W_next, V = 2, 16, 8, 300
+    rng = np.random.default_rng(7)
+    z = rng.standard_normal((R * W_t, V)).astype(np.float32)
+    lse = np.log(np.exp(z.astype(np.float64)).sum(1)).astype(np.float32)
+    cum = np.zeros(R * W_t, np.float32)
+    if bad == "nan_logit":
+        z[5, 17] = np.nan
+    elif bad == "inf_logit":
+        z[20, 299] = np.inf
+    else:
+        lse[3] = np.nan
+    lib = gb.load()
+    assert device_status_clear() == 0
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    scratch = torch.empty(lib.gdnbeam_select_scratch_bytes(R, W_t, W_next, V), dtype=torch.uint8, device=DEV)
+    par = torch.empty(R, W_next, dtype=torch.int32, device=DEV)
+    tok = torch.empty_like(par)
+    cn = torch.empty(R, W_next, device=DEV)
+    assert lib.gdnbeam_select_topw(R, W_t, W_next, V, gb.BF16 if dtype == "bf16" else gb.F32,
+                                   gb.ptr(to_dev(z, td)), gb.ptr(to_dev(lse)), gb.ptr(to_dev(cum)), None,
+                                   gb.ptr(par), gb.ptr(tok), gb.ptr(cn), gb.ptr(scratch), scratch.numel(),
+                                   None) == 0
+    assert device_status_clear() & gb.DERR_NONFINITE
