@@ -33,6 +33,7 @@ namespace {
 constexpr int kTile = 256;           // codes per hint tile (the logits GEMM tile width)
 constexpr int kBoundThreads = 1024;
 constexpr int kFilterThreads = 256;
+constexpr int kFilterBlocksPerReq = 32;  // 256 warps share a request's listed tiles
 constexpr int kFinalThreads = 1024;
 constexpr int kFinalSmemKeys = 16384; // candidates a final block keeps on chip
 constexpr int kRowThreads = 512;
@@ -47,33 +48,11 @@ __device__ __forceinline__ float score(float cp, float zv, float l) {
   return __fadd_rn(cp, __fsub_rn(zv, l));
 }
 
-// Unpacks one 16-byte load into VEC stored values, as floats.
-template <typename T, int VEC> struct Unpack;
-template <> struct Unpack<__nv_bfloat16, 8> {
-  static __device__ __forceinline__ void run(const uint4& r, float (&f)[8]) {
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __uint_as_float(w[i] << 16);
-      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
-};
-template <> struct Unpack<float, 4> {
-  static __device__ __forceinline__ void run(const uint4& r, float (&f)[4]) {
-    f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
-    f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
-  }
-};
-
 // Order-preserving integer keys of stored logits (larger value, larger key;
 // NaN patterns sort beyond the infinities).
 template <typename T> struct SKey;
 template <> struct SKey<__nv_bfloat16> {
   static constexpr uint32_t kNegInf = 0x007Fu, kPosInf = 0xFF80u;
-  static __device__ __forceinline__ uint32_t of_bits(uint32_t b) {
-    return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
-  }
   static __device__ __forceinline__ float value(uint32_t k) {
     const uint32_t b = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
     return __uint_as_float(b << 16);
@@ -81,9 +60,6 @@ template <> struct SKey<__nv_bfloat16> {
 };
 template <> struct SKey<float> {
   static constexpr uint32_t kNegInf = 0x007FFFFFu, kPosInf = 0xFF800000u;
-  static __device__ __forceinline__ uint32_t of_bits(uint32_t b) {
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  }
   static __device__ __forceinline__ float value(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
   }
@@ -192,12 +168,22 @@ struct SelScratch {
   uint64_t* cand;   // [R][cap]
   uint64_t* pre;    // [R*W_t][K] fallback precut keys
   float2* hint;     // [R*W_t][n_tiles] tile maxima computed here when not supplied
-  uint32_t* zcut;   // [R*W_t] per row: storage key of the smallest logit whose score
-                    // reaches the bound (scores are monotone in the stored logit)
+  int* tcount;      // [R] (row, tile) pairs whose tile maximum reaches the bound
+  uint32_t* tlist;  // [R][cap_tiles] those pairs, as b * n_tiles + tile
   int cap;
+  int cap_tiles;
 };
 
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Room for the listed tiles of one request: the bound keeps at least W_next
+// tiles (ties at the bound add more); a longer list sends the request to the
+// exact fallback.
+int cap_tiles_of(int W_t, int W_next, int V) {
+  const long long n_h = (long long)W_t * ((V + kTile - 1) / kTile);
+  long long c = 2LL * W_next + 256;
+  return (int)(c < n_h ? c : n_h);
+}
 
 int cap_of(int W_t, int W_next, int V) {
   long long cap = 16LL * W_next;
@@ -211,6 +197,7 @@ SelScratch carve_sel(void* base, int R, int W_t, int W_next, int V, size_t* tota
   const int K = W_next < V ? W_next : V;
   const int n_tiles = (V + kTile - 1) / kTile;
   s.cap = cap_of(W_t, W_next, V);
+  s.cap_tiles = cap_tiles_of(W_t, W_next, V);
   char* p = (char*)base;
   size_t off = 0;
   auto take = [&](size_t b) { char* q = p ? p + off : nullptr; off += a256(b); return q; };
@@ -221,7 +208,8 @@ SelScratch carve_sel(void* base, int R, int W_t, int W_next, int V, size_t* tota
   s.cand = (uint64_t*)take((size_t)R * s.cap * 8);
   s.pre = (uint64_t*)take((size_t)R * W_t * K * 8);
   s.hint = (float2*)take((size_t)R * W_t * n_tiles * sizeof(float2));
-  s.zcut = (uint32_t*)take((size_t)R * W_t * 4);
+  s.tcount = (int*)take((size_t)R * 4);
+  s.tlist = (uint32_t*)take((size_t)R * s.cap_tiles * 4);
   if (total) *total = off;
   return s;
 }
@@ -248,25 +236,31 @@ __global__ void tile_max_kernel(int n, int V, int n_tiles, const T* __restrict__
   if (bad) raise_error(err, GDNBEAM_DERR_NONFINITE);
 }
 
-// ---- bound: the W_next-th largest hint score of each request
+// ---- bound: the W_next-th largest hint score of each request, and the tiles
+// that can hold a candidate. A code scores at most its tile's maximum (the
+// score is monotone in the stored logit within a row), so only tiles whose
+// maximum reaches the bound are listed for the filter.
 template <typename T>
 __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
     int W_t, int V, int n_tiles, int W_next, const float2* __restrict__ hint,
     const float* __restrict__ lse, const float* __restrict__ cum, const float* __restrict__ bias,
-    SelScratch ss, int smem_keys) {
+    SelScratch ss, int smem_keys, unsigned* err) {
   extern __shared__ uint32_t hkeys[];
   __shared__ unsigned hist[256];
   __shared__ unsigned sh[3];
+  __shared__ int s_cnt;
   const int r = blockIdx.x;
   const int n_h = W_t * n_tiles;
   if (threadIdx.x == 0) {
     ss.count[r] = 0;
+    s_cnt = 0;
     if (r == 0) *ss.fb_any = 0;
   }
-  if (W_next > n_h) {  // too few hints for a bound: keep every candidate
-    if (threadIdx.x == 0) ss.thr[r] = 0u;
-    for (int b = threadIdx.x; b < W_t; b += blockDim.x) ss.zcut[(size_t)r * W_t + b] = SKey<T>::kNegInf;
-    return;
+  // a row whose lse or cumulative score is not finite is flagged
+  for (int b = threadIdx.x; b < W_t; b += blockDim.x) {
+    const size_t row = (size_t)r * W_t + b;
+    if (!isfinite(lse[row]) || !isfinite(cum_prime(cum, bias, row)))
+      raise_error(err, GDNBEAM_DERR_NONFINITE);
   }
   auto key_of = [&](int i) -> uint32_t {
     const int b = i / n_tiles;
@@ -275,18 +269,54 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
     const float zs = St<T>::to_f(St<T>::from_f(zm));  // stored value of the tile's top element
     return orderable(score(cum_prime(cum, bias, row), zs, lse[row]));
   };
-  uint32_t t;
-  if (n_h <= smem_keys) {
-    for (int i = threadIdx.x; i < n_h; i += blockDim.x) hkeys[i] = key_of(i);
-    __syncthreads();
-    t = radix_kth<uint32_t>(n_h, (unsigned)W_next, [&](int i) { return hkeys[i]; }, hist, sh);
-  } else {
-    t = radix_kth<uint32_t>(n_h, (unsigned)W_next, key_of, hist, sh);
+  const bool on_chip = n_h <= smem_keys;
+  uint32_t t = 0u;  // too few hints for a bound: keep every tile
+  if (W_next <= n_h) {
+    if (on_chip) {
+      for (int i = threadIdx.x; i < n_h; i += blockDim.x) hkeys[i] = key_of(i);
+      __syncthreads();
+      t = radix_kth<uint32_t>(n_h, (unsigned)W_next, [&](int i) { return hkeys[i]; }, hist, sh);
+    } else {
+      t = radix_kth<uint32_t>(n_h, (unsigned)W_next, key_of, hist, sh);
+    }
   }
   if (threadIdx.x == 0) ss.thr[r] = t;
-  // per row, the smallest stored logit whose score reaches t (bisection over
-  // the storage keys; the score is monotone in the logit)
-  for (int b = threadIdx.x; b < W_t; b += blockDim.x) {
+  __syncthreads();
+  uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
+  for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
+    const bool take = t == 0u || (on_chip ? hkeys[i] : key_of(i)) >= t;
+    if (take) {
+      const int pos = atomicAdd(&s_cnt, 1);
+      if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) ss.tcount[r] = s_cnt;
+}
+
+// ---- filter: append every code of the listed tiles whose score reaches the
+// bound. One warp per listed tile (256 codes, eight per lane). The row's
+// cutoff logit (the smallest stored value whose score reaches the bound) is
+// found by bisection over the storage keys, so codes are compared as stored
+// values and scores are computed only for hits.
+template <typename T>
+__global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
+    int W_t, int V, int n_tiles, int blocks_per_req, const T* __restrict__ z,
+    const float* __restrict__ lse, const float* __restrict__ cum, const float* __restrict__ bias,
+    SelScratch ss) {
+  constexpr int EPL = kTile / 32;          // codes per lane
+  const int r = blockIdx.x / blocks_per_req;
+  const int lane = threadIdx.x & 31;
+  const int warps = blocks_per_req * (kFilterThreads / 32);
+  const int n_list = min(ss.tcount[r], ss.cap_tiles);
+  const uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
+  const uint32_t t = ss.thr[r];
+  uint64_t* out = ss.cand + (size_t)r * ss.cap;
+  const bool vec = (V % 8) == 0 && ((uintptr_t)z & 15) == 0;
+  for (int j = (blockIdx.x % blocks_per_req) * (kFilterThreads / 32) + (threadIdx.x >> 5); j < n_list;
+       j += warps) {
+    const uint32_t i = list[j];
+    const int b = (int)(i / (uint32_t)n_tiles), tile = (int)(i % (uint32_t)n_tiles);
     const size_t row = (size_t)r * W_t + b;
     const float cp = cum_prime(cum, bias, row), l = lse[row];
     uint32_t lo = SKey<T>::kNegInf, hi = SKey<T>::kPosInf + 1u;  // hi: none reaches t
@@ -294,109 +324,53 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
       const uint32_t mid = lo + ((hi - lo) >> 1);
       if (orderable(score(cp, SKey<T>::value(mid), l)) >= t) hi = mid; else lo = mid + 1u;
     }
-    ss.zcut[row] = lo;
-  }
-}
-
-// ---- filter: append every candidate whose score reaches the bound
-// A candidate qualifies when its stored logit reaches the row's cutoff value
-// (the logit whose storage key is the cutoff key: for non-NaN logits the two
-// orders agree, -0 and +0 scoring alike). bf16 logits are compared two at a
-// time with packed compares; scores are evaluated only for the rare hits.
-// Each thread keeps U 16-byte loads in flight; a warp votes before it scans
-// for append slots. Non-finite logits show in the row's lse (NaN or +inf
-// logits make it non-finite), which is checked here.
-template <typename T, int VEC>
-__global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
-    int W_t, int V, const T* __restrict__ z, const float* __restrict__ lse,
-    const float* __restrict__ cum, const float* __restrict__ bias, SelScratch ss, unsigned* err) {
-  constexpr int U = VEC > 1 ? 4 : 1;
-  constexpr int WORDS = VEC > 1 ? 4 : 1;  // 32-bit words per 16-byte load
-  const int row = blockIdx.x;
-  const int r = row / W_t, b = row % W_t;
-  const float thr = SKey<T>::value(ss.zcut[row]);  // NaN when no logit qualifies
-  const __nv_bfloat16 thr_b = __float2bfloat16_rn(thr);  // exact: thr is a storage value
-  const __nv_bfloat162 thr2 = __halves2bfloat162(thr_b, thr_b);
-  const T* zr = z + (size_t)row * V;
-  const int lane = threadIdx.x & 31;
-  const uint32_t flat0 = (uint32_t)b * (uint32_t)V;
-  uint64_t* out = ss.cand + (size_t)r * ss.cap;
-  // the row's scalars are read up front, beside the logits
-  const float cp = cum_prime(cum, bias, row), l = lse[row];
-  auto zval = [&](const uint32_t* wu, int j) {
-    return sizeof(T) == 2 ? __uint_as_float(((wu[j >> 1] >> (16 * (j & 1))) & 0xFFFFu) << 16)
-                          : __uint_as_float(wu[j]);
-  };
-  for (int v00 = 0; v00 < V; v00 += kFilterThreads * VEC * U) {
-    uint32_t w[U][WORDS];
+    const float thr = SKey<T>::value(lo);  // NaN when no code can qualify
+    const int v0 = tile * kTile + lane * EPL;
+    const T* zr = z + row * (size_t)V;
+    float zv[EPL];
+    if (vec && v0 + EPL <= V) {
+      if constexpr (sizeof(T) == 2) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(zr + v0));
+        const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = v00 + (u * kFilterThreads + threadIdx.x) * VEC;
-      if constexpr (VEC > 1) {
-        if (v < V) {
-          const uint4 x = __ldg(reinterpret_cast<const uint4*>(zr + v));
-          w[u][0] = x.x; w[u][1] = x.y; w[u][2] = x.z; w[u][3] = x.w;
-        } else {
-          w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0u;  // never tested (v >= V)
-        }
+        for (int e = 0; e < EPL; ++e) zv[e] = __uint_as_float(((wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
       } else {
-        w[u][0] = (v < V) ? (uint32_t)(sizeof(T) == 2
-                                           ? (uint32_t)__bfloat16_as_ushort(*(const __nv_bfloat16*)(zr + v))
-                                           : __float_as_uint(*(const float*)(zr + v)))
-                          : 0u;
+        const float4 a = __ldg(reinterpret_cast<const float4*>(zr + v0));
+        const float4 c = __ldg(reinterpret_cast<const float4*>(zr + v0 + 4));
+        zv[0] = a.x; zv[1] = a.y; zv[2] = a.z; zv[3] = a.w;
+        zv[4] = c.x; zv[5] = c.y; zv[6] = c.z; zv[7] = c.w;
       }
+    } else {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) zv[e] = v0 + e < V ? ldf(zr + v0 + e) : __int_as_float(0x7FC00000);
     }
+    unsigned hits = 0;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = v00 + (u * kFilterThreads + threadIdx.x) * VEC;
-      bool any = false;
-      if (v < V) {
-        if constexpr (sizeof(T) == 2 && VEC > 1) {
-          uint32_t m = 0;
+    for (int e = 0; e < EPL; ++e)
+      if (zv[e] >= thr) hits |= 1u << e;  // NaN never compares true
+    if (!__any_sync(0xffffffffu, hits != 0)) continue;
+    const int mine = __popc(hits);
+    int incl = mine;
 #pragma unroll
-          for (int q = 0; q < WORDS; ++q) {
-            __nv_bfloat162 x2;
-            *reinterpret_cast<uint32_t*>(&x2) = w[u][q];
-            m |= __hge2_mask(x2, thr2);
-          }
-          any = m != 0;
-        } else {
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int base = 0;
+    if (lane == 31) base = atomicAdd(ss.count + r, total);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    int idx = base + incl - mine;
+    const uint32_t flat0 = (uint32_t)b * (uint32_t)V;
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) any |= (v + j < V) && zval(w[u], j) >= thr;
-        }
-      }
-      if (!__any_sync(0xffffffffu, any)) continue;
-      unsigned hits = 0;
-      if (any) {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j)
-          if (v + j < V && zval(w[u], j) >= thr) hits |= 1u << j;
-      }
-      const int mine = __popc(hits);
-      int incl = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int total = __shfl_sync(0xffffffffu, incl, 31);
-      int base = 0;
-      if (lane == 31) base = atomicAdd(ss.count + r, total);
-      base = __shfl_sync(0xffffffffu, base, 31);
-      int idx = base + incl - mine;
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) {
-        if (hits & (1u << j)) {
-          const uint32_t o = orderable(score(cp, zval(w[u], j), l));
-          if (idx < ss.cap) out[idx] = make_key(o, flat0 + (uint32_t)(v + j));
-          ++idx;
-        }
+    for (int e = 0; e < EPL; ++e) {
+      if (hits & (1u << e)) {
+        const uint32_t o = orderable(score(cp, zv[e], l));
+        if (idx < ss.cap) out[idx] = make_key(o, flat0 + (uint32_t)(v0 + e));
+        ++idx;
       }
     }
   }
-  bool bad = false;
-  if (!isfinite(l) || !isfinite(cp)) bad = true;
-  if (bad) raise_error(err, GDNBEAM_DERR_NONFINITE);
 }
 
 // ---- final: exact top-W_next of the filtered candidates, sorted
@@ -409,7 +383,7 @@ __global__ void __launch_bounds__(kFinalThreads) select_final_kernel(
   __shared__ uint64_t win[kMaxSort];
   const int r = blockIdx.x;
   const int n_c = ss.count[r];
-  if (n_c < W_next || n_c > ss.cap) {
+  if (n_c < W_next || n_c > ss.cap || ss.tcount[r] > ss.cap_tiles) {
     if (threadIdx.x == 0) {
       ss.fb_flag[r] = 1;
       atomicOr(ss.fb_any, 1);
@@ -568,15 +542,13 @@ int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, 
   GDN_CUDA(cudaFuncSetAttribute(select_bound_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)(bound_smem > 0 ? bound_smem : 4)));
   select_bound_kernel<T><<<R, kBoundThreads, bound_smem, s>>>(W_t, V, n_tiles, W_next, hint, lse,
-                                                              cum, bias, ss, bound_keys);
+                                                              cum, bias, ss, bound_keys, err);
   GDN_LAUNCH_CHECK();
-  // filter
-  constexpr int VEC = 16 / sizeof(T);
-  const bool vec_ok = (V % VEC) == 0 && ((uintptr_t)z & 15) == 0;
-  if (vec_ok)
-    select_filter_kernel<T, VEC><<<n, kFilterThreads, 0, s>>>(W_t, V, z, lse, cum, bias, ss, err);
-  else
-    select_filter_kernel<T, 1><<<n, kFilterThreads, 0, s>>>(W_t, V, z, lse, cum, bias, ss, err);
+  // filter over the listed tiles
+  const int per_req = (ss.cap_tiles + kFilterThreads / 32 - 1) / (kFilterThreads / 32);
+  const int bpr = per_req < kFilterBlocksPerReq ? per_req : kFilterBlocksPerReq;
+  select_filter_kernel<T><<<R * bpr, kFilterThreads, 0, s>>>(W_t, V, n_tiles, bpr, z, lse, cum,
+                                                              bias, ss);
   GDN_LAUNCH_CHECK();
   // final
   const size_t fin_smem = (size_t)kFinalSmemKeys * 8;
