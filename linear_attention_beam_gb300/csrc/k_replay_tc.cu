@@ -22,10 +22,12 @@
 //     the per-tile path.
 //   * One thread issues tcgen05.mma into a double-buffered TMEM accumulator:
 //     column b holds u_q of beam b, column 32 + b its u_k, lane = value row.
-//   * Eight epilogue warps (thread = value row; two warps per TMEM lane
-//     group, 16 beams each) compute the replay scalars k_j.q_t, k_j.k_t and
-//     k_t.q_t one tile ahead, fold the records, apply eq. 8 and write delta_t
-//     and o_t into a double-buffered shared tile that TMA stores to memory.
+//   * Four scalar warps compute the replay scalars k_j.q_t, k_j.k_t and
+//     k_t.q_t of each tile and turn them into per-beam coefficients of the
+//     fold; eight epilogue warps (thread = value row; two warps per TMEM lane
+//     group, 16 beams each) fold the records, apply eq. 8 and write delta_t
+//     and o_t into double-buffered shared boxes that TMA stores to memory.
+//     Roles hand tiles over through mbarriers only, so warps drift freely.
 // Every wait is bounded in time (GDNBEAM_DERR_TIMEOUT on expiry).
 #include <cuda.h>
 #include <string.h>
@@ -42,7 +44,9 @@ constexpr int D = 128;            // head width (d_k = d_v)
 constexpr int NB = 32;            // beams per tile
 constexpr int kEpiWarps = 8;      // two per TMEM lane group; each folds 16 beams of a tile
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 64 + kEpiThreads + 64;  // producer, MMA, epilogue, two record loaders
+constexpr int kScalWarps = 4;     // replay-scalar warps, eight beams of a tile each
+constexpr int kThreads = 64 + kEpiThreads + 64 + 32 * kScalWarps;  // producer, MMA, epilogue,
+                                                                   // two record loaders, scalars
 constexpr int kMaxDepth = 6;      // replay depths this kernel stages
 constexpr int B_BYTES = 2 * NB * D * 2;     // q and k rows: 16 KiB
 constexpr int V_BYTES = NB * D * 2;         // v rows: 8 KiB
@@ -93,18 +97,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 //            [REC per depth: delta_j rows | k_j rows, each as two [32][64] halves]
 //   table: (alpha_t, beta_t) per beam, then per beam and depth the ancestor
 //          slot and its decay (negative for a slot outside its depth).
-template <int TD>  // replay depth t of this call
+// EXTRA: the fp32 dumps or the residual stream are written as well.
+template <int TD, bool EXTRA>  // replay depth t of this call
 __global__ void __launch_bounds__(kThreads, 1)
     replay_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_d,
                      const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ RecMaps rm,
                      TcReplayParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 7];
-  // replay scalars of two tiles (the fold reads one while the next is computed)
-  // per beam (beta_t, K0, Q0, k_t.q_t) and per ancestor record (K_j, Q_j): the
-  // fold written out, delta_t = beta_t v + K0 u_k + sum_j K_j delta_j and
-  // o_t = Q0 u_q + sum_j Q_j delta_j + (k_t.q_t) delta_t
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages + 11];
+  // replay scalars of two tiles: per beam (beta_t, K0, Q0, k_t.q_t) and per
+  // ancestor record (K_j, Q_j), the fold written out:
+  //   delta_t = beta_t v + K0 u_k + sum_j K_j delta_j,
+  //   o_t = Q0 u_q + sum_j Q_j delta_j + (k_t.q_t) delta_t
   __shared__ float4 s_beam[2][NB];
   __shared__ float2 s_rec[2][NB][TD > 0 ? TD : 1];
   // delta_t and o_t of two tiles, per epilogue warp a [16 beams][32 rows] box of each
@@ -124,24 +129,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty = [&](int s) { return bar(kMaxStages + s); };
   auto tfull = [&](int a) { return bar(2 * kMaxStages + a); };
   auto tempty = [&](int a) { return bar(2 * kMaxStages + 2 + a); };
-  const uint32_t a_ready = bar(2 * kMaxStages + 4);
-  const uint32_t tab_ready = bar(2 * kMaxStages + 5);
-  const uint32_t drain_bar = bar(2 * kMaxStages + 6);
+  auto sfull = [&](int a) { return bar(2 * kMaxStages + 4 + a); };   // scalars of a tile written
+  auto sempty = [&](int a) { return bar(2 * kMaxStages + 6 + a); };  // scalars of a tile used
+  const uint32_t a_ready = bar(2 * kMaxStages + 8);
+  const uint32_t tab_ready = bar(2 * kMaxStages + 9);
+  const uint32_t drain_bar = bar(2 * kMaxStages + 10);
   volatile int* abort = &s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x / p.H, h = blockIdx.x % p.H;
   constexpr int v_off = B_BYTES;
   constexpr int rec_off = B_BYTES + V_BYTES;
+  constexpr int kEpi0 = 2, kRec0 = 2 + kEpiWarps, kScal0 = kRec0 + 2;  // first warp of each role
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       tc::mbar_init(full(s), TD > 0 ? 3 : 1);  // the producer and the record loaders
-      tc::mbar_init(empty(s), 2);  // released by the MMA commit and by the epilogue
+      // released by the MMA commit, every epilogue warp and every scalar warp
+      tc::mbar_init(empty(s), 1 + kEpiWarps + kScalWarps);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull(a), 1);
       tc::mbar_init(tempty(a), kEpiWarps);
+      tc::mbar_init(sfull(a), kScalWarps);
+      tc::mbar_init(sempty(a), kEpiWarps);
     }
     tc::mbar_init(a_ready, kEpiWarps);
     tc::mbar_init(tab_ready, kEpiWarps);
@@ -184,13 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < p.stages; ++s)
         if (issued[s]) tc::mbar_wait_drain(full(s), issued_ph[s]);
     }
-  } else if (warp >= 2 + kEpiWarps) {
+  } else if (warp >= kRec0 && warp < kScal0) {
     // ---------------------------------------------------------------- records
     // warp kind (0: delta_j, 1: k_j) gathers its record rows of every tile,
     // four beams and one 64-column half per request; beams past the tile's
     // end repeat a valid row
     if (t > 0) {
-      const int kind = warp - (2 + kEpiWarps);
+      const int kind = warp - kRec0;
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait_sleep(tab_ready, 0, abort, p.err) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -231,6 +242,90 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < p.stages; ++s)
           if (issued[s]) tc::mbar_wait_drain(full(s), issued_ph[s]);
     }
+  } else if (warp >= kScal0) {
+    // ---------------------------------------------------------------- scalars
+    // replay scalars k_j.q_t, k_j.k_t (eqs. 6-7) and k_t.q_t (eq. 8) of every
+    // tile into buffer i & 1, turned into the fold's combined coefficients:
+    // four lanes per beam, 32 dimensions each; warp sw takes beams 8 sw ..
+    // 8 sw + 7
+    const int sw = warp - kScal0;
+    const int bl = sw * 8 + (lane >> 2);
+    const int c0 = (lane & 3) * 32;
+    bool ok = true;
+    if (lane == 0) ok = tc::mbar_wait_sleep(tab_ready, 0, abort, p.err);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    for (int i = 0; ok && i < p.n_tiles; ++i) {
+      const int s = i % p.stages;
+      const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+      const int sb = i & 1;
+      const uint32_t sph = (uint32_t)(i >> 1) & 1u;
+      const int b0 = i * NB;
+      const int nb = min(NB, p.W_t - b0);
+      // the buffer's previous tile has been folded, and this tile has landed
+      if (__any_sync(0xffffffffu, !tc::mbar_wait_sleep(sempty(sb), sph ^ 1u, abort, p.err) ||
+                                      !tc::mbar_wait_sleep(full(s), ph, abort, p.err))) {
+        ok = false;
+        break;
+      }
+      const uint8_t* gst = gbase + s * p.stage_bytes;
+      float part[1 + 2 * TD];
+#pragma unroll
+      for (int x = 0; x < 1 + 2 * TD; ++x) part[x] = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {  // 8 dimensions per step
+        const int c = c0 + ch * 8, kb = c >> 6, cc = c & 63;
+        const uint8_t* bk = gst + kb * (2 * NB * 128);
+        const uint4 qw = *reinterpret_cast<const uint4*>(bk + sw128_off(bl, cc));
+        const uint4 kw = *reinterpret_cast<const uint4*>(bk + sw128_off(NB + bl, cc));
+        const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, ka[4] = {kw.x, kw.y, kw.z, kw.w};
+        float q8[8], k8[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          q8[2 * e] = bf(qa[e] & 0xFFFFu); q8[2 * e + 1] = bf(qa[e] >> 16);
+          k8[2 * e] = bf(ka[e] & 0xFFFFu); k8[2 * e + 1] = bf(ka[e] >> 16);
+        }
+#pragma unroll
+        for (int x = 0; x < 8; ++x) part[0] = fmaf(k8[x], q8[x], part[0]);
+#pragma unroll
+        for (int j = 0; j < t; ++j) {
+          const uint4 rw = *reinterpret_cast<const uint4*>(
+              gst + rec_off + j * REC_BYTES + NB * D * 2 + kb * (NB * 128) + bl * 128 + cc * 2);
+          const uint32_t ra[4] = {rw.x, rw.y, rw.z, rw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float r0 = bf(ra[e] & 0xFFFFu), r1 = bf(ra[e] >> 16);
+            part[1 + 2 * j] = fmaf(r0, q8[2 * e], fmaf(r1, q8[2 * e + 1], part[1 + 2 * j]));
+            part[2 + 2 * j] = fmaf(r0, k8[2 * e], fmaf(r1, k8[2 * e + 1], part[2 + 2 * j]));
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 2; o > 0; o >>= 1)
+#pragma unroll
+        for (int x = 0; x < 1 + 2 * TD; ++x) part[x] += __shfl_xor_sync(0xffffffffu, part[x], o);
+      if ((lane & 3) == 0 && bl < nb) {
+        // The fold u <- alpha_j u + delta_j c_j over j = 0 .. t-1 (eqs. 6-7)
+        // leaves u = (prod_j alpha_j) u_ctx + sum_j (c_j prod_{m > j} alpha_m)
+        // delta_j; eq. 8 is linear in both projections.
+        const float2 ab = tab_ab[b0 + bl];  // (alpha_t, beta_t)
+        float tail = 1.f;                   // prod_{m > j} alpha_m
+#pragma unroll
+        for (int j = t - 1; j >= 0; --j) {
+          const float a = tab_aj[(b0 + bl) * t + j];
+          const bool use = a >= 0.f;  // a skipped record leaves both projections unchanged
+          const float wq = use ? part[1 + 2 * j] * tail : 0.f;
+          const float wk = use ? part[2 + 2 * j] * tail : 0.f;
+          s_rec[sb][bl][j] = make_float2(-ab.y * ab.x * wk, ab.x * wq);
+          if (use) tail *= a;
+        }
+        s_beam[sb][bl] = make_float4(ab.y, -ab.y * ab.x * tail, ab.x * tail, part[0]);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(sfull(sb));
+        tc::mbar_arrive(empty(s));  // this warp is done reading the stage
+      }
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -264,15 +359,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;                   // 0..7
-    const int ep = threadIdx.x - 64;           // 0..255
+    const int ew = warp - kEpi0;               // 0..7
     const int hb = ew >> 2;                    // which half of a tile (beams) / of K this warp takes
     const int lg = warp & 3;                   // TMEM lane group
     const int i_row = lg * 32 + lane;          // value row = TMEM lane
     const uint32_t lane_base = tmem_base + ((uint32_t)(lg * 32) << 16);
 
     // the block's table: gates, ancestor slots and decays of every beam
-    for (int b = ep; b < p.W_t; b += kEpiThreads) {
+    for (int b = ew * 32 + lane; b < p.W_t; b += kEpiThreads) {
       const size_t row = (size_t)r * p.W_t + b;
       tab_ab[b] = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
 #pragma unroll
@@ -292,20 +386,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(tab_ready);
 
-    // S_ctx row i_row, K half hb -> bf16 hi / lo words in TMEM
+    // S_ctx row i_row, K half hb -> bf16 hi / lo words in TMEM, 32 values at a time
     {
       const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * D * D +
                        (size_t)i_row * D + hb * 64;
-      float4 x[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) x[c] = __ldg(reinterpret_cast<const float4*>(S) + c);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
+        float4 x[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) x[c] = __ldg(reinterpret_cast<const float4*>(S) + half * 8 + c);
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const float4 v4 = x[half * 8 + c];
-          const float xs[4] = {v4.x, v4.y, v4.z, v4.w};
+          const float xs[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const float a0 = xs[2 * e], a1 = xs[2 * e + 1];
@@ -324,89 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(a_ready);
     }
-    // the scalar pass below reads the whole table
-    tc::named_sync(1, kEpiThreads);
 
-    // replay scalars k_j.q_t, k_j.k_t (eqs. 6-7) and k_t.q_t (eq. 8) of tile
-    // i into buffer i & 1: eight lanes per beam, 16 dimensions each; warp ew
-    // takes beams 4 ew .. 4 ew + 3
-    auto scalars = [&](int i) -> bool {
-      const int s = i % p.stages;
-      const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
-      const int b0 = i * NB;
-      const int nb = min(NB, p.W_t - b0);
-      if (__any_sync(0xffffffffu, !tc::mbar_wait_sleep(full(s), ph, abort, p.err))) return false;
-      const uint8_t* gst = gbase + s * p.stage_bytes;
-      const int bl = ew * 4 + (lane >> 3);
-      const int c0 = (lane & 7) * 16, kb = c0 >> 6, cc = c0 & 63;
-      const uint8_t* bk = gst + kb * (2 * NB * 128);
-      float q16[16], k16[16];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint4 qw = *reinterpret_cast<const uint4*>(bk + sw128_off(bl, cc + 8 * u));
-        const uint4 kw = *reinterpret_cast<const uint4*>(bk + sw128_off(NB + bl, cc + 8 * u));
-        const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, ka[4] = {kw.x, kw.y, kw.z, kw.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          q16[8 * u + 2 * e] = bf(qa[e] & 0xFFFFu); q16[8 * u + 2 * e + 1] = bf(qa[e] >> 16);
-          k16[8 * u + 2 * e] = bf(ka[e] & 0xFFFFu); k16[8 * u + 2 * e + 1] = bf(ka[e] >> 16);
-        }
-      }
-      float part[1 + 2 * TD];
-      float kq0 = 0.f, kq1 = 0.f;
-#pragma unroll
-      for (int x = 0; x < 16; x += 2) {
-        kq0 = fmaf(k16[x], q16[x], kq0);
-        kq1 = fmaf(k16[x + 1], q16[x + 1], kq1);
-      }
-      part[0] = kq0 + kq1;
-#pragma unroll
-      for (int j = 0; j < t; ++j) {
-        const uint8_t* kr = gst + rec_off + j * REC_BYTES + NB * D * 2 + kb * (NB * 128) + bl * 128 + cc * 2;
-        float cq0 = 0.f, ck0 = 0.f, cq1 = 0.f, ck1 = 0.f;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint4 rw = *reinterpret_cast<const uint4*>(kr + 16 * u);
-          const uint32_t ra[4] = {rw.x, rw.y, rw.z, rw.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float r0 = bf(ra[e] & 0xFFFFu), r1 = bf(ra[e] >> 16);
-            cq0 = fmaf(r0, q16[8 * u + 2 * e], cq0); cq1 = fmaf(r1, q16[8 * u + 2 * e + 1], cq1);
-            ck0 = fmaf(r0, k16[8 * u + 2 * e], ck0); ck1 = fmaf(r1, k16[8 * u + 2 * e + 1], ck1);
-          }
-        }
-        part[1 + 2 * j] = cq0 + cq1;
-        part[2 + 2 * j] = ck0 + ck1;
-      }
-#pragma unroll
-      for (int o = 4; o > 0; o >>= 1)
-#pragma unroll
-        for (int x = 0; x < 1 + 2 * TD; ++x) part[x] += __shfl_xor_sync(0xffffffffu, part[x], o);
-      if ((lane & 7) == 0 && bl < nb) {
-        // The fold u <- alpha_j u + delta_j c_j over j = 0 .. t-1 (eqs. 6-7)
-        // leaves u = (prod_j alpha_j) u_ctx + sum_j (c_j prod_{m > j} alpha_m)
-        // delta_j; eq. 8 is linear in both projections.
-        const int sb = i & 1;
-        const float2 ab = tab_ab[b0 + bl];  // (alpha_t, beta_t)
-        float tail = 1.f;                   // prod_{m > j} alpha_m
-#pragma unroll
-        for (int j = t - 1; j >= 0; --j) {
-          const float a = tab_aj[(b0 + bl) * t + j];
-          const bool use = a >= 0.f;  // a skipped record leaves both projections unchanged
-          const float wq = use ? part[1 + 2 * j] * tail : 0.f;
-          const float wk = use ? part[2 + 2 * j] * tail : 0.f;
-          s_rec[sb][bl][j] = make_float2(-ab.y * ab.x * wk, ab.x * wq);
-          if (use) tail *= a;
-        }
-        s_beam[sb][bl] = make_float4(ab.y, -ab.y * ab.x * tail, ab.x * tail, part[0]);
-      }
-      return true;
-    };
-
-    // A failed wait marks the epilogue dead: it then skips all work but keeps
-    // taking part in the named barriers, so no epilogue warp waits forever.
-    bool dead = p.n_tiles > 0 ? !scalars(0) : false;
-    tc::named_sync(1, kEpiThreads);
+    // A failed wait marks this warp dead: it then skips all work but keeps
+    // making its arrivals, so no other role waits on it forever.
+    bool dead = false;
     for (int i = 0; i < p.n_tiles; ++i) {
       const int s = i % p.stages;
       const int acc = i & 1;
@@ -414,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sb = i & 1;
       const int b0 = i * NB;
       const int nb = min(NB, p.W_t - b0);
-      if (!dead && i + 1 < p.n_tiles) dead = !scalars(i + 1);
+      if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(sfull(sb), aph, abort, p.err));
       if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(tfull(acc), aph, abort, p.err));
       if (!dead) {
         tc::fence_after_sync();
@@ -430,10 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* rd = gst + rec_off + (i_row >> 6) * (NB * 128) + (i_row & 63) * 2;
         const uint8_t* vs = gst + v_off + (i_row >> 6) * (NB * 128) + (i_row & 63) * 2;
         uint8_t* os = &s_out[sb][(hb * 4 + lg) * OUT_WARP] + lane * 2;
+        // the store of two tiles ago has read this output buffer (the one
+        // after it, to the other buffer, may still be in flight)
+        if (lane == 0) tc::bulk_wait_read<1>();
+        __syncwarp();
         // every beam of the half tile is computed; rows past the last beam
-        // are never stored (the tile store clips them). The loop touches
-        // shared memory only, so its loads overlap freely.
-        float dl[16], ov[16];
+        // are never stored (the tile store clips them)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int b = hb * 16 + e;
@@ -451,23 +467,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           o = fmaf(bm.w, delta, o);
           *reinterpret_cast<__nv_bfloat16*>(os + e * 64) = __float2bfloat16_rn(delta);
           *reinterpret_cast<__nv_bfloat16*>(os + OUT_WARP / 2 + e * 64) = __float2bfloat16_rn(o);
-          dl[e] = delta;
-          ov[e] = o;
-        }
-        if (p.delta_dump || p.o_dump || p.x_inout) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int b = hb * 16 + e;
+          if constexpr (EXTRA) {
             if (b < nb) {
               const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * D + i_row;
-              if (p.delta_dump) p.delta_dump[goff] = dl[e];
-              if (p.o_dump) p.o_dump[goff] = ov[e];
-              if (p.x_inout) p.x_inout[goff] += ov[e];
+              if (p.delta_dump) p.delta_dump[goff] = delta;
+              if (p.o_dump) p.o_dump[goff] = o;
+              if (p.x_inout) p.x_inout[goff] += o;
             }
           }
         }
-        // this warp's boxes go out by TMA; the store of two tiles ago has
-        // read the other buffer before the next tile writes it
+        // this warp's boxes go out by TMA
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -477,13 +486,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tma_store_3d(&tm_o, h * D + lg * 32, b0 + hb * 16, r, ob + OUT_WARP / 2);
           }
           tc::bulk_commit();
-          tc::bulk_wait_read<1>();
         }
-        __syncwarp();
       }
-      // every epilogue warp is done with stage s and scalar buffer sb
-      tc::named_sync(1, kEpiThreads);
-      if (ep == 0 && !dead) tc::mbar_arrive(empty(s));
+      // this warp is done with the tile's stage and scalars
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(sempty(sb));
+        tc::mbar_arrive(empty(s));
+      }
     }
     if (lane == 0) tc::bulk_wait_all();
   }
@@ -586,12 +596,19 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
       !beam_map(&mo, a.o_out, a.R, a.W_t, a.H, false, 32, 16))
     return GDNBEAM_ECUDA;
   const size_t dyn = 1024 + (size_t)p.stages * p.stage_bytes + table;
+  const bool extra = a.delta_dump || a.o_dump || a.x_inout;
   switch (a.t) {
 #define GDN_REPLAY_TC(TD_)                                                                   \
   case TD_:                                                                                  \
-    GDN_CUDA(cudaFuncSetAttribute(replay_tc_kernel<TD_>,                                     \
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));   \
-    replay_tc_kernel<TD_><<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, mv, md, mo, rm, p);       \
+    if (extra) {                                                                             \
+      GDN_CUDA(cudaFuncSetAttribute(replay_tc_kernel<TD_, true>,                             \
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn)); \
+      replay_tc_kernel<TD_, true><<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, mv, md, mo, rm, p); \
+    } else {                                                                                 \
+      GDN_CUDA(cudaFuncSetAttribute(replay_tc_kernel<TD_, false>,                            \
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn)); \
+      replay_tc_kernel<TD_, false><<<a.R * a.H, kThreads, dyn, s>>>(mq, mk, mv, md, mo, rm, p); \
+    }                                                                                        \
     break;
     GDN_REPLAY_TC(0) GDN_REPLAY_TC(1) GDN_REPLAY_TC(2) GDN_REPLAY_TC(3) GDN_REPLAY_TC(4)
     GDN_REPLAY_TC(5) GDN_REPLAY_TC(6)
