@@ -87,7 +87,11 @@ typedef struct gdnbeam_config {
   int state_path; /* 0: shared context + records + projection replay (OneLA);
                      1: FullState baseline, one d_v x d_k state per beam copied
                         on reorder (OneLA §3 "Controlled FullState"): same
-                        pipeline, only the state path swapped */
+                        pipeline, only the state path swapped;
+                     2: ReplaySSM baseline (OneLA §1, Fig. 2): no per-beam
+                        state; every step rebuilds each beam's parent state
+                        from the stored S_ctx by replaying its ancestors'
+                        records, then applies the current token */
 } gdnbeam_config;
 
 /* Weights, storage type, row-major, owned by the caller and kept alive for

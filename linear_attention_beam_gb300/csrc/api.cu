@@ -51,7 +51,7 @@ int validate(const gdnbeam_config* c) {
   if (!c->residual && c->layers != 1) return GDNBEAM_EUNSUPPORTED;
   if (c->residual && c->H * c->d_v != c->d_model) return GDNBEAM_EUNSUPPORTED;
   if ((long long)c->W_max * c->V >= (1ll << 31)) return GDNBEAM_EUNSUPPORTED;
-  if (c->state_path != 0 && c->state_path != 1) return GDNBEAM_EUNSUPPORTED;
+  if (c->state_path < 0 || c->state_path > 2) return GDNBEAM_EUNSUPPORTED;
   if ((long long)c->R * c->L_max >= (1ll << 31) || (long long)c->R * c->W_max * c->V >= (1ll << 40))
     return GDNBEAM_EUNSUPPORTED;
   return GDNBEAM_OK;
@@ -192,7 +192,7 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
   char* p_gemm = take(gemm_b);
   const int n_hint_tiles = (c.V + kHintTile - 1) / kHintTile;
   char* p_tst = take((rows > (size_t)c.R ? rows : (size_t)c.R) * n_hint_tiles * sizeof(float2));
-  const size_t st_b = c.state_path ? rows * c.layers * c.H * c.d_v * c.d_k * es : 0;
+  const size_t st_b = c.state_path == 1 ? rows * c.layers * c.H * c.d_v * c.d_k * es : 0;
   char* p_st0 = take(st_b);
   char* p_st1 = take(st_b);
   char* p_sst = take(c.state_path ? (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * es : 0);
@@ -319,8 +319,9 @@ int gdnbeam_create(const gdnbeam_config* cfg, const gdnbeam_weights* w, void* wo
   x->tc_replay = tc_replay_supported(cfg->dtype, cfg->d_k, cfg->d_v);
   carve(*cfg, tc, (char*)workspace, x, nullptr);
   if (cfg->state_path)
-    snprintf(x->variant, sizeof(x->variant), "proj=%s state=fullstate logits=%s select=bound",
-             tc ? "tc" : "simt", tc ? "tc" : "simt");
+    snprintf(x->variant, sizeof(x->variant), "proj=%s state=%s logits=%s select=bound",
+             tc ? "tc" : "simt", cfg->state_path == 1 ? "fullstate" : "replayssm",
+             tc ? "tc" : "simt");
   else
     snprintf(x->variant, sizeof(x->variant), "proj=%s replay=%s logits=%s select=bound",
              tc ? "tc" : "simt", x->tc_replay ? "tc" : "simt", tc ? "tc" : "simt");
@@ -379,7 +380,7 @@ int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* 
     ctx->toc(ev, s);
     if (st) return st;
   }
-  if (c.state_path) {  // the FullState path keeps every state in the storage type
+  if (c.state_path) {  // the baselines read S_ctx in the storage type
     st = launch_to_storage(c.dtype, (size_t)c.R * c.layers * c.H * c.d_v * c.d_k,
                            (const float*)ctx->sctx, ctx->sctx_store, s);
     if (st) return st;
@@ -459,7 +460,18 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
     a.delta_dump = ld.delta; a.o_dump = ld.o;
     a.err = err;
     ev = ctx->tic(GDNBEAM_STAGE_REPLAY, s);
-    if (c.state_path) {
+    if (c.state_path == 2) {
+      ReplaySsmArgs g{};
+      g.R = c.R; g.H = c.H; g.d_k = c.d_k; g.d_v = c.d_v; g.t = t; g.W_t = W_t;
+      g.sctx_store = (const char*)ctx->sctx_store + (size_t)layer * c.H * c.d_v * c.d_k * es;
+      g.sctx_rstride = a.sctx_rstride;
+      g.q = a.q; g.k = a.k; g.v = a.v; g.alpha = a.alpha; g.beta = a.beta;
+      for (int j = 0; j < t; ++j) g.depth[j] = a.depth[j];
+      g.anc = a.anc; g.anc_stride = a.anc_stride;
+      g.delta_out = a.delta_out; g.o_out = a.o_out; g.x_inout = a.x_inout;
+      g.delta_dump = a.delta_dump; g.o_dump = a.o_dump; g.err = err;
+      st = launch_replayssm(c.dtype, g, s);
+    } else if (c.state_path) {
       FullStateArgs f{};
       f.R = c.R; f.H = c.H; f.d_k = c.d_k; f.d_v = c.d_v; f.t = t; f.W_t = W_t;
       f.W_prev = W_prev; f.layers = c.layers; f.layer = layer;

@@ -83,6 +83,24 @@ struct FullStateArgs {
   unsigned* err;
 };
 int launch_fullstate(int dtype, const FullStateArgs& a, cudaStream_t s);
+
+// ReplaySSM baseline step for one layer: every (beam, head) re-applies its
+// ancestors' records to the request's stored S_ctx, then the current token.
+struct ReplaySsmArgs {
+  int R, H, d_k, d_v, t, W_t;
+  const void* sctx_store;      // storage copy of S_ctx [R][...] (request stride below)
+  long long sctx_rstride;      // elements
+  const void *q, *k, *v;
+  const float *alpha, *beta;
+  gdnbeam_records depth[GDNBEAM_MAX_T];
+  const int32_t* anc;
+  int anc_stride;
+  void *delta_out, *o_out;
+  float* x_inout;
+  float *delta_dump, *o_dump;
+  unsigned* err;
+};
+int launch_replayssm(int dtype, const ReplaySsmArgs& a, cudaStream_t s);
 // dst[i] = storage(src[i]) for n elements (S_ctx copy for the FullState path).
 int launch_to_storage(int dtype, size_t n, const float* src, void* dst, cudaStream_t s);
 

@@ -80,7 +80,8 @@ class BeamDecoder:
     @classmethod
     def for_workload(cls, wl, weights, L_max: Optional[int] = None, device="cuda",
                      state_path: int = 0):
-        """state_path 0: shared context + records + replay; 1: FullState baseline."""
+        """state_path 0: shared context + records + replay; 1: FullState baseline;
+        2: ReplaySSM baseline."""
         return cls(R=wl.R, layers=wl.layers, H=wl.H, d_k=wl.d_k, d_v=wl.d_v, d_model=wl.d_model,
                    V=wl.V, T=wl.T, W_max=wl.W_max, L_max=L_max or wl.L,
                    dtype=BF16 if wl.dtype == "bf16" else F32, residual=wl.residual,

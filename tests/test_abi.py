@@ -84,11 +84,23 @@ def test_record_size_and_capacity_match_the_page():
 @pytest.mark.parametrize("field,value,status", [
     ("d_k", 96, gb.EUNSUPPORTED), ("d_v", 256, gb.EUNSUPPORTED), ("T", 9, gb.EUNSUPPORTED),
     ("V", 20000, gb.EUNSUPPORTED), ("layers", 2, gb.EUNSUPPORTED), ("dtype", 7, gb.EUNSUPPORTED),
-    ("R", 0, gb.EINVAL), ("W_max", 0, gb.EINVAL), ("V", 1, gb.EINVAL)])
+    ("R", 0, gb.EINVAL), ("W_max", 0, gb.EINVAL), ("V", 1, gb.EINVAL), ("state_path", 3, gb.EUNSUPPORTED),
+    ("state_path", -1, gb.EUNSUPPORTED)])
 def test_config_rejections(field, value, status):
     c = cfg(synth.TINY)
     setattr(c, field, value)
     assert footprint(c)[0] == status
+
+
+def test_state_path_workspaces():
+    # FullState keeps two per-beam state buffers; ReplaySSM only a storage copy
+    # of S_ctx beside the records; the replay path neither
+    wl = synth.BATCHED
+    sizes = [footprint(cfg(wl, state_path=sp))[1].workspace_bytes for sp in (0, 1, 2)]
+    per_beam_states = wl.R * wl.W_max * wl.layers * wl.H * wl.d_v * wl.d_k * 2
+    sctx_copy = wl.R * wl.layers * wl.H * wl.d_v * wl.d_k * 2
+    assert sizes[1] - sizes[0] >= 2 * per_beam_states + sctx_copy
+    assert sctx_copy <= sizes[2] - sizes[0] < sctx_copy + (1 << 20)
 
 
 def test_residual_needs_matching_width():

@@ -73,11 +73,12 @@ SMALL = {
 }
 
 
-@pytest.mark.parametrize("state_path", [0, 1], ids=["replay", "fullstate"])
+@pytest.mark.parametrize("state_path", [0, 1, 2], ids=["replay", "fullstate", "replayssm"])
 @pytest.mark.parametrize("name", list(SMALL))
 def test_decode_forced_on_oracle_lineage(name, state_path):
     # state_path 1 is the FullState baseline (per-beam states copied on
-    # reorder): the same comparisons hold for it
+    # reorder), 2 the ReplaySSM baseline (states rebuilt from S_ctx and the
+    # ancestors' records every call): the same comparisons hold for both
     wl = SMALL[name]
     p = synth.make_params(wl)
     prompt = synth.make_prompt(wl)
