@@ -67,7 +67,8 @@ def write_gate(z: np.ndarray) -> np.ndarray:
 def gdn_inputs(wl, params, layer: int, u: np.ndarray):
     """Projections of layer inputs u [n, d_model] for every head.
 
-    Returns q_hat, k_hat [n, H, d_k], v [n, H, d_v], alpha, beta [n, H].
+    Returns q_hat, k_hat [n, Hk, d_k] (one per key head), v [n, H, d_v],
+    alpha, beta [n, H] (one per value head).
     """
     n = u.shape[0]
     u = np.asarray(u, dtype=F64)
@@ -76,9 +77,16 @@ def gdn_inputs(wl, params, layer: int, u: np.ndarray):
     v = u @ params.Wv[layer].astype(F64).T
     za = u @ params.w_alpha[layer].astype(F64).T
     zb = u @ params.w_beta[layer].astype(F64).T
-    q_hat = l2_normalize(q.reshape(n, wl.H, wl.d_k))
-    k_hat = l2_normalize(k.reshape(n, wl.H, wl.d_k))
+    q_hat = l2_normalize(q.reshape(n, wl.Hk, wl.d_k))
+    k_hat = l2_normalize(k.reshape(n, wl.Hk, wl.d_k))
     return q_hat, k_hat, v.reshape(n, wl.H, wl.d_v), decay_gate(za), write_gate(zb)
+
+
+def per_value_head(wl, x: np.ndarray) -> np.ndarray:
+    """Key-head arrays [n, Hk, d_k] seen from the value heads [n, H, d_k]:
+    grouped query attention with consecutive value heads sharing a key head
+    (value head h reads key head h // (H // Hk))."""
+    return np.repeat(x, wl.H // wl.Hk, axis=1)
 
 
 # --------------------------------------------------------------------------
@@ -248,7 +256,7 @@ def token_paths(parents: Sequence[np.ndarray], tokens: Sequence[np.ndarray]) -> 
 class CallTrace:
     """Everything decode call t computed for one request (fp64 unless noted)."""
     tokens: np.ndarray                 # [n] input tokens of the beams
-    q: List[np.ndarray] = field(default_factory=list)      # per layer [n,H,dk]
+    q: List[np.ndarray] = field(default_factory=list)      # per layer [n,Hk,dk]
     k: List[np.ndarray] = field(default_factory=list)
     v: List[np.ndarray] = field(default_factory=list)
     alpha: List[np.ndarray] = field(default_factory=list)  # per layer [n,H]
@@ -284,7 +292,7 @@ def prefill(wl, params, prompt: np.ndarray):
     for layer in range(wl.layers):
         u = rms_normalize(x) if wl.residual else x
         q, k, v, a, b = gdn_inputs(wl, params, layer, u)
-        S_ctx[layer], o = prefill_scan(q, k, v, a, b)
+        S_ctx[layer], o = prefill_scan(per_value_head(wl, q), per_value_head(wl, k), v, a, b)
         if wl.residual:
             x = x + o.reshape(len(x), wl.H * wl.d_v)
         else:
@@ -328,7 +336,8 @@ def decode_request(wl, params, prompt: np.ndarray, bias: Optional[np.ndarray] = 
         for layer in range(wl.layers):
             u = rms_normalize(x) if wl.residual else x
             q, k, v, a, b = gdn_inputs(wl, params, layer, u)
-            states[:, layer], delta, o = gdn_transition(states[:, layer], q, k, v, a, b)
+            states[:, layer], delta, o = gdn_transition(
+                states[:, layer], per_value_head(wl, q), per_value_head(wl, k), v, a, b)
             tr.q.append(q); tr.k.append(k); tr.v.append(v)
             tr.alpha.append(a); tr.beta.append(b)
             tr.delta.append(delta); tr.o.append(o)
@@ -377,7 +386,8 @@ def chain_trace(wl, params, S_ctx: np.ndarray, path: Sequence[int]) -> List[Call
         for layer in range(wl.layers):
             u = rms_normalize(x) if wl.residual else x
             q, k, v, a, b = gdn_inputs(wl, params, layer, u)
-            S[layer], delta, o = gdn_transition(S[layer], q[0], k[0], v[0], a[0], b[0])
+            S[layer], delta, o = gdn_transition(S[layer], per_value_head(wl, q)[0],
+                                                per_value_head(wl, k)[0], v[0], a[0], b[0])
             tr.q.append(q); tr.k.append(k); tr.v.append(v); tr.alpha.append(a); tr.beta.append(b)
             tr.delta.append(delta[None]); tr.o.append(o[None])
             if wl.residual:

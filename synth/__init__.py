@@ -55,6 +55,12 @@ class Workload:
     seed: int
     residual: bool = False # residual stream + RMSNorm glue between layers
     bias_var: float = 0.0  # variance of the per-parent score bias (0 = none)
+    H_k: int = 0           # key heads (0: one per value head); H is a multiple
+
+    @property
+    def Hk(self) -> int:
+        """Key (query/key) heads; value head h reads key head h // (H // Hk)."""
+        return self.H_k or self.H
 
     @property
     def W_max(self) -> int:
@@ -133,8 +139,8 @@ def make_params(wl: Workload) -> Params:
     s_in = np.float32(1.0 / np.sqrt(wl.d_model))
     Wq, Wk, Wv, wa, wb = [], [], [], [], []
     for _ in range(wl.layers):
-        Wq.append(st(rng.standard_normal((wl.H * wl.d_k, wl.d_model), dtype=np.float32) * s_in))
-        Wk.append(st(rng.standard_normal((wl.H * wl.d_k, wl.d_model), dtype=np.float32) * s_in))
+        Wq.append(st(rng.standard_normal((wl.Hk * wl.d_k, wl.d_model), dtype=np.float32) * s_in))
+        Wk.append(st(rng.standard_normal((wl.Hk * wl.d_k, wl.d_model), dtype=np.float32) * s_in))
         Wv.append(st(rng.standard_normal((wl.H * wl.d_v, wl.d_model), dtype=np.float32) * s_in))
         wa.append(st(rng.standard_normal((wl.H, wl.d_model), dtype=np.float32) * s_in))
         wb.append(st(rng.standard_normal((wl.H, wl.d_model), dtype=np.float32) * s_in))
@@ -179,9 +185,10 @@ def random_lineage(wl: Workload, seed: int) -> Tuple[list, list]:
 
 
 def tiny_workload(d=4, V=3, T=3, W=(3, 9, 27), H=1, layers=1, d_model=None,
-                  residual=False, seed=11, L=5, dtype="f32", R=1) -> Workload:
-    """Small shapes for brute-force checks."""
-    d_model = d_model or (H * d if not residual else H * d)
-    return Workload(f"tiny_d{d}_V{V}_T{T}", R=R, layers=layers, H=H, d_k=d, d_v=d,
+                  residual=False, seed=11, L=5, dtype="f32", R=1, H_k=0, d_v=None) -> Workload:
+    """Small shapes for brute-force checks (d_v defaults to d = d_k)."""
+    d_v = d_v or d
+    d_model = d_model or H * d_v
+    return Workload(f"tiny_d{d}_V{V}_T{T}", R=R, layers=layers, H=H, d_k=d, d_v=d_v,
                     d_model=d_model, V=V, T=T, W=tuple(W), L=L, dtype=dtype,
-                    seed=seed, residual=residual)
+                    seed=seed, residual=residual, H_k=H_k)

@@ -445,3 +445,47 @@ def test_page_record_size_figures():
     c = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "recogem_candidates.json")))
     assert round(c["C"] * c["W"] / 1e6, 1) == c["candidates_millions_approx"]
     assert c["C"] * c["W"] * 2 / 2 ** 20 == c["fp16_MiB"]
+
+
+# ---------------------------------------------------------------- grouped key heads
+
+@pytest.mark.parametrize("residual", [False, True])
+def test_gqa_equals_mha_with_repeated_key_weights(residual):
+    # Grouped query attention (Hk key heads shared by consecutive value heads)
+    # is the multi-head model whose query/key weight rows are repeated per
+    # group: the two decodes must agree to rounding.
+    layers = 2 if residual else 1
+    g = synth.tiny_workload(d=4, V=5, T=3, W=(4, 6, 5), H=4, H_k=2, d_v=3, layers=layers,
+                            residual=residual, d_model=12, L=6, seed=21)
+    m = g.with_(H_k=0)
+    pg = synth.make_params(g)
+    rep = lambda Ws: [np.repeat(Wl.reshape(g.Hk, g.d_k, -1), g.H // g.Hk, axis=0).reshape(g.H * g.d_k, -1)
+                      for Wl in Ws]
+    import dataclasses
+    pm = dataclasses.replace(pg, Wq=rep(pg.Wq), Wk=rep(pg.Wk))
+    prompt = synth.make_prompt(g)[0]
+    tg = oracle.decode_request(g, pg, prompt)
+    tm = oracle.decode_request(m, pm, prompt)
+    np.testing.assert_allclose(tg.S_ctx, tm.S_ctx, rtol=1e-12, atol=1e-14)
+    for cg, cm in zip(tg.calls, tm.calls):
+        np.testing.assert_allclose(cg.z, cm.z, rtol=1e-12, atol=1e-14)
+        for layer in range(layers):
+            np.testing.assert_allclose(oracle.per_value_head(g, cg.k[layer]), cm.k[layer], rtol=1e-12)
+            np.testing.assert_allclose(cg.delta[layer], cm.delta[layer], rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(tg.sid, tm.sid)
+
+
+def test_gqa_value_heads_share_their_group_key():
+    # value heads 0,1 read key head 0 and heads 2,3 key head 1: a decode where
+    # only key head 1's weights change leaves value heads 0 and 1 untouched
+    import dataclasses
+    wl = synth.tiny_workload(d=4, V=5, T=2, W=(3, 3), H=4, H_k=2, d_model=10, L=5, seed=5)
+    p = synth.make_params(wl)
+    Wk2 = [w.copy() for w in p.Wk]
+    Wk2[0][wl.d_k:] *= -0.5
+    p2 = dataclasses.replace(p, Wk=Wk2)
+    prompt = synth.make_prompt(wl)[0]
+    S1 = oracle.prefill(wl, p, prompt)[0]
+    S2 = oracle.prefill(wl, p2, prompt)[0]
+    np.testing.assert_array_equal(S1[:, :2], S2[:, :2])
+    assert np.abs(S1[:, 2:] - S2[:, 2:]).max() > 1e-6
