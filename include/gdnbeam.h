@@ -92,13 +92,18 @@ typedef struct gdnbeam_config {
                         state; every step rebuilds each beam's parent state
                         from the stored S_ctx by replaying its ancestors'
                         records, then applies the current token */
+  int H_k;      /* query/key heads (0: H). H must be a multiple of H_k; value
+                   head h reads key head h / (H / H_k), consecutive value
+                   heads sharing one (grouped query attention, OneLA §4's
+                   H_K != H_V geometries). q, k and the records' keys hold
+                   H_k heads; v, gates, states, delta and o hold H. */
 } gdnbeam_config;
 
 /* Weights, storage type, row-major, owned by the caller and kept alive for
  * the life of the context.
  *   E       [V][d_model]                      token embedding
- *   W_proj  [layers][N_proj][d_model]         N_proj = 2*H*d_k + H*d_v + 2*H rows:
- *             H*d_k query rows, H*d_k key rows, H*d_v value rows, then the H
+ *   W_proj  [layers][N_proj][d_model]         N_proj = 2*H_k*d_k + H*d_v + 2*H rows:
+ *             H_k*d_k query rows, H_k*d_k key rows, H*d_v value rows, then the H
  *             decay-gate vectors w_alpha and the H write-gate vectors w_beta
  *   W_o     [V][F]                            codebook head; F = H*d_v (single
  *             layer) or d_model (residual) */
@@ -110,7 +115,7 @@ typedef struct gdnbeam_weights {
 
 /* Optional fp32 copies of intermediate values before storage rounding, for
  * parity checks. Any member may be NULL. Shapes for a call on n = R*W_t rows:
- *   q, k [layers][n][H*d_k]; v, delta, o [layers][n][H*d_v];
+ *   q, k [layers][n][H_k*d_k]; v, delta, o [layers][n][H*d_v];
  *   alpha, beta [layers][n][H]; logits [n][V]. */
 typedef struct gdnbeam_dumps {
   float* q;
@@ -253,7 +258,7 @@ long long gdnbeam_launches(int clear);
 
 /* Projections for n rows of one layer (OneLA §1.2 eq. 3 inputs).
  *   u [n][d_model] storage, W_proj [N_proj][d_model] storage (one layer);
- *   q [n][H*d_k], k [n][H*d_k], v [n][H*d_v] storage; alpha, beta [n][H] fp32.
+ *   q [n][H_k*d_k], k [n][H_k*d_k], v [n][H*d_v] storage; alpha, beta [n][H] fp32.
  *   q and k are L2-normalised per head (eps 1e-6 inside the root);
  *   alpha = exp(-softplus(w_alpha.u)), beta = sigmoid(w_beta.u).
  * scratch: device buffer of gdnbeam_project_scratch_bytes(cfg, n) bytes
@@ -267,7 +272,7 @@ int gdnbeam_project(const gdnbeam_config* cfg, int n, const void* u, const void*
 
 /* Records of one depth (OneLA §2.2 eq. 5), rows packed [R][W_j][H]. */
 typedef struct gdnbeam_records {
-  const void* k;       /* [R*W_j][H*d_k] storage */
+  const void* k;       /* [R*W_j][H_k*d_k] storage */
   const void* delta;   /* [R*W_j][H*d_v] storage */
   const float* alpha;  /* [R*W_j][H] */
   int W_j;             /* beams per request at that depth */
@@ -279,7 +284,7 @@ typedef struct gdnbeam_records {
  *   slot anc[r*W_t+b][j] of depth j; delta = beta (v - alpha u_k);
  *   o = alpha u_q + delta (k_b . q_b).
  *   sctx [R][H][d_v][d_k] fp32 (stride between requests: sctx_rstride elements)
- *   q, k [R*W_t][H*d_k], v [R*W_t][H*d_v] storage; alpha, beta [R*W_t][H]
+ *   q, k [R*W_t][H_k*d_k], v [R*W_t][H*d_v] storage; alpha, beta [R*W_t][H]
  *   depth: host array of t record descriptors; anc [R*W_t][anc_stride] int32
  *   delta_out, o_out [R*W_t][H*d_v] storage; x_inout optional fp32
  *   [R*W_t][H*d_v] residual stream to which o is added (NULL: none).
@@ -339,7 +344,7 @@ int gdnbeam_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int3
 
 /* Prefill recurrence over L tokens for every (request, head) from S = 0
  * (OneLA §1.2 eq. 3).
- *   q, k [R*L][H*d_k], v [R*L][H*d_v] storage; alpha, beta [R*L][H] fp32;
+ *   q, k [R*L][H_k*d_k], v [R*L][H*d_v] storage; alpha, beta [R*L][H] fp32;
  *   sctx_out [R][H][d_v][d_k] fp32 (request stride sctx_rstride elements);
  *   o_last [R][H*d_v] storage output at the last position (or NULL);
  *   x_inout optional fp32 [R*L][H*d_v]: o of every position is added to it. */

@@ -33,7 +33,8 @@ DERR = {"token": 1, "parent": 2, "slot": 4, "nonfinite": 8, "timeout": 16, "sele
 
 class Config(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("R", "layers", "H", "d_k", "d_v", "d_model", "V", "T",
-                                       "W_max", "L_max", "dtype", "residual", "state_path")]
+                                       "W_max", "L_max", "dtype", "residual", "state_path",
+                                       "H_k")]
 
 
 class Weights(C.Structure):

@@ -36,7 +36,7 @@ unsigned* err_ptr() {
 
 inline size_t elem_size(int dtype) { return dtype == GDNBEAM_BF16 ? 2 : 4; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-inline int n_proj(const gdnbeam_config& c) { return 2 * c.H * c.d_k + c.H * c.d_v + 2 * c.H; }
+inline int n_proj(const gdnbeam_config& c) { return 2 * key_heads(c) * c.d_k + c.H * c.d_v + 2 * c.H; }
 inline int feat_dim(const gdnbeam_config& c) { return c.residual ? c.d_model : c.H * c.d_v; }
 inline bool pow2_head(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
@@ -52,6 +52,7 @@ int validate(const gdnbeam_config* c) {
   if (c->residual && c->H * c->d_v != c->d_model) return GDNBEAM_EUNSUPPORTED;
   if ((long long)c->W_max * c->V >= (1ll << 31)) return GDNBEAM_EUNSUPPORTED;
   if (c->state_path < 0 || c->state_path > 2) return GDNBEAM_EUNSUPPORTED;
+  if (c->H_k < 0 || (c->H_k > 0 && c->H % c->H_k != 0)) return GDNBEAM_EINVAL;
   if ((long long)c->R * c->L_max >= (1ll << 31) || (long long)c->R * c->W_max * c->V >= (1ll << 40))
     return GDNBEAM_EUNSUPPORTED;
   return GDNBEAM_OK;
@@ -70,7 +71,7 @@ struct gdnbeam_ctx {
   char variant[96];
   // persistent state
   void* sctx;        // [R][layers][H][d_v][d_k]
-  void* gtr_k;       // [layers][T-1][R*W_max][H*d_k]
+  void* gtr_k;       // [layers][T-1][R*W_max][H_k*d_k]
   void* gtr_delta;   // [layers][T-1][R*W_max][H*d_v]
   float* gtr_alpha;  // [layers][T-1][R*W_max][H]
   int32_t* anc[2];   // [R*W_max][T]
@@ -130,7 +131,7 @@ struct gdnbeam_ctx {
 
   size_t rec_rows() const { return (size_t)c.R * c.W_max; }
   char* gk(int layer, int j) const {
-    return (char*)gtr_k + ((size_t)layer * (c.T - 1) + j) * rec_rows() * c.H * c.d_k * elem_size(c.dtype);
+    return (char*)gtr_k + ((size_t)layer * (c.T - 1) + j) * rec_rows() * key_heads(c) * c.d_k * elem_size(c.dtype);
   }
   char* gd(int layer, int j) const {
     return (char*)gtr_delta + ((size_t)layer * (c.T - 1) + j) * rec_rows() * c.H * c.d_v * elem_size(c.dtype);
@@ -158,7 +159,7 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
   // S_ctx is kept in fp32 whatever the storage type: it is read once per
   // (request, head) tile and shared by every beam, so its width costs little.
   size_t sctx_b = (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * sizeof(float);
-  size_t gk_b = (size_t)c.layers * depths * rows * c.H * c.d_k * es;
+  size_t gk_b = (size_t)c.layers * depths * rows * key_heads(c) * c.d_k * es;
   size_t gd_b = (size_t)c.layers * depths * rows * c.H * c.d_v * es;
   size_t ga_b = (size_t)c.layers * depths * rows * c.H * sizeof(float);
   size_t anc_b = rows * c.T * sizeof(int32_t);
@@ -172,7 +173,7 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
   char* p_sid1 = take(anc_b);
   char* p_u = take(rows * c.d_model * es);
   char* p_x = take(c.residual ? rows * c.d_model * sizeof(float) : 0);
-  char* p_q = take(rows * c.H * c.d_k * es);
+  char* p_q = take(rows * key_heads(c) * c.d_k * es);
   char* p_v = take(rows * c.H * c.d_v * es);
   char* p_beta = take(rows * c.H * sizeof(float));
   char* p_o = take(rows * c.H * c.d_v * es);
@@ -198,8 +199,8 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
   char* p_sst = take(c.state_path ? (size_t)c.R * c.layers * c.H * c.d_v * c.d_k * es : 0);
   char* p_pfu = take(pf_rows * c.d_model * es);
   char* p_pfx = take(c.residual ? pf_rows * c.d_model * sizeof(float) : 0);
-  char* p_pfq = take(pf_rows * c.H * c.d_k * es);
-  char* p_pfk = take(pf_rows * c.H * c.d_k * es);
+  char* p_pfq = take(pf_rows * key_heads(c) * c.d_k * es);
+  char* p_pfk = take(pf_rows * key_heads(c) * c.d_k * es);
   char* p_pfv = take(pf_rows * c.H * c.d_v * es);
   char* p_pfa = take(pf_rows * c.H * sizeof(float));
   char* p_pfb = take(pf_rows * c.H * sizeof(float));
@@ -262,8 +263,8 @@ gdnbeam_dumps layer_dumps(const gdnbeam_dumps* d, const gdnbeam_config& c, int l
   gdnbeam_dumps o{};
   if (!d) return o;
   auto sh = [&](float* p, size_t per) { return p ? p + (size_t)layer * n * per : nullptr; };
-  o.q = sh(d->q, (size_t)c.H * c.d_k);
-  o.k = sh(d->k, (size_t)c.H * c.d_k);
+  o.q = sh(d->q, (size_t)key_heads(c) * c.d_k);
+  o.k = sh(d->k, (size_t)key_heads(c) * c.d_k);
   o.v = sh(d->v, (size_t)c.H * c.d_v);
   o.alpha = sh(d->alpha, c.H);
   o.beta = sh(d->beta, c.H);
@@ -443,7 +444,7 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
     ctx->toc(ev, s);
     if (st) return st;
     ReplayArgs a{};
-    a.R = c.R; a.H = c.H; a.d_k = c.d_k; a.d_v = c.d_v; a.t = t; a.W_t = W_t;
+    a.R = c.R; a.H = c.H; a.d_k = c.d_k; a.d_v = c.d_v; a.t = t; a.W_t = W_t; a.Hk = key_heads(c);
     a.sctx = (const float*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k;
     a.sctx_rstride = (long long)c.layers * c.H * c.d_v * c.d_k;
     a.q = ctx->q; a.k = ctx->gk(layer, t); a.v = ctx->v;
@@ -462,7 +463,7 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
     ev = ctx->tic(GDNBEAM_STAGE_REPLAY, s);
     if (c.state_path == 2) {
       ReplaySsmArgs g{};
-      g.R = c.R; g.H = c.H; g.d_k = c.d_k; g.d_v = c.d_v; g.t = t; g.W_t = W_t;
+      g.R = c.R; g.H = c.H; g.d_k = c.d_k; g.d_v = c.d_v; g.t = t; g.W_t = W_t; g.Hk = key_heads(c);
       g.sctx_store = (const char*)ctx->sctx_store + (size_t)layer * c.H * c.d_v * c.d_k * es;
       g.sctx_rstride = a.sctx_rstride;
       g.q = a.q; g.k = a.k; g.v = a.v; g.alpha = a.alpha; g.beta = a.beta;
@@ -473,7 +474,7 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
       st = launch_replayssm(c.dtype, g, s);
     } else if (c.state_path) {
       FullStateArgs f{};
-      f.R = c.R; f.H = c.H; f.d_k = c.d_k; f.d_v = c.d_v; f.t = t; f.W_t = W_t;
+      f.R = c.R; f.H = c.H; f.d_k = c.d_k; f.d_v = c.d_v; f.t = t; f.W_t = W_t; f.Hk = key_heads(c);
       f.W_prev = W_prev; f.layers = c.layers; f.layer = layer;
       f.sctx_store = (const char*)ctx->sctx_store + (size_t)layer * c.H * c.d_v * c.d_k * es;
       f.sctx_rstride = a.sctx_rstride;
@@ -642,7 +643,7 @@ int gdnbeam_replay(const gdnbeam_config* cfg, int t, int W_t, const float* sctx,
     return GDNBEAM_EINVAL;
   if (t > 0 && (!depth || !anc || anc_stride < t)) return GDNBEAM_EINVAL;
   ReplayArgs a{};
-  a.R = c.R; a.H = c.H; a.d_k = c.d_k; a.d_v = c.d_v; a.t = t; a.W_t = W_t;
+  a.R = c.R; a.H = c.H; a.d_k = c.d_k; a.d_v = c.d_v; a.t = t; a.W_t = W_t; a.Hk = key_heads(c);
   a.sctx = sctx; a.sctx_rstride = sctx_rstride;
   a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta;
   for (int j = 0; j < t; ++j) {

@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(128) fullstate_step_kernel(FullStateArgs a) {
   const int r = row / a.W_t;
   const int i = threadIdx.x;
   const int H = a.H, dv = a.d_v;
+  const int hk = h / (H / a.Hk);  // the key head this value head reads
   const uint32_t bytes = (uint32_t)(dv * DK * sizeof(T));
   const uint32_t sbar = tc::smem_u32(&bar), stile = tc::smem_u32(tile);
   if (i == 0) {
@@ -43,8 +44,8 @@ __global__ void __launch_bounds__(128) fullstate_step_kernel(FullStateArgs a) {
     s_abort = 0;
     tc::fence_mbar_init();
   }
-  const T* q = (const T*)a.q + ((size_t)row * H + h) * DK;
-  const T* k = (const T*)a.k + ((size_t)row * H + h) * DK;
+  const T* q = (const T*)a.q + ((size_t)row * a.Hk + hk) * DK;
+  const T* k = (const T*)a.k + ((size_t)row * a.Hk + hk) * DK;
   for (int c = threadIdx.x; c < DK; c += blockDim.x) {
     kq[0][c] = ldf(k + c);
     kq[1][c] = ldf(q + c);
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(256, 2) replayssm_step_kernel(ReplaySsmArgs a)
   const int tid = threadIdx.x;
   const int i = tid / TPR, part = tid % TPR, c0 = part * NCOL;
   const int H = a.H, dv = a.d_v;
+  const int hk = h / (H / a.Hk);  // the key head this value head reads
   constexpr int t = TD;
   const T* srow_g = (const T*)a.sctx_store + (size_t)r * a.sctx_rstride + (size_t)h * dv * DK;
   const uint32_t sbar = tc::smem_u32(&bar), stile = tc::smem_u32(tile);
@@ -201,15 +203,15 @@ __global__ void __launch_bounds__(256, 2) replayssm_step_kernel(ReplaySsmArgs a)
     if (!use[j] && tid == 0) raise_error(a.err, GDNBEAM_DERR_SLOT);
     slot[j] = use[j] ? sl : 0;
   }
-  const T* q = (const T*)a.q + ((size_t)row * H + h) * DK;
-  const T* k = (const T*)a.k + ((size_t)row * H + h) * DK;
+  const T* q = (const T*)a.q + ((size_t)row * a.Hk + hk) * DK;
+  const T* k = (const T*)a.k + ((size_t)row * a.Hk + hk) * DK;
   for (int c = tid; c < DK; c += blockDim.x) {
     kq[0][c] = ldf(k + c);
     kq[1][c] = ldf(q + c);
 #pragma unroll
     for (int j = 0; j < TD; ++j)
         kjs[j][c] = use[j] ? ldf((const T*)a.depth[j].k +
-                                 (((size_t)r * a.depth[j].W_j + slot[j]) * H + h) * DK + c)
+                                 (((size_t)r * a.depth[j].W_j + slot[j]) * a.Hk + hk) * DK + c)
                            : 0.f;
   }
 #pragma unroll

@@ -47,7 +47,7 @@ struct EpiArgs {
   float* z_dump;
   float2* part;  // [M][n_tiles] (max, sum exp(z - max))
   // projections
-  int H;
+  int H, Hk;  // value heads, key heads
   __nv_bfloat16 *q, *k, *v;
   float *alpha, *beta;
   float *dq, *dk, *dv, *da, *db;
@@ -113,9 +113,9 @@ __device__ __forceinline__ void epi_logits(const EpiArgs& ea, uint32_t taddr, in
 
 // Projection epilogue for one tile row; head width 128, tile of two heads.
 __device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int m, int n0) {
-  const int H = ea.H, D = 128;
+  const int H = ea.H, Hk = ea.Hk, D = 128;
   const bool row_ok = m < ea.M;
-  const int q_end = H * D, k_end = 2 * H * D, v_end = 3 * H * D;
+  const int q_end = Hk * D, k_end = 2 * Hk * D, v_end = k_end + H * D;
 #pragma unroll 1
   for (int g = 0; g < BN / D; ++g) {
     const int col0 = n0 + g * D;
@@ -135,7 +135,7 @@ __device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int 
       const float inv = 1.0f / sqrtf(ss + 1e-6f);
       __nv_bfloat16* dst = is_q ? ea.q : ea.k;
       float* dmp = is_q ? ea.dq : ea.dk;
-      const size_t off = (size_t)m * H * D + (size_t)head * D;
+      const size_t off = (size_t)m * Hk * D + (size_t)head * D;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float v[32];
@@ -407,9 +407,10 @@ int launch_tc_project(const gdnbeam_config& c, int n, const void* u, const void*
                       cudaStream_t s) {
   EpiArgs ea{};
   ea.M = n;
-  ea.N = 2 * c.H * c.d_k + c.H * c.d_v + 2 * c.H;
+  ea.N = 2 * key_heads(c) * c.d_k + c.H * c.d_v + 2 * c.H;
   ea.K = c.d_model;
   ea.H = c.H;
+  ea.Hk = key_heads(c);
   ea.q = (__nv_bfloat16*)q;
   ea.k = (__nv_bfloat16*)k;
   ea.v = (__nv_bfloat16*)v;

@@ -45,7 +45,7 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
 // threads of a row pair read different banks.
 template <typename T, int DK, int TPR, int CH>
 __global__ void __launch_bounds__(64 * TPR, 2) prefill_scan_kernel(
-    int L, int H, int dv, const T* __restrict__ q, const T* __restrict__ k,
+    int L, int H, int Hk, int dv, const T* __restrict__ q, const T* __restrict__ k,
     const T* __restrict__ v, const float* __restrict__ alpha, const float* __restrict__ beta,
     float* __restrict__ sctx, long long rstride, T* __restrict__ o_last, float* __restrict__ x) {
   constexpr int NC = DK / TPR;            // columns per thread
@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(64 * TPR, 2) prefill_scan_kernel(
   float* vs = qs + 2 * CH * RS;            // [2][CH][128]
   float2* gs = reinterpret_cast<float2*>(vs + 2 * CH * 128);  // [2][CH]
   const int r = blockIdx.x / H, h = blockIdx.x % H;
+  const int hk = h / (H / Hk);  // the key head this value head reads
   const int tid = threadIdx.x;
   const int i = tid / TPR, part = tid % TPR, c0 = part * NC;  // rows i and i + 64
   const int VV = dv / EPV;                 // 16-byte pieces per v row
@@ -84,12 +85,13 @@ __global__ void __launch_bounds__(64 * TPR, 2) prefill_scan_kernel(
         int t, piece;
         const T* base;
         int width;
-        if (u < CH * KV) { t = u / KV; piece = u % KV; base = k; width = DK; }
-        else if (u < 2 * CH * KV) { t = (u - CH * KV) / KV; piece = (u - CH * KV) % KV; base = q; width = DK; }
-        else { t = (u - 2 * CH * KV) / VV; piece = (u - 2 * CH * KV) % VV; base = v; width = dv; }
+        int heads, head;
+        if (u < CH * KV) { t = u / KV; piece = u % KV; base = k; width = DK; heads = Hk; head = hk; }
+        else if (u < 2 * CH * KV) { t = (u - CH * KV) / KV; piece = (u - CH * KV) % KV; base = q; width = DK; heads = Hk; head = hk; }
+        else { t = (u - 2 * CH * KV) / VV; piece = (u - 2 * CH * KV) % VV; base = v; width = dv; heads = H; head = h; }
         const int pos = chunk * CH + t;
         if (pos < L)
-          buf[e] = __ldg(reinterpret_cast<const uint4*>(base + ((row0 + pos) * H + h) * width) + piece);
+          buf[e] = __ldg(reinterpret_cast<const uint4*>(base + ((row0 + pos) * heads + head) * width) + piece);
       }
     }
     g = make_float2(0.f, 0.f);
@@ -224,7 +226,8 @@ int launch_scan(const gdnbeam_config& c, int L, const void* q, const void* k, co
   GDN_CUDA(cudaFuncSetAttribute(prefill_scan_kernel<T, DK, TPR, CH>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   prefill_scan_kernel<T, DK, TPR, CH><<<c.R * c.H, 64 * TPR, smem, s>>>(
-      L, c.H, c.d_v, (const T*)q, (const T*)k, (const T*)v, alpha, beta, sctx, rs, (T*)o_last, x);
+      L, c.H, key_heads(c), c.d_v, (const T*)q, (const T*)k, (const T*)v, alpha, beta, sctx, rs,
+      (T*)o_last, x);
   return GDNBEAM_OK;
 }
 
@@ -234,7 +237,7 @@ int dispatch_dk(const gdnbeam_config& c, int L, const void* q, const void* k, co
                 float* x, cudaStream_t s) {
   const int epv = 16 / (int)sizeof(T);
   if (c.d_v % epv != 0 || ((uintptr_t)q & 15) || ((uintptr_t)k & 15) || ((uintptr_t)v & 15) ||
-      (c.H * c.d_k) % epv != 0)
+      (key_heads(c) * c.d_k) % epv != 0)
     return GDNBEAM_EUNSUPPORTED;
   int st;
   switch (c.d_k) {

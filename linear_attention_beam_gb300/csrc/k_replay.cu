@@ -19,8 +19,9 @@ constexpr int kChunk = 32;    // key columns of S_ctx staged per pass
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) replay_simt_kernel(ReplayArgs a) {
-  const int H = a.H, dk = a.d_k, dv = a.d_v, t = a.t;
+  const int H = a.H, Hk = a.Hk, dk = a.d_k, dv = a.d_v, t = a.t;
   const int r = blockIdx.x / H, h = blockIdx.x % H;
+  const int hk = h / (H / Hk);  // the key head this value head reads
   const int b0 = blockIdx.y * kBeams;
   const int nb = min(kBeams, a.W_t - b0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -41,7 +42,7 @@ __global__ void __launch_bounds__(kThreads) replay_simt_kernel(ReplayArgs a) {
   // 1. this tile's queries and keys, and the ancestors' slots
   for (int i = tid; i < nb * dk; i += kThreads) {
     int b = i / dk, c = i % dk;
-    size_t off = ((size_t)(r * a.W_t + b0 + b) * H + h) * dk + c;
+    size_t off = ((size_t)(r * a.W_t + b0 + b) * Hk + hk) * dk + c;
     qs[i] = ldf(q + off);
     ks[i] = ldf(k + off);
   }
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kThreads) replay_simt_kernel(ReplayArgs a) {
     if (j < t) {
       int s = slot[b * GDNBEAM_MAX_T + j];
       if (s >= 0) {
-        const T* kr = (const T*)a.depth[j].k + ((size_t)(r * a.depth[j].W_j + s) * H + h) * dk;
+        const T* kr = (const T*)a.depth[j].k + ((size_t)(r * a.depth[j].W_j + s) * Hk + hk) * dk;
         for (int c = lane; c < dk; c += 32) {
           float kv = ldf(kr + c);
           sq += kv * qs[b * dk + c];

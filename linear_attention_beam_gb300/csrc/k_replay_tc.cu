@@ -64,7 +64,7 @@ struct RecMaps {
 };
 
 struct TcReplayParams {
-  int R, H, t, W_t, n_tiles, stages, stage_bytes;
+  int R, H, Hk, t, W_t, n_tiles, stages, stage_bytes;
   const float* sctx;
   long long sctx_rstride;
   const float *alpha, *beta;
@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x / p.H, h = blockIdx.x % p.H;
+  const int hk = h / (p.H / p.Hk);  // the key head this value head reads
   constexpr int v_off = B_BYTES;
   constexpr int rec_off = B_BYTES + V_BYTES;
   constexpr int kEpi0 = 2, kRec0 = 2 + kEpiWarps, kScal0 = kRec0 + 2;  // first warp of each role
@@ -185,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive_expect_tx(full(s), (uint32_t)(B_BYTES + V_BYTES));
         for (int kb = 0; kb < 2; ++kb) {
           const uint32_t bk = st + kb * (2 * NB * 128);
-          tc::tma_load_3d(bk, &tm_q, h * D + kb * 64, b0, r, full(s));
-          tc::tma_load_3d(bk + NB * 128, &tm_k, h * D + kb * 64, b0, r, full(s));
+          tc::tma_load_3d(bk, &tm_q, hk * D + kb * 64, b0, r, full(s));
+          tc::tma_load_3d(bk + NB * 128, &tm_k, hk * D + kb * 64, b0, r, full(s));
           tc::tma_load_3d(st + v_off + kb * (NB * 128), &tm_v, h * D + kb * 64, b0, r, full(s));
         }
         issued[s] = true;
@@ -224,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 4; ++u) {
             const int b = 4 * g + u;
             const int sl = b < nb ? tab_slot[(b0 + b) * t + j] : 0;
-            y[u] = (r * p.W_j[j] + sl) * p.H + h;
+            // delta_j rows are per value head, k_j rows per key head
+            y[u] = kind == 0 ? (r * p.W_j[j] + sl) * p.H + h : (r * p.W_j[j] + sl) * p.Hk + hk;
           }
           const uint32_t dst = st + rec_off + (uint32_t)(j * REC_BYTES + kind * (NB * D * 2) +
                                                          half * (NB * 128) + g * (4 * 128));
@@ -564,7 +566,7 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
   if (a.W_t <= 0) return GDNBEAM_OK;
   if (a.t > kMaxDepth || a.d_k != D || a.d_v != D) return launch_replay(GDNBEAM_BF16, a, s);
   TcReplayParams p{};
-  p.R = a.R; p.H = a.H; p.t = a.t; p.W_t = a.W_t;
+  p.R = a.R; p.H = a.H; p.Hk = a.Hk; p.t = a.t; p.W_t = a.W_t;
   p.n_tiles = (a.W_t + NB - 1) / NB;
   p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES;
   const size_t table = (size_t)a.W_t * (8 + 8 * a.t);
@@ -582,15 +584,16 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s) {
     p.W_j[j] = a.depth[j].W_j;
     if (((uintptr_t)a.depth[j].k & 15) || ((uintptr_t)a.depth[j].delta & 15)) return GDNBEAM_EINVAL;
     const long long rows = (long long)a.R * a.depth[j].W_j * a.H;
+    const long long krows = (long long)a.R * a.depth[j].W_j * a.Hk;
     if (rows > 0x7FFFFFFFLL) return launch_replay(GDNBEAM_BF16, a, s);
-    if (!rows_map(&rm.d[j], a.depth[j].delta, rows) || !rows_map(&rm.k[j], a.depth[j].k, rows))
+    if (!rows_map(&rm.d[j], a.depth[j].delta, rows) || !rows_map(&rm.k[j], a.depth[j].k, krows))
       return GDNBEAM_ECUDA;
   }
   p.anc = a.anc; p.anc_stride = a.anc_stride;
   p.x_inout = a.x_inout; p.delta_dump = a.delta_dump; p.o_dump = a.o_dump; p.err = a.err;
   if (((uintptr_t)a.sctx & 15) || (a.sctx_rstride % 4) != 0) return GDNBEAM_EINVAL;
   CUtensorMap mq, mk, mv, md, mo;
-  if (!beam_map(&mq, a.q, a.R, a.W_t, a.H, true) || !beam_map(&mk, a.k, a.R, a.W_t, a.H, true) ||
+  if (!beam_map(&mq, a.q, a.R, a.W_t, a.Hk, true) || !beam_map(&mk, a.k, a.R, a.W_t, a.Hk, true) ||
       !beam_map(&mv, a.v, a.R, a.W_t, a.H, false) ||
       !beam_map(&md, a.delta_out, a.R, a.W_t, a.H, false, 32, 16) ||
       !beam_map(&mo, a.o_out, a.R, a.W_t, a.H, false, 32, 16))

@@ -183,41 +183,44 @@ int launch_simt_gemm_nt(int dtype, int M, int N, int K, const void* A, int lda, 
 // Projection epilogue: one warp per (row, head)
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void proj_epilogue_kernel(int n, int H, int dk, int dv, const float* __restrict__ P,
+__global__ void proj_epilogue_kernel(int n, int H, int Hk, int dk, int dv, const float* __restrict__ P,
                                      T* __restrict__ q, T* __restrict__ k, T* __restrict__ v,
                                      float* __restrict__ alpha, float* __restrict__ beta,
                                      gdnbeam_dumps dmp) {
   int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   int lane = threadIdx.x & 31;
   if (gw >= n * H) return;
-  int m = gw / H, h = gw % H;
-  const int Np = 2 * H * dk + H * dv + 2 * H;
+  int m = gw / H, h = gw % H;  // value head h; key head h as well while h < Hk
+  const int Np = 2 * Hk * dk + H * dv + 2 * H;
   const float* row = P + (size_t)m * Np;
-  const float* pq = row + h * dk;
-  const float* pk = row + H * dk + h * dk;
-  const float* pv = row + 2 * H * dk + h * dv;
-  float sq = 0.0f, sk = 0.0f;
-  for (int c = lane; c < dk; c += 32) { sq += pq[c] * pq[c]; sk += pk[c] * pk[c]; }
-  for (int o = 16; o > 0; o >>= 1) {
-    sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    sk += __shfl_xor_sync(0xffffffffu, sk, o);
+  const float* pv = row + 2 * Hk * dk + h * dv;
+  if (h < Hk) {
+    const float* pq = row + h * dk;
+    const float* pk = row + Hk * dk + h * dk;
+    float sq = 0.0f, sk = 0.0f;
+    for (int c = lane; c < dk; c += 32) { sq += pq[c] * pq[c]; sk += pk[c] * pk[c]; }
+    for (int o = 16; o > 0; o >>= 1) {
+      sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    }
+    float iq = 1.0f / sqrtf(sq + 1e-6f), ik = 1.0f / sqrtf(sk + 1e-6f);
+    const size_t oq = (size_t)m * Hk * dk + (size_t)h * dk;
+    for (int c = lane; c < dk; c += 32) {
+      float qq = pq[c] * iq, kk = pk[c] * ik;
+      stf(q + oq + c, qq);
+      stf(k + oq + c, kk);
+      if (dmp.q) dmp.q[oq + c] = qq;
+      if (dmp.k) dmp.k[oq + c] = kk;
+    }
   }
-  float iq = 1.0f / sqrtf(sq + 1e-6f), ik = 1.0f / sqrtf(sk + 1e-6f);
-  size_t oq = (size_t)m * H * dk + (size_t)h * dk, ov = (size_t)m * H * dv + (size_t)h * dv;
-  for (int c = lane; c < dk; c += 32) {
-    float qq = pq[c] * iq, kk = pk[c] * ik;
-    stf(q + oq + c, qq);
-    stf(k + oq + c, kk);
-    if (dmp.q) dmp.q[oq + c] = qq;
-    if (dmp.k) dmp.k[oq + c] = kk;
-  }
+  const size_t ov = (size_t)m * H * dv + (size_t)h * dv;
   for (int c = lane; c < dv; c += 32) {
     stf(v + ov + c, pv[c]);
     if (dmp.v) dmp.v[ov + c] = pv[c];
   }
   if (lane == 0) {
-    float a = decay_gate(row[2 * H * dk + H * dv + h]);
-    float b = write_gate(row[2 * H * dk + H * dv + H + h]);
+    float a = decay_gate(row[2 * Hk * dk + H * dv + h]);
+    float b = write_gate(row[2 * Hk * dk + H * dv + H + h]);
     alpha[(size_t)m * H + h] = a;
     beta[(size_t)m * H + h] = b;
     if (dmp.alpha) dmp.alpha[(size_t)m * H + h] = a;
@@ -233,10 +236,10 @@ int launch_proj_epilogue(const gdnbeam_config& c, int n, const float* P, void* q
   long long warps = (long long)n * c.H;
   int blocks = (int)((warps + 7) / 8);
   if (c.dtype == GDNBEAM_BF16)
-    proj_epilogue_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(n, c.H, c.d_k, c.d_v, P,
+    proj_epilogue_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(n, c.H, key_heads(c), c.d_k, c.d_v, P,
         (__nv_bfloat16*)q, (__nv_bfloat16*)k, (__nv_bfloat16*)v, alpha, beta, dm);
   else
-    proj_epilogue_kernel<float><<<blocks, 256, 0, s>>>(n, c.H, c.d_k, c.d_v, P, (float*)q,
+    proj_epilogue_kernel<float><<<blocks, 256, 0, s>>>(n, c.H, key_heads(c), c.d_k, c.d_v, P, (float*)q,
         (float*)k, (float*)v, alpha, beta, dm);
   GDN_LAUNCH_CHECK();
   return GDNBEAM_OK;

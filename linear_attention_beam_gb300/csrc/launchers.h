@@ -49,8 +49,13 @@ int launch_tc_logits(const gdnbeam_config& c, int n, const void* feat, const voi
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Query/key heads of a configuration (value head h reads key head
+// h / (H / key_heads)).
+inline int key_heads(const gdnbeam_config& c) { return c.H_k > 0 ? c.H_k : c.H; }
+
 struct ReplayArgs {
   int R, H, d_k, d_v, t, W_t;
+  int Hk;             // key heads: q, k and the records' keys hold Hk heads
   const float* sctx;  // fp32 [R][H][d_v][d_k], request stride sctx_rstride
   long long sctx_rstride;
   const void *q, *k, *v;
@@ -70,6 +75,7 @@ int launch_tc_replay(const ReplayArgs& a, cudaStream_t s);
 // FullState baseline step for one layer (one d_v x d_k state per beam).
 struct FullStateArgs {
   int R, H, d_k, d_v, t, W_t, W_prev, layers, layer;
+  int Hk;                      // key heads (q, k hold Hk heads)
   const void* sctx_store;      // storage copy of S_ctx [R][...] (the t = 0 parent)
   long long sctx_rstride;      // request stride of sctx_store, elements
   const void* states_prev;     // storage [R*W_prev][layers][H][d_v][d_k]
@@ -88,6 +94,7 @@ int launch_fullstate(int dtype, const FullStateArgs& a, cudaStream_t s);
 // ancestors' records to the request's stored S_ctx, then the current token.
 struct ReplaySsmArgs {
   int R, H, d_k, d_v, t, W_t;
+  int Hk;                      // key heads (q, k and the records' keys hold Hk heads)
   const void* sctx_store;      // storage copy of S_ctx [R][...] (request stride below)
   long long sctx_rstride;      // elements
   const void *q, *k, *v;

@@ -50,11 +50,12 @@ class DecodeResult:
 class BeamDecoder:
     def __init__(self, *, R: int, layers: int, H: int, d_k: int, d_v: int, d_model: int, V: int,
                  T: int, W_max: int, L_max: int, dtype: int, residual: bool,
-                 weights: Dict[str, torch.Tensor], device="cuda", state_path: int = 0):
+                 weights: Dict[str, torch.Tensor], device="cuda", state_path: int = 0,
+                 H_k: int = 0):
         self.lib = load()
         self.cfg = Config(R=R, layers=layers, H=H, d_k=d_k, d_v=d_v, d_model=d_model, V=V, T=T,
                           W_max=W_max, L_max=L_max, dtype=dtype, residual=int(residual),
-                          state_path=int(state_path))
+                          state_path=int(state_path), H_k=int(H_k))
         self.device = torch.device(device)
         self.dtype = dtype
         self.tdtype = TORCH_DTYPE[dtype]
@@ -85,7 +86,7 @@ class BeamDecoder:
         return cls(R=wl.R, layers=wl.layers, H=wl.H, d_k=wl.d_k, d_v=wl.d_v, d_model=wl.d_model,
                    V=wl.V, T=wl.T, W_max=wl.W_max, L_max=L_max or wl.L,
                    dtype=BF16 if wl.dtype == "bf16" else F32, residual=wl.residual,
-                   weights=weights, device=device, state_path=state_path)
+                   weights=weights, device=device, state_path=state_path, H_k=wl.Hk)
 
     def __del__(self):
         try:
@@ -208,7 +209,8 @@ class BeamDecoder:
     def _dump_buffers(self, n: int) -> Dict[str, torch.Tensor]:
         c = self.cfg
         f = lambda *s: torch.zeros(*s, dtype=torch.float32, device=self.device)
-        return {"q": f(c.layers, n, c.H * c.d_k), "k": f(c.layers, n, c.H * c.d_k),
+        hk = c.H_k or c.H
+        return {"q": f(c.layers, n, hk * c.d_k), "k": f(c.layers, n, hk * c.d_k),
                 "v": f(c.layers, n, c.H * c.d_v), "alpha": f(c.layers, n, c.H),
                 "beta": f(c.layers, n, c.H), "delta": f(c.layers, n, c.H * c.d_v),
                 "o": f(c.layers, n, c.H * c.d_v), "logits": f(n, c.V)}

@@ -105,7 +105,11 @@ SKEWED = Workload("skewed_r128", R=128, layers=1, H=16, d_k=128, d_v=128,
                   d_model=2048, V=8192, T=4, W=(256, 1024, 1024, 1024),
                   L=2048, dtype="bf16", seed=4, bias_var=4.0)
 
-WORKLOADS: Dict[str, Workload] = {w.name: w for w in (TINY, SINGLE, BATCHED, DEEP, SKEWED)}
+# Grouped key heads on the tensor-core path: 8 value heads reading 4 key heads.
+GQA = Workload("gqa_w128", R=2, layers=1, H=8, d_k=128, d_v=128, d_model=1024, V=2048, T=3,
+               W=(128, 128, 128), L=256, dtype="bf16", seed=4, H_k=4)
+
+WORKLOADS: Dict[str, Workload] = {w.name: w for w in (TINY, SINGLE, BATCHED, DEEP, SKEWED, GQA)}
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:

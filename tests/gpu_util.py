@@ -67,7 +67,8 @@ def decoder_for(wl, params, L_max=None, state_path=0):
 
 def cfg_for(wl, **over) -> gb.Config:
     d = dict(R=wl.R, layers=wl.layers, H=wl.H, d_k=wl.d_k, d_v=wl.d_v, d_model=wl.d_model,
-             V=wl.V, T=wl.T, W_max=wl.W_max, L_max=wl.L, dtype=dt(wl), residual=int(wl.residual))
+             V=wl.V, T=wl.T, W_max=wl.W_max, L_max=wl.L, dtype=dt(wl), residual=int(wl.residual),
+             H_k=wl.Hk)
     d.update(over)
     return gb.Config(**d)
 

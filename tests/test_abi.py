@@ -43,7 +43,7 @@ def test_binding_constants_match_the_header():
 def cfg(wl, **kw):
     d = dict(R=wl.R, layers=wl.layers, H=wl.H, d_k=wl.d_k, d_v=wl.d_v, d_model=wl.d_model, V=wl.V,
              T=wl.T, W_max=wl.W_max, L_max=wl.L, dtype=gb.BF16 if wl.dtype == "bf16" else gb.F32,
-             residual=int(wl.residual))
+             residual=int(wl.residual), H_k=wl.Hk)
     d.update(kw)
     return gb.Config(**d)
 

@@ -70,6 +70,12 @@ SMALL = {
     "tiny_f32": synth.TINY,
     "single_w256": synth.SINGLE,
     "single_w256_f32": synth.SINGLE.with_(name="single_w256_f32", dtype="f32"),
+    # grouped key heads (value heads 2h, 2h + 1 read key head h) with d_v != d_k
+    "tiny_gqa_f32": synth.tiny_workload(d=16, d_v=32, H=4, H_k=2, V=24, T=3, W=(8, 12, 10),
+                                        d_model=64, L=40, seed=3),
+    # the same grouping on the tensor-core paths (d = 128, bf16); one request,
+    # as the forced lineage is one request's
+    "gqa_w128": synth.GQA.with_(R=1),
 }
 
 
@@ -145,6 +151,7 @@ FULL = {
     "batched_r64_w512": (synth.BATCHED, (0, 63)),
     "deep4_w1024": (synth.DEEP, (5,)),
     "skewed_r128": (synth.SKEWED, (127,)),
+    "gqa_w128": (synth.GQA, (0, 1)),
 }
 
 
@@ -174,7 +181,7 @@ def test_decode_full_size_sampled(name):
         W_t = wl.W[t]
         n = wl.R * W_t
         f = lambda *s: torch.zeros(*s, device=DEV)
-        dd = {"q": f(wl.layers, n, wl.H * wl.d_k), "k": f(wl.layers, n, wl.H * wl.d_k),
+        dd = {"q": f(wl.layers, n, wl.Hk * wl.d_k), "k": f(wl.layers, n, wl.Hk * wl.d_k),
               "v": f(wl.layers, n, wl.H * wl.d_v), "alpha": f(wl.layers, n, wl.H),
               "beta": f(wl.layers, n, wl.H), "delta": f(wl.layers, n, wl.H * wl.d_v),
               "o": f(wl.layers, n, wl.H * wl.d_v), "logits": f(n, wl.V)}

@@ -143,16 +143,30 @@ def test_ancestry_op_matches_walk():
     ("bf16", 128, 2, 1, 96, 5, False), ("bf16", 128, 2, 2, 40, 1, True),
     ("bf16", 128, 3, 2, 512, 2, False), ("bf16", 128, 2, 2, 70, 4, False)])
 def test_replay_op(dtype, d, H, R, W_t, t, resid):
-    wl = synth.tiny_workload(d=d, V=7, H=H, R=R, dtype=dtype)
-    rng = np.random.default_rng(d + H + W_t + t)
+    _replay_op(dtype, d, H, R, W_t, t, resid, H)
+
+
+@pytest.mark.parametrize("dtype,d,H,Hk,R,W_t,t", [
+    ("f32", 16, 4, 2, 2, 9, 2), ("f32", 32, 6, 3, 1, 20, 3), ("bf16", 128, 4, 1, 2, 70, 2),
+    ("bf16", 128, 8, 4, 2, 96, 1)])
+def test_replay_op_grouped_key_heads(dtype, d, H, Hk, R, W_t, t):
+    # value head h reads query/key head h // (H // Hk) and that head's
+    # ancestor keys; the tensor-core kernel and the CUDA-core one alike
+    _replay_op(dtype, d, H, R, W_t, t, False, Hk)
+
+
+def _replay_op(dtype, d, H, R, W_t, t, resid, Hk):
+    wl = synth.tiny_workload(d=d, V=7, H=H, R=R, dtype=dtype, H_k=Hk)
+    g = H // Hk
+    rng = np.random.default_rng(d + H + W_t + t + 100 * Hk)
     st_ = lambda a: store(a, wl)
     S_ctx = (rng.standard_normal((R, H, d, d)) * 0.05).astype(np.float32).astype(np.float64)
     Wj = [int(rng.integers(1, 40)) for _ in range(t)]
-    rec_k = [st_(_unit_rows(rng, (R, Wj[j], H, d))) for j in range(t)]
+    rec_k = [st_(_unit_rows(rng, (R, Wj[j], Hk, d))) for j in range(t)]
     rec_d = [st_(rng.standard_normal((R, Wj[j], H, d)) * 0.5) for j in range(t)]
     rec_a = [rng.uniform(0.2, 1.0, (R, Wj[j], H)).astype(np.float32).astype(np.float64) for j in range(t)]
-    q = st_(_unit_rows(rng, (R, W_t, H, d)))
-    k = st_(_unit_rows(rng, (R, W_t, H, d)))
+    q = st_(_unit_rows(rng, (R, W_t, Hk, d)))
+    k = st_(_unit_rows(rng, (R, W_t, Hk, d)))
     v = st_(rng.standard_normal((R, W_t, H, d)))
     al = rng.uniform(0.1, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
     be = rng.uniform(0.0, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
@@ -173,7 +187,7 @@ def test_replay_op(dtype, d, H, R, W_t, t, resid):
     o_dump = torch.zeros_like(d_dump)
     x_dev = to_dev(x0.reshape(n, H * d)) if resid else None
     dm = gb.dumps(delta=d_dump, o=o_dump)
-    cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d, T=max(t + 1, 2))
+    cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d, T=max(t + 1, 2), H_k=Hk)
     lib = gb.load()
     st = lib.gdnbeam_replay(C.byref(cfg), t, W_t, gb.ptr(to_dev(S_ctx.reshape(-1))), H * d * d,
                             gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
@@ -187,9 +201,10 @@ def test_replay_op(dtype, d, H, R, W_t, t, resid):
     for r in range(R):
         for b in range(W_t):
             for h in range(H):
-                chain = [(rec_a[j][r, anc[r, b, j], h], rec_d[j][r, anc[r, b, j], h], rec_k[j][r, anc[r, b, j], h]) for j in range(t)]
+                hk = h // g
+                chain = [(rec_a[j][r, anc[r, b, j], h], rec_d[j][r, anc[r, b, j], h], rec_k[j][r, anc[r, b, j], hk]) for j in range(t)]
                 exp_d[r, b, h], exp_o[r, b, h] = oracle.step_from_records(
-                    S_ctx[r, h], chain, q[r, b, h], k[r, b, h], v[r, b, h], al[r, b, h], be[r, b, h])
+                    S_ctx[r, h], chain, q[r, b, hk], k[r, b, hk], v[r, b, h], al[r, b, h], be[r, b, h])
     tol = _tol(wl)
     assert maxrel(host(d_dump).reshape(exp_d.shape), exp_d) <= tol
     assert maxrel(host(o_dump).reshape(exp_o.shape), exp_o) <= tol
