@@ -66,7 +66,8 @@ enum {
 
 #define GDNBEAM_MAX_T 8        /* longest SID (selections) supported */
 
-/* Shape of one decode job. d_k, d_v in {16, 32, 64, 128}; 1 <= T <= GDNBEAM_MAX_T;
+/* Shape of one decode job. d_k in {16, 32, 64, 128, 256}, d_v in {16, 32, 64,
+ * 128, 256, 512} (the state-path baselines: both at most 128); 1 <= T <= GDNBEAM_MAX_T;
  * V <= 16384; W_max <= 4096. residual = 0 requires layers = 1 and reads the
  * codebook logits off concat_h(o) (OneLA §1.2 eq. 3 output); residual = 1 runs
  * a residual stream with unit-gain RMSNorm (eps 1e-6) before each layer and
@@ -74,7 +75,7 @@ enum {
 typedef struct gdnbeam_config {
   int R;        /* requests decoded together */
   int layers;   /* stacked GDN layers */
-  int H;        /* heads per layer */
+  int H;        /* (value) heads per layer */
   int d_k;      /* key / query width per head */
   int d_v;      /* value width per head */
   int d_model;  /* embedding width */

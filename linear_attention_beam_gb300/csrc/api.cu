@@ -38,14 +38,18 @@ inline size_t elem_size(int dtype) { return dtype == GDNBEAM_BF16 ? 2 : 4; }
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline int n_proj(const gdnbeam_config& c) { return 2 * key_heads(c) * c.d_k + c.H * c.d_v + 2 * c.H; }
 inline int feat_dim(const gdnbeam_config& c) { return c.residual ? c.d_model : c.H * c.d_v; }
-inline bool pow2_head(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+inline bool key_width_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128 || d == 256; }
+inline bool value_width_ok(int d) { return key_width_ok(d) || d == 512; }
 
 int validate(const gdnbeam_config* c) {
   if (!c) return GDNBEAM_EINVAL;
   if (c->R < 1 || c->layers < 1 || c->H < 1 || c->d_model < 1 || c->V < 2 || c->T < 1 ||
       c->W_max < 1 || c->L_max < 1)
     return GDNBEAM_EINVAL;
-  if (c->T > GDNBEAM_MAX_T || !pow2_head(c->d_k) || !pow2_head(c->d_v)) return GDNBEAM_EUNSUPPORTED;
+  if (c->T > GDNBEAM_MAX_T || !key_width_ok(c->d_k) || !value_width_ok(c->d_v))
+    return GDNBEAM_EUNSUPPORTED;
+  // the state-path baselines keep a whole d_v x d_k state per block
+  if (c->state_path != 0 && (c->d_k > 128 || c->d_v > 128)) return GDNBEAM_EUNSUPPORTED;
   if (c->dtype != GDNBEAM_F32 && c->dtype != GDNBEAM_BF16) return GDNBEAM_EUNSUPPORTED;
   if (c->V > 16384 || c->W_max > 4096) return GDNBEAM_EUNSUPPORTED;
   if (!c->residual && c->layers != 1) return GDNBEAM_EUNSUPPORTED;

@@ -44,7 +44,7 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
 // barrier. Each thread's column segment is padded by 16 bytes so the TPR
 // threads of a row pair read different banks.
 template <typename T, int DK, int TPR, int CH>
-__global__ void __launch_bounds__(64 * TPR, 2) prefill_scan_kernel(
+__global__ void __launch_bounds__(64 * TPR, TPR <= 4 ? 2 : 1) prefill_scan_kernel(
     int L, int H, int Hk, int dv, const T* __restrict__ q, const T* __restrict__ k,
     const T* __restrict__ v, const float* __restrict__ alpha, const float* __restrict__ beta,
     float* __restrict__ sctx, long long rstride, T* __restrict__ o_last, float* __restrict__ x) {
@@ -63,9 +63,11 @@ __global__ void __launch_bounds__(64 * TPR, 2) prefill_scan_kernel(
   float2* gs = reinterpret_cast<float2*>(vs + 2 * CH * 128);  // [2][CH]
   const int r = blockIdx.x / H, h = blockIdx.x % H;
   const int hk = h / (H / Hk);  // the key head this value head reads
+  const int v0 = blockIdx.y * 128;  // this block's 128 value rows
+  const int dvb = min(128, dv - v0);
   const int tid = threadIdx.x;
   const int i = tid / TPR, part = tid % TPR, c0 = part * NC;  // rows i and i + 64
-  const int VV = dv / EPV;                 // 16-byte pieces per v row
+  const int VV = dvb / EPV;                // 16-byte pieces of this block's v slice
   const int per_chunk = CH * (2 * KV + VV);
   uint64_t S[2][NP];
 #pragma unroll
@@ -88,7 +90,7 @@ __global__ void __launch_bounds__(64 * TPR, 2) prefill_scan_kernel(
         int heads, head;
         if (u < CH * KV) { t = u / KV; piece = u % KV; base = k; width = DK; heads = Hk; head = hk; }
         else if (u < 2 * CH * KV) { t = (u - CH * KV) / KV; piece = (u - CH * KV) % KV; base = q; width = DK; heads = Hk; head = hk; }
-        else { t = (u - 2 * CH * KV) / VV; piece = (u - 2 * CH * KV) % VV; base = v; width = dv; heads = H; head = h; }
+        else { t = (u - 2 * CH * KV) / VV; piece = (u - 2 * CH * KV) % VV + v0 / EPV; base = v; width = dv; heads = H; head = h; }
         const int pos = chunk * CH + t;
         if (pos < L)
           buf[e] = __ldg(reinterpret_cast<const uint4*>(base + ((row0 + pos) * heads + head) * width) + piece);
@@ -125,7 +127,7 @@ __global__ void __launch_bounds__(64 * TPR, 2) prefill_scan_kernel(
     stash(0, buf, g);
   }
   __syncthreads();
-  const bool act0 = i < dv, act1 = i + 64 < dv;
+  const bool act0 = i < dvb, act1 = i + 64 < dvb;
   for (int chunk = 0; chunk < n_chunks; ++chunk) {
     const int sb = chunk & 1;
     uint4 nxt[PF];
@@ -186,12 +188,12 @@ __global__ void __launch_bounds__(64 * TPR, 2) prefill_scan_kernel(
         const int pos = chunk * CH + t;
         const size_t row = row0 + pos;
         if (act0) {
-          if (x) x[(row * H + h) * dv + i] += o0;
-          if (o_last && pos == L - 1) stf(o_last + ((size_t)r * H + h) * dv + i, o0);
+          if (x) x[(row * H + h) * dv + v0 + i] += o0;
+          if (o_last && pos == L - 1) stf(o_last + ((size_t)r * H + h) * dv + v0 + i, o0);
         }
         if (act1) {
-          if (x) x[(row * H + h) * dv + i + 64] += o1;
-          if (o_last && pos == L - 1) stf(o_last + ((size_t)r * H + h) * dv + i + 64, o1);
+          if (x) x[(row * H + h) * dv + v0 + i + 64] += o1;
+          if (o_last && pos == L - 1) stf(o_last + ((size_t)r * H + h) * dv + v0 + i + 64, o1);
         }
       }
     }
@@ -202,8 +204,8 @@ __global__ void __launch_bounds__(64 * TPR, 2) prefill_scan_kernel(
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     const int ri = i + 64 * rr;
-    if (ri < dv) {
-      float* out = sctx + (size_t)r * rstride + ((size_t)h * dv + ri) * DK + c0;
+    if (ri < dvb) {
+      float* out = sctx + (size_t)r * rstride + ((size_t)h * dv + v0 + ri) * DK + c0;
 #pragma unroll
       for (int c = 0; c < NP; ++c) {
         const float2 f = up2(S[rr][c]);
@@ -225,7 +227,7 @@ int launch_scan(const gdnbeam_config& c, int L, const void* q, const void* k, co
   const size_t smem = (size_t)(2 * CH * RS * 2 + 2 * CH * 128) * sizeof(float) + 2 * CH * sizeof(float2);
   GDN_CUDA(cudaFuncSetAttribute(prefill_scan_kernel<T, DK, TPR, CH>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  prefill_scan_kernel<T, DK, TPR, CH><<<c.R * c.H, 64 * TPR, smem, s>>>(
+  prefill_scan_kernel<T, DK, TPR, CH><<<dim3(c.R * c.H, (c.d_v + 127) / 128), 64 * TPR, smem, s>>>(
       L, c.H, key_heads(c), c.d_v, (const T*)q, (const T*)k, (const T*)v, alpha, beta, sctx, rs,
       (T*)o_last, x);
   return GDNBEAM_OK;
@@ -245,6 +247,7 @@ int dispatch_dk(const gdnbeam_config& c, int L, const void* q, const void* k, co
     case 32: st = launch_scan<T, 32, 1>(c, L, q, k, v, alpha, beta, sctx, rs, o_last, x, s); break;
     case 64: st = launch_scan<T, 64, 2>(c, L, q, k, v, alpha, beta, sctx, rs, o_last, x, s); break;
     case 128: st = launch_scan<T, 128, 4>(c, L, q, k, v, alpha, beta, sctx, rs, o_last, x, s); break;
+    case 256: st = launch_scan<T, 256, 8>(c, L, q, k, v, alpha, beta, sctx, rs, o_last, x, s); break;
     default: return GDNBEAM_EUNSUPPORTED;
   }
   if (st) return st;
@@ -258,7 +261,7 @@ int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const voi
                         const void* v, const float* alpha, const float* beta, float* sctx,
                         long long rs, void* o_last, float* x, cudaStream_t s) {
   if (L <= 0) return GDNBEAM_EINVAL;
-  if (c.d_v > 128) return GDNBEAM_EUNSUPPORTED;
+  if (c.d_v > 128 && c.d_v % 128 != 0) return GDNBEAM_EUNSUPPORTED;
   if (c.dtype == GDNBEAM_BF16)
     return dispatch_dk<__nv_bfloat16>(c, L, q, k, v, alpha, beta, sctx, rs, o_last, x, s);
   return dispatch_dk<float>(c, L, q, k, v, alpha, beta, sctx, rs, o_last, x, s);

@@ -14,7 +14,7 @@ namespace gdnbeam {
 namespace {
 
 constexpr int kBeams = 16;    // beams per block
-constexpr int kThreads = 128; // one thread per value row (d_v <= 128)
+constexpr int kThreads = 128; // one thread per value row of a 128-row block
 constexpr int kChunk = 32;    // key columns of S_ctx staged per pass
 
 template <typename T>
@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kThreads) replay_simt_kernel(ReplayArgs a) {
   const int hk = h / (H / Hk);  // the key head this value head reads
   const int b0 = blockIdx.y * kBeams;
   const int nb = min(kBeams, a.W_t - b0);
+  const int v0 = blockIdx.z * kThreads;     // first value row of this block
+  const int dvb = min(kThreads, dv - v0);    // value rows of this block
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   extern __shared__ float sm[];
@@ -92,15 +94,15 @@ __global__ void __launch_bounds__(kThreads) replay_simt_kernel(ReplayArgs a) {
   float uq[kBeams], uk[kBeams];
 #pragma unroll
   for (int b = 0; b < kBeams; ++b) { uq[b] = 0.0f; uk[b] = 0.0f; }
-  const float* S = a.sctx + (size_t)r * a.sctx_rstride + (size_t)h * dv * dk;
+  const float* S = a.sctx + (size_t)r * a.sctx_rstride + ((size_t)h * dv + v0) * dk;
   for (int c0 = 0; c0 < dk; c0 += kChunk) {
     __syncthreads();
-    for (int i = tid; i < dv * kChunk; i += kThreads) {
+    for (int i = tid; i < dvb * kChunk; i += kThreads) {
       int row = i / kChunk, c = i % kChunk;
       sc[row * (kChunk + 1) + c] = (c0 + c < dk) ? S[(size_t)row * dk + c0 + c] : 0.0f;
     }
     __syncthreads();
-    if (tid < dv) {
+    if (tid < dvb) {
       const int cn = min(kChunk, dk - c0);
       for (int c = 0; c < cn; ++c) {
         float sv = sc[tid * (kChunk + 1) + c];
@@ -117,8 +119,8 @@ __global__ void __launch_bounds__(kThreads) replay_simt_kernel(ReplayArgs a) {
   __syncthreads();
 
   // 4. fold the ancestors' records, then eq. 8
-  if (tid < dv) {
-    const int i = tid;
+  if (tid < dvb) {
+    const int i = v0 + tid;
 #pragma unroll
     for (int b = 0; b < kBeams; ++b) {
       if (b >= nb) break;
@@ -150,16 +152,21 @@ __global__ void __launch_bounds__(kThreads) replay_simt_kernel(ReplayArgs a) {
 
 int launch_replay(int dtype, const ReplayArgs& a, cudaStream_t s) {
   if (a.W_t <= 0) return GDNBEAM_OK;
-  if (a.d_v > 128 || a.t >= GDNBEAM_MAX_T) return GDNBEAM_EUNSUPPORTED;
-  dim3 grid(a.R * a.H, (a.W_t + kBeams - 1) / kBeams);
+  if (a.t >= GDNBEAM_MAX_T) return GDNBEAM_EUNSUPPORTED;
+  dim3 grid(a.R * a.H, (a.W_t + kBeams - 1) / kBeams, (a.d_v + kThreads - 1) / kThreads);
   if (grid.y > 65535) return GDNBEAM_EUNSUPPORTED;
   size_t smem = sizeof(float) * (2 * kBeams * a.d_k + 128 * (kChunk + 1) +
                                  2 * kBeams * GDNBEAM_MAX_T + kBeams) +
                 sizeof(int) * kBeams * GDNBEAM_MAX_T;
-  if (dtype == GDNBEAM_BF16)
+  if (dtype == GDNBEAM_BF16) {
+    GDN_CUDA(cudaFuncSetAttribute(replay_simt_kernel<__nv_bfloat16>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     replay_simt_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(a);
-  else
+  } else {
+    GDN_CUDA(cudaFuncSetAttribute(replay_simt_kernel<float>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     replay_simt_kernel<float><<<grid, kThreads, smem, s>>>(a);
+  }
   GDN_LAUNCH_CHECK();
   return GDNBEAM_OK;
 }

@@ -82,7 +82,8 @@ def test_record_size_and_capacity_match_the_page():
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("d_k", 96, gb.EUNSUPPORTED), ("d_v", 256, gb.EUNSUPPORTED), ("T", 9, gb.EUNSUPPORTED),
+    ("d_k", 96, gb.EUNSUPPORTED), ("d_k", 512, gb.EUNSUPPORTED), ("d_v", 1024, gb.EUNSUPPORTED),
+    ("T", 9, gb.EUNSUPPORTED),
     ("V", 20000, gb.EUNSUPPORTED), ("layers", 2, gb.EUNSUPPORTED), ("dtype", 7, gb.EUNSUPPORTED),
     ("R", 0, gb.EINVAL), ("W_max", 0, gb.EINVAL), ("V", 1, gb.EINVAL), ("state_path", 3, gb.EUNSUPPORTED),
     ("state_path", -1, gb.EUNSUPPORTED)])
@@ -90,6 +91,13 @@ def test_config_rejections(field, value, status):
     c = cfg(synth.TINY)
     setattr(c, field, value)
     assert footprint(c)[0] == status
+
+
+def test_wide_heads_are_accepted_on_the_replay_path_only():
+    for dk, dv in ((256, 256), (128, 512), (256, 512)):
+        assert footprint(cfg(synth.TINY, d_k=dk, d_v=dv, d_model=dv))[0] == 0
+        for sp in (1, 2):  # the baselines keep whole states on chip
+            assert footprint(cfg(synth.TINY, d_k=dk, d_v=dv, d_model=dv, state_path=sp))[0] == gb.EUNSUPPORTED
 
 
 def test_state_path_workspaces():

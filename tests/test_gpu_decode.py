@@ -76,12 +76,20 @@ SMALL = {
     # the same grouping on the tensor-core paths (d = 128, bf16); one request,
     # as the forced lineage is one request's
     "gqa_w128": synth.GQA.with_(R=1),
+    # wide heads: d_k 256, d_v 512 on the CUDA-core paths (fp32), and d_v 256
+    # through the tensor-core replay (bf16)
+    "wide_f32": synth.tiny_workload(d=256, d_v=512, H=2, H_k=1, V=40, T=3, W=(6, 9, 7),
+                                    d_model=96, L=24, seed=12),
+    "wide_v256": synth.Workload("wide_v256", R=1, layers=1, H=4, d_k=128, d_v=256, d_model=512,
+                                V=1024, T=3, W=(64, 64, 64), L=96, dtype="bf16", seed=13, H_k=2),
 }
 
 
 @pytest.mark.parametrize("state_path", [0, 1, 2], ids=["replay", "fullstate", "replayssm"])
 @pytest.mark.parametrize("name", list(SMALL))
 def test_decode_forced_on_oracle_lineage(name, state_path):
+    if state_path and max(SMALL[name].d_k, SMALL[name].d_v) > 128:
+        pytest.skip("the state-path baselines keep heads of width <= 128")
     # state_path 1 is the FullState baseline (per-beam states copied on
     # reorder), 2 the ReplaySSM baseline (states rebuilt from S_ctx and the
     # ancestors' records every call): the same comparisons hold for both

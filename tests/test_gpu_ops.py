@@ -146,6 +146,16 @@ def test_replay_op(dtype, d, H, R, W_t, t, resid):
     _replay_op(dtype, d, H, R, W_t, t, resid, H)
 
 
+@pytest.mark.parametrize("dtype,dk,dv,H,Hk,R,W_t,t", [
+    ("bf16", 256, 256, 2, 1, 2, 70, 1), ("bf16", 128, 512, 2, 2, 1, 40, 2), ("bf16", 256, 128, 2, 1, 2, 33, 0),
+    ("bf16", 256, 512, 2, 1, 1, 64, 2), ("f32", 256, 512, 2, 1, 1, 19, 2), ("f32", 32, 256, 3, 3, 2, 17, 1)])
+def test_replay_op_wide_heads(dtype, dk, dv, H, Hk, R, W_t, t):
+    # key widths up to 256 and value widths up to 512 (blocks of 128 value
+    # rows); d_k = 256 at depth 2 leaves one pipeline stage and runs on the
+    # CUDA cores
+    _replay_op(dtype, dk, H, R, W_t, t, False, Hk, dv=dv)
+
+
 @pytest.mark.parametrize("dtype,d,H,Hk,R,W_t,t", [
     ("f32", 16, 4, 2, 2, 9, 2), ("f32", 32, 6, 3, 1, 20, 3), ("bf16", 128, 4, 1, 2, 70, 2),
     ("bf16", 128, 8, 4, 2, 96, 1)])
@@ -155,23 +165,25 @@ def test_replay_op_grouped_key_heads(dtype, d, H, Hk, R, W_t, t):
     _replay_op(dtype, d, H, R, W_t, t, False, Hk)
 
 
-def _replay_op(dtype, d, H, R, W_t, t, resid, Hk):
-    wl = synth.tiny_workload(d=d, V=7, H=H, R=R, dtype=dtype, H_k=Hk)
+def _replay_op(dtype, d, H, R, W_t, t, resid, Hk, dv=None):
+    dk = d
+    dv = dv or d
+    wl = synth.tiny_workload(d=dk, d_v=dv, V=7, H=H, R=R, dtype=dtype, H_k=Hk)
     g = H // Hk
-    rng = np.random.default_rng(d + H + W_t + t + 100 * Hk)
+    rng = np.random.default_rng(d + H + W_t + t + 100 * Hk + dv)
     st_ = lambda a: store(a, wl)
-    S_ctx = (rng.standard_normal((R, H, d, d)) * 0.05).astype(np.float32).astype(np.float64)
+    S_ctx = (rng.standard_normal((R, H, dv, dk)) * 0.05).astype(np.float32).astype(np.float64)
     Wj = [int(rng.integers(1, 40)) for _ in range(t)]
-    rec_k = [st_(_unit_rows(rng, (R, Wj[j], Hk, d))) for j in range(t)]
-    rec_d = [st_(rng.standard_normal((R, Wj[j], H, d)) * 0.5) for j in range(t)]
+    rec_k = [st_(_unit_rows(rng, (R, Wj[j], Hk, dk))) for j in range(t)]
+    rec_d = [st_(rng.standard_normal((R, Wj[j], H, dv)) * 0.5) for j in range(t)]
     rec_a = [rng.uniform(0.2, 1.0, (R, Wj[j], H)).astype(np.float32).astype(np.float64) for j in range(t)]
-    q = st_(_unit_rows(rng, (R, W_t, Hk, d)))
-    k = st_(_unit_rows(rng, (R, W_t, Hk, d)))
-    v = st_(rng.standard_normal((R, W_t, H, d)))
+    q = st_(_unit_rows(rng, (R, W_t, Hk, dk)))
+    k = st_(_unit_rows(rng, (R, W_t, Hk, dk)))
+    v = st_(rng.standard_normal((R, W_t, H, dv)))
     al = rng.uniform(0.1, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
     be = rng.uniform(0.0, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
     anc = np.stack([rng.integers(0, Wj[j], (R, W_t)) for j in range(t)], -1).astype(np.int32) if t else np.zeros((R, W_t, 1), np.int32)
-    x0 = rng.standard_normal((R, W_t, H * d)) if resid else None
+    x0 = rng.standard_normal((R, W_t, H * dv)) if resid else None
 
     td = tdt(wl)
     keep = []
@@ -181,15 +193,15 @@ def _replay_op(dtype, d, H, R, W_t, t, resid, Hk):
         keep += [tk, tdl, ta]
         recs[j] = gb.Records(gb.ptr(tk), gb.ptr(tdl), gb.ptr(ta), Wj[j])
     n = R * W_t
-    d_out = torch.empty(n, H * d, dtype=td, device=DEV)
+    d_out = torch.empty(n, H * dv, dtype=td, device=DEV)
     o_out = torch.empty_like(d_out)
-    d_dump = torch.zeros(n, H * d, device=DEV)
+    d_dump = torch.zeros(n, H * dv, device=DEV)
     o_dump = torch.zeros_like(d_dump)
-    x_dev = to_dev(x0.reshape(n, H * d)) if resid else None
+    x_dev = to_dev(x0.reshape(n, H * dv)) if resid else None
     dm = gb.dumps(delta=d_dump, o=o_dump)
-    cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d, T=max(t + 1, 2), H_k=Hk)
+    cfg = cfg_for(wl, R=R, H=H, d_k=dk, d_v=dv, d_model=H * dv, T=max(t + 1, 2), H_k=Hk)
     lib = gb.load()
-    st = lib.gdnbeam_replay(C.byref(cfg), t, W_t, gb.ptr(to_dev(S_ctx.reshape(-1))), H * d * d,
+    st = lib.gdnbeam_replay(C.byref(cfg), t, W_t, gb.ptr(to_dev(S_ctx.reshape(-1))), H * dv * dk,
                             gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
                             gb.ptr(to_dev(v.reshape(-1), td)), gb.ptr(to_dev(al.reshape(-1))),
                             gb.ptr(to_dev(be.reshape(-1))), recs,
@@ -197,7 +209,7 @@ def _replay_op(dtype, d, H, R, W_t, t, resid, Hk):
                             gb.ptr(d_out), gb.ptr(o_out), gb.ptr(x_dev), C.byref(dm), None)
     assert st == 0
     assert device_status_clear() == 0
-    exp_d = np.zeros((R, W_t, H, d)); exp_o = np.zeros_like(exp_d)
+    exp_d = np.zeros((R, W_t, H, dv)); exp_o = np.zeros_like(exp_d)
     for r in range(R):
         for b in range(W_t):
             for h in range(H):
@@ -211,7 +223,7 @@ def _replay_op(dtype, d, H, R, W_t, t, resid, Hk):
     _check_stored(host(d_out).reshape(exp_d.shape), exp_d, wl, "delta")
     _check_stored(host(o_out).reshape(exp_o.shape), exp_o, wl, "o")
     if resid:
-        assert maxrel(host(x_dev).reshape(R, W_t, H * d), x0 + exp_o.reshape(R, W_t, H * d)) <= tol
+        assert maxrel(host(x_dev).reshape(R, W_t, H * dv), x0 + exp_o.reshape(R, W_t, H * dv)) <= tol
 
 
 @pytest.mark.parametrize("dtype,d", [("f32", 16), ("bf16", 128)])
@@ -302,30 +314,45 @@ def test_logits_op(dtype, F, V, n):
 @pytest.mark.parametrize("dtype,d,H,R,L,resid", [("f32", 16, 1, 1, 32, False), ("bf16", 32, 2, 2, 33, True),
                                                  ("bf16", 128, 2, 2, 65, False)])
 def test_prefill_scan_op(dtype, d, H, R, L, resid):
-    wl = synth.tiny_workload(d=d, V=5, H=H, R=R, dtype=dtype)
-    rng = np.random.default_rng(L + d)
-    q = store(_unit_rows(rng, (R, L, H, d)), wl)
-    k = store(_unit_rows(rng, (R, L, H, d)), wl)
-    v = store(rng.standard_normal((R, L, H, d)), wl)
+    _prefill_scan_op(dtype, d, d, H, H, R, L, resid)
+
+
+@pytest.mark.parametrize("dtype,dk,dv,H,Hk,R,L", [
+    ("bf16", 256, 512, 2, 1, 1, 70), ("f32", 256, 256, 2, 2, 1, 33), ("bf16", 128, 256, 4, 2, 2, 40),
+    ("f32", 16, 32, 4, 2, 1, 50)])
+def test_prefill_scan_op_wide_and_grouped(dtype, dk, dv, H, Hk, R, L):
+    # key widths up to 256, value widths up to 512 (blocks of 128 value rows),
+    # grouped key heads
+    _prefill_scan_op(dtype, dk, dv, H, Hk, R, L, False)
+
+
+def _prefill_scan_op(dtype, dk, dv, H, Hk, R, L, resid):
+    wl = synth.tiny_workload(d=dk, d_v=dv, V=5, H=H, R=R, dtype=dtype, H_k=Hk)
+    rng = np.random.default_rng(L + dk + dv)
+    q = store(_unit_rows(rng, (R, L, Hk, dk)), wl)
+    k = store(_unit_rows(rng, (R, L, Hk, dk)), wl)
+    v = store(rng.standard_normal((R, L, H, dv)), wl)
     a = rng.uniform(0.3, 1.0, (R, L, H)).astype(np.float32).astype(np.float64)
     b = rng.uniform(0.0, 1.0, (R, L, H)).astype(np.float32).astype(np.float64)
-    x0 = rng.standard_normal((R, L, H * d)) if resid else None
+    x0 = rng.standard_normal((R, L, H * dv)) if resid else None
     td = tdt(wl)
     lib = gb.load()
-    cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d)
-    sc = torch.empty(R, H, d, d, dtype=torch.float32, device=DEV)
-    ol = torch.empty(R, H * d, dtype=td, device=DEV)
-    xd = to_dev(x0.reshape(R * L, H * d)) if resid else None
+    cfg = cfg_for(wl, R=R, H=H, d_k=dk, d_v=dv, d_model=H * dv, H_k=Hk)
+    sc = torch.empty(R, H, dv, dk, dtype=torch.float32, device=DEV)
+    ol = torch.empty(R, H * dv, dtype=td, device=DEV)
+    xd = to_dev(x0.reshape(R * L, H * dv)) if resid else None
     st = lib.gdnbeam_prefill_scan(C.byref(cfg), L, gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
                                   gb.ptr(to_dev(v.reshape(-1), td)), gb.ptr(to_dev(a.reshape(-1))),
-                                  gb.ptr(to_dev(b.reshape(-1))), gb.ptr(sc), H * d * d, gb.ptr(ol), gb.ptr(xd), None)
+                                  gb.ptr(to_dev(b.reshape(-1))), gb.ptr(sc), H * dv * dk, gb.ptr(ol), gb.ptr(xd), None)
     assert st == 0
+    g = H // Hk
     for r in range(R):
-        S, o = oracle.prefill_scan(q[r], k[r], v[r], a[r], b[r])
+        qe, ke = np.repeat(q[r], g, axis=1), np.repeat(k[r], g, axis=1)
+        S, o = oracle.prefill_scan(qe, ke, v[r], a[r], b[r])
         assert maxrel(host(sc[r]), S) <= _tol(wl), "S_ctx"
-        _check_stored(host(ol[r]).reshape(H, d), o[-1], wl, "o_last")
+        _check_stored(host(ol[r]).reshape(H, dv), o[-1], wl, "o_last")
         if resid:
-            assert maxrel(host(xd).reshape(R, L, H * d)[r], x0[r] + o.reshape(L, H * d)) <= _tol(wl)
+            assert maxrel(host(xd).reshape(R, L, H * dv)[r], x0[r] + o.reshape(L, H * dv)) <= _tol(wl)
 
 
 # ------------------------------------------------------------------ tensor-core GEMMs
