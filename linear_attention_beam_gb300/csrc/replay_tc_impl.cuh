@@ -590,7 +590,9 @@ int launch_tc_replay_dk(const ReplayArgs& a, cudaStream_t s) {
   const long long budget = 227LL * 1024 - static_bytes - 1024 - (long long)table;
   p.stages = budget > 0 ? (int)(budget / p.stage_bytes) : 0;
   if (p.stages > kMaxStages) p.stages = kMaxStages;
-  if (p.stages < 2) return launch_replay(GDNBEAM_BF16, a, s);
+  // one stage still runs (loads of a tile then wait for the previous tile's
+  // consumers); none left (deep replay on a wide beam) takes the CUDA cores
+  if (p.stages < 1) return launch_replay(GDNBEAM_BF16, a, s);
   p.sctx = a.sctx; p.sctx_rstride = a.sctx_rstride;
   p.alpha = a.alpha; p.beta = a.beta;
   RecMaps rm;

@@ -111,6 +111,28 @@ GQA = Workload("gqa_w128", R=2, layers=1, H=8, d_k=128, d_v=128, d_model=1024, V
 
 WORKLOADS: Dict[str, Workload] = {w.name: w for w in (TINY, SINGLE, BATCHED, DEEP, SKEWED, GQA)}
 
+# Operator sweep (OneLA §3, operator experiments; results in §4.2): R in
+# {4, 8, 16}, W in {128, 256, 512}, T = 2..6 decode calls (there T = O - 1,
+# so the replay depths of a shape are 0 .. T-1), and nine recurrent
+# geometries spanning H_K 4-32, H_V 4-64, K 128-256, V 128-512: 405 shapes.
+# The pages give only those ranges and the largest "Qwen" geometry
+# (H_K = H_V = 16, K = V = 128); the other eight below are chosen to reach
+# the ends of every range, with grouped key heads and wide heads.
+SWEEP_R = (4, 8, 16)
+SWEEP_W = (128, 256, 512)
+SWEEP_T = (2, 3, 4, 5, 6)
+SWEEP_GEOMETRIES = (  # (H_K, H_V, K, V)
+    (16, 16, 128, 128),
+    (4, 4, 128, 128),
+    (32, 32, 128, 128),
+    (8, 16, 128, 128),
+    (16, 64, 128, 128),
+    (8, 8, 256, 256),
+    (4, 8, 256, 256),
+    (8, 8, 128, 512),
+    (4, 16, 256, 512),
+)
+
 
 def round_bf16(x: np.ndarray) -> np.ndarray:
     """Round float values to the nearest bf16 (ties to even); float32 result."""

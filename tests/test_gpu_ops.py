@@ -151,8 +151,7 @@ def test_replay_op(dtype, d, H, R, W_t, t, resid):
     ("bf16", 256, 512, 2, 1, 1, 64, 2), ("f32", 256, 512, 2, 1, 1, 19, 2), ("f32", 32, 256, 3, 3, 2, 17, 1)])
 def test_replay_op_wide_heads(dtype, dk, dv, H, Hk, R, W_t, t):
     # key widths up to 256 and value widths up to 512 (blocks of 128 value
-    # rows); d_k = 256 at depth 2 leaves one pipeline stage and runs on the
-    # CUDA cores
+    # rows)
     _replay_op(dtype, dk, H, R, W_t, t, False, Hk, dv=dv)
 
 
