@@ -9,11 +9,12 @@
 // (the new record) and o_t. No per-beam d_v x d_k state exists anywhere.
 //
 // Mapping to sm_103a:
-//   * One block per (request, head, 128 value rows). Its S_ctx rows (fp32 in
-//     memory) are split into bf16 hi + lo halves and kept in tensor memory as
-//     the A operand (M = 128 value rows) of two MMAs per K step, so the
-//     contraction keeps ~16 mantissa bits of S_ctx and shared memory is left
-//     to the beam pipeline.
+//   * One block per (request, head, 128 value rows), or per range of its beam
+//     tiles when those triples alone are too few to fill the SMs. Its S_ctx
+//     rows (fp32 in memory) are split into bf16 hi + lo halves and kept in
+//     tensor memory as the A operand (M = 128 value rows) of two MMAs per K
+//     step, so the contraction keeps ~16 mantissa bits of S_ctx and shared
+//     memory is left to the beam pipeline.
 //   * Beams go in tiles of 32. A producer warp stages per tile, by TMA, the
 //     32 queries and keys (the B operand, N = 64: q rows then k rows, 128-byte
 //     swizzled) and the 32 value rows; two more warps gather each beam's
@@ -75,6 +76,7 @@ struct RecMaps {
 
 struct TcReplayParams {
   int R, H, Hk, dv, t, W_t, n_tiles, stages, stage_bytes;
+  int tiles_per_block;  // beam tiles of one block; blockIdx.z picks the range
   const float* sctx;
   long long sctx_rstride;
   const float *alpha, *beta;
@@ -135,9 +137,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = tc::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
+  // this block's beam tiles: tile0 .. tile0 + nt - 1, beams bb .. bb + nbeams - 1
+  const int tile0 = blockIdx.z * p.tiles_per_block;
+  const int nt = min(p.tiles_per_block, p.n_tiles - tile0);
+  const int bb = tile0 * NB;
+  const int nbeams = min(nt * NB, p.W_t - bb);
+  // the table holds this block's beams, indexed from bb
   float2* tab_ab = reinterpret_cast<float2*>(gbase + p.stages * p.stage_bytes);
-  int* tab_slot = reinterpret_cast<int*>(tab_ab + p.W_t);
-  float* tab_aj = reinterpret_cast<float*>(tab_slot + p.W_t * t);
+  int* tab_slot = reinterpret_cast<int*>(tab_ab + p.tiles_per_block * NB);
+  float* tab_aj = reinterpret_cast<float*>(tab_slot + p.tiles_per_block * NB * t);
   auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
   auto full = [&](int s) { return bar(s); };
   auto empty = [&](int s) { return bar(kMaxStages + s); };
@@ -191,12 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool issued[kMaxStages] = {};
     uint32_t issued_ph[kMaxStages] = {};
     if (lane == 0) {
-      for (int i = 0; i < p.n_tiles; ++i) {
+      for (int i = 0; i < nt; ++i) {
         const int s = i % p.stages;
         const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
         if (!tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err)) break;
         const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
-        const int b0 = i * NB;
+        const int b0 = bb + i * NB;
         tc::mbar_arrive_expect_tx(full(s), (uint32_t)(B_BYTES + V_BYTES));
         for (int kb = 0; kb < DK / 64; ++kb) {
           const uint32_t bk = st + kb * (2 * NB * 128);
@@ -224,14 +232,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       bool issued[kMaxStages] = {};
       uint32_t issued_ph[kMaxStages] = {};
-      for (int i = 0; ok && i < p.n_tiles; ++i) {
+      for (int i = 0; ok && i < nt; ++i) {
         const int s = i % p.stages;
         const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
         if (lane == 0) ok = tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // the whole warp stops together
         const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
-        const int b0 = i * NB;
-        const int nb = min(NB, p.W_t - b0);
+        const int l0 = i * NB;  // the tile's first beam in the table
+        const int nb = min(NB, nbeams - l0);
         // per depth: delta_j, this block's 128 values (two 64-column halves),
         // or k_j (DK / 64 column blocks), eight four-beam groups each
         const int blocks = kind == 0 ? 2 : DK / 64;
@@ -244,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int b = 4 * g + u;
-            const int sl = b < nb ? tab_slot[(b0 + b) * t + j] : 0;
+            const int sl = b < nb ? tab_slot[(l0 + b) * t + j] : 0;
             // delta_j rows are per value head, k_j rows per key head
             y[u] = kind == 0 ? (r * p.W_j[j] + sl) * p.H + h : (r * p.W_j[j] + sl) * p.Hk + hk;
           }
@@ -276,13 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (lane == 0) ok = tc::mbar_wait_sleep(tab_ready, 0, abort, p.err);
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    for (int i = 0; ok && i < p.n_tiles; ++i) {
+    for (int i = 0; ok && i < nt; ++i) {
       const int s = i % p.stages;
       const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
       const int sb = i & 1;
       const uint32_t sph = (uint32_t)(i >> 1) & 1u;
-      const int b0 = i * NB;
-      const int nb = min(NB, p.W_t - b0);
+      const int l0 = i * NB;  // the tile's first beam in the table
+      const int nb = min(NB, nbeams - l0);
       // the buffer's previous tile has been folded, and this tile has landed
       if (__any_sync(0xffffffffu, !tc::mbar_wait_sleep(sempty(sb), sph ^ 1u, abort, p.err) ||
                                       !tc::mbar_wait_sleep(full(s), ph, abort, p.err))) {
@@ -329,11 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The fold u <- alpha_j u + delta_j c_j over j = 0 .. t-1 (eqs. 6-7)
         // leaves u = (prod_j alpha_j) u_ctx + sum_j (c_j prod_{m > j} alpha_m)
         // delta_j; eq. 8 is linear in both projections.
-        const float2 ab = tab_ab[b0 + bl];  // (alpha_t, beta_t)
+        const float2 ab = tab_ab[l0 + bl];  // (alpha_t, beta_t)
         float tail = 1.f;                   // prod_{m > j} alpha_m
 #pragma unroll
         for (int j = t - 1; j >= 0; --j) {
-          const float a = tab_aj[(b0 + bl) * t + j];
+          const float a = tab_aj[(l0 + bl) * t + j];
           const bool use = a >= 0.f;  // a skipped record leaves both projections unchanged
           const float wq = use ? part[1 + 2 * j] * tail : 0.f;
           const float wk = use ? part[2 + 2 * j] * tail : 0.f;
@@ -353,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(VR, 2 * NB);
       bool ok = tc::mbar_wait_sleep(a_ready, 0, abort, p.err);
-      for (int i = 0; ok && i < p.n_tiles; ++i) {
+      for (int i = 0; ok && i < nt; ++i) {
         const int s = i % p.stages;
         const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
         const int acc = i & 1;
@@ -388,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem_base + ((uint32_t)(lg * 32) << 16);
 
     // the block's table: gates, ancestor slots and decays of every beam
-    for (int b = ew * 32 + lane; b < p.W_t; b += kEpiThreads) {
-      const size_t row = (size_t)r * p.W_t + b;
+    for (int b = ew * 32 + lane; b < nbeams; b += kEpiThreads) {
+      const size_t row = (size_t)r * p.W_t + bb + b;
       tab_ab[b] = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
 #pragma unroll
       for (int j = 0; j < t; ++j) {
@@ -444,12 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A failed wait marks this warp dead: it then skips all work but keeps
     // making its arrivals, so no other role waits on it forever.
     bool dead = false;
-    for (int i = 0; i < p.n_tiles; ++i) {
+    for (int i = 0; i < nt; ++i) {
       const int s = i % p.stages;
       const int acc = i & 1;
       const uint32_t aph = (uint32_t)(i >> 1) & 1u;
       const int sb = i & 1;
-      const int b0 = i * NB;
+      const int b0 = bb + i * NB;
       const int nb = min(NB, p.W_t - b0);
       if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(sfull(sb), aph, abort, p.err));
       if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(tfull(acc), aph, abort, p.err));
@@ -584,8 +592,28 @@ int launch_tc_replay_dk(const ReplayArgs& a, cudaStream_t s) {
   TcReplayParams p{};
   p.R = a.R; p.H = a.H; p.Hk = a.Hk; p.dv = a.d_v; p.t = a.t; p.W_t = a.W_t;
   p.n_tiles = (a.W_t + NB - 1) / NB;
+  // Beam tiles per block. When (request, head, value block) triples are too
+  // few to fill the SMs, the tiles of one triple are split over several
+  // blocks (each reads its own copy of S_ctx). The split minimises
+  // waves x (tiles per block + a prologue worth about three tiles: TMEM
+  // set-up, S_ctx and the table), one block per SM.
+  {
+    const long long base = (long long)a.R * a.H * (a.d_v / VR);
+    const long long sms = sm_count();
+    long long best_cost = -1;
+    for (int ns = 1; ns <= p.n_tiles; ++ns) {
+      const int tpb = (p.n_tiles + ns - 1) / ns;
+      if ((p.n_tiles + tpb - 1) / tpb != ns) continue;  // same as a smaller split
+      const long long cost = (base * ns + sms - 1) / sms * (tpb + 3);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        p.tiles_per_block = tpb;
+      }
+    }
+  }
+  const int nsplit = (p.n_tiles + p.tiles_per_block - 1) / p.tiles_per_block;
   p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES;
-  const size_t table = (size_t)a.W_t * (8 + 8 * a.t);
+  const size_t table = (size_t)p.tiles_per_block * NB * (8 + 8 * a.t);
   const int static_bytes = 2 * OUT_BYTES + 10 * 1024;  // output tiles, scalar buffers, barriers
   const long long budget = 227LL * 1024 - static_bytes - 1024 - (long long)table;
   p.stages = budget > 0 ? (int)(budget / p.stage_bytes) : 0;
@@ -620,7 +648,7 @@ int launch_tc_replay_dk(const ReplayArgs& a, cudaStream_t s) {
     return GDNBEAM_ECUDA;
   const size_t dyn = 1024 + (size_t)p.stages * p.stage_bytes + table;
   const bool extra = a.delta_dump || a.o_dump || a.x_inout;
-  const dim3 grid(a.R * a.H, a.d_v / VR);
+  const dim3 grid(a.R * a.H, a.d_v / VR, nsplit);
   switch (a.t) {
 #define GDN_REPLAY_TC(TD_)                                                                      \
   case TD_:                                                                                     \
