@@ -111,6 +111,12 @@ int launch_replayssm(int dtype, const ReplaySsmArgs& a, cudaStream_t s);
 // dst[i] = storage(src[i]) for n elements (S_ctx copy for the FullState path).
 int launch_to_storage(int dtype, size_t n, const float* src, void* dst, cudaStream_t s);
 
+// Chunked tensor-core prefill (bf16, d_k = d_v = 128, no residual stream):
+// S_ctx and o at the last token, as launch_prefill_scan.
+bool tc_prefill_supported(const gdnbeam_config& c, const float* x_inout);
+int launch_prefill_tc(const gdnbeam_config& c, int L, const void* q, const void* k, const void* v,
+                      const float* alpha, const float* beta, float* sctx, long long rstride,
+                      void* o_last, cudaStream_t s);
 int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const void* k,
                         const void* v, const float* alpha, const float* beta, float* sctx,
                         long long sctx_rstride, void* o_last, float* x_inout, cudaStream_t s);

@@ -325,13 +325,24 @@ def test_prefill_scan_op_wide_and_grouped(dtype, dk, dv, H, Hk, R, L):
     _prefill_scan_op(dtype, dk, dv, H, Hk, R, L, False)
 
 
-def _prefill_scan_op(dtype, dk, dv, H, Hk, R, L, resid):
+@pytest.mark.parametrize("H,Hk,R,L,a_lo,a_hi", [
+    (2, 2, 1, 1, 0.3, 1.0), (2, 2, 2, 63, 0.3, 1.0), (2, 1, 1, 128, 0.3, 1.0),
+    (4, 2, 2, 129, 0.3, 1.0), (2, 2, 1, 300, 0.01, 0.3), (1, 1, 1, 1000, 0.9, 1.0),
+    (2, 2, 3, 257, 0.5, 1.0)])
+def test_prefill_chunked_tensor_cores(H, Hk, R, L, a_lo, a_hi):
+    # bf16, d_k = d_v = 128 without a residual stream: the chunked tcgen05
+    # prefill (64-token chunks, 128-token stages; lengths around both
+    # boundaries, fast and slow decay, grouped key heads)
+    _prefill_scan_op("bf16", 128, 128, H, Hk, R, L, False, a_lo, a_hi)
+
+
+def _prefill_scan_op(dtype, dk, dv, H, Hk, R, L, resid, a_lo=0.3, a_hi=1.0):
     wl = synth.tiny_workload(d=dk, d_v=dv, V=5, H=H, R=R, dtype=dtype, H_k=Hk)
     rng = np.random.default_rng(L + dk + dv)
     q = store(_unit_rows(rng, (R, L, Hk, dk)), wl)
     k = store(_unit_rows(rng, (R, L, Hk, dk)), wl)
     v = store(rng.standard_normal((R, L, H, dv)), wl)
-    a = rng.uniform(0.3, 1.0, (R, L, H)).astype(np.float32).astype(np.float64)
+    a = rng.uniform(a_lo, a_hi, (R, L, H)).astype(np.float32).astype(np.float64)
     b = rng.uniform(0.0, 1.0, (R, L, H)).astype(np.float32).astype(np.float64)
     x0 = rng.standard_normal((R, L, H * dv)) if resid else None
     td = tdt(wl)
