@@ -5,13 +5,17 @@
 //   * codebook logits Z = F . W_o^T, with the bf16 store of z and per-tile
 //     (max, sum exp) partials of the row log-normaliser fused in.
 //
-// One persistent CTA per SM, 192 threads in three roles:
-//   warp 0      one thread issues TMA tile loads (A 128x64, B 256x64 bf16,
+// Persistent CTAs in clusters of two, one CTA per SM, 192 threads in three
+// roles. The two CTAs of a cluster take vertically adjacent tiles (m, n) and
+// (m + 1, n) in lockstep and share the B tile: each loads its own A tile and
+// one 128-row half of B, multicast into both CTAs, so B leaves L2 once per
+// pair of tiles.
+//   warp 0      one thread issues TMA tile loads (A 128x64, B 2 x 128x64 bf16,
 //               128-byte swizzle) into a 4-stage shared-memory ring;
 //   warp 1      owns the TMEM allocation (2 x 256 fp32 columns) and one thread
 //               issues tcgen05.mma (M=128, N=256, K=16) into the accumulator
 //               of the current tile, committing each stage back to the
-//               producer and each finished tile to the epilogue;
+//               producers of both CTAs and each finished tile to the epilogue;
 //   warps 2-5   read the accumulator rows out of TMEM (lane = tile row) and
 //               run the fused epilogue while the next tile accumulates into
 //               the other TMEM buffer.
@@ -29,6 +33,7 @@ namespace gdnbeam {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int CLUSTER = 2;  // CTAs sharing a B tile
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -185,7 +190,7 @@ __device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int 
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    EpiArgs ea) {
   extern __shared__ uint8_t smem_raw[];
@@ -205,13 +210,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (ea.M + BM - 1) / BM, n_tiles = (ea.N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles;
+  // pair tiles: rows 2 mp and 2 mp + 1 (the second may lie past M: its A
+  // box reads zeros and its rows are not stored) against one B tile
+  const int num_tiles = ((m_tiles + 1) / 2) * n_tiles;
   const int k_blocks = (ea.K + BK - 1) / BK;
+  const int rank = (int)tc::cluster_ctarank();
+  const int cid = blockIdx.x / CLUSTER, n_clusters = gridDim.x / CLUSTER;
+  const uint16_t both = (uint16_t)((1u << CLUSTER) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(full(s), 1);
-      tc::mbar_init(empty(s), 1);
+      tc::mbar_init(empty(s), CLUSTER);  // the MMA commits of both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull(a), 1);
@@ -228,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
   tc::fence_before_sync();
   __syncthreads();
+  // the peer's barriers are initialised before any copy or commit reaches them
+  tc::cluster_sync();
   tc::fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -239,13 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued[STAGES];
       for (int i = 0; i < STAGES; ++i) issued[i] = false;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+      for (int tile = cid; tile < num_tiles && ok; tile += n_clusters) {
+        const int m0 = (2 * (tile / n_tiles) + rank) * BM, n0 = (tile % n_tiles) * BN;
         for (int kb = 0; kb < k_blocks; ++kb) {
+          // the stage is free in both CTAs (the peer's half of B lands here too)
           if (!tc::mbar_wait(empty(s), ph ^ 1u, abort, ea.err)) { ok = false; break; }
           tc::mbar_arrive_expect_tx(full(s), STAGE_BYTES);
           tc::tma_load_2d(sA(s), &tmA, kb * BK, m0, full(s));
-          tc::tma_load_2d(sB(s), &tmB, kb * BK, n0, full(s));
+          tc::tma_load_2d_mc(sB(s) + rank * (BN / 2) * 128, &tmB, kb * BK, n0 + rank * (BN / 2),
+                             full(s), both);
           issued[s] = true;
           issued_phase[s] = ph;
           if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -262,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       bool ok = true;
       int i = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++i) {
+      for (int tile = cid; tile < num_tiles && ok; tile += n_clusters, ++i) {
         const int acc = i & 1;
         const uint32_t aph = (uint32_t)(i >> 1) & 1u;
         if (!tc::mbar_wait(tempty(acc), aph ^ 1u, abort, ea.err)) break;
@@ -275,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc::mma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0);
-          tc::mma_commit(empty(s));
+          tc::mma_commit_mc(empty(s), both);
           if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
         if (ok) tc::mma_commit(tfull(acc));
@@ -288,14 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane_grp = warp & 3;  // TMEM lanes 32*lane_grp .. +31
     const int row = lane_grp * 32 + lane;
     int i = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++i) {
+    for (int tile = cid; tile < num_tiles; tile += n_clusters, ++i) {
       const int acc = i & 1;
       const uint32_t aph = (uint32_t)(i >> 1) & 1u;
       const bool got = tc::mbar_wait(tfull(acc), aph, abort, ea.err);
       __syncwarp();  // the TMEM loads below are warp-collective
       if (!got) break;
       tc::fence_after_sync();
-      const int m_tile = tile / n_tiles, n_tile = tile % n_tiles;
+      const int m_tile = 2 * (tile / n_tiles) + rank, n_tile = tile % n_tiles;
       const uint32_t taddr = tmem_base + ((uint32_t)(lane_grp * 32) << 16) + (uint32_t)(acc * BN);
       if (EPI == EPI_LOGITS)
         epi_logits(ea, taddr, m_tile * BM + row, n_tile * BN, n_tile, n_tiles);
@@ -308,6 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
+  // neither CTA leaves while the other may still multicast into it or
+  // arrive on its barriers
+  tc::cluster_sync();
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem_base, kTmemCols);
@@ -374,22 +391,50 @@ int num_sms() {
   return sms[dev];
 }
 
+// Clusters of this kernel that fit on the device at once (one CTA per SM;
+// a GPC with an odd number of free SMs leaves one of them out).
+template <int EPI>
+int max_clusters() {
+  static int cached[64][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cached[dev][EPI]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CLUSTER * (num_sms() / CLUSTER), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = CLUSTER;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<EPI>, &cfg) != cudaSuccess || n <= 0)
+      n = num_sms() / CLUSTER;
+    cached[dev][EPI] = n;
+  }
+  return cached[dev][EPI];
+}
+
 template <int EPI>
 int launch_gemm(const void* A, const void* B, const EpiArgs& ea, cudaStream_t s) {
   if (ea.M <= 0) return GDNBEAM_OK;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, A, ea.M, ea.K, BM) || !make_map(&tb, B, ea.N, ea.K, BN)) return GDNBEAM_ECUDA;
+  if (!make_map(&ta, A, ea.M, ea.K, BM) || !make_map(&tb, B, ea.N, ea.K, BN / 2))
+    return GDNBEAM_ECUDA;
   static bool attr_set[2] = {false, false};
   if (!attr_set[EPI]) {
     GDN_CUDA(cudaFuncSetAttribute(tc_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kSmemBytes));
     attr_set[EPI] = true;
   }
-  const int tiles = ((ea.M + BM - 1) / BM) * ((ea.N + BN - 1) / BN);
-  int grid = num_sms();
-  if (grid <= 0) return GDNBEAM_ECUDA;
-  if (grid > tiles) grid = tiles;
-  tc_gemm_kernel<EPI><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, ea);
+  const int pair_tiles = ((ea.M + BM - 1) / BM + 1) / 2 * ((ea.N + BN - 1) / BN);
+  int clusters = max_clusters<EPI>();
+  if (clusters <= 0) return GDNBEAM_ECUDA;
+  if (clusters > pair_tiles) clusters = pair_tiles;
+  tc_gemm_kernel<EPI><<<CLUSTER * clusters, kThreads, kSmemBytes, s>>>(ta, tb, ea);
   GDN_LAUNCH_CHECK();
   return GDNBEAM_OK;
 }
