@@ -17,13 +17,15 @@
 //     memory is left to the beam pipeline.
 //   * Beams go in tiles of 32. A producer warp stages per tile, by TMA, the
 //     32 queries and keys (the B operand, N = 64: q rows then k rows, 128-byte
-//     swizzled) and the 32 value rows; two more warps gather each beam's
-//     ancestor records delta_j and k_j, four rows per request (small TMA
-//     requests are issued at a per-warp rate, so the work is spread). Stages
+//     swizzled) and the 32 value rows; that warp and two more gather each
+//     beam's ancestor records delta_j and k_j, four rows per request (small
+//     TMA requests are issued at a per-warp rate, so the work is spread over
+//     three warps). Stages
 //     sit on an mbarrier ring several tiles deep.
 //   * Gates, ancestor slots and ancestor decays of all the block's beams are
-//     read once into a shared table at block start, so no global load sits on
-//     the per-tile path.
+//     read once into a shared table at block start by every thread (while
+//     the epilogue warps' S_ctx loads are in flight), so no global load sits
+//     on the per-tile path.
 //   * One thread issues tcgen05.mma into a double-buffered TMEM accumulator:
 //     column b holds u_q of beam b, column 32 + b its u_k, lane = value row.
 //   * Four scalar warps compute the replay scalars k_j.q_t, k_j.k_t and
@@ -154,7 +156,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sfull = [&](int a) { return bar(2 * kMaxStages + 4 + a); };   // scalars of a tile written
   auto sempty = [&](int a) { return bar(2 * kMaxStages + 6 + a); };  // scalars of a tile used
   const uint32_t a_ready = bar(2 * kMaxStages + 8);
-  const uint32_t tab_ready = bar(2 * kMaxStages + 9);
   const uint32_t drain_bar = bar(2 * kMaxStages + 10);
   volatile int* abort = &s_abort;
 
@@ -178,7 +179,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(sempty(a), kEpiWarps);
     }
     tc::mbar_init(a_ready, kEpiWarps);
-    tc::mbar_init(tab_ready, kEpiWarps);
     tc::mbar_init(drain_bar, 1);
     s_abort = 0;
     tc::fence_mbar_init();
@@ -193,19 +193,96 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem_base = s_tmem;
 
+  // Epilogue warps: their S_ctx row (vb * 128 + i_row, K half hb) in batches
+  // of 32 values; the first batches are loaded before the table is built,
+  // so the two latencies overlap.
+  const bool epi_warp = warp >= kEpi0 && warp < kEpi0 + kEpiWarps;
+  const int e_hb = (warp - kEpi0) >> 2, e_row = (warp & 3) * 32 + lane;
+  const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * p.dv * DK +
+                   (size_t)(vb * VR + e_row) * DK + e_hb * (DK / 2);
+  constexpr int kBatches = DK / 64;
+  constexpr int kEarly = kBatches < 2 ? kBatches : 2;
+  float4 xe[kEarly][8];
+  if (epi_warp) {
+#pragma unroll
+    for (int bt = 0; bt < kEarly; ++bt)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) xe[bt][c] = __ldg(reinterpret_cast<const float4*>(S) + bt * 8 + c);
+  }
+  // The block's table, built by every thread (one beam each at W = 512):
+  // gates, ancestor slots and decays of every beam. The slot loads go out
+  // together before the dependent decay loads.
+  for (int b = threadIdx.x; b < nbeams; b += kThreads) {
+    const size_t row = (size_t)r * p.W_t + bb + b;
+    int sl[TD > 0 ? TD : 1];
+#pragma unroll
+    for (int j = 0; j < t; ++j) sl[j] = p.anc[row * p.anc_stride + j];
+    tab_ab[b] = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
+#pragma unroll
+    for (int j = 0; j < t; ++j) {
+      float a = -1.0f;  // marks a slot outside its depth: the record is skipped
+      if (sl[j] < 0 || sl[j] >= p.W_j[j]) {
+        raise_error(p.err, GDNBEAM_DERR_SLOT);
+        sl[j] = 0;
+      } else {
+        a = p.rec_a[j][((size_t)r * p.W_j[j] + sl[j]) * p.H + h];
+      }
+      tab_slot[b * t + j] = sl[j];
+      tab_aj[b * t + j] = a;
+    }
+  }
+  __syncthreads();  // the table is complete
+
+  // A tile's record requests (four beams, one 64-column block of one depth's
+  // delta_j or k_j rows each) are split round-robin over three warps: the
+  // producer (w = 0) and the two record loaders (w = 1, 2); small TMA
+  // requests issue at a per-warp rate, so three streams move more.
+  constexpr int kRecReq = 8 * t * (2 + DK / 64);  // requests per tile
+  auto rec_share = [](int w) { return (kRecReq - w + 2) / 3; };
+  auto issue_records = [&](int w, int i, uint32_t st, int s) {
+    const int l0 = i * NB;  // the tile's first beam in the table
+    const int nb = min(NB, nbeams - l0);
+    for (int m = lane;; m += 32) {
+      const int rq = 3 * m + w;
+      if (rq >= kRecReq) break;
+      int kind, j, cb, gq;
+      if (rq < 16 * t) {
+        kind = 0; j = rq >> 4; cb = (rq >> 3) & 1; gq = rq & 7;
+      } else {
+        const int idx = rq - 16 * t;
+        kind = 1; j = idx / (8 * (DK / 64)); cb = (idx >> 3) % (DK / 64); gq = idx & 7;
+      }
+      int y[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int b = 4 * gq + u;  // beams past the tile's end repeat a valid row
+        const int sl = b < nb ? tab_slot[(l0 + b) * t + j] : 0;
+        // delta_j rows are per value head, k_j rows per key head
+        y[u] = kind == 0 ? (r * p.W_j[j] + sl) * p.H + h : (r * p.W_j[j] + sl) * p.Hk + hk;
+      }
+      const uint32_t dst = st + rec_off + (uint32_t)(j * REC_BYTES + kind * REC_D +
+                                                     cb * (NB * 128) + gq * (4 * 128));
+      tc::tma_gather4(dst, kind == 0 ? &rm.d[j] : &rm.k[j],
+                      kind == 0 ? vb * VR + cb * 64 : cb * 64, y[0], y[1], y[2], y[3], full(s));
+    }
+    __syncwarp();
+  };
+
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    // q, k and v boxes of every tile (lane 0)
+    // q, k and v boxes of every tile (lane 0) and its share of the records
     bool issued[kMaxStages] = {};
     uint32_t issued_ph[kMaxStages] = {};
-    if (lane == 0) {
-      for (int i = 0; i < nt; ++i) {
-        const int s = i % p.stages;
-        const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
-        if (!tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err)) break;
-        const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
-        const int b0 = bb + i * NB;
-        tc::mbar_arrive_expect_tx(full(s), (uint32_t)(B_BYTES + V_BYTES));
+    int ok = 1;
+    for (int i = 0; i < nt; ++i) {
+      const int s = i % p.stages;
+      const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
+      if (lane == 0) ok = tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // the whole warp stops together
+      const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
+      const int b0 = bb + i * NB;
+      if (lane == 0) {
+        tc::mbar_arrive_expect_tx(full(s), (uint32_t)(B_BYTES + V_BYTES + rec_share(0) * 512));
         for (int kb = 0; kb < DK / 64; ++kb) {
           const uint32_t bk = st + kb * (2 * NB * 128);
           tc::tma_load_3d(bk, &tm_q, hk * DK + kb * 64, b0, r, full(s));
@@ -217,19 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued[s] = true;
         issued_ph[s] = ph;
       }
+      if (t > 0) issue_records(0, i, st, s);
+    }
+    if (lane == 0)
       for (int s = 0; s < p.stages; ++s)
         if (issued[s]) tc::mbar_wait_drain(full(s), issued_ph[s]);
-    }
   } else if (warp >= kRec0 && warp < kScal0) {
     // ---------------------------------------------------------------- records
-    // warp kind (0: delta_j, 1: k_j) gathers its record rows of every tile,
-    // four beams and one 64-column half per request; beams past the tile's
-    // end repeat a valid row
+    // record loader w = 1 or 2: its share of every tile's record requests
     if (t > 0) {
-      const int kind = warp - kRec0;
+      const int w = 1 + warp - kRec0;
       int ok = 1;
-      if (lane == 0) ok = tc::mbar_wait_sleep(tab_ready, 0, abort, p.err) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
       bool issued[kMaxStages] = {};
       uint32_t issued_ph[kMaxStages] = {};
       for (int i = 0; ok && i < nt; ++i) {
@@ -238,30 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ok = tc::mbar_wait_sleep(empty(s), ph ^ 1u, abort, p.err) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;  // the whole warp stops together
         const uint32_t st = base + (uint32_t)(s * p.stage_bytes);
-        const int l0 = i * NB;  // the tile's first beam in the table
-        const int nb = min(NB, nbeams - l0);
-        // per depth: delta_j, this block's 128 values (two 64-column halves),
-        // or k_j (DK / 64 column blocks), eight four-beam groups each
-        const int blocks = kind == 0 ? 2 : DK / 64;
-        if (lane == 0)
-          tc::mbar_expect_tx(full(s), (uint32_t)(t * (kind == 0 ? REC_D : NB * DK * 2)));
+        if (lane == 0) tc::mbar_expect_tx(full(s), (uint32_t)(rec_share(w) * 512));
         __syncwarp();
-        for (int req = lane; req < 8 * blocks * t; req += 32) {
-          const int j = req / (8 * blocks), cb = (req >> 3) % blocks, g = req & 7;
-          int y[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int b = 4 * g + u;
-            const int sl = b < nb ? tab_slot[(l0 + b) * t + j] : 0;
-            // delta_j rows are per value head, k_j rows per key head
-            y[u] = kind == 0 ? (r * p.W_j[j] + sl) * p.H + h : (r * p.W_j[j] + sl) * p.Hk + hk;
-          }
-          const uint32_t dst = st + rec_off + (uint32_t)(j * REC_BYTES + kind * REC_D +
-                                                         cb * (NB * 128) + g * (4 * 128));
-          tc::tma_gather4(dst, kind == 0 ? &rm.d[j] : &rm.k[j],
-                          kind == 0 ? vb * VR + cb * 64 : cb * 64, y[0], y[1], y[2], y[3], full(s));
-        }
-        __syncwarp();
+        issue_records(w, i, st, s);
         if (lane == 0) {
           tc::mbar_arrive(full(s));
           issued[s] = true;
@@ -282,8 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bl = sw * 8 + (lane >> 2);
     const int c0 = (lane & 3) * (DK / 4);
     bool ok = true;
-    if (lane == 0) ok = tc::mbar_wait_sleep(tab_ready, 0, abort, p.err);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     for (int i = 0; ok && i < nt; ++i) {
       const int s = i % p.stages;
       const uint32_t ph = (uint32_t)(i / p.stages) & 1u;
@@ -395,37 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_row = lg * 32 + lane;          // value row = TMEM lane
     const uint32_t lane_base = tmem_base + ((uint32_t)(lg * 32) << 16);
 
-    // the block's table: gates, ancestor slots and decays of every beam
-    for (int b = ew * 32 + lane; b < nbeams; b += kEpiThreads) {
-      const size_t row = (size_t)r * p.W_t + bb + b;
-      tab_ab[b] = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
-#pragma unroll
-      for (int j = 0; j < t; ++j) {
-        int sl = p.anc[row * p.anc_stride + j];
-        float a = -1.0f;  // marks a slot outside its depth: the record is skipped
-        if (sl < 0 || sl >= p.W_j[j]) {
-          raise_error(p.err, GDNBEAM_DERR_SLOT);
-          sl = 0;
-        } else {
-          a = p.rec_a[j][((size_t)r * p.W_j[j] + sl) * p.H + h];
-        }
-        tab_slot[b * t + j] = sl;
-        tab_aj[b * t + j] = a;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(tab_ready);
-
-    // S_ctx row vb * 128 + i_row, K half hb -> bf16 hi / lo words in TMEM,
-    // 32 values at a time
+    // the S_ctx batches -> bf16 hi / lo words in TMEM
     {
-      const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * p.dv * DK +
-                       (size_t)(vb * VR + i_row) * DK + hb * (DK / 2);
-#pragma unroll
-      for (int half = 0; half < DK / 64; ++half) {
-        float4 x[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) x[c] = __ldg(reinterpret_cast<const float4*>(S) + half * 8 + c);
+      auto put = [&](const float4 (&x)[8], int bt) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -439,9 +463,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo[2 * c + e] = pack_bf16(a0 - h0, a1 - h1);
           }
         }
-        const uint32_t col = (uint32_t)(hb * (DK / 4) + half * 16);
+        const uint32_t col = (uint32_t)(hb * (DK / 4) + bt * 16);
         tc::tmem_st16(lane_base + kColAHi + col, hi);
         tc::tmem_st16(lane_base + kColALo + col, lo);
+      };
+#pragma unroll
+      for (int bt = 0; bt < kEarly; ++bt) put(xe[bt], bt);
+#pragma unroll
+      for (int bt = kEarly; bt < kBatches; ++bt) {
+        float4 x[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) x[c] = __ldg(reinterpret_cast<const float4*>(S) + bt * 8 + c);
+        put(x, bt);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
