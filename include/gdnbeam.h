@@ -41,7 +41,7 @@ typedef struct CUstream_st* gdnbeam_stream_t; /* a cudaStream_t; NULL = legacy d
 enum {
   GDNBEAM_OK = 0,
   GDNBEAM_EINVAL = -1,       /* null pointer, size out of range, bad index argument */
-  GDNBEAM_EUNSUPPORTED = -2, /* shape or dtype this build does not handle */
+  GDNBEAM_EUNSUPPORTED = -2, /* shape or dtype this library does not handle */
   GDNBEAM_EWORKSPACE = -3,   /* workspace or scratch smaller than required */
   GDNBEAM_ESTATE = -4,       /* call out of order (step before prefill, t out of sequence) */
   GDNBEAM_ECUDA = -5,        /* a CUDA runtime/driver call or a launch failed */
@@ -146,7 +146,7 @@ typedef struct gdnbeam_ctx gdnbeam_ctx;
  * ------------------------------------------------------------------------- */
 
 /* Validates cfg and fills *out (host). Returns GDNBEAM_EINVAL/EUNSUPPORTED on
- * a configuration this build rejects. */
+ * a configuration this library rejects. */
 int gdnbeam_footprint_of(const gdnbeam_config* cfg, gdnbeam_footprint* out);
 
 /* Creates a context over a caller-allocated workspace of at least

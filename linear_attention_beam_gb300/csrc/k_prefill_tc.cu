@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------------ T builders
     const int tt = threadIdx.x - 32 * kT0;  // 0 .. 255
-    // one thread waits, all T builders take its verdict (they share named
+    // one thread waits, all T builders take its outcome (they share named
     // barriers, so they must leave together)
     auto t_wait = [&](uint32_t b, uint32_t ph) -> bool {
       if (tt == 0) s_tok = tc::mbar_wait_sleep(b, ph, abort, p.err) ? 1 : 0;
