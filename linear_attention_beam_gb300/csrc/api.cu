@@ -372,12 +372,33 @@ int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* 
       if (st) return st;
     }
     const char* Wp = (const char*)ctx->w.W_proj + (size_t)layer * Np * c.d_model * es;
+    float* sc = (float*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k;
+    if (ctx->tc_gemm && tc_prefill_supported(c, c.residual ? ctx->pf_x : nullptr)) {
+      // The chunked prefill reads the query only at each request's last
+      // token: the projection over all prompt rows skips the query columns,
+      // and a second one forms the last rows' queries (into rows 0 .. R-1
+      // of the query buffer).
+      ev = ctx->tic(GDNBEAM_STAGE_PROJECT, s);
+      st = launch_tc_project(c, n, ctx->pf_u, Wp, ctx->pf_q, ctx->pf_k, ctx->pf_v, ctx->pf_alpha,
+                             ctx->pf_beta, nullptr, s, PROJ_NO_Q);
+      if (!st)
+        st = launch_tc_project(c, c.R, (const char*)ctx->pf_u + (size_t)(L - 1) * c.d_model * es, Wp,
+                               ctx->pf_q, nullptr, nullptr, nullptr, nullptr, nullptr, s,
+                               PROJ_Q_ONLY, (long long)L * c.d_model);
+      ctx->toc(ev, s);
+      if (st) return st;
+      ev = ctx->tic(GDNBEAM_STAGE_PREFILL, s);
+      st = launch_prefill_tc(c, L, ctx->pf_q, (long long)key_heads(c) * c.d_k, ctx->pf_k, ctx->pf_v,
+                             ctx->pf_alpha, ctx->pf_beta, sc, rstride, ctx->pf_feat, s);
+      ctx->toc(ev, s);
+      if (st) return st;
+      continue;
+    }
     ev = ctx->tic(GDNBEAM_STAGE_PROJECT, s);
     st = project_any(c, ctx->tc_gemm, n, ctx->pf_u, Wp, ctx->pf_q, ctx->pf_k, ctx->pf_v,
                      ctx->pf_alpha, ctx->pf_beta, ctx->gemm, ctx->gemm_bytes, nullptr, s);
     ctx->toc(ev, s);
     if (st) return st;
-    float* sc = (float*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k;
     ev = ctx->tic(GDNBEAM_STAGE_PREFILL, s);
     st = launch_prefill_scan(c, L, ctx->pf_q, ctx->pf_k, ctx->pf_v, ctx->pf_alpha, ctx->pf_beta,
                              sc, rstride, c.residual ? nullptr : ctx->pf_feat,

@@ -52,7 +52,8 @@ struct EpiArgs {
   float* z_dump;
   float2* part;  // [M][n_tiles] (max, sum exp(z - max))
   // projections
-  int H, Hk;  // value heads, key heads
+  int H, Hk;    // value heads, key heads
+  int col_off;  // absolute projection column of GEMM column 0 (a multiple of 128)
   __nv_bfloat16 *q, *k, *v;
   float *alpha, *beta;
   float *dq, *dk, *dv, *da, *db;
@@ -123,8 +124,8 @@ __device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int 
   const int q_end = Hk * D, k_end = 2 * Hk * D, v_end = k_end + H * D;
 #pragma unroll 1
   for (int g = 0; g < BN / D; ++g) {
-    const int col0 = n0 + g * D;
-    if (col0 >= ea.N) break;
+    if (n0 + g * D >= ea.N) break;
+    const int col0 = n0 + g * D + ea.col_off;  // column of the full projection
     const uint32_t ta = taddr + g * D;
     if (col0 < k_end) {
       const bool is_q = col0 < q_end;
@@ -368,14 +369,17 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows][cols] as a 2-D tensor map with a box of
-// 64 columns x box_rows rows and 128-byte swizzling.
-bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int box_rows) {
+// Row-major bf16 matrix [rows][cols] (rows ld elements apart; ld = 0 means
+// cols) as a 2-D tensor map with a box of 64 columns x box_rows rows and
+// 128-byte swizzling.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int box_rows,
+              long long ld = 0) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  if (((uintptr_t)ptr & 15) != 0 || (cols * 2) % 16 != 0) return false;
+  if (ld == 0) ld = cols;
+  if (((uintptr_t)ptr & 15) != 0 || (ld * 2) % 16 != 0 || ld < cols) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
   cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
@@ -419,10 +423,11 @@ int max_clusters() {
 }
 
 template <int EPI>
-int launch_gemm(const void* A, const void* B, const EpiArgs& ea, cudaStream_t s) {
+int launch_gemm(const void* A, const void* B, const EpiArgs& ea, cudaStream_t s,
+                long long lda = 0) {
   if (ea.M <= 0) return GDNBEAM_OK;
   CUtensorMap ta, tb;
-  if (!make_map(&ta, A, ea.M, ea.K, BM) || !make_map(&tb, B, ea.N, ea.K, BN / 2))
+  if (!make_map(&ta, A, ea.M, ea.K, BM, lda) || !make_map(&tb, B, ea.N, ea.K, BN / 2))
     return GDNBEAM_ECUDA;
   static bool attr_set[2] = {false, false};
   if (!attr_set[EPI]) {
@@ -449,11 +454,24 @@ bool tc_gemm_supported(const gdnbeam_config& c) {
 
 int launch_tc_project(const gdnbeam_config& c, int n, const void* u, const void* W_proj, void* q,
                       void* k, void* v, float* alpha, float* beta, const gdnbeam_dumps* d,
-                      cudaStream_t s) {
+                      cudaStream_t s, int cols, long long ldu) {
+  const int n_full = 2 * key_heads(c) * c.d_k + c.H * c.d_v + 2 * c.H;
+  const int q_cols = key_heads(c) * c.d_k;
   EpiArgs ea{};
   ea.M = n;
-  ea.N = 2 * key_heads(c) * c.d_k + c.H * c.d_v + 2 * c.H;
   ea.K = c.d_model;
+  // the projection columns computed: all, all but the queries, or only them
+  if (cols == PROJ_ALL) {
+    ea.N = n_full;
+  } else if (cols == PROJ_NO_Q) {
+    ea.col_off = q_cols;
+    ea.N = n_full - q_cols;
+    W_proj = (const char*)W_proj + (size_t)q_cols * c.d_model * 2;
+  } else if (cols == PROJ_Q_ONLY) {
+    ea.N = q_cols;
+  } else {
+    return GDNBEAM_EINVAL;
+  }
   ea.H = c.H;
   ea.Hk = key_heads(c);
   ea.q = (__nv_bfloat16*)q;
@@ -464,7 +482,7 @@ int launch_tc_project(const gdnbeam_config& c, int n, const void* u, const void*
   if (d) {
     ea.dq = d->q; ea.dk = d->k; ea.dv = d->v; ea.da = d->alpha; ea.db = d->beta;
   }
-  return launch_gemm<EPI_PROJ>(u, W_proj, ea, s);
+  return launch_gemm<EPI_PROJ>(u, W_proj, ea, s, ldu);
 }
 
 size_t tc_logits_scratch_bytes(const gdnbeam_config& c, int n) {

@@ -262,7 +262,12 @@ int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const voi
                         long long rs, void* o_last, float* x, cudaStream_t s) {
   if (L <= 0) return GDNBEAM_EINVAL;
   if (c.d_v > 128 && c.d_v % 128 != 0) return GDNBEAM_EUNSUPPORTED;
-  if (tc_prefill_supported(c, x)) return launch_prefill_tc(c, L, q, k, v, alpha, beta, sctx, rs, o_last, s);
+  if (tc_prefill_supported(c, x)) {
+    const long long qw = (long long)key_heads(c) * c.d_k;
+    // (bf16 queries: two bytes each)
+    return launch_prefill_tc(c, L, (const char*)q + (size_t)(L - 1) * qw * 2,
+                             (long long)L * qw, k, v, alpha, beta, sctx, rs, o_last, s);
+  }
   if (c.dtype == GDNBEAM_BF16)
     return dispatch_dk<__nv_bfloat16>(c, L, q, k, v, alpha, beta, sctx, rs, o_last, x, s);
   return dispatch_dk<float>(c, L, q, k, v, alpha, beta, sctx, rs, o_last, x, s);

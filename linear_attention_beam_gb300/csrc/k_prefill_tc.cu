@@ -82,7 +82,8 @@ constexpr int kThreads = 32 * (kT0 + kTWarps);
 struct PrefillTcParams {
   int R, H, Hk, L, n_pairs;
   const float *alpha, *beta;  // [R*L][H]
-  const uint16_t* q;          // [R*L][Hk*128] bf16
+  const uint16_t* q_last;     // per request its last token's query row (Hk*128 bf16)
+  long long q_last_ld;        // elements between the requests' rows
   float* sctx;                // S_ctx of head h of request r at sctx + r*rstride + h*128*128
   long long rstride;
   __nv_bfloat16* o_last;      // [R][H*128] or null
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && wait(s_full, (uint32_t)(n_chunks - 1) & 1u)) {
       tc::fence_after_sync();
       float* out = p.sctx + (size_t)r * p.rstride + (size_t)h * DH * DH + (size_t)v * DH;
-      const uint16_t* ql = p.q + ((size_t)r * p.L + (p.L - 1)) * ((size_t)p.Hk * DH) + (size_t)hk * DH;
+      const uint16_t* ql = p.q_last + (size_t)r * p.q_last_ld + (size_t)hk * DH;
       float o = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -675,9 +676,9 @@ bool tc_prefill_supported(const gdnbeam_config& c, const float* x_inout) {
   return c.dtype == GDNBEAM_BF16 && c.d_k == DH && c.d_v == DH && x_inout == nullptr;
 }
 
-int launch_prefill_tc(const gdnbeam_config& c, int L, const void* q, const void* k, const void* v,
-                      const float* alpha, const float* beta, float* sctx, long long rstride,
-                      void* o_last, cudaStream_t s) {
+int launch_prefill_tc(const gdnbeam_config& c, int L, const void* q_last, long long q_last_ld,
+                      const void* k, const void* v, const float* alpha, const float* beta,
+                      float* sctx, long long rstride, void* o_last, cudaStream_t s) {
   if (L <= 0) return GDNBEAM_EINVAL;
   const int Hk = key_heads(c);
   if ((long long)c.R * L > 0x7FFFFFFFLL) return GDNBEAM_EUNSUPPORTED;
@@ -688,7 +689,8 @@ int launch_prefill_tc(const gdnbeam_config& c, int L, const void* q, const void*
   p.R = c.R; p.H = c.H; p.Hk = Hk; p.L = L;
   p.n_pairs = (L + PAIR - 1) / PAIR;
   p.alpha = alpha; p.beta = beta;
-  p.q = reinterpret_cast<const uint16_t*>(q);
+  p.q_last = reinterpret_cast<const uint16_t*>(q_last);
+  p.q_last_ld = q_last_ld;
   p.sctx = sctx; p.rstride = rstride;
   p.o_last = reinterpret_cast<__nv_bfloat16*>(o_last);
   p.err = error_word();

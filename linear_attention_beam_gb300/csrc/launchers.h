@@ -36,9 +36,14 @@ int launch_logits_rows(int dtype, int n, int V, const float* Z, void* z, float* 
 // ---- tcgen05 tensor-core GEMMs (bf16, d = 128, d_model % 64 == 0) --------
 
 bool tc_gemm_supported(const gdnbeam_config& c);
+// Projection columns to compute: all of them, all but the queries (a
+// prefill that needs the query only at the last token), or only the queries.
+enum { PROJ_ALL = 0, PROJ_NO_Q = 1, PROJ_Q_ONLY = 2 };
+// ldu: elements between consecutive rows of u (0: d_model).
 int launch_tc_project(const gdnbeam_config& c, int n, const void* u, const void* W_proj,
                       void* q, void* k, void* v, float* alpha, float* beta,
-                      const gdnbeam_dumps* d, cudaStream_t s);
+                      const gdnbeam_dumps* d, cudaStream_t s, int cols = PROJ_ALL,
+                      long long ldu = 0);
 size_t tc_logits_scratch_bytes(const gdnbeam_config& c, int n);
 int launch_tc_logits(const gdnbeam_config& c, int n, const void* feat, const void* W_o,
                      void* z, float* lse, void* scratch, const gdnbeam_dumps* d,
@@ -114,9 +119,11 @@ int launch_to_storage(int dtype, size_t n, const float* src, void* dst, cudaStre
 // Chunked tensor-core prefill (bf16, d_k = d_v = 128, no residual stream):
 // S_ctx and o at the last token, as launch_prefill_scan.
 bool tc_prefill_supported(const gdnbeam_config& c, const float* x_inout);
-int launch_prefill_tc(const gdnbeam_config& c, int L, const void* q, const void* k, const void* v,
-                      const float* alpha, const float* beta, float* sctx, long long rstride,
-                      void* o_last, cudaStream_t s);
+// q_last: each request's query row at its last prompt token, q_last_ld
+// elements apart.
+int launch_prefill_tc(const gdnbeam_config& c, int L, const void* q_last, long long q_last_ld,
+                      const void* k, const void* v, const float* alpha, const float* beta,
+                      float* sctx, long long rstride, void* o_last, cudaStream_t s);
 int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const void* k,
                         const void* v, const float* alpha, const float* beta, float* sctx,
                         long long sctx_rstride, void* o_last, float* x_inout, cudaStream_t s);
