@@ -170,6 +170,7 @@ struct SelScratch {
   float2* hint;     // [R*W_t][n_tiles] tile maxima computed here when not supplied
   int* tcount;      // [R] (row, tile) pairs whose tile maximum reaches the bound
   uint32_t* tlist;  // [R][cap_tiles] those pairs, as b * n_tiles + tile
+  float* cut;       // [R*W_t] per row the smallest stored logit whose score reaches the bound
   int cap;
   int cap_tiles;
 };
@@ -210,6 +211,7 @@ SelScratch carve_sel(void* base, int R, int W_t, int W_next, int V, size_t* tota
   s.hint = (float2*)take((size_t)R * W_t * n_tiles * sizeof(float2));
   s.tcount = (int*)take((size_t)R * 4);
   s.tlist = (uint32_t*)take((size_t)R * s.cap_tiles * 4);
+  s.cut = (float*)take((size_t)R * W_t * 4);
   if (total) *total = off;
   return s;
 }
@@ -281,6 +283,19 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
     }
   }
   if (threadIdx.x == 0) ss.thr[r] = t;
+  // each row's cutoff: the smallest stored value whose score reaches t, by
+  // bisection over the storage keys (scores are monotone in the stored
+  // value within a row); NaN when no code of the row can qualify
+  for (int b = threadIdx.x; b < W_t; b += blockDim.x) {
+    const size_t row = (size_t)r * W_t + b;
+    const float cp = cum_prime(cum, bias, row), l = lse[row];
+    uint32_t lo = SKey<T>::kNegInf, hi = SKey<T>::kPosInf + 1u;  // hi: none reaches t
+    while (lo < hi) {
+      const uint32_t mid = lo + ((hi - lo) >> 1);
+      if (orderable(score(cp, SKey<T>::value(mid), l)) >= t) hi = mid; else lo = mid + 1u;
+    }
+    ss.cut[row] = SKey<T>::value(lo);
+  }
   __syncthreads();
   uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
   for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
@@ -295,10 +310,9 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
 }
 
 // ---- filter: append every code of the listed tiles whose score reaches the
-// bound. One warp per listed tile (256 codes, eight per lane). The row's
-// cutoff logit (the smallest stored value whose score reaches the bound) is
-// found by bisection over the storage keys, so codes are compared as stored
-// values and scores are computed only for hits.
+// bound. One warp per listed tile (256 codes, eight per lane). Codes are
+// compared as stored values with the row's cutoff logit from the bound
+// kernel; scores are computed only for hits.
 template <typename T>
 __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
     int W_t, int V, int n_tiles, int blocks_per_req, const T* __restrict__ z,
@@ -310,7 +324,6 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
   const int warps = blocks_per_req * (kFilterThreads / 32);
   const int n_list = min(ss.tcount[r], ss.cap_tiles);
   const uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
-  const uint32_t t = ss.thr[r];
   uint64_t* out = ss.cand + (size_t)r * ss.cap;
   const bool vec = (V % 8) == 0 && ((uintptr_t)z & 15) == 0;
   for (int j = (blockIdx.x % blocks_per_req) * (kFilterThreads / 32) + (threadIdx.x >> 5); j < n_list;
@@ -319,12 +332,7 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
     const int b = (int)(i / (uint32_t)n_tiles), tile = (int)(i % (uint32_t)n_tiles);
     const size_t row = (size_t)r * W_t + b;
     const float cp = cum_prime(cum, bias, row), l = lse[row];
-    uint32_t lo = SKey<T>::kNegInf, hi = SKey<T>::kPosInf + 1u;  // hi: none reaches t
-    while (lo < hi) {
-      const uint32_t mid = lo + ((hi - lo) >> 1);
-      if (orderable(score(cp, SKey<T>::value(mid), l)) >= t) hi = mid; else lo = mid + 1u;
-    }
-    const float thr = SKey<T>::value(lo);  // NaN when no code can qualify
+    const float thr = ss.cut[row];  // NaN when no code can qualify
     const int v0 = tile * kTile + lane * EPL;
     const T* zr = z + row * (size_t)V;
     float zv[EPL];
