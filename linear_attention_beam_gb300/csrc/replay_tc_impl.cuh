@@ -18,9 +18,9 @@
 //   * Beams go in tiles of 32. A producer warp stages per tile, by TMA, the
 //     32 queries and keys (the B operand, N = 64: q rows then k rows, 128-byte
 //     swizzled) and the 32 value rows; that warp and two more gather each
-//     beam's ancestor records delta_j and k_j, four rows per request (small
-//     TMA requests are issued at a per-warp rate, so the work is spread over
-//     three warps). Stages
+//     beam's ancestor records delta_j, four rows per request. (The SM issues
+//     small TMA requests at a limited rate, so the ancestor keys k_j, which
+//     only the scalar warps read, are loaded by those warps directly.) Stages
 //     sit on an mbarrier ring several tiles deep.
 //   * Gates, ancestor slots and ancestor decays of all the block's beams are
 //     read once into a shared table at block start by every thread (while
@@ -64,7 +64,7 @@ constexpr int kMaxStages = 6;
 // for this block's values, then k_j)
 template <int DK> struct Width {
   static constexpr int B_BYTES = 2 * NB * DK * 2;
-  static constexpr int REC_BYTES = REC_D + NB * DK * 2;
+  static constexpr int REC_BYTES = REC_D;  // the scalar warps read k_j from global memory
   // TMEM columns: two accumulators of 2 * NB, then S_ctx hi and lo (DK / 2 each)
   static constexpr uint32_t kColAHi = 4 * NB, kColALo = 4 * NB + DK / 2;
   static constexpr uint32_t kTmemCols = DK == 128 ? 256 : 512;
@@ -73,7 +73,7 @@ template <int DK> struct Width {
 // Ancestor records of each depth as 2-D maps [R * W_j * heads rows][width]
 // with a one-row, 64-column box, read four rows at a time.
 struct RecMaps {
-  CUtensorMap d[kMaxDepth], k[kMaxDepth];
+  CUtensorMap d[kMaxDepth];
 };
 
 struct TcReplayParams {
@@ -83,6 +83,7 @@ struct TcReplayParams {
   long long sctx_rstride;
   const float *alpha, *beta;
   const float* rec_a[kMaxDepth];
+  const uint16_t* rec_k[kMaxDepth];  // ancestor keys [R * W_j][Hk * DK] bf16
   int W_j[kMaxDepth];
   const int32_t* anc;
   int anc_stride;
@@ -233,11 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();  // the table is complete
 
-  // A tile's record requests (four beams, one 64-column block of one depth's
-  // delta_j or k_j rows each) are split round-robin over three warps: the
-  // producer (w = 0) and the two record loaders (w = 1, 2); small TMA
-  // requests issue at a per-warp rate, so three streams move more.
-  constexpr int kRecReq = 8 * t * (2 + DK / 64);  // requests per tile
+  // A tile's record requests (four beams, one 64-column half of one depth's
+  // delta_j rows each; the keys k_j are read by the scalar warps) are split
+  // round-robin over three warps: the producer (w = 0) and the two record
+  // loaders (w = 1, 2).
+  constexpr int kRecReq = 16 * t;  // requests per tile
   auto rec_share = [](int w) { return (kRecReq - w + 2) / 3; };
   auto issue_records = [&](int w, int i, uint32_t st, int s) {
     const int l0 = i * NB;  // the tile's first beam in the table
@@ -245,25 +246,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = lane;; m += 32) {
       const int rq = 3 * m + w;
       if (rq >= kRecReq) break;
-      int kind, j, cb, gq;
-      if (rq < 16 * t) {
-        kind = 0; j = rq >> 4; cb = (rq >> 3) & 1; gq = rq & 7;
-      } else {
-        const int idx = rq - 16 * t;
-        kind = 1; j = idx / (8 * (DK / 64)); cb = (idx >> 3) % (DK / 64); gq = idx & 7;
-      }
+      const int j = rq >> 4, cb = (rq >> 3) & 1, gq = rq & 7;
       int y[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int b = 4 * gq + u;  // beams past the tile's end repeat a valid row
         const int sl = b < nb ? tab_slot[(l0 + b) * t + j] : 0;
-        // delta_j rows are per value head, k_j rows per key head
-        y[u] = kind == 0 ? (r * p.W_j[j] + sl) * p.H + h : (r * p.W_j[j] + sl) * p.Hk + hk;
+        y[u] = (r * p.W_j[j] + sl) * p.H + h;  // delta_j rows are per value head
       }
-      const uint32_t dst = st + rec_off + (uint32_t)(j * REC_BYTES + kind * REC_D +
-                                                     cb * (NB * 128) + gq * (4 * 128));
-      tc::tma_gather4(dst, kind == 0 ? &rm.d[j] : &rm.k[j],
-                      kind == 0 ? vb * VR + cb * 64 : cb * 64, y[0], y[1], y[2], y[3], full(s));
+      const uint32_t dst = st + rec_off + (uint32_t)(j * REC_BYTES + cb * (NB * 128) + gq * (4 * 128));
+      tc::tma_gather4(dst, &rm.d[j], vb * VR + cb * 64, y[0], y[1], y[2], y[3], full(s));
     }
     __syncwarp();
   };
@@ -335,6 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sw = warp - kScal0;
     const int bl = sw * 8 + (lane >> 2);
     const int c0 = (lane & 3) * (DK / 4);
+    // The ancestor keys come from global memory (the lane's DK / 4
+    // dimensions of each depth's row, kChunks 16-byte pieces); the first
+    // kPre depths are requested before the tile's stage is awaited.
+    constexpr int kChunks = DK / 32;
+    constexpr int kPre = TD < 12 / kChunks ? TD : 12 / kChunks;
+    auto key_row = [&](int l0, int j) {
+      const int sl = l0 + bl < nbeams ? tab_slot[(l0 + bl) * t + j] : 0;
+      return reinterpret_cast<const uint4*>(
+          p.rec_k[j] + ((size_t)(r * p.W_j[j] + sl) * p.Hk + hk) * DK + c0);
+    };
     bool ok = true;
     for (int i = 0; ok && i < nt; ++i) {
       const int s = i % p.stages;
@@ -343,6 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sph = (uint32_t)(i >> 1) & 1u;
       const int l0 = i * NB;  // the tile's first beam in the table
       const int nb = min(NB, nbeams - l0);
+      uint4 kr[kPre > 0 ? kPre : 1][kChunks];
+#pragma unroll
+      for (int j = 0; j < kPre; ++j) {
+        const uint4* kp = key_row(l0, j);
+#pragma unroll
+        for (int ch = 0; ch < kChunks; ++ch) kr[j][ch] = __ldg(kp + ch);
+      }
       // the buffer's previous tile has been folded, and this tile has landed
       if (__any_sync(0xffffffffu, !tc::mbar_wait_sleep(sempty(sb), sph ^ 1u, abort, p.err) ||
                                       !tc::mbar_wait_sleep(full(s), ph, abort, p.err))) {
@@ -370,8 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 8; ++x) part[0] = fmaf(k8[x], q8[x], part[0]);
 #pragma unroll
         for (int j = 0; j < t; ++j) {
-          const uint4 rw = *reinterpret_cast<const uint4*>(
-              gst + rec_off + j * REC_BYTES + REC_D + kb * (NB * 128) + bl * 128 + cc * 2);
+          const uint4 rw = j < kPre ? kr[j < kPre ? j : 0][ch] : __ldg(key_row(l0, j) + ch);
           const uint32_t ra[4] = {rw.x, rw.y, rw.z, rw.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -660,14 +668,12 @@ int launch_tc_replay_dk(const ReplayArgs& a, cudaStream_t s) {
   memset(&rm, 0, sizeof(rm));
   for (int j = 0; j < a.t; ++j) {
     p.rec_a[j] = a.depth[j].alpha;
+    p.rec_k[j] = reinterpret_cast<const uint16_t*>(a.depth[j].k);
     p.W_j[j] = a.depth[j].W_j;
     if (((uintptr_t)a.depth[j].k & 15) || ((uintptr_t)a.depth[j].delta & 15)) return GDNBEAM_EINVAL;
     const long long rows = (long long)a.R * a.depth[j].W_j * a.H;
-    const long long krows = (long long)a.R * a.depth[j].W_j * a.Hk;
     if (rows > 0x7FFFFFFFLL) return launch_replay(GDNBEAM_BF16, a, s);
-    if (!rows_map(&rm.d[j], a.depth[j].delta, rows, a.d_v) ||
-        !rows_map(&rm.k[j], a.depth[j].k, krows, DK))
-      return GDNBEAM_ECUDA;
+    if (!rows_map(&rm.d[j], a.depth[j].delta, rows, a.d_v)) return GDNBEAM_ECUDA;
   }
   p.anc = a.anc; p.anc_stride = a.anc_stride;
   p.x_inout = a.x_inout; p.delta_dump = a.delta_dump; p.o_dump = a.o_dump; p.err = a.err;
