@@ -1,0 +1,37 @@
+"""Host-side figures the benchmark reports: the operator-sweep shapes and
+the algorithmic bytes of one replay call."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+import bench  # noqa: E402
+
+
+def test_sweep_shapes_span_the_pages_ranges():
+    # OneLA §3 (operator experiments): R 4/8/16, W 128/256/512, T 2..6 and
+    # nine geometries with H_K 4-32, H_V 4-64, K 128-256, V 128-512; 405 shapes
+    shapes = [(g, R, W, T) for g in synth.SWEEP_GEOMETRIES for R in synth.SWEEP_R
+              for W in synth.SWEEP_W for T in synth.SWEEP_T]
+    assert len(shapes) == 405 and len(set(synth.SWEEP_GEOMETRIES)) == 9
+    for Hk, H, K, V in synth.SWEEP_GEOMETRIES:
+        assert 4 <= Hk <= 32 and 4 <= H <= 64 and 128 <= K <= 256 and 128 <= V <= 512
+        assert H % Hk == 0  # value heads share key heads in whole groups
+    assert (16, 16, 128, 128) in synth.SWEEP_GEOMETRIES  # the pages' Qwen geometry
+    # every end of every range is reached
+    for i, ends in enumerate([(4, 32), (4, 64), (128, 256), (128, 512)]):
+        vals = {g[i] for g in synth.SWEEP_GEOMETRIES}
+        assert min(vals) == ends[0] and max(vals) == ends[1]
+
+
+def test_replay_bytes_of_the_batched_depth_two_call():
+    # 64 requests x 512 beams, 16 heads of width 128, bf16, two ancestors:
+    # per beam q,k 8192 + v 4096 + gates 128 + 2 x (k_j 4096 + delta_j 4096 +
+    # alpha_j 64) + delta_t,o_t 8192 = 37120 bytes, plus S_ctx (fp32) once
+    # per request and head: 64 * 16 * 128 * 128 * 4 bytes
+    assert bench.replay_bytes(64, 512, 16, 16, 128, 128, 2, 2) == 32768 * 37120 + 67108864
+    # grouped key heads read one key row per key head
+    assert (bench.replay_bytes(1, 1, 16, 4, 128, 128, 0, 2)
+            == 2 * 4 * 128 * 2 + 16 * 128 * 2 + 2 * 16 * 4 + 2 * 16 * 128 * 2 + 16 * 128 * 128 * 4)
