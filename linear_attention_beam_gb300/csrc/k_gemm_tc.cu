@@ -272,12 +272,17 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      constexpr uint32_t idesc_full = tc::idesc_bf16_f32(BM, BN);
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
       int i = 0;
       for (int tile = cid; tile < num_tiles && ok; tile += n_clusters, ++i) {
+        // a last column tile narrower than BN runs MMAs only as wide as its
+        // columns (rounded up to 16); the epilogues never read past N
+        const int n_here = ea.N - (tile % n_tiles) * BN;
+        const uint32_t idesc =
+            n_here >= BN ? idesc_full : tc::idesc_bf16_f32(BM, (n_here + 15) & ~15);
         const int acc = i & 1;
         const uint32_t aph = (uint32_t)(i >> 1) & 1u;
         if (!tc::mbar_wait(tempty(acc), aph ^ 1u, abort, ea.err)) break;
