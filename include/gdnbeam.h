@@ -296,6 +296,39 @@ int gdnbeam_replay(const gdnbeam_config* cfg, int t, int W_t, const float* sctx,
                    const int32_t* anc, int anc_stride, void* delta_out, void* o_out,
                    float* x_inout, const gdnbeam_dumps* dumps, gdnbeam_stream_t stream);
 
+/* The pages' two baselines of the same step, for one layer (gdnbeam_step runs
+ * them inside the decode loop when state_path is 1 or 2). Head widths d_k, d_v
+ * at most 128; storage-precision states; outputs as gdnbeam_replay.
+ *
+ * FullState (OneLA §3, the "Controlled FullState" path): every beam keeps its
+ * own d_v x d_k state. For request r, beam b < W_t and head h, the parent
+ * state S_par is sctx_store's head h of request r at t = 0, else
+ * states_prev[r*W_prev + parents[r*W_t+b]]; then (eq. 3)
+ *   delta = beta (v - alpha S_par k), S = alpha S_par + delta k^T, o = S q,
+ * and S is stored to states_cur[r*W_t+b].
+ *   sctx_store [R][H][d_v][d_k] storage, sctx_rstride elements between requests
+ *   states_prev [R*W_prev][H][d_v][d_k], states_cur [R*W_t][H][d_v][d_k] storage
+ *   parents [R*W_t] int32 (read when t > 0; out-of-range entries set
+ *   GDNBEAM_DERR_PARENT). Returns GDNBEAM_EUNSUPPORTED for wider heads. */
+int gdnbeam_fullstate_step(const gdnbeam_config* cfg, int t, int W_t, int W_prev,
+                           const void* sctx_store, long long sctx_rstride,
+                           const void* states_prev, void* states_cur, const int32_t* parents,
+                           const void* q, const void* k, const void* v, const float* alpha,
+                           const float* beta, void* delta_out, void* o_out,
+                           gdnbeam_stream_t stream);
+
+/* ReplaySSM (OneLA §1.3 and §7.2, the baseline that recomputes instead of
+ * storing): no per-beam state is kept. Each (beam, head) rebuilds its parent
+ * state from the request's S_ctx (sctx_store, storage precision) by applying
+ * its t ancestors' records in depth order (eq. 4), then takes the step as
+ * FullState does. Records, anc and the other arguments as gdnbeam_replay.
+ * Returns GDNBEAM_EUNSUPPORTED for wider heads. */
+int gdnbeam_replayssm_step(const gdnbeam_config* cfg, int t, int W_t, const void* sctx_store,
+                           long long sctx_rstride, const void* q, const void* k, const void* v,
+                           const float* alpha, const float* beta, const gdnbeam_records* depth,
+                           const int32_t* anc, int anc_stride, void* delta_out, void* o_out,
+                           gdnbeam_stream_t stream);
+
 /* Codebook logits for n rows: z = W_o feat, lse = log sum exp z.
  *   feat [n][F] storage; W_o [V][F]; z [n][V] storage; lse [n] fp32. */
 size_t gdnbeam_logits_scratch_bytes(const gdnbeam_config* cfg, int n);

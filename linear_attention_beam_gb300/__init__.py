@@ -96,6 +96,10 @@ _SIGS = {
     "gdnbeam_select_topw_noalloc": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _S]),
     "gdnbeam_ancestry": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S]),
     "gdnbeam_prefill_scan": (_I, [C.POINTER(Config), _I, _P, _P, _P, _P, _P, _P, _LL, _P, _P, _S]),
+    "gdnbeam_fullstate_step": (_I, [C.POINTER(Config), _I, _I, _I, _P, _LL, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _P, _P, _S]),
+    "gdnbeam_replayssm_step": (_I, [C.POINTER(Config), _I, _I, _P, _LL, _P, _P, _P, _P, _P,
+                                    C.POINTER(Records), _P, _I, _P, _P, _S]),
 }
 
 _lib: Optional[C.CDLL] = None

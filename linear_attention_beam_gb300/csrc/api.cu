@@ -684,6 +684,58 @@ int gdnbeam_replay(const gdnbeam_config* cfg, int t, int W_t, const float* sctx,
   return launch_replay(c.dtype, a, (cudaStream_t)stream);
 }
 
+int gdnbeam_fullstate_step(const gdnbeam_config* cfg, int t, int W_t, int W_prev,
+                           const void* sctx_store, long long sctx_rstride,
+                           const void* states_prev, void* states_cur, const int32_t* parents,
+                           const void* q, const void* k, const void* v, const float* alpha,
+                           const float* beta, void* delta_out, void* o_out,
+                           gdnbeam_stream_t stream) {
+  int st = validate(cfg);
+  if (st) return st;
+  const gdnbeam_config& c = *cfg;
+  if (c.d_k > 128 || c.d_v > 128) return GDNBEAM_EUNSUPPORTED;
+  if (t < 0 || t >= GDNBEAM_MAX_T || W_t < 1 || !sctx_store || !states_cur || !q || !k || !v ||
+      !alpha || !beta || !delta_out || !o_out)
+    return GDNBEAM_EINVAL;
+  if (t > 0 && (!states_prev || !parents || W_prev < 1)) return GDNBEAM_EINVAL;
+  FullStateArgs f{};
+  f.R = c.R; f.H = c.H; f.d_k = c.d_k; f.d_v = c.d_v; f.t = t; f.W_t = W_t; f.Hk = key_heads(c);
+  f.W_prev = t > 0 ? W_prev : 1; f.layers = 1; f.layer = 0;
+  f.sctx_store = sctx_store; f.sctx_rstride = sctx_rstride;
+  f.states_prev = states_prev; f.states_cur = states_cur; f.parents = parents;
+  f.q = q; f.k = k; f.v = v; f.alpha = alpha; f.beta = beta;
+  f.delta_out = delta_out; f.o_out = o_out;
+  f.err = err_ptr();
+  return launch_fullstate(c.dtype, f, (cudaStream_t)stream);
+}
+
+int gdnbeam_replayssm_step(const gdnbeam_config* cfg, int t, int W_t, const void* sctx_store,
+                           long long sctx_rstride, const void* q, const void* k, const void* v,
+                           const float* alpha, const float* beta, const gdnbeam_records* depth,
+                           const int32_t* anc, int anc_stride, void* delta_out, void* o_out,
+                           gdnbeam_stream_t stream) {
+  int st = validate(cfg);
+  if (st) return st;
+  const gdnbeam_config& c = *cfg;
+  if (c.d_k > 128 || c.d_v > 128) return GDNBEAM_EUNSUPPORTED;
+  if (t < 0 || t >= GDNBEAM_MAX_T || W_t < 1 || !sctx_store || !q || !k || !v || !alpha ||
+      !beta || !delta_out || !o_out)
+    return GDNBEAM_EINVAL;
+  if (t > 0 && (!depth || !anc || anc_stride < t)) return GDNBEAM_EINVAL;
+  ReplaySsmArgs g{};
+  g.R = c.R; g.H = c.H; g.d_k = c.d_k; g.d_v = c.d_v; g.t = t; g.W_t = W_t; g.Hk = key_heads(c);
+  g.sctx_store = sctx_store; g.sctx_rstride = sctx_rstride;
+  g.q = q; g.k = k; g.v = v; g.alpha = alpha; g.beta = beta;
+  for (int j = 0; j < t; ++j) {
+    if (!depth[j].k || !depth[j].delta || !depth[j].alpha || depth[j].W_j < 1) return GDNBEAM_EINVAL;
+    g.depth[j] = depth[j];
+  }
+  g.anc = anc; g.anc_stride = anc_stride;
+  g.delta_out = delta_out; g.o_out = o_out;
+  g.err = err_ptr();
+  return launch_replayssm(c.dtype, g, (cudaStream_t)stream);
+}
+
 size_t gdnbeam_logits_scratch_bytes(const gdnbeam_config* cfg, int n) {
   if (validate(cfg) || n < 0) return 0;
   if (tc_gemm_supported(*cfg)) return tc_logits_scratch_bytes(*cfg, n);

@@ -431,3 +431,112 @@ def test_select_flags_non_finite_inputs(dtype, bad):
                                    gb.ptr(par), gb.ptr(tok), gb.ptr(cn), gb.ptr(scratch), scratch.numel(),
                                    None) == 0
     assert device_status_clear() & gb.DERR_NONFINITE
+
+
+# ------------------------------------------------------------------ baselines
+
+@pytest.mark.parametrize("dtype,d,H,Hk,R,W_t,W_prev,t", [
+    ("f32", 16, 2, 2, 2, 9, 5, 0), ("f32", 16, 2, 1, 2, 9, 5, 1), ("bf16", 128, 2, 1, 2, 40, 17, 1),
+    ("bf16", 128, 3, 3, 1, 70, 33, 0), ("bf16", 64, 4, 2, 2, 33, 20, 3)])
+def test_fullstate_step_op(dtype, d, H, Hk, R, W_t, W_prev, t):
+    # the FullState baseline: each beam's own state from its parent's (S_ctx
+    # at t = 0), one eq. 3 transition, the child's state stored
+    wl = synth.tiny_workload(d=d, V=7, H=H, R=R, dtype=dtype, H_k=Hk)
+    g = H // Hk
+    rng = np.random.default_rng(d + 7 * H + W_t + t)
+    st_ = lambda a: store(a, wl)
+    S_ctx = st_(rng.standard_normal((R, H, d, d)) * 0.05)
+    prev = st_(rng.standard_normal((R, W_prev, H, d, d)) * 0.05)
+    par = rng.integers(0, W_prev, (R, W_t)).astype(np.int32)
+    q = st_(_unit_rows(rng, (R, W_t, Hk, d)))
+    k = st_(_unit_rows(rng, (R, W_t, Hk, d)))
+    v = st_(rng.standard_normal((R, W_t, H, d)))
+    al = rng.uniform(0.1, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
+    be = rng.uniform(0.0, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
+    td = tdt(wl)
+    n = R * W_t
+    cur = torch.zeros(n, H, d, d, dtype=td, device=DEV)
+    d_out = torch.empty(n, H * d, dtype=td, device=DEV)
+    o_out = torch.empty_like(d_out)
+    cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d, T=t + 2, H_k=Hk)
+    st = gb.load().gdnbeam_fullstate_step(
+        C.byref(cfg), t, W_t, W_prev, gb.ptr(to_dev(S_ctx.reshape(-1), td)), H * d * d,
+        gb.ptr(to_dev(prev.reshape(-1), td)), gb.ptr(cur), gb.ptr(to_dev(par.reshape(-1), torch.int32)),
+        gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
+        gb.ptr(to_dev(v.reshape(-1), td)), gb.ptr(to_dev(al.reshape(-1))), gb.ptr(to_dev(be.reshape(-1))),
+        gb.ptr(d_out), gb.ptr(o_out), None)
+    assert st == 0
+    assert device_status_clear() == 0
+    exp_S = np.zeros((R, W_t, H, d, d)); exp_d = np.zeros((R, W_t, H, d)); exp_o = np.zeros_like(exp_d)
+    for r in range(R):
+        for b in range(W_t):
+            for h in range(H):
+                S_par = S_ctx[r, h] if t == 0 else prev[r, par[r, b], h]
+                exp_S[r, b, h], exp_d[r, b, h], exp_o[r, b, h] = oracle.gdn_transition(
+                    S_par, q[r, b, h // g], k[r, b, h // g], v[r, b, h], al[r, b, h], be[r, b, h])
+    _check_stored(host(cur).reshape(exp_S.shape), exp_S, wl, "states")
+    _check_stored(host(d_out).reshape(exp_d.shape), exp_d, wl, "delta")
+    _check_stored(host(o_out).reshape(exp_o.shape), exp_o, wl, "o")
+
+
+@pytest.mark.parametrize("dtype,d,H,Hk,R,W_t,t", [
+    ("f32", 16, 2, 2, 2, 9, 2), ("bf16", 128, 2, 1, 2, 40, 1), ("bf16", 128, 3, 3, 1, 70, 3),
+    ("bf16", 64, 4, 2, 2, 33, 0), ("f32", 32, 2, 2, 1, 17, 5)])
+def test_replayssm_step_op(dtype, d, H, Hk, R, W_t, t):
+    # the ReplaySSM baseline: each (beam, head) rebuilds its parent state
+    # from S_ctx (storage precision) and its ancestors' records, then steps
+    wl = synth.tiny_workload(d=d, V=7, H=H, R=R, dtype=dtype, H_k=Hk)
+    g = H // Hk
+    rng = np.random.default_rng(3 * d + H + W_t + 11 * t)
+    st_ = lambda a: store(a, wl)
+    S_ctx = st_(rng.standard_normal((R, H, d, d)) * 0.05)
+    Wj = [int(rng.integers(1, 40)) for _ in range(t)]
+    rec_k = [st_(_unit_rows(rng, (R, Wj[j], Hk, d))) for j in range(t)]
+    rec_d = [st_(rng.standard_normal((R, Wj[j], H, d)) * 0.5) for j in range(t)]
+    rec_a = [rng.uniform(0.2, 1.0, (R, Wj[j], H)).astype(np.float32).astype(np.float64) for j in range(t)]
+    q = st_(_unit_rows(rng, (R, W_t, Hk, d)))
+    k = st_(_unit_rows(rng, (R, W_t, Hk, d)))
+    v = st_(rng.standard_normal((R, W_t, H, d)))
+    al = rng.uniform(0.1, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
+    be = rng.uniform(0.0, 1.0, (R, W_t, H)).astype(np.float32).astype(np.float64)
+    anc = (np.stack([rng.integers(0, Wj[j], (R, W_t)) for j in range(t)], -1) if t
+           else np.zeros((R, W_t, 1))).astype(np.int32)
+    td = tdt(wl)
+    recs = (gb.Records * max(t, 1))()
+    for j in range(t):
+        recs[j] = gb.Records(gb.ptr(to_dev(rec_k[j].reshape(-1), td)), gb.ptr(to_dev(rec_d[j].reshape(-1), td)),
+                             gb.ptr(to_dev(rec_a[j].reshape(-1))), Wj[j])
+    n = R * W_t
+    d_out = torch.empty(n, H * d, dtype=td, device=DEV)
+    o_out = torch.empty_like(d_out)
+    cfg = cfg_for(wl, R=R, H=H, d_k=d, d_v=d, d_model=H * d, T=t + 2, H_k=Hk)
+    st = gb.load().gdnbeam_replayssm_step(
+        C.byref(cfg), t, W_t, gb.ptr(to_dev(S_ctx.reshape(-1), td)), H * d * d,
+        gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)), gb.ptr(to_dev(v.reshape(-1), td)),
+        gb.ptr(to_dev(al.reshape(-1))), gb.ptr(to_dev(be.reshape(-1))), recs,
+        gb.ptr(to_dev(anc.reshape(n, -1), torch.int32)), anc.shape[-1], gb.ptr(d_out), gb.ptr(o_out), None)
+    assert st == 0
+    assert device_status_clear() == 0
+    exp_d = np.zeros((R, W_t, H, d)); exp_o = np.zeros_like(exp_d)
+    for r in range(R):
+        for b in range(W_t):
+            for h in range(H):
+                chain = [(rec_a[j][r, anc[r, b, j], h], rec_d[j][r, anc[r, b, j], h],
+                          rec_k[j][r, anc[r, b, j], h // g]) for j in range(t)]
+                exp_d[r, b, h], exp_o[r, b, h] = oracle.step_from_records(
+                    S_ctx[r, h], chain, q[r, b, h // g], k[r, b, h // g], v[r, b, h], al[r, b, h], be[r, b, h])
+    _check_stored(host(d_out).reshape(exp_d.shape), exp_d, wl, "delta")
+    _check_stored(host(o_out).reshape(exp_o.shape), exp_o, wl, "o")
+
+
+def test_baseline_steps_reject_wide_heads():
+    wl = synth.tiny_workload(d=16, V=7, H=1, R=1, dtype="bf16")
+    cfg = cfg_for(wl, d_k=256, d_v=128, d_model=128)
+    lib = gb.load()
+    z = torch.zeros(16, device=DEV)
+    assert lib.gdnbeam_fullstate_step(C.byref(cfg), 0, 1, 1, gb.ptr(z), 0, None, gb.ptr(z), None, gb.ptr(z),
+                                      gb.ptr(z), gb.ptr(z), gb.ptr(z), gb.ptr(z), gb.ptr(z), gb.ptr(z),
+                                      None) == gb.EUNSUPPORTED
+    assert lib.gdnbeam_replayssm_step(C.byref(cfg), 0, 1, gb.ptr(z), 0, gb.ptr(z), gb.ptr(z), gb.ptr(z),
+                                      gb.ptr(z), gb.ptr(z), None, None, 0, gb.ptr(z), gb.ptr(z),
+                                      None) == gb.EUNSUPPORTED
