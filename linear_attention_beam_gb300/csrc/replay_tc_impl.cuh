@@ -522,6 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         // every beam of the half tile is computed; rows past the last beam
         // are never stored (the tile store clips them)
+        // (all 16 beams are folded into registers first and stored after,
+        // so no shared-memory store sits between the loads)
+        float dl[16], ol[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int b = hb * 16 + e;
@@ -536,15 +539,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             delta = fmaf(rc.x, dj, delta);
             o = fmaf(rc.y, dj, o);
           }
-          o = fmaf(bm.w, delta, o);
-          *reinterpret_cast<__nv_bfloat16*>(os + e * 64) = __float2bfloat16_rn(delta);
-          *reinterpret_cast<__nv_bfloat16*>(os + OUT_WARP / 2 + e * 64) = __float2bfloat16_rn(o);
+          dl[e] = delta;
+          ol[e] = fmaf(bm.w, delta, o);
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          *reinterpret_cast<__nv_bfloat16*>(os + e * 64) = __float2bfloat16_rn(dl[e]);
+          *reinterpret_cast<__nv_bfloat16*>(os + OUT_WARP / 2 + e * 64) = __float2bfloat16_rn(ol[e]);
           if constexpr (EXTRA) {
+            const int b = hb * 16 + e;
             if (b < nb) {
               const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * p.dv + vb * VR + i_row;
-              if (p.delta_dump) p.delta_dump[goff] = delta;
-              if (p.o_dump) p.o_dump[goff] = o;
-              if (p.x_inout) p.x_inout[goff] += o;
+              if (p.delta_dump) p.delta_dump[goff] = dl[e];
+              if (p.o_dump) p.o_dump[goff] = ol[e];
+              if (p.x_inout) p.x_inout[goff] += ol[e];
             }
           }
         }
