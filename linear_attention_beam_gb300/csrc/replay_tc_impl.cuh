@@ -546,13 +546,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e) {
           *reinterpret_cast<__nv_bfloat16*>(os + e * 64) = __float2bfloat16_rn(dl[e]);
           *reinterpret_cast<__nv_bfloat16*>(os + OUT_WARP / 2 + e * 64) = __float2bfloat16_rn(ol[e]);
-          if constexpr (EXTRA) {
-            const int b = hb * 16 + e;
-            if (b < nb) {
-              const size_t goff = (((size_t)r * p.W_t + b0 + b) * p.H + h) * p.dv + vb * VR + i_row;
-              if (p.delta_dump) p.delta_dump[goff] = dl[e];
-              if (p.o_dump) p.o_dump[goff] = ol[e];
-              if (p.x_inout) p.x_inout[goff] += ol[e];
+        }
+        if constexpr (EXTRA) {
+          // the residual stream's 16 values are read before any is written,
+          // so the loads are not serialised behind the stores
+          auto goff = [&](int e) {
+            return (((size_t)r * p.W_t + b0 + hb * 16 + e) * p.H + h) * p.dv + vb * VR + i_row;
+          };
+          if (p.x_inout) {
+            float xr[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) xr[e] = hb * 16 + e < nb ? p.x_inout[goff(e)] : 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (hb * 16 + e < nb) p.x_inout[goff(e)] = xr[e] + ol[e];
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            if (hb * 16 + e < nb) {
+              if (p.delta_dump) p.delta_dump[goff(e)] = dl[e];
+              if (p.o_dump) p.o_dump[goff(e)] = ol[e];
             }
           }
         }
