@@ -16,10 +16,17 @@
 //   final   exact top-W of the buffer by radix search on the keys, sorted.
 // If the buffer holds at least W candidates, every candidate left out scores
 // below the W-th largest kept one, so the result is exact whatever tau was.
-// Otherwise (or if the buffer overflows) the request falls back to the two
-// exact stages of RecoGEM §4.3: a per-row precut to the local top-K
-// (K = min(W, V)), then a request-level selection among the survivors; a
-// candidate the precut drops is beaten by K candidates of its own row.
+// tau is the score of a real candidate, so at least W candidates reach it and
+// the W best all lie in listed tiles. When more candidates reach tau than the
+// buffer holds (scores dominated by a few parents, every code of whose rows
+// clears the bound), the final kernel narrows the bound over the listed
+// tiles' codes by an 11-bit radix histogram of the 32-bit score keys until
+// the codes reaching it fit, then refills the buffer: still exact.
+// A request that cannot be narrowed (more candidates tie at one score than
+// the buffer holds) falls back to the two exact stages of RecoGEM §4.3: a
+// per-row precut to the local top-K (K = min(W, V)), then a request-level
+// selection among the survivors; a candidate the precut drops is beaten by K
+// candidates of its own row.
 //
 // Ancestry (OneLA §2.4 eq. 9): each child copies its parent's slot list and
 // appends the parent's row as the slot of the previous depth.
@@ -171,19 +178,19 @@ struct SelScratch {
   int* tcount;      // [R] (row, tile) pairs whose tile maximum reaches the bound
   uint32_t* tlist;  // [R][cap_tiles] those pairs, as b * n_tiles + tile
   float* cut;       // [R*W_t] per row the smallest stored logit whose score reaches the bound
+  uint32_t* hmax;   // [R] the largest tile-maximum score key (the request's best score)
   int cap;
   int cap_tiles;
 };
 
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Room for the listed tiles of one request: the bound keeps at least W_next
-// tiles (ties at the bound add more); a longer list sends the request to the
-// exact fallback.
+// Room for the listed tiles of one request: every (row, tile) pair, so the
+// list never overflows and always holds every tile that can hold one of the
+// W best (4 bytes per pair, 1/128 of the bf16 logits).
 int cap_tiles_of(int W_t, int W_next, int V) {
-  const long long n_h = (long long)W_t * ((V + kTile - 1) / kTile);
-  long long c = 2LL * W_next + 256;
-  return (int)(c < n_h ? c : n_h);
+  (void)W_next;
+  return W_t * ((V + kTile - 1) / kTile);
 }
 
 int cap_of(int W_t, int W_next, int V) {
@@ -212,6 +219,7 @@ SelScratch carve_sel(void* base, int R, int W_t, int W_next, int V, size_t* tota
   s.tcount = (int*)take((size_t)R * 4);
   s.tlist = (uint32_t*)take((size_t)R * s.cap_tiles * 4);
   s.cut = (float*)take((size_t)R * W_t * 4);
+  s.hmax = (uint32_t*)take((size_t)R * 4);
   if (total) *total = off;
   return s;
 }
@@ -251,11 +259,13 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
   __shared__ unsigned hist[256];
   __shared__ unsigned sh[3];
   __shared__ int s_cnt;
+  __shared__ unsigned s_max;
   const int r = blockIdx.x;
   const int n_h = W_t * n_tiles;
   if (threadIdx.x == 0) {
     ss.count[r] = 0;
     s_cnt = 0;
+    s_max = 0u;
     if (r == 0) *ss.fb_any = 0;
   }
   // a row whose lse or cumulative score is not finite is flagged
@@ -298,15 +308,45 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
   }
   __syncthreads();
   uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
+  unsigned my_max = 0u;
   for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
-    const bool take = t == 0u || (on_chip ? hkeys[i] : key_of(i)) >= t;
-    if (take) {
+    const uint32_t key = on_chip ? hkeys[i] : key_of(i);
+    my_max = max(my_max, key);
+    if (key >= t) {
       const int pos = atomicAdd(&s_cnt, 1);
       if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
     }
   }
+  for (int o = 16; o > 0; o >>= 1) my_max = max(my_max, __shfl_xor_sync(0xffffffffu, my_max, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(&s_max, my_max);
   __syncthreads();
-  if (threadIdx.x == 0) ss.tcount[r] = s_cnt;
+  if (threadIdx.x == 0) {
+    ss.tcount[r] = s_cnt;
+    ss.hmax[r] = s_max;
+  }
+}
+
+// Loads the eight codes v0 .. v0+7 of row zr into zv (NaN past V).
+template <typename T>
+__device__ __forceinline__ void load_codes(const T* __restrict__ zr, int v0, int V, bool vec,
+                                           float (&zv)[kTile / 32]) {
+  constexpr int EPL = kTile / 32;
+  if (vec && v0 + EPL <= V) {
+    if constexpr (sizeof(T) == 2) {
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(zr + v0));
+      const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) zv[e] = __uint_as_float(((wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+    } else {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(zr + v0));
+      const float4 c = __ldg(reinterpret_cast<const float4*>(zr + v0 + 4));
+      zv[0] = a.x; zv[1] = a.y; zv[2] = a.z; zv[3] = a.w;
+      zv[4] = c.x; zv[5] = c.y; zv[6] = c.z; zv[7] = c.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) zv[e] = v0 + e < V ? ldf(zr + v0 + e) : __int_as_float(0x7FC00000);
+  }
 }
 
 // ---- filter: append every code of the listed tiles whose score reaches the
@@ -334,24 +374,8 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
     const float cp = cum_prime(cum, bias, row), l = lse[row];
     const float thr = ss.cut[row];  // NaN when no code can qualify
     const int v0 = tile * kTile + lane * EPL;
-    const T* zr = z + row * (size_t)V;
     float zv[EPL];
-    if (vec && v0 + EPL <= V) {
-      if constexpr (sizeof(T) == 2) {
-        const uint4 x = __ldg(reinterpret_cast<const uint4*>(zr + v0));
-        const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) zv[e] = __uint_as_float(((wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
-      } else {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(zr + v0));
-        const float4 c = __ldg(reinterpret_cast<const float4*>(zr + v0 + 4));
-        zv[0] = a.x; zv[1] = a.y; zv[2] = a.z; zv[3] = a.w;
-        zv[4] = c.x; zv[5] = c.y; zv[6] = c.z; zv[7] = c.w;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) zv[e] = v0 + e < V ? ldf(zr + v0 + e) : __int_as_float(0x7FC00000);
-    }
+    load_codes<T>(z + row * (size_t)V, v0, V, vec, zv);
     unsigned hits = 0;
 #pragma unroll
     for (int e = 0; e < EPL; ++e)
@@ -381,16 +405,179 @@ __global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
   }
 }
 
+// Visits the listed tiles of request r with the whole block, one warp per
+// tile. Every lane of the warp calls f(hits, o, flat0): hits masks the lane's
+// eight codes whose stored value reaches the row's cutoff, o holds their
+// score keys (other entries are 0) and flat0 is the flat index of code 0.
+template <typename T, typename F>
+__device__ __forceinline__ void for_listed_codes(int r, int W_t, int V, int n_tiles, int n_list,
+                                                 const T* __restrict__ z, const float* __restrict__ lse,
+                                                 const float* __restrict__ cum,
+                                                 const float* __restrict__ bias, const SelScratch& ss,
+                                                 F&& f) {
+  constexpr int EPL = kTile / 32;
+  const int lane = threadIdx.x & 31;
+  const uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
+  const bool vec = (V % 8) == 0 && ((uintptr_t)z & 15) == 0;
+  for (int j = threadIdx.x >> 5; j < n_list; j += blockDim.x >> 5) {
+    const uint32_t i = list[j];
+    const int b = (int)(i / (uint32_t)n_tiles), tile = (int)(i % (uint32_t)n_tiles);
+    const size_t row = (size_t)r * W_t + b;
+    const int v0 = tile * kTile + lane * EPL;
+    float zv[EPL];
+    load_codes<T>(z + row * (size_t)V, v0, V, vec, zv);
+    const float thr = ss.cut[row];
+    unsigned hits = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e)
+      if (zv[e] >= thr) hits |= 1u << e;
+    uint32_t o[EPL];
+    const float cp = cum_prime(cum, bias, row), l = lse[row];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = (hits >> e) & 1u ? orderable(score(cp, zv[e], l)) : 0u;
+    f(hits, o, (uint32_t)b * (uint32_t)V + (uint32_t)v0);
+  }
+}
+
+// ---- refine: more codes reach the bound than the buffer holds. Narrows the
+// bound t over the listed codes until at most `target` codes reach it (and
+// still at least W_next), then writes those codes' keys to keys[]. Each
+// round histograms the score keys inside the window [lo, hi] on the 11 bits
+// below the highest bit where lo and hi differ, counts the codes above hi,
+// and keeps the bin holding the W_next-th largest. Returns the number of
+// keys written, or -1 when the codes tying at one score are too many.
+constexpr int kRefineBins = 2048;
+static_assert(kRefineBins * 4 <= kFinalSmemKeys * 8, "the bins live in the final block's key area");
+
+template <typename T>
+__device__ int refine_bound(int r, int W_t, int V, int n_tiles, int W_next, int target,
+                            const T* __restrict__ z, const float* __restrict__ lse,
+                            const float* __restrict__ cum, const float* __restrict__ bias,
+                            const SelScratch& ss, uint64_t* keys) {
+  __shared__ unsigned s_above, s_cnt, s_res[4];
+  uint32_t* bins = reinterpret_cast<uint32_t*>(keys);
+  const int n_list = min(ss.tcount[r], ss.cap_tiles);
+  const int lane = threadIdx.x & 31;
+  uint32_t lo = ss.thr[r], hi = ss.hmax[r];
+  bool fit = false;
+  for (int round = 0; round < 8 && lo <= hi; ++round) {
+    const int p = lo == hi ? 0 : 31 - __clz(lo ^ hi);
+    const int shift = p >= 10 ? p - 10 : 0;
+    const uint32_t base = lo >> shift;  // (hi >> shift) - base < kRefineBins
+    for (int i = threadIdx.x; i < kRefineBins; i += blockDim.x) bins[i] = 0u;
+    if (threadIdx.x == 0) s_above = 0u;
+    __syncthreads();
+    for_listed_codes<T>(r, W_t, V, n_tiles, n_list, z, lse, cum, bias, ss,
+                        [&](unsigned hits, const uint32_t (&o)[kTile / 32], uint32_t) {
+      unsigned over = 0;
+#pragma unroll
+      for (int e = 0; e < kTile / 32; ++e) {
+        if (!((hits >> e) & 1u)) continue;
+        if (o[e] > hi) ++over;
+        else if (o[e] >= lo) atomicAdd(&bins[(o[e] >> shift) - base], 1u);
+      }
+      over = __reduce_add_sync(0xffffffffu, over);
+      if (lane == 0 && over) atomicAdd(&s_above, over);
+    });
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // highest bin d whose count from the top of the window reaches the
+      // remaining rank; lane l owns bins 2047 - 64 l - k, k = 0..63
+      const unsigned above = s_above;
+      const unsigned remaining = above < (unsigned)W_next ? (unsigned)W_next - above : 0u;
+      unsigned tot = 0;
+      for (int k = 0; k < 64; ++k) tot += bins[kRefineBins - 1 - 64 * lane - ((k + lane) & 63)];
+      unsigned incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned excl = incl - tot;
+      const unsigned hit = __ballot_sync(0xffffffffu, remaining > 0 && excl < remaining && incl >= remaining);
+      if (lane == 0) s_res[3] = hit ? 1u : 0u;
+      if (hit && lane == __ffs(hit) - 1) {
+        unsigned acc = excl;
+        for (int k = 0; k < 64; ++k) {
+          const int bin = kRefineBins - 1 - 64 * lane - k;
+          const unsigned c = bins[bin];
+          if (acc + c >= remaining) {
+            s_res[0] = (unsigned)bin;
+            s_res[1] = acc;  // codes of the window above bin
+            s_res[2] = c;
+            break;
+          }
+          acc += c;
+        }
+      }
+    }
+    __syncthreads();
+    if (!s_res[3]) return -1;  // fewer than W_next codes reach lo: bound inconsistent
+    const uint32_t d = s_res[0];
+    const unsigned total = s_above + s_res[1] + s_res[2];
+    const uint32_t blo = max(lo, (uint32_t)((uint64_t)(base + d) << shift));
+    const uint32_t bhi = min(hi, (uint32_t)(((uint64_t)(base + d + 1) << shift) - 1));
+    __syncthreads();  // everyone has read s_res and the bins
+    lo = blo;
+    if (total <= (unsigned)target) {
+      fit = true;
+      break;
+    }
+    if (blo == bhi) return -1;  // more codes tie at one score than fit
+    hi = bhi;
+  }
+  if (!fit) return -1;
+  // every listed code with key >= lo, as a 64-bit selection key
+  if (threadIdx.x == 0) s_cnt = 0u;
+  __syncthreads();
+  for_listed_codes<T>(r, W_t, V, n_tiles, n_list, z, lse, cum, bias, ss,
+                      [&](unsigned hits, const uint32_t (&o)[kTile / 32], uint32_t flat0) {
+    unsigned keep = 0;
+#pragma unroll
+    for (int e = 0; e < kTile / 32; ++e)
+      if (((hits >> e) & 1u) && o[e] >= lo) keep |= 1u << e;
+    const int mine = __popc(keep);
+    int incl = mine;
+#pragma unroll
+    for (int q = 1; q < 32; q <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, q);
+      if (lane >= q) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    unsigned pos = 0;
+    if (lane == 31 && total) pos = atomicAdd(&s_cnt, (unsigned)total);
+    pos = __shfl_sync(0xffffffffu, pos, 31) + (unsigned)(incl - mine);
+#pragma unroll
+    for (int e = 0; e < kTile / 32; ++e) {
+      if ((keep >> e) & 1u) {
+        if (pos < (unsigned)target) keys[pos] = make_key(o[e], flat0 + (uint32_t)e);
+        ++pos;
+      }
+    }
+  });
+  __syncthreads();
+  const unsigned n = s_cnt;
+  return n >= (unsigned)W_next && n <= (unsigned)target ? (int)n : -1;
+}
+
 // ---- final: exact top-W_next of the filtered candidates, sorted
+template <typename T>
 __global__ void __launch_bounds__(kFinalThreads) select_final_kernel(
-    int V, int W_next, SelScratch ss, int32_t* __restrict__ parents, int32_t* __restrict__ tokens,
-    float* __restrict__ cum_next) {
+    int W_t, int V, int n_tiles, int W_next, const T* __restrict__ z, const float* __restrict__ lse,
+    const float* __restrict__ cum, const float* __restrict__ bias, SelScratch ss,
+    int32_t* __restrict__ parents, int32_t* __restrict__ tokens, float* __restrict__ cum_next) {
   extern __shared__ uint64_t keys[];  // [kFinalSmemKeys]
   __shared__ unsigned hist[256];
   __shared__ unsigned sh[4];
   __shared__ uint64_t win[kMaxSort];
   const int r = blockIdx.x;
-  const int n_c = ss.count[r];
+  int n_c = ss.count[r];
+  bool on_chip = false;
+  if (n_c >= W_next && ss.tcount[r] <= ss.cap_tiles && n_c > ss.cap) {
+    n_c = refine_bound<T>(r, W_t, V, n_tiles, W_next, min(ss.cap, kFinalSmemKeys), z, lse, cum,
+                          bias, ss, keys);
+    on_chip = true;
+  }
   if (n_c < W_next || n_c > ss.cap || ss.tcount[r] > ss.cap_tiles) {
     if (threadIdx.x == 0) {
       ss.fb_flag[r] = 1;
@@ -400,8 +587,8 @@ __global__ void __launch_bounds__(kFinalThreads) select_final_kernel(
   }
   if (threadIdx.x == 0) ss.fb_flag[r] = 0;
   const uint64_t* c = ss.cand + (size_t)r * ss.cap;
-  const bool on_chip = n_c <= kFinalSmemKeys;
-  if (on_chip) {
+  if (!on_chip && n_c <= kFinalSmemKeys) {
+    on_chip = true;
     for (int i = threadIdx.x; i < n_c; i += blockDim.x) keys[i] = c[i];
     __syncthreads();
   }
@@ -560,9 +747,10 @@ int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, 
   GDN_LAUNCH_CHECK();
   // final
   const size_t fin_smem = (size_t)kFinalSmemKeys * 8;
-  GDN_CUDA(cudaFuncSetAttribute(select_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  GDN_CUDA(cudaFuncSetAttribute(select_final_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)fin_smem));
-  select_final_kernel<<<R, kFinalThreads, fin_smem, s>>>(V, W_next, ss, parents, tokens, cum_next);
+  select_final_kernel<T><<<R, kFinalThreads, fin_smem, s>>>(W_t, V, n_tiles, W_next, z, lse, cum,
+                                                            bias, ss, parents, tokens, cum_next);
   GDN_LAUNCH_CHECK();
   // exact fallback for requests whose buffer was short or overflowed
   const size_t row_smem = (size_t)V * 8;

@@ -403,6 +403,42 @@ def test_select_massive_ties_take_the_exact_fallback(dtype):
         np.testing.assert_array_equal(tok[r].cpu().numpy(), [0, 1, 2, 3, 4])
 
 
+@pytest.mark.parametrize("R,W_t,W_next,V,dtype,z_std,b_std,spike", [
+    (3, 300, 64, 2000, "bf16", 0.05, 3.0, None),    # ragged last tile, many stored-value ties
+    (2, 77, 200, 513, "f32", 0.01, 2.0, None),      # nearly every tile listed
+    (2, 1024, 1024, 8192, "bf16", 1.0, 2.0, None),  # the skewed workload's selection shape
+    (2, 200, 64, 1000, "f32", 0.01, 0.01, 20.0),    # one far outlier: two narrowing rounds
+    (2, 300, 64, 2000, "bf16", 0.01, 0.01, 20.0),
+])
+def test_select_parent_dominated_scores_narrow_the_bound(R, W_t, W_next, V, dtype, z_std, b_std, spike):
+    # per-parent score offsets much wider than the logit spread: whole rows of
+    # the best parents clear the tile-maximum bound, far more candidates than
+    # the buffer holds, and the selection must narrow the bound and stay exact
+    rng = np.random.default_rng(W_t + V)
+    z = synth.to_storage(rng.standard_normal((R, W_t, V)).astype(np.float32) * z_std, dtype)
+    if spike is not None:
+        z[:, 0, 0] = spike  # the best score sits far above the crowd at the bound
+    lse = np.stack([oracle.log_normalizer(z[r]) for r in range(R)]).astype(np.float32)
+    cum = np.sort(rng.standard_normal((R, W_t)).astype(np.float32) * 0.5)[:, ::-1].copy()
+    bias = (rng.standard_normal((R, W_t)) * b_std).astype(np.float32)
+    lib = gb.load()
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    scratch = torch.empty(lib.gdnbeam_select_scratch_bytes(R, W_t, W_next, V), dtype=torch.uint8, device=DEV)
+    par = torch.empty(R, W_next, dtype=torch.int32, device=DEV)
+    tok = torch.empty_like(par)
+    cn = torch.empty(R, W_next, device=DEV)
+    assert lib.gdnbeam_select_topw(R, W_t, W_next, V, gb.BF16 if dtype == "bf16" else gb.F32,
+                                   gb.ptr(to_dev(z.reshape(R * W_t, V), td)), gb.ptr(to_dev(lse)),
+                                   gb.ptr(to_dev(cum)), gb.ptr(to_dev(bias)), gb.ptr(par), gb.ptr(tok),
+                                   gb.ptr(cn), gb.ptr(scratch), scratch.numel(), None) == 0
+    assert device_status_clear() == 0
+    for r in range(R):
+        p, t, s = oracle.select_top(z[r], lse[r], cum[r], W_next, bias[r])
+        np.testing.assert_array_equal(par[r].cpu().numpy(), p)
+        np.testing.assert_array_equal(tok[r].cpu().numpy(), t)
+        np.testing.assert_array_equal(cn[r].cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("bad", ["nan_logit", "inf_logit", "nan_lse"])
 def test_select_flags_non_finite_inputs(dtype, bad):
