@@ -481,7 +481,8 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
       a.depth[j].W_j = ctx->W_hist[j];
     }
     a.anc = ctx->anc[cur]; a.anc_stride = c.T;
-    a.delta_out = ctx->gd(layer, t); a.o_out = ctx->o;
+    // with a residual stream o_t is only added to it (the features read x)
+    a.delta_out = ctx->gd(layer, t); a.o_out = c.residual ? nullptr : ctx->o;
     a.x_inout = c.residual ? ctx->x : nullptr;
     a.delta_dump = ld.delta; a.o_dump = ld.o;
     a.err = err;

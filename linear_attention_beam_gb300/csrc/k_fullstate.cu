@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(128) fullstate_step_kernel(FullStateArgs a) {
       *reinterpret_cast<uint4*>(rowp + ch * EPC) = out;  // each thread rewrites its own row
     }
     stf((T*)a.delta_out + gi, delta);
-    stf((T*)a.o_out + gi, o);
+    if (a.o_out) stf((T*)a.o_out + gi, o);
     if (a.delta_dump) a.delta_dump[gi] = delta;
     if (a.o_dump) a.o_dump[gi] = o;
     if (a.x_inout) a.x_inout[gi] += o;
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(256, 2) replayssm_step_kernel(ReplaySsmArgs a)
     }
     if (active && part == 0) {
       stf((T*)a.delta_out + gi, delta);
-      stf((T*)a.o_out + gi, o);
+      if (a.o_out) stf((T*)a.o_out + gi, o);
       if (a.delta_dump) a.delta_dump[gi] = delta;
       if (a.o_dump) a.o_dump[gi] = o;
       if (a.x_inout) a.x_inout[gi] += o;

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) replay_simt_kernel(ReplayArgs a) {
       float delta = be * (ldf(v + off) - al * u_k);
       float o = al * u_q + delta * kq[b];
       stf((T*)a.delta_out + off, delta);
-      stf((T*)a.o_out + off, o);
+      if (a.o_out) stf((T*)a.o_out + off, o);
       if (a.delta_dump) a.delta_dump[off] = delta;
       if (a.o_dump) a.o_dump[off] = o;
       if (a.x_inout) a.x_inout[off] += o;

@@ -101,10 +101,62 @@ __global__ void rmsnorm_rows_kernel(int n, int d, const float* __restrict__ x, l
   for (int c = lane; c < d; c += 32) stf(u + (size_t)warp * d + c, row[c] * inv);
 }
 
+// Same, for d a multiple of 128 up to 2048 on 16-byte aligned rows: each
+// lane keeps its d / 32 values in registers (float4 loads), so the row is
+// read once, and writes them back packed.
+constexpr int kNormMaxVec = 16;  // float4 per lane: d <= 2048
+
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_rows_vec_kernel(int n, int nv, const float* __restrict__ x,
+                                                               long long xs, T* __restrict__ u) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= n) return;
+  const float4* row = reinterpret_cast<const float4*>(x + (size_t)warp * xs);
+  float4 v[kNormMaxVec];
+  float ss = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kNormMaxVec; ++k) {
+    if (k < nv) {
+      v[k] = __ldg(row + lane + 32 * k);
+      ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const int d = nv * 128;
+  const float inv = 1.0f / sqrtf(ss / (float)d + 1e-6f);
+#pragma unroll
+  for (int k = 0; k < kNormMaxVec; ++k) {
+    if (k < nv) {
+      const size_t c = (size_t)warp * d + 4 * (lane + 32 * k);
+      if constexpr (sizeof(T) == 2) {
+        const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[k].x * inv)) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[k].y * inv)) << 16);
+        const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[k].z * inv)) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[k].w * inv)) << 16);
+        *reinterpret_cast<uint2*>(u + c) = make_uint2(lo, hi);
+      } else {
+        *reinterpret_cast<float4*>(u + c) =
+            make_float4(v[k].x * inv, v[k].y * inv, v[k].z * inv, v[k].w * inv);
+      }
+    }
+  }
+}
+
 int launch_rmsnorm_rows(int dtype, int n, int d, const float* x, long long xs, void* u,
                         cudaStream_t s) {
   if (n <= 0) return GDNBEAM_OK;
   int blocks = (n + 7) / 8;
+  if (d % 128 == 0 && d <= 128 * kNormMaxVec && xs % 4 == 0 && ((uintptr_t)x & 15) == 0 &&
+      ((uintptr_t)u & 15) == 0) {
+    if (dtype == GDNBEAM_BF16)
+      rmsnorm_rows_vec_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(n, d / 128, x, xs,
+                                                                    (__nv_bfloat16*)u);
+    else
+      rmsnorm_rows_vec_kernel<float><<<blocks, 256, 0, s>>>(n, d / 128, x, xs, (float*)u);
+    GDN_LAUNCH_CHECK();
+    return GDNBEAM_OK;
+  }
   if (dtype == GDNBEAM_BF16)
     rmsnorm_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(n, d, x, xs, (__nv_bfloat16*)u);
   else

@@ -68,7 +68,7 @@ struct ReplayArgs {
   gdnbeam_records depth[GDNBEAM_MAX_T];
   const int32_t* anc;
   int anc_stride;
-  void *delta_out, *o_out;
+  void *delta_out, *o_out;  // o_out may be null when x_inout takes o_t
   float* x_inout;
   float *delta_dump, *o_dump;
   unsigned* err;
@@ -88,7 +88,7 @@ struct FullStateArgs {
   const int32_t* parents;      // [R*W_t] rows of the previous call (t >= 1)
   const void *q, *k, *v;
   const float *alpha, *beta;
-  void *delta_out, *o_out;
+  void *delta_out, *o_out;     // o_out may be null when x_inout takes o_t
   float* x_inout;
   float *delta_dump, *o_dump;
   unsigned* err;
@@ -107,7 +107,7 @@ struct ReplaySsmArgs {
   gdnbeam_records depth[GDNBEAM_MAX_T];
   const int32_t* anc;
   int anc_stride;
-  void *delta_out, *o_out;
+  void *delta_out, *o_out;     // o_out may be null when x_inout takes o_t
   float* x_inout;
   float *delta_dump, *o_dump;
   unsigned* err;

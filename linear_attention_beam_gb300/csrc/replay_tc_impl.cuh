@@ -87,6 +87,7 @@ struct TcReplayParams {
   int W_j[kMaxDepth];
   const int32_t* anc;
   int anc_stride;
+  int store_o;  // 0: o_t goes only to x_inout and the dumps
   float* x_inout;
   float *delta_dump, *o_dump;
   unsigned* err;
@@ -576,7 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (hb * 16 < nb) {
             const uint32_t ob = tc::smem_u32(&s_out[sb][(hb * 4 + lg) * OUT_WARP]);
             tc::tma_store_3d(&tm_d, h * p.dv + vb * VR + lg * 32, b0 + hb * 16, r, ob);
-            tc::tma_store_3d(&tm_o, h * p.dv + vb * VR + lg * 32, b0 + hb * 16, r, ob + OUT_WARP / 2);
+            if (p.store_o)
+              tc::tma_store_3d(&tm_o, h * p.dv + vb * VR + lg * 32, b0 + hb * 16, r, ob + OUT_WARP / 2);
           }
           tc::bulk_commit();
         }
@@ -698,13 +700,15 @@ int launch_tc_replay_dk(const ReplayArgs& a, cudaStream_t s) {
   }
   p.anc = a.anc; p.anc_stride = a.anc_stride;
   p.x_inout = a.x_inout; p.delta_dump = a.delta_dump; p.o_dump = a.o_dump; p.err = a.err;
+  p.store_o = a.o_out != nullptr;
+  if (!a.o_out && !a.x_inout) return GDNBEAM_EINVAL;
   if (((uintptr_t)a.sctx & 15) || (a.sctx_rstride % 4) != 0) return GDNBEAM_EINVAL;
   CUtensorMap mq, mk, mv, md, mo;
   const int kw = a.Hk * DK, vw = a.H * a.d_v;
   if (!beam_map(&mq, a.q, a.R, a.W_t, kw, true) || !beam_map(&mk, a.k, a.R, a.W_t, kw, true) ||
       !beam_map(&mv, a.v, a.R, a.W_t, vw, false) ||
       !beam_map(&md, a.delta_out, a.R, a.W_t, vw, false, 32, 16) ||
-      !beam_map(&mo, a.o_out, a.R, a.W_t, vw, false, 32, 16))
+      !beam_map(&mo, a.o_out ? a.o_out : a.delta_out, a.R, a.W_t, vw, false, 32, 16))
     return GDNBEAM_ECUDA;
   const size_t dyn = 1024 + (size_t)p.stages * p.stage_bytes + table;
   const bool extra = a.delta_dump || a.o_dump || a.x_inout;

@@ -35,3 +35,12 @@ def test_replay_bytes_of_the_batched_depth_two_call():
     # grouped key heads read one key row per key head
     assert (bench.replay_bytes(1, 1, 16, 4, 128, 128, 0, 2)
             == 2 * 4 * 128 * 2 + 16 * 128 * 2 + 2 * 16 * 4 + 2 * 16 * 128 * 2 + 16 * 128 * 128 * 4)
+
+
+def test_replay_bytes_with_a_residual_stream():
+    # stacked layers: delta_t is stored (bf16) but o_t only updates the fp32
+    # residual row, read and written: 8 heads x 128 values x (2 + 4 + 4) bytes
+    # in place of delta_t and o_t's 2 x 2 bytes
+    plain = bench.replay_bytes(32, 1024, 8, 8, 128, 128, 1, 2)
+    resid = bench.replay_bytes(32, 1024, 8, 8, 128, 128, 1, 2, residual=True)
+    assert resid - plain == 32 * 1024 * 8 * 128 * (10 - 4)
