@@ -5,8 +5,8 @@
 //   * codebook logits Z = F . W_o^T, with the bf16 store of z and per-tile
 //     (max, sum exp) partials of the row log-normaliser fused in.
 //
-// Persistent CTAs in clusters of two, one CTA per SM, 192 threads in three
-// roles. The two CTAs of a cluster take vertically adjacent tiles (m, n) and
+// Persistent CTAs in clusters of two, one CTA per SM, 192 (projections) or
+// 320 (logits) threads in three roles. The two CTAs of a cluster take vertically adjacent tiles (m, n) and
 // (m + 1, n) in lockstep and share the B tile: each loads its own A tile and
 // one 128-row half of B, multicast into both CTAs, so B leaves L2 once per
 // pair of tiles.
@@ -17,7 +17,7 @@
 //               of the current tile, committing each stage back to the
 //               producers of both CTAs and each finished tile to the epilogue;
 //   warps 2-5   read the accumulator rows out of TMEM (lane = tile row) and
-//               run the fused epilogue while the next tile accumulates into
+//   (2-9)       run the fused epilogue while the next tile accumulates into
 //               the other TMEM buffer.
 // Every mbarrier wait is bounded in time; on a time-out the kernel raises
 // GDNBEAM_DERR_TIMEOUT, all roles leave their loops, in-flight copies and
@@ -37,12 +37,20 @@ constexpr int CLUSTER = 2;  // CTAs sharing a B tile
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kNumBars = 2 * STAGES + 4 + 1;
 constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + 1024 + kNumBars * 8 + 16;
 
 enum { EPI_LOGITS = 0, EPI_PROJ = 1 };
+
+// Epilogue warps: one per TMEM lane group for the projections, whose
+// epilogue hides under the tile's MMAs; two for the logits, each taking half
+// the columns, since 256 exponentials per row outlast the MMAs of a short-K
+// tile (d_model = 1024).
+template <int EPI> struct Epi {
+  static constexpr int kWarps = EPI == EPI_LOGITS ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kWarps;
+};
 
 struct EpiArgs {
   int M, N, K;
@@ -79,14 +87,14 @@ __device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32]) {
   for (int w = 0; w < 8; ++w) d4[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
 }
 
-// Logits epilogue for one tile row: bf16 z, optional fp32 dump, and the
-// row's (max, sum exp) over this tile's columns.
-__device__ __forceinline__ void epi_logits(const EpiArgs& ea, uint32_t taddr, int m, int n0,
-                                           int n_tile, int n_tiles) {
+// Logits epilogue for one tile row and one half of the tile's columns: bf16
+// z, optional fp32 dump, and the half row's (max, sum exp), returned.
+__device__ __forceinline__ float2 epi_logits(const EpiArgs& ea, uint32_t taddr, int m, int n0,
+                                             int half) {
   float run_max = -INFINITY, run_sum = 0.0f;
   const bool row_ok = m < ea.M;
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
     float v[32];
     tc::tmem_ld32(taddr + c * 32, v);
     const int n = n0 + c * 32;
@@ -114,17 +122,17 @@ __device__ __forceinline__ void epi_logits(const EpiArgs& ea, uint32_t taddr, in
     run_sum = s;
     run_max = nm;
   }
-  if (row_ok) ea.part[(size_t)m * n_tiles + n_tile] = make_float2(run_max, run_sum);
+  return make_float2(run_max, run_sum);
 }
 
-// Projection epilogue for one tile row; head width 128, tile of two heads.
-__device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int m, int n0) {
+// Projection epilogue for one tile row and one of the tile's two heads
+// (head width 128).
+__device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int m, int n0, int g) {
   const int H = ea.H, Hk = ea.Hk, D = 128;
   const bool row_ok = m < ea.M;
   const int q_end = Hk * D, k_end = 2 * Hk * D, v_end = k_end + H * D;
-#pragma unroll 1
-  for (int g = 0; g < BN / D; ++g) {
-    if (n0 + g * D >= ea.N) break;
+  {
+    if (n0 + g * D >= ea.N) return;
     const int col0 = n0 + g * D + ea.col_off;  // column of the full projection
     const uint32_t ta = taddr + g * D;
     if (col0 < k_end) {
@@ -191,7 +199,7 @@ __device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int 
 }
 
 template <int EPI>
-__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    EpiArgs ea) {
   extern __shared__ uint8_t smem_raw[];
@@ -226,7 +234,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull(a), 1);
-      tc::mbar_init(tempty(a), 4);
+      tc::mbar_init(tempty(a), Epi<EPI>::kWarps);
     }
     tc::mbar_init(drain_bar, 1);
     *abort = 0;
@@ -305,22 +313,47 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(kThreads, 1)
       tc::mbar_wait_drain(drain_bar, 0);
     }
   } else {
-    const int lane_grp = warp & 3;  // TMEM lanes 32*lane_grp .. +31
+    // one or two warps per TMEM lane group (lanes 32*lane_grp .. +31); with
+    // two, each takes half the tile's columns and the pair meets at named
+    // barrier 1 + lane_grp
+    constexpr bool kPairs = Epi<EPI>::kWarps == 8;
+    const int lane_grp = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int pair_bar = 1 + lane_grp;
     const int row = lane_grp * 32 + lane;
+    __shared__ float2 s_half[2][4][32];  // the second half's row partials, per accumulator
     int i = 0;
     for (int tile = cid; tile < num_tiles; tile += n_clusters, ++i) {
       const int acc = i & 1;
       const uint32_t aph = (uint32_t)(i >> 1) & 1u;
       const bool got = tc::mbar_wait(tfull(acc), aph, abort, ea.err);
-      __syncwarp();  // the TMEM loads below are warp-collective
-      if (!got) break;
+      // both warps of a pair go on only if both saw the tile, so neither
+      // waits at the pair barrier for a partner that left
+      if (kPairs) {
+        if (!tc::named_sync_and(pair_bar, 64, got)) break;
+      } else {
+        __syncwarp();  // the TMEM loads below are warp-collective
+        if (!got) break;
+      }
       tc::fence_after_sync();
       const int m_tile = 2 * (tile / n_tiles) + rank, n_tile = tile % n_tiles;
       const uint32_t taddr = tmem_base + ((uint32_t)(lane_grp * 32) << 16) + (uint32_t)(acc * BN);
-      if (EPI == EPI_LOGITS)
-        epi_logits(ea, taddr, m_tile * BM + row, n_tile * BN, n_tile, n_tiles);
-      else
-        epi_proj(ea, taddr, m_tile * BM + row, n_tile * BN);
+      const int m = m_tile * BM + row;
+      if (EPI == EPI_LOGITS) {
+        const float2 pr = epi_logits(ea, taddr, m, n_tile * BN, half);
+        if (half) s_half[acc][lane_grp][lane] = pr;
+        tc::named_sync(pair_bar, 64);
+        if (!half && m < ea.M) {
+          // merge the halves' (max, sum exp); an empty half has max -inf
+          const float2 q = s_half[acc][lane_grp][lane];
+          const float nm = fmaxf(pr.x, q.x);
+          const float sum = (pr.x == -INFINITY ? 0.0f : pr.y * expf(pr.x - nm)) +
+                            (q.x == -INFINITY ? 0.0f : q.y * expf(q.x - nm));
+          ea.part[(size_t)m * n_tiles + n_tile] = make_float2(nm, sum);
+        }
+      } else {
+        for (int g = 0; g < BN / 128; ++g) epi_proj(ea, taddr, m, n_tile * BN, g);
+      }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tempty(acc));
@@ -410,7 +443,7 @@ int max_clusters() {
   if (!cached[dev][EPI]) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CLUSTER * (num_sms() / CLUSTER), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(Epi<EPI>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -444,7 +477,7 @@ int launch_gemm(const void* A, const void* B, const EpiArgs& ea, cudaStream_t s,
   int clusters = max_clusters<EPI>();
   if (clusters <= 0) return GDNBEAM_ECUDA;
   if (clusters > pair_tiles) clusters = pair_tiles;
-  tc_gemm_kernel<EPI><<<CLUSTER * clusters, kThreads, kSmemBytes, s>>>(ta, tb, ea);
+  tc_gemm_kernel<EPI><<<CLUSTER * clusters, Epi<EPI>::kThreads, kSmemBytes, s>>>(ta, tb, ea);
   GDN_LAUNCH_CHECK();
   return GDNBEAM_OK;
 }

@@ -494,6 +494,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A failed wait marks this warp dead: it then skips all work but keeps
     // making its arrivals, so no other role waits on it forever.
     bool dead = false;
+    // residual stream element of beam e of this thread's half of tile i
+    auto goff = [&](int i, int e) {
+      return (((size_t)r * p.W_t + bb + i * NB + hb * 16 + e) * p.H + h) * p.dv + vb * VR + i_row;
+    };
+    // the residual values of a tile are loaded one tile ahead
+    float xr[EXTRA ? 16 : 1];
+    auto load_x = [&](int i, float (&dst)[EXTRA ? 16 : 1]) {
+      if constexpr (EXTRA) {
+        const int nbi = i < nt ? min(NB, p.W_t - (bb + i * NB)) : 0;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dst[e] = hb * 16 + e < nbi ? p.x_inout[goff(i, e)] : 0.f;
+      }
+    };
+    if (EXTRA && p.x_inout) load_x(0, xr);
     for (int i = 0; i < nt; ++i) {
       const int s = i % p.stages;
       const int acc = i & 1;
@@ -501,6 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sb = i & 1;
       const int b0 = bb + i * NB;
       const int nb = min(NB, p.W_t - b0);
+      float xn[EXTRA ? 16 : 1];
+      if (EXTRA && p.x_inout) load_x(i + 1, xn);
       if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(sfull(sb), aph, abort, p.err));
       if (!dead) dead = __any_sync(0xffffffffu, !tc::mbar_wait_sleep(tfull(acc), aph, abort, p.err));
       if (!dead) {
@@ -549,24 +565,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<__nv_bfloat16*>(os + OUT_WARP / 2 + e * 64) = __float2bfloat16_rn(ol[e]);
         }
         if constexpr (EXTRA) {
-          // the residual stream's 16 values are read before any is written,
-          // so the loads are not serialised behind the stores
-          auto goff = [&](int e) {
-            return (((size_t)r * p.W_t + b0 + hb * 16 + e) * p.H + h) * p.dv + vb * VR + i_row;
-          };
           if (p.x_inout) {
-            float xr[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) xr[e] = hb * 16 + e < nb ? p.x_inout[goff(e)] : 0.f;
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              if (hb * 16 + e < nb) p.x_inout[goff(e)] = xr[e] + ol[e];
+              if (hb * 16 + e < nb) p.x_inout[goff(i, e)] = xr[e] + ol[e];
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             if (hb * 16 + e < nb) {
-              if (p.delta_dump) p.delta_dump[goff(e)] = dl[e];
-              if (p.o_dump) p.o_dump[goff(e)] = ol[e];
+              if (p.delta_dump) p.delta_dump[goff(i, e)] = dl[e];
+              if (p.o_dump) p.o_dump[goff(i, e)] = ol[e];
             }
           }
         }
@@ -588,6 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         tc::mbar_arrive(sempty(sb));
         tc::mbar_arrive(empty(s));
+      }
+      if constexpr (EXTRA) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) xr[e] = xn[e];
       }
     }
     if (lane == 0) tc::bulk_wait_all();

@@ -389,6 +389,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// The same barrier, returning whether pred held in every participating thread.
+__device__ __forceinline__ bool named_sync_and(int id, int nthreads, bool pred) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.s32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((int)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
 
 }  // namespace tc
 }  // namespace gdnbeam
