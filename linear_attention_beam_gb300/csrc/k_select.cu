@@ -8,25 +8,26 @@
 // (2^32 - 1 - flat) in the low word, so larger keys rank first and keys are
 // unique within a request.
 //
-// Fast path (one read of the logits):
-//   bound   per request, the scores of one real candidate per (row, 256-code
-//           tile) — the tile maximum, which the logits GEMM already produces
-//           for the log-normaliser — and the W-th largest of them, tau;
-//   filter  every candidate with s >= tau is appended to the request's buffer;
-//   final   exact top-W of the buffer by radix search on the keys, sorted.
-// If the buffer holds at least W candidates, every candidate left out scores
-// below the W-th largest kept one, so the result is exact whatever tau was.
+// Fast path, one block per request (a read of only the listed logit tiles):
+//   bound   the scores of one real candidate per (row, 256-code tile) — the
+//           tile maximum, which the logits GEMM already produces for the
+//           log-normaliser — and the W-th largest of them, tau; the tiles
+//           whose maximum reaches tau are listed;
+//   filter  every code of the listed tiles with s >= tau is kept on chip;
+//   select  exact top-W of the kept codes by radix search on the keys, sorted.
+// If at least W candidates are kept, every candidate left out scores below
+// the W-th largest kept one, so the result is exact whatever tau was.
 // tau is the score of a real candidate, so at least W candidates reach it and
-// the W best all lie in listed tiles. When more candidates reach tau than the
-// buffer holds (scores dominated by a few parents, every code of whose rows
-// clears the bound), the final kernel narrows the bound over the listed
-// tiles' codes by an 11-bit radix histogram of the 32-bit score keys until
-// the codes reaching it fit, then refills the buffer: still exact.
+// the W best all lie in listed tiles. When more candidates reach tau than fit
+// on chip (scores dominated by a few parents, every code of whose rows clears
+// the bound), the bound is narrowed over the listed tiles' codes by an
+// 11-bit radix histogram of the 32-bit score keys until the codes reaching
+// it fit, and they are collected again: still exact.
 // A request that cannot be narrowed (more candidates tie at one score than
-// the buffer holds) falls back to the two exact stages of RecoGEM §4.3: a
-// per-row precut to the local top-K (K = min(W, V)), then a request-level
-// selection among the survivors; a candidate the precut drops is beaten by K
-// candidates of its own row.
+// fit) falls back to the two exact stages of RecoGEM §4.3: a per-row precut
+// to the local top-K (K = min(W, V)), then a request-level selection among
+// the survivors; a candidate the precut drops is beaten by K candidates of
+// its own row.
 //
 // Ancestry (OneLA §2.4 eq. 9): each child copies its parent's slot list and
 // appends the parent's row as the slot of the previous depth.
@@ -38,9 +39,6 @@ namespace gdnbeam {
 namespace {
 
 constexpr int kTile = 256;           // codes per hint tile (the logits GEMM tile width)
-constexpr int kBoundThreads = 1024;
-constexpr int kFilterThreads = 256;
-constexpr int kFilterBlocksPerReq = 32;  // 256 warps share a request's listed tiles
 constexpr int kFinalThreads = 1024;
 constexpr int kFinalSmemKeys = 16384; // candidates a final block keeps on chip
 constexpr int kRowThreads = 512;
@@ -168,18 +166,13 @@ __device__ void sort_and_emit(uint64_t* win, int P, int W_next, int V, int32_t* 
 }
 
 struct SelScratch {
-  int* count;       // [R] candidates appended by the filter
-  uint32_t* thr;    // [R] orderable score bound
   int* fb_flag;     // [R] request needs the fallback
-  int* fb_any;      // [1]
-  uint64_t* cand;   // [R][cap]
+  int* fb_any;      // [1] some request needs the fallback (reset by the fallback's last kernel)
   uint64_t* pre;    // [R*W_t][K] fallback precut keys
   float2* hint;     // [R*W_t][n_tiles] tile maxima computed here when not supplied
-  int* tcount;      // [R] (row, tile) pairs whose tile maximum reaches the bound
-  uint32_t* tlist;  // [R][cap_tiles] those pairs, as b * n_tiles + tile
+  uint32_t* tlist;  // [R][cap_tiles] (row, tile) pairs whose maximum reaches the bound, b * n_tiles + tile
   float* cut;       // [R*W_t] per row the smallest stored logit whose score reaches the bound
-  uint32_t* hmax;   // [R] the largest tile-maximum score key (the request's best score)
-  int cap;
+  int cap;          // candidates a request may keep on chip before the bound is narrowed
   int cap_tiles;
 };
 
@@ -209,17 +202,12 @@ SelScratch carve_sel(void* base, int R, int W_t, int W_next, int V, size_t* tota
   char* p = (char*)base;
   size_t off = 0;
   auto take = [&](size_t b) { char* q = p ? p + off : nullptr; off += a256(b); return q; };
-  s.count = (int*)take((size_t)R * 4);
-  s.thr = (uint32_t*)take((size_t)R * 4);
   s.fb_flag = (int*)take((size_t)R * 4);
   s.fb_any = (int*)take(16);
-  s.cand = (uint64_t*)take((size_t)R * s.cap * 8);
   s.pre = (uint64_t*)take((size_t)R * W_t * K * 8);
   s.hint = (float2*)take((size_t)R * W_t * n_tiles * sizeof(float2));
-  s.tcount = (int*)take((size_t)R * 4);
   s.tlist = (uint32_t*)take((size_t)R * s.cap_tiles * 4);
   s.cut = (float*)take((size_t)R * W_t * 4);
-  s.hmax = (uint32_t*)take((size_t)R * 4);
   if (total) *total = off;
   return s;
 }
@@ -246,27 +234,32 @@ __global__ void tile_max_kernel(int n, int V, int n_tiles, const T* __restrict__
   if (bad) raise_error(err, GDNBEAM_DERR_NONFINITE);
 }
 
-// ---- bound: the W_next-th largest hint score of each request, and the tiles
+// ---- bound: the W_next-th largest hint score of request r, and the tiles
 // that can hold a candidate. A code scores at most its tile's maximum (the
 // score is monotone in the stored logit within a row), so only tiles whose
-// maximum reaches the bound are listed for the filter.
+// maximum reaches the bound are listed. Writes ss.cut and ss.tlist of the
+// request (the list also to slist, up to slist_cap entries) and returns the
+// bound, the largest hint key and the list length (the same in every
+// thread); hkeys holds smem_keys 32-bit keys.
+struct Bound {
+  uint32_t t, hmax;
+  int n_list;
+};
+
 template <typename T>
-__global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
-    int W_t, int V, int n_tiles, int W_next, const float2* __restrict__ hint,
-    const float* __restrict__ lse, const float* __restrict__ cum, const float* __restrict__ bias,
-    SelScratch ss, int smem_keys, unsigned* err) {
-  extern __shared__ uint32_t hkeys[];
+__device__ Bound bound_phase(int r, int W_t, int V, int n_tiles, int W_next,
+                            const float2* __restrict__ hint, const float* __restrict__ lse,
+                            const float* __restrict__ cum, const float* __restrict__ bias,
+                            const SelScratch& ss, uint32_t* hkeys, int smem_keys, uint32_t* slist,
+                            int slist_cap, unsigned* err) {
   __shared__ unsigned hist[256];
   __shared__ unsigned sh[3];
   __shared__ int s_cnt;
   __shared__ unsigned s_max;
-  const int r = blockIdx.x;
   const int n_h = W_t * n_tiles;
   if (threadIdx.x == 0) {
-    ss.count[r] = 0;
     s_cnt = 0;
     s_max = 0u;
-    if (r == 0) *ss.fb_any = 0;
   }
   // a row whose lse or cumulative score is not finite is flagged
   for (int b = threadIdx.x; b < W_t; b += blockDim.x) {
@@ -283,16 +276,16 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
   };
   const bool on_chip = n_h <= smem_keys;
   uint32_t t = 0u;  // too few hints for a bound: keep every tile
-  if (W_next <= n_h) {
-    if (on_chip) {
-      for (int i = threadIdx.x; i < n_h; i += blockDim.x) hkeys[i] = key_of(i);
-      __syncthreads();
-      t = radix_kth<uint32_t>(n_h, (unsigned)W_next, [&](int i) { return hkeys[i]; }, hist, sh);
-    } else {
-      t = radix_kth<uint32_t>(n_h, (unsigned)W_next, key_of, hist, sh);
-    }
+  if (on_chip) {
+    for (int i = threadIdx.x; i < n_h; i += blockDim.x) hkeys[i] = key_of(i);
   }
-  if (threadIdx.x == 0) ss.thr[r] = t;
+  __syncthreads();
+  if (W_next <= n_h) {
+    if (on_chip)
+      t = radix_kth<uint32_t>(n_h, (unsigned)W_next, [&](int i) { return hkeys[i]; }, hist, sh);
+    else
+      t = radix_kth<uint32_t>(n_h, (unsigned)W_next, key_of, hist, sh);
+  }
   // each row's cutoff: the smallest stored value whose score reaches t, by
   // bisection over the storage keys (scores are monotone in the stored
   // value within a row); NaN when no code of the row can qualify
@@ -306,7 +299,6 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
     }
     ss.cut[row] = SKey<T>::value(lo);
   }
-  __syncthreads();
   uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
   unsigned my_max = 0u;
   for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
@@ -315,151 +307,173 @@ __global__ void __launch_bounds__(kBoundThreads) select_bound_kernel(
     if (key >= t) {
       const int pos = atomicAdd(&s_cnt, 1);
       if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
+      if (pos < slist_cap) slist[pos] = (uint32_t)i;  // the on-chip copy, when it fits
     }
   }
   for (int o = 16; o > 0; o >>= 1) my_max = max(my_max, __shfl_xor_sync(0xffffffffu, my_max, o));
   if ((threadIdx.x & 31) == 0) atomicMax(&s_max, my_max);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    ss.tcount[r] = s_cnt;
-    ss.hmax[r] = s_max;
-  }
+  __syncthreads();  // the list, the cutoffs and the counters are complete
+  return Bound{t, s_max, s_cnt};
 }
 
-// Loads the eight codes v0 .. v0+7 of row zr into zv (NaN past V).
-template <typename T>
-__device__ __forceinline__ void load_codes(const T* __restrict__ zr, int v0, int V, bool vec,
-                                           float (&zv)[kTile / 32]) {
-  constexpr int EPL = kTile / 32;
-  if (vec && v0 + EPL <= V) {
-    if constexpr (sizeof(T) == 2) {
-      const uint4 x = __ldg(reinterpret_cast<const uint4*>(zr + v0));
-      const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) zv[e] = __uint_as_float(((wd[e >> 1] >> (16 * (e & 1))) & 0xFFFFu) << 16);
+// Eight stored codes as loaded: one 16-byte word of bf16, two of fp32.
+template <typename T> struct Codes8;
+template <> struct Codes8<__nv_bfloat16> {
+  uint4 w;
+  __device__ __forceinline__ void load(const __nv_bfloat16* __restrict__ zr, int v0, int V, bool vec) {
+    if (vec && v0 + 8 <= V) {
+      w = __ldg(reinterpret_cast<const uint4*>(zr + v0));
     } else {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(zr + v0));
-      const float4 c = __ldg(reinterpret_cast<const float4*>(zr + v0 + 4));
-      zv[0] = a.x; zv[1] = a.y; zv[2] = a.z; zv[3] = a.w;
-      zv[4] = c.x; zv[5] = c.y; zv[6] = c.z; zv[7] = c.w;
-    }
-  } else {
+      uint16_t h[8];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) zv[e] = v0 + e < V ? ldf(zr + v0 + e) : __int_as_float(0x7FC00000);
-  }
-}
-
-// ---- filter: append every code of the listed tiles whose score reaches the
-// bound. One warp per listed tile (256 codes, eight per lane). Codes are
-// compared as stored values with the row's cutoff logit from the bound
-// kernel; scores are computed only for hits.
-template <typename T>
-__global__ void __launch_bounds__(kFilterThreads) select_filter_kernel(
-    int W_t, int V, int n_tiles, int blocks_per_req, const T* __restrict__ z,
-    const float* __restrict__ lse, const float* __restrict__ cum, const float* __restrict__ bias,
-    SelScratch ss) {
-  constexpr int EPL = kTile / 32;          // codes per lane
-  const int r = blockIdx.x / blocks_per_req;
-  const int lane = threadIdx.x & 31;
-  const int warps = blocks_per_req * (kFilterThreads / 32);
-  const int n_list = min(ss.tcount[r], ss.cap_tiles);
-  const uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
-  uint64_t* out = ss.cand + (size_t)r * ss.cap;
-  const bool vec = (V % 8) == 0 && ((uintptr_t)z & 15) == 0;
-  for (int j = (blockIdx.x % blocks_per_req) * (kFilterThreads / 32) + (threadIdx.x >> 5); j < n_list;
-       j += warps) {
-    const uint32_t i = list[j];
-    const int b = (int)(i / (uint32_t)n_tiles), tile = (int)(i % (uint32_t)n_tiles);
-    const size_t row = (size_t)r * W_t + b;
-    const float cp = cum_prime(cum, bias, row), l = lse[row];
-    const float thr = ss.cut[row];  // NaN when no code can qualify
-    const int v0 = tile * kTile + lane * EPL;
-    float zv[EPL];
-    load_codes<T>(z + row * (size_t)V, v0, V, vec, zv);
-    unsigned hits = 0;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e)
-      if (zv[e] >= thr) hits |= 1u << e;  // NaN never compares true
-    if (!__any_sync(0xffffffffu, hits != 0)) continue;
-    const int mine = __popc(hits);
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    int base = 0;
-    if (lane == 31) base = atomicAdd(ss.count + r, total);
-    base = __shfl_sync(0xffffffffu, base, 31);
-    int idx = base + incl - mine;
-    const uint32_t flat0 = (uint32_t)b * (uint32_t)V;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      if (hits & (1u << e)) {
-        const uint32_t o = orderable(score(cp, zv[e], l));
-        if (idx < ss.cap) out[idx] = make_key(o, flat0 + (uint32_t)(v0 + e));
-        ++idx;
-      }
+      for (int e = 0; e < 8; ++e) h[e] = v0 + e < V ? __bfloat16_as_ushort(zr[v0 + e]) : (uint16_t)0x7FC0u;
+      w = make_uint4(h[0] | (uint32_t)h[1] << 16, h[2] | (uint32_t)h[3] << 16,
+                     h[4] | (uint32_t)h[5] << 16, h[6] | (uint32_t)h[7] << 16);
     }
   }
-}
+  __device__ __forceinline__ float at(int e) const {
+    const uint32_t x = e < 2 ? w.x : e < 4 ? w.y : e < 6 ? w.z : w.w;
+    return __uint_as_float(((x >> (16 * (e & 1))) & 0xFFFFu) << 16);
+  }
+};
+template <> struct Codes8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* __restrict__ zr, int v0, int V, bool vec) {
+    if (vec && v0 + 8 <= V) {
+      a = __ldg(reinterpret_cast<const float4*>(zr + v0));
+      b = __ldg(reinterpret_cast<const float4*>(zr + v0 + 4));
+    } else {
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = v0 + e < V ? zr[v0 + e] : __int_as_float(0x7FC00000);
+      a = make_float4(f[0], f[1], f[2], f[3]);
+      b = make_float4(f[4], f[5], f[6], f[7]);
+    }
+  }
+  __device__ __forceinline__ float at(int e) const {
+    const float4& q = e < 4 ? a : b;
+    const int k = e & 3;
+    return k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w;
+  }
+};
 
-// Visits the listed tiles of request r with the whole block, one warp per
-// tile. Every lane of the warp calls f(hits, o, flat0): hits masks the lane's
-// eight codes whose stored value reaches the row's cutoff, o holds their
-// score keys (other entries are 0) and flat0 is the flat index of code 0.
+// Visits the listed tiles of request r (list: n_list entries, on chip or in
+// global memory) with the whole block, one warp per tile, several tiles per
+// warp at a time so their loads overlap. Every lane of the warp calls
+// f(hits, o, flat0): hits masks the lane's eight codes whose stored value
+// reaches the row's cutoff, o holds their score keys (other entries are 0)
+// and flat0 is the flat index of code 0.
 template <typename T, typename F>
 __device__ __forceinline__ void for_listed_codes(int r, int W_t, int V, int n_tiles, int n_list,
-                                                 const T* __restrict__ z, const float* __restrict__ lse,
+                                                 const uint32_t* list, const T* __restrict__ z,
+                                                 const float* __restrict__ lse,
                                                  const float* __restrict__ cum,
                                                  const float* __restrict__ bias, const SelScratch& ss,
                                                  F&& f) {
   constexpr int EPL = kTile / 32;
+  constexpr int U = sizeof(T) == 2 ? 4 : 2;  // tiles in flight per warp
   const int lane = threadIdx.x & 31;
-  const uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
+  const int warps = blockDim.x >> 5;
   const bool vec = (V % 8) == 0 && ((uintptr_t)z & 15) == 0;
-  for (int j = threadIdx.x >> 5; j < n_list; j += blockDim.x >> 5) {
-    const uint32_t i = list[j];
-    const int b = (int)(i / (uint32_t)n_tiles), tile = (int)(i % (uint32_t)n_tiles);
-    const size_t row = (size_t)r * W_t + b;
-    const int v0 = tile * kTile + lane * EPL;
-    float zv[EPL];
-    load_codes<T>(z + row * (size_t)V, v0, V, vec, zv);
-    const float thr = ss.cut[row];
-    unsigned hits = 0;
+  for (int j0 = (threadIdx.x >> 5) * U; j0 < n_list; j0 += warps * U) {
+    uint32_t ids[U];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e)
-      if (zv[e] >= thr) hits |= 1u << e;
-    uint32_t o[EPL];
-    const float cp = cum_prime(cum, bias, row), l = lse[row];
+    for (int u = 0; u < U; ++u) ids[u] = j0 + u < n_list ? list[j0 + u] : 0xFFFFFFFFu;
+    Codes8<T> zc[U];
+    float thr[U];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] = (hits >> e) & 1u ? orderable(score(cp, zv[e], l)) : 0u;
-    f(hits, o, (uint32_t)b * (uint32_t)V + (uint32_t)v0);
+    for (int u = 0; u < U; ++u) {
+      if (ids[u] == 0xFFFFFFFFu) continue;
+      const int b = (int)(ids[u] / (uint32_t)n_tiles), tile = (int)(ids[u] % (uint32_t)n_tiles);
+      const size_t row = (size_t)r * W_t + b;
+      zc[u].load(z + row * (size_t)V, tile * kTile + lane * EPL, V, vec);
+      thr[u] = ss.cut[row];
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (ids[u] == 0xFFFFFFFFu) continue;  // the same for every lane of the warp
+      const int b = (int)(ids[u] / (uint32_t)n_tiles), tile = (int)(ids[u] % (uint32_t)n_tiles);
+      unsigned hits = 0;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        if (zc[u].at(e) >= thr[u]) hits |= 1u << e;  // NaN never compares true
+      uint32_t o[EPL];
+      if (__any_sync(0xffffffffu, hits != 0)) {
+        const size_t row = (size_t)r * W_t + b;
+        const float cp = cum_prime(cum, bias, row), l = lse[row];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = (hits >> e) & 1u ? orderable(score(cp, zc[u].at(e), l)) : 0u;
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = 0u;
+      }
+      f(hits, o, (uint32_t)b * (uint32_t)V + (uint32_t)(tile * kTile + lane * EPL));
+    }
   }
 }
 
-// ---- refine: more codes reach the bound than the buffer holds. Narrows the
-// bound t over the listed codes until at most `target` codes reach it (and
-// still at least W_next), then writes those codes' keys to keys[]. Each
-// round histograms the score keys inside the window [lo, hi] on the 11 bits
-// below the highest bit where lo and hi differ, counts the codes above hi,
-// and keeps the bin holding the W_next-th largest. Returns the number of
-// keys written, or -1 when the codes tying at one score are too many.
+// Writes the 64-bit selection keys of every listed code whose score key
+// reaches lo into keys[0 .. target) and returns how many there are (those
+// past target are counted, not written).
+template <typename T>
+__device__ int append_listed(int r, int W_t, int V, int n_tiles, int n_list, const uint32_t* list,
+                             uint32_t lo, int target,
+                             const T* __restrict__ z, const float* __restrict__ lse,
+                             const float* __restrict__ cum, const float* __restrict__ bias,
+                             const SelScratch& ss, uint64_t* keys) {
+  __shared__ unsigned s_cnt;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) s_cnt = 0u;
+  __syncthreads();
+  for_listed_codes<T>(r, W_t, V, n_tiles, n_list, list, z, lse, cum, bias, ss,
+                      [&](unsigned hits, const uint32_t (&o)[kTile / 32], uint32_t flat0) {
+    unsigned keep = 0;
+#pragma unroll
+    for (int e = 0; e < kTile / 32; ++e)
+      if (((hits >> e) & 1u) && o[e] >= lo) keep |= 1u << e;
+    if (!__any_sync(0xffffffffu, keep != 0)) return;
+    const int mine = __popc(keep);
+    int incl = mine;
+#pragma unroll
+    for (int q = 1; q < 32; q <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, q);
+      if (lane >= q) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    unsigned pos = 0;
+    if (lane == 31) pos = atomicAdd(&s_cnt, (unsigned)total);
+    pos = __shfl_sync(0xffffffffu, pos, 31) + (unsigned)(incl - mine);
+#pragma unroll
+    for (int e = 0; e < kTile / 32; ++e) {
+      if ((keep >> e) & 1u) {
+        if (pos < (unsigned)target) keys[pos] = make_key(o[e], flat0 + (uint32_t)e);
+        ++pos;
+      }
+    }
+  });
+  __syncthreads();
+  return (int)s_cnt;
+}
+
+// ---- narrowing: more codes reach the bound than fit on chip. Raises the
+// bound from t until at most `target` listed codes reach it (and still at
+// least W_next). Each round histograms the score keys inside the window
+// [lo, hi] on the 11 bits below the highest bit where lo and hi differ,
+// counts the codes above hi, and keeps the bin holding the W_next-th
+// largest. Returns false when more codes tie at one score than fit.
 constexpr int kRefineBins = 2048;
 static_assert(kRefineBins * 4 <= kFinalSmemKeys * 8, "the bins live in the final block's key area");
 
 template <typename T>
-__device__ int refine_bound(int r, int W_t, int V, int n_tiles, int W_next, int target,
-                            const T* __restrict__ z, const float* __restrict__ lse,
-                            const float* __restrict__ cum, const float* __restrict__ bias,
-                            const SelScratch& ss, uint64_t* keys) {
-  __shared__ unsigned s_above, s_cnt, s_res[4];
-  uint32_t* bins = reinterpret_cast<uint32_t*>(keys);
-  const int n_list = min(ss.tcount[r], ss.cap_tiles);
+__device__ bool narrow_bound(int r, int W_t, int V, int n_tiles, int n_list, const uint32_t* list,
+                             int W_next, int target,
+                             const T* __restrict__ z, const float* __restrict__ lse,
+                             const float* __restrict__ cum, const float* __restrict__ bias,
+                             const SelScratch& ss, uint32_t* bins, uint32_t t, uint32_t hmax,
+                             uint32_t* lo_out) {
+  __shared__ unsigned s_above, s_res[4];
   const int lane = threadIdx.x & 31;
-  uint32_t lo = ss.thr[r], hi = ss.hmax[r];
-  bool fit = false;
+  uint32_t lo = t, hi = hmax;
   for (int round = 0; round < 8 && lo <= hi; ++round) {
     const int p = lo == hi ? 0 : 31 - __clz(lo ^ hi);
     const int shift = p >= 10 ? p - 10 : 0;
@@ -467,7 +481,7 @@ __device__ int refine_bound(int r, int W_t, int V, int n_tiles, int W_next, int 
     for (int i = threadIdx.x; i < kRefineBins; i += blockDim.x) bins[i] = 0u;
     if (threadIdx.x == 0) s_above = 0u;
     __syncthreads();
-    for_listed_codes<T>(r, W_t, V, n_tiles, n_list, z, lse, cum, bias, ss,
+    for_listed_codes<T>(r, W_t, V, n_tiles, n_list, list, z, lse, cum, bias, ss,
                         [&](unsigned hits, const uint32_t (&o)[kTile / 32], uint32_t) {
       unsigned over = 0;
 #pragma unroll
@@ -512,7 +526,7 @@ __device__ int refine_bound(int r, int W_t, int V, int n_tiles, int W_next, int 
       }
     }
     __syncthreads();
-    if (!s_res[3]) return -1;  // fewer than W_next codes reach lo: bound inconsistent
+    if (!s_res[3]) return false;  // fewer than W_next codes reach lo: bound inconsistent
     const uint32_t d = s_res[0];
     const unsigned total = s_above + s_res[1] + s_res[2];
     const uint32_t blo = max(lo, (uint32_t)((uint64_t)(base + d) << shift));
@@ -520,65 +534,53 @@ __device__ int refine_bound(int r, int W_t, int V, int n_tiles, int W_next, int 
     __syncthreads();  // everyone has read s_res and the bins
     lo = blo;
     if (total <= (unsigned)target) {
-      fit = true;
-      break;
+      *lo_out = lo;
+      return true;
     }
-    if (blo == bhi) return -1;  // more codes tie at one score than fit
+    if (blo == bhi) return false;  // more codes tie at one score than fit
     hi = bhi;
   }
-  if (!fit) return -1;
-  // every listed code with key >= lo, as a 64-bit selection key
-  if (threadIdx.x == 0) s_cnt = 0u;
-  __syncthreads();
-  for_listed_codes<T>(r, W_t, V, n_tiles, n_list, z, lse, cum, bias, ss,
-                      [&](unsigned hits, const uint32_t (&o)[kTile / 32], uint32_t flat0) {
-    unsigned keep = 0;
-#pragma unroll
-    for (int e = 0; e < kTile / 32; ++e)
-      if (((hits >> e) & 1u) && o[e] >= lo) keep |= 1u << e;
-    const int mine = __popc(keep);
-    int incl = mine;
-#pragma unroll
-    for (int q = 1; q < 32; q <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, q);
-      if (lane >= q) incl += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    unsigned pos = 0;
-    if (lane == 31 && total) pos = atomicAdd(&s_cnt, (unsigned)total);
-    pos = __shfl_sync(0xffffffffu, pos, 31) + (unsigned)(incl - mine);
-#pragma unroll
-    for (int e = 0; e < kTile / 32; ++e) {
-      if ((keep >> e) & 1u) {
-        if (pos < (unsigned)target) keys[pos] = make_key(o[e], flat0 + (uint32_t)e);
-        ++pos;
-      }
-    }
-  });
-  __syncthreads();
-  const unsigned n = s_cnt;
-  return n >= (unsigned)W_next && n <= (unsigned)target ? (int)n : -1;
+  return false;
 }
 
-// ---- final: exact top-W_next of the filtered candidates, sorted
+// ---- the fast path, one block per request: the bound, the candidates of
+// the listed tiles (narrowing the bound if they do not fit on chip), and
+// their exact top-W_next, sorted. A request it cannot finish is flagged for
+// the exact fallback.
 template <typename T>
-__global__ void __launch_bounds__(kFinalThreads) select_final_kernel(
-    int W_t, int V, int n_tiles, int W_next, const T* __restrict__ z, const float* __restrict__ lse,
-    const float* __restrict__ cum, const float* __restrict__ bias, SelScratch ss,
-    int32_t* __restrict__ parents, int32_t* __restrict__ tokens, float* __restrict__ cum_next) {
-  extern __shared__ uint64_t keys[];  // [kFinalSmemKeys]
+__global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
+    int W_t, int V, int n_tiles, int W_next, const float2* __restrict__ hint,
+    const T* __restrict__ z, const float* __restrict__ lse, const float* __restrict__ cum,
+    const float* __restrict__ bias, SelScratch ss, int bound_keys, int32_t* __restrict__ parents,
+    int32_t* __restrict__ tokens, float* __restrict__ cum_next, unsigned* err) {
+  // first the bound's hint keys (32-bit), then the candidates' keys (64-bit)
+  extern __shared__ uint64_t keys[];
   __shared__ unsigned hist[256];
   __shared__ unsigned sh[4];
   __shared__ uint64_t win[kMaxSort];
   const int r = blockIdx.x;
-  int n_c = ss.count[r];
-  bool on_chip = false;
-  if (n_c >= W_next && ss.tcount[r] <= ss.cap_tiles && n_c > ss.cap) {
-    n_c = refine_bound<T>(r, W_t, V, n_tiles, W_next, min(ss.cap, kFinalSmemKeys), z, lse, cum,
-                          bias, ss, keys);
-    on_chip = true;
+  // the tile list is kept on chip in the sort window (idle until the end)
+  // when it fits
+  uint32_t* slist = reinterpret_cast<uint32_t*>(win);
+  constexpr int kSlist = 2 * kMaxSort;
+  const Bound bd = bound_phase<T>(r, W_t, V, n_tiles, W_next, hint, lse, cum, bias, ss,
+                                  reinterpret_cast<uint32_t*>(keys), bound_keys, slist, kSlist, err);
+  const uint32_t t = bd.t, hmax = bd.hmax;
+  const int n_tc = bd.n_list;
+  const int n_list = min(n_tc, ss.cap_tiles);
+  const uint32_t* list = n_list <= kSlist ? slist : ss.tlist + (size_t)r * ss.cap_tiles;
+  const int target = min(ss.cap, kFinalSmemKeys);
+  int n_c = append_listed<T>(r, W_t, V, n_tiles, n_list, list, t, target, z, lse, cum, bias, ss,
+                             keys);
+  if (n_c > target && n_c >= W_next && n_tc <= ss.cap_tiles) {
+    uint32_t lo = t;
+    n_c = narrow_bound<T>(r, W_t, V, n_tiles, n_list, list, W_next, target, z, lse, cum, bias, ss,
+                          reinterpret_cast<uint32_t*>(keys), t, hmax, &lo)
+              ? append_listed<T>(r, W_t, V, n_tiles, n_list, list, lo, target, z, lse, cum, bias,
+                                 ss, keys)
+              : -1;
   }
-  if (n_c < W_next || n_c > ss.cap || ss.tcount[r] > ss.cap_tiles) {
+  if (n_c < W_next || n_c > target || n_tc > ss.cap_tiles) {
     if (threadIdx.x == 0) {
       ss.fb_flag[r] = 1;
       atomicOr(ss.fb_any, 1);
@@ -586,22 +588,16 @@ __global__ void __launch_bounds__(kFinalThreads) select_final_kernel(
     return;
   }
   if (threadIdx.x == 0) ss.fb_flag[r] = 0;
-  const uint64_t* c = ss.cand + (size_t)r * ss.cap;
-  if (!on_chip && n_c <= kFinalSmemKeys) {
-    on_chip = true;
-    for (int i = threadIdx.x; i < n_c; i += blockDim.x) keys[i] = c[i];
-    __syncthreads();
-  }
-  auto get = [&](int i) { return on_chip ? keys[i] : c[i]; };
   uint64_t prefix = 0;
-  if (W_next < n_c) prefix = radix_kth<uint64_t>(n_c, (unsigned)W_next, get, hist, sh);
+  if (W_next < n_c)
+    prefix = radix_kth<uint64_t>(n_c, (unsigned)W_next, [&](int i) { return keys[i]; }, hist, sh);
   int P = 1;
   while (P < W_next) P <<= 1;
   for (int i = threadIdx.x; i < P; i += blockDim.x) win[i] = 0;
   if (threadIdx.x == 0) sh[3] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < n_c; i += blockDim.x) {
-    uint64_t key = get(i);
+    const uint64_t key = keys[i];
     if (key >= prefix) {
       unsigned idx = atomicAdd(&sh[3], 1u);
       if (idx < (unsigned)W_next) win[idx] = key;
@@ -658,6 +654,8 @@ __global__ void __launch_bounds__(kReqThreads) select_request_kernel(
   __shared__ unsigned sh[4];
   __shared__ uint64_t win[kMaxSort];
   const int r = blockIdx.x;
+  // the row precut has read the flag: clear it for the next selection
+  if (r == 0 && threadIdx.x == 0) *ss.fb_any = 0;
   if (!ss.fb_flag[r]) return;
   const int n = W_t * K;
   const uint64_t* c = ss.pre + (size_t)r * n;
@@ -730,27 +728,15 @@ int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, 
     GDN_LAUNCH_CHECK();
     hint = ss.hint;
   }
-  // bound
+  // bound, filter and exact top-W of each request in one block
   const int n_h = W_t * n_tiles;
-  const int bound_keys = n_h <= 49152 ? n_h : 0;
-  const size_t bound_smem = (size_t)bound_keys * 4;
-  GDN_CUDA(cudaFuncSetAttribute(select_bound_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(bound_smem > 0 ? bound_smem : 4)));
-  select_bound_kernel<T><<<R, kBoundThreads, bound_smem, s>>>(W_t, V, n_tiles, W_next, hint, lse,
-                                                              cum, bias, ss, bound_keys, err);
-  GDN_LAUNCH_CHECK();
-  // filter over the listed tiles
-  const int per_req = (ss.cap_tiles + kFilterThreads / 32 - 1) / (kFilterThreads / 32);
-  const int bpr = per_req < kFilterBlocksPerReq ? per_req : kFilterBlocksPerReq;
-  select_filter_kernel<T><<<R * bpr, kFilterThreads, 0, s>>>(W_t, V, n_tiles, bpr, z, lse, cum,
-                                                              bias, ss);
-  GDN_LAUNCH_CHECK();
-  // final
-  const size_t fin_smem = (size_t)kFinalSmemKeys * 8;
-  GDN_CUDA(cudaFuncSetAttribute(select_final_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)fin_smem));
-  select_final_kernel<T><<<R, kFinalThreads, fin_smem, s>>>(W_t, V, n_tiles, W_next, z, lse, cum,
-                                                            bias, ss, parents, tokens, cum_next);
+  const int bound_keys = n_h <= 2 * kFinalSmemKeys ? n_h : 0;  // 32-bit keys in the key area
+  const size_t fused_smem = (size_t)kFinalSmemKeys * 8;
+  GDN_CUDA(cudaFuncSetAttribute(select_fused_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)fused_smem));
+  select_fused_kernel<T><<<R, kFinalThreads, fused_smem, s>>>(W_t, V, n_tiles, W_next, hint, z, lse,
+                                                              cum, bias, ss, bound_keys, parents,
+                                                              tokens, cum_next, err);
   GDN_LAUNCH_CHECK();
   // exact fallback for requests whose buffer was short or overflowed
   const size_t row_smem = (size_t)V * 8;
