@@ -165,6 +165,24 @@ __device__ void sort_and_emit(uint64_t* win, int P, int W_next, int V, int32_t* 
   }
 }
 
+// Writes the W_next unique keys of win[] in descending order: each key goes
+// to its rank, the number of keys above it. W_next^2 comparisons: used up to
+// kRankMax keys, a bitonic sort above.
+constexpr int kRankMax = 512;
+__device__ void rank_and_emit(const uint64_t* win, int W_next, int V, int32_t* parents,
+                              int32_t* tokens, float* cum_next) {
+  for (int i = threadIdx.x; i < W_next; i += blockDim.x) {
+    const uint64_t key = win[i];
+    int rank = 0;
+#pragma unroll 8
+    for (int j = 0; j < W_next; ++j) rank += win[j] > key ? 1 : 0;
+    const uint32_t flat = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFu);
+    parents[rank] = (int32_t)(flat / (uint32_t)V);
+    tokens[rank] = (int32_t)(flat % (uint32_t)V);
+    cum_next[rank] = from_orderable((uint32_t)(key >> 32));
+  }
+}
+
 struct SelScratch {
   int* fb_flag;     // [R] request needs the fallback
   int* fb_any;      // [1] some request needs the fallback (reset by the fallback's last kernel)
@@ -237,19 +255,39 @@ __global__ void tile_max_kernel(int n, int V, int n_tiles, const T* __restrict__
 // ---- bound: the W_next-th largest hint score of request r, and the tiles
 // that can hold a candidate. A code scores at most its tile's maximum (the
 // score is monotone in the stored logit within a row), so only tiles whose
-// maximum reaches the bound are listed. Writes ss.cut and ss.tlist of the
-// request (the list also to slist, up to slist_cap entries) and returns the
-// bound, the largest hint key and the list length (the same in every
-// thread); hkeys holds smem_keys 32-bit keys.
+// maximum reaches the bound are listed. Writes the rows' parameters and
+// ss.tlist of the request (the list also to slist, up to slist_cap entries)
+// and returns the bound, the largest hint key and the list length (the same
+// in every thread); hkeys holds smem_keys 32-bit keys.
 struct Bound {
   uint32_t t, hmax;
   int n_list;
 };
 
+// Per-row parameters of a request: cum' and lse, and the row's cutoff logit
+// once the bound is known. They sit in shared memory (cum', lse, cutoff, -)
+// when the request's rows fit, else they are read from global memory and the
+// cutoffs kept in ss.cut.
+constexpr int kSmemRows = 4000;
+
+struct Rows {
+  float4* s;  // [W_t] on chip, or null
+  const float *lse, *cum, *bias;
+  float* cut;
+  size_t base;  // the request's first row
+  __device__ __forceinline__ float4 get(int b) const {
+    if (s) return s[b];
+    const size_t row = base + b;
+    return make_float4(cum_prime(cum, bias, row), lse[row], cut[row], 0.0f);
+  }
+  __device__ __forceinline__ void set_cut(int b, float c) const {
+    if (s) s[b].z = c; else cut[base + b] = c;
+  }
+};
+
 template <typename T>
-__device__ Bound bound_phase(int r, int W_t, int V, int n_tiles, int W_next,
-                            const float2* __restrict__ hint, const float* __restrict__ lse,
-                            const float* __restrict__ cum, const float* __restrict__ bias,
+__device__ Bound bound_phase(int r, int W_t, int n_tiles, int W_next,
+                            const float2* __restrict__ hint, const Rows& rows,
                             const SelScratch& ss, uint32_t* hkeys, int smem_keys, uint32_t* slist,
                             int slist_cap, unsigned* err) {
   __shared__ unsigned hist[256];
@@ -261,18 +299,21 @@ __device__ Bound bound_phase(int r, int W_t, int V, int n_tiles, int W_next,
     s_cnt = 0;
     s_max = 0u;
   }
-  // a row whose lse or cumulative score is not finite is flagged
+  // the rows' parameters; a row whose lse or cumulative score is not finite
+  // is flagged
   for (int b = threadIdx.x; b < W_t; b += blockDim.x) {
-    const size_t row = (size_t)r * W_t + b;
-    if (!isfinite(lse[row]) || !isfinite(cum_prime(cum, bias, row)))
-      raise_error(err, GDNBEAM_DERR_NONFINITE);
+    const size_t row = rows.base + b;
+    const float cp = cum_prime(rows.cum, rows.bias, row), l = rows.lse[row];
+    if (!isfinite(l) || !isfinite(cp)) raise_error(err, GDNBEAM_DERR_NONFINITE);
+    if (rows.s) rows.s[b] = make_float4(cp, l, 0.0f, 0.0f);
   }
+  __syncthreads();
   auto key_of = [&](int i) -> uint32_t {
     const int b = i / n_tiles;
-    const size_t row = (size_t)r * W_t + b;
-    const float zm = hint[row * n_tiles + (i % n_tiles)].x;
+    const float4 rp = rows.get(b);
+    const float zm = hint[(rows.base + b) * n_tiles + (i % n_tiles)].x;
     const float zs = St<T>::to_f(St<T>::from_f(zm));  // stored value of the tile's top element
-    return orderable(score(cum_prime(cum, bias, row), zs, lse[row]));
+    return orderable(score(rp.x, zs, rp.y));
   };
   const bool on_chip = n_h <= smem_keys;
   uint32_t t = 0u;  // too few hints for a bound: keep every tile
@@ -290,14 +331,14 @@ __device__ Bound bound_phase(int r, int W_t, int V, int n_tiles, int W_next,
   // bisection over the storage keys (scores are monotone in the stored
   // value within a row); NaN when no code of the row can qualify
   for (int b = threadIdx.x; b < W_t; b += blockDim.x) {
-    const size_t row = (size_t)r * W_t + b;
-    const float cp = cum_prime(cum, bias, row), l = lse[row];
+    const float4 rp = rows.get(b);
+    const float cp = rp.x, l = rp.y;
     uint32_t lo = SKey<T>::kNegInf, hi = SKey<T>::kPosInf + 1u;  // hi: none reaches t
     while (lo < hi) {
       const uint32_t mid = lo + ((hi - lo) >> 1);
       if (orderable(score(cp, SKey<T>::value(mid), l)) >= t) hi = mid; else lo = mid + 1u;
     }
-    ss.cut[row] = SKey<T>::value(lo);
+    rows.set_cut(b, SKey<T>::value(lo));
   }
   uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
   unsigned my_max = 0u;
@@ -357,21 +398,18 @@ template <> struct Codes8<float> {
   }
 };
 
-// Visits the listed tiles of request r (list: n_list entries, on chip or in
+// Visits the listed tiles of a request (list: n_list entries, on chip or in
 // global memory) with the whole block, one warp per tile, several tiles per
-// warp at a time so their loads overlap. Every lane of the warp calls
-// f(hits, o, flat0): hits masks the lane's eight codes whose stored value
-// reaches the row's cutoff, o holds their score keys (other entries are 0)
-// and flat0 is the flat index of code 0.
+// warp at a time so their loads overlap. Each lane compares its eight codes
+// with the row's cutoff and calls f(o, flat) for every code that reaches it,
+// with the code's score key and flat index; lanes do this independently (f
+// must not use warp collectives), since a listed tile holds only a few such
+// codes.
 template <typename T, typename F>
-__device__ __forceinline__ void for_listed_codes(int r, int W_t, int V, int n_tiles, int n_list,
-                                                 const uint32_t* list, const T* __restrict__ z,
-                                                 const float* __restrict__ lse,
-                                                 const float* __restrict__ cum,
-                                                 const float* __restrict__ bias, const SelScratch& ss,
-                                                 F&& f) {
+__device__ __forceinline__ void for_listed_codes(int V, int n_tiles, int n_list, const uint32_t* list,
+                                                 const T* __restrict__ z, const Rows& rows, F&& f) {
   constexpr int EPL = kTile / 32;
-  constexpr int U = sizeof(T) == 2 ? 4 : 2;  // tiles in flight per warp
+  constexpr int U = sizeof(T) == 2 ? 6 : 3;  // tiles in flight per warp
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const bool vec = (V % 8) == 0 && ((uintptr_t)z & 15) == 0;
@@ -380,34 +418,27 @@ __device__ __forceinline__ void for_listed_codes(int r, int W_t, int V, int n_ti
 #pragma unroll
     for (int u = 0; u < U; ++u) ids[u] = j0 + u < n_list ? list[j0 + u] : 0xFFFFFFFFu;
     Codes8<T> zc[U];
-    float thr[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (ids[u] == 0xFFFFFFFFu) continue;
       const int b = (int)(ids[u] / (uint32_t)n_tiles), tile = (int)(ids[u] % (uint32_t)n_tiles);
-      const size_t row = (size_t)r * W_t + b;
-      zc[u].load(z + row * (size_t)V, tile * kTile + lane * EPL, V, vec);
-      thr[u] = ss.cut[row];
+      zc[u].load(z + (rows.base + b) * (size_t)V, tile * kTile + lane * EPL, V, vec);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (ids[u] == 0xFFFFFFFFu) continue;  // the same for every lane of the warp
+      if (ids[u] == 0xFFFFFFFFu) continue;
       const int b = (int)(ids[u] / (uint32_t)n_tiles), tile = (int)(ids[u] % (uint32_t)n_tiles);
+      const float4 rp = rows.get(b);
       unsigned hits = 0;
 #pragma unroll
       for (int e = 0; e < EPL; ++e)
-        if (zc[u].at(e) >= thr[u]) hits |= 1u << e;  // NaN never compares true
-      uint32_t o[EPL];
-      if (__any_sync(0xffffffffu, hits != 0)) {
-        const size_t row = (size_t)r * W_t + b;
-        const float cp = cum_prime(cum, bias, row), l = lse[row];
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) o[e] = (hits >> e) & 1u ? orderable(score(cp, zc[u].at(e), l)) : 0u;
-      } else {
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) o[e] = 0u;
+        if (zc[u].at(e) >= rp.z) hits |= 1u << e;  // NaN never compares true
+      const uint32_t flat0 = (uint32_t)b * (uint32_t)V + (uint32_t)(tile * kTile + lane * EPL);
+      while (hits) {
+        const int e = __ffs(hits) - 1;
+        hits &= hits - 1u;
+        f(orderable(score(rp.x, zc[u].at(e), rp.y)), flat0 + (uint32_t)e);
       }
-      f(hits, o, (uint32_t)b * (uint32_t)V + (uint32_t)(tile * kTile + lane * EPL));
     }
   }
 }
@@ -416,39 +447,15 @@ __device__ __forceinline__ void for_listed_codes(int r, int W_t, int V, int n_ti
 // reaches lo into keys[0 .. target) and returns how many there are (those
 // past target are counted, not written).
 template <typename T>
-__device__ int append_listed(int r, int W_t, int V, int n_tiles, int n_list, const uint32_t* list,
-                             uint32_t lo, int target,
-                             const T* __restrict__ z, const float* __restrict__ lse,
-                             const float* __restrict__ cum, const float* __restrict__ bias,
-                             const SelScratch& ss, uint64_t* keys) {
+__device__ int append_listed(int V, int n_tiles, int n_list, const uint32_t* list, uint32_t lo,
+                             int target, const T* __restrict__ z, const Rows& rows, uint64_t* keys) {
   __shared__ unsigned s_cnt;
-  const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) s_cnt = 0u;
   __syncthreads();
-  for_listed_codes<T>(r, W_t, V, n_tiles, n_list, list, z, lse, cum, bias, ss,
-                      [&](unsigned hits, const uint32_t (&o)[kTile / 32], uint32_t flat0) {
-    unsigned keep = 0;
-#pragma unroll
-    for (int e = 0; e < kTile / 32; ++e)
-      if (((hits >> e) & 1u) && o[e] >= lo) keep |= 1u << e;
-    if (!__any_sync(0xffffffffu, keep != 0)) return;
-    const int mine = __popc(keep);
-    int incl = mine;
-#pragma unroll
-    for (int q = 1; q < 32; q <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, q);
-      if (lane >= q) incl += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    unsigned pos = 0;
-    if (lane == 31) pos = atomicAdd(&s_cnt, (unsigned)total);
-    pos = __shfl_sync(0xffffffffu, pos, 31) + (unsigned)(incl - mine);
-#pragma unroll
-    for (int e = 0; e < kTile / 32; ++e) {
-      if ((keep >> e) & 1u) {
-        if (pos < (unsigned)target) keys[pos] = make_key(o[e], flat0 + (uint32_t)e);
-        ++pos;
-      }
+  for_listed_codes<T>(V, n_tiles, n_list, list, z, rows, [&](uint32_t o, uint32_t flat) {
+    if (o >= lo) {
+      const unsigned pos = atomicAdd(&s_cnt, 1u);
+      if (pos < (unsigned)target) keys[pos] = make_key(o, flat);
     }
   });
   __syncthreads();
@@ -465,12 +472,9 @@ constexpr int kRefineBins = 2048;
 static_assert(kRefineBins * 4 <= kFinalSmemKeys * 8, "the bins live in the final block's key area");
 
 template <typename T>
-__device__ bool narrow_bound(int r, int W_t, int V, int n_tiles, int n_list, const uint32_t* list,
-                             int W_next, int target,
-                             const T* __restrict__ z, const float* __restrict__ lse,
-                             const float* __restrict__ cum, const float* __restrict__ bias,
-                             const SelScratch& ss, uint32_t* bins, uint32_t t, uint32_t hmax,
-                             uint32_t* lo_out) {
+__device__ bool narrow_bound(int V, int n_tiles, int n_list, const uint32_t* list, int W_next,
+                             int target, const T* __restrict__ z, const Rows& rows, uint32_t* bins,
+                             uint32_t t, uint32_t hmax, uint32_t* lo_out) {
   __shared__ unsigned s_above, s_res[4];
   const int lane = threadIdx.x & 31;
   uint32_t lo = t, hi = hmax;
@@ -481,17 +485,9 @@ __device__ bool narrow_bound(int r, int W_t, int V, int n_tiles, int n_list, con
     for (int i = threadIdx.x; i < kRefineBins; i += blockDim.x) bins[i] = 0u;
     if (threadIdx.x == 0) s_above = 0u;
     __syncthreads();
-    for_listed_codes<T>(r, W_t, V, n_tiles, n_list, list, z, lse, cum, bias, ss,
-                        [&](unsigned hits, const uint32_t (&o)[kTile / 32], uint32_t) {
-      unsigned over = 0;
-#pragma unroll
-      for (int e = 0; e < kTile / 32; ++e) {
-        if (!((hits >> e) & 1u)) continue;
-        if (o[e] > hi) ++over;
-        else if (o[e] >= lo) atomicAdd(&bins[(o[e] >> shift) - base], 1u);
-      }
-      over = __reduce_add_sync(0xffffffffu, over);
-      if (lane == 0 && over) atomicAdd(&s_above, over);
+    for_listed_codes<T>(V, n_tiles, n_list, list, z, rows, [&](uint32_t o, uint32_t) {
+      if (o > hi) atomicAdd(&s_above, 1u);
+      else if (o >= lo) atomicAdd(&bins[(o >> shift) - base], 1u);
     });
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -551,9 +547,11 @@ template <typename T>
 __global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
     int W_t, int V, int n_tiles, int W_next, const float2* __restrict__ hint,
     const T* __restrict__ z, const float* __restrict__ lse, const float* __restrict__ cum,
-    const float* __restrict__ bias, SelScratch ss, int bound_keys, int32_t* __restrict__ parents,
-    int32_t* __restrict__ tokens, float* __restrict__ cum_next, unsigned* err) {
-  // first the bound's hint keys (32-bit), then the candidates' keys (64-bit)
+    const float* __restrict__ bias, SelScratch ss, int bound_keys, int rows_on_chip,
+    int32_t* __restrict__ parents, int32_t* __restrict__ tokens, float* __restrict__ cum_next,
+    unsigned* err) {
+  // first the bound's hint keys (32-bit), then the candidates' keys (64-bit);
+  // after them the rows' parameters when they fit
   extern __shared__ uint64_t keys[];
   __shared__ unsigned hist[256];
   __shared__ unsigned sh[4];
@@ -563,21 +561,21 @@ __global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
   // when it fits
   uint32_t* slist = reinterpret_cast<uint32_t*>(win);
   constexpr int kSlist = 2 * kMaxSort;
-  const Bound bd = bound_phase<T>(r, W_t, V, n_tiles, W_next, hint, lse, cum, bias, ss,
+  const Rows rows{rows_on_chip ? reinterpret_cast<float4*>(keys + kFinalSmemKeys) : nullptr, lse, cum,
+                  bias, ss.cut, (size_t)r * W_t};
+  const Bound bd = bound_phase<T>(r, W_t, n_tiles, W_next, hint, rows, ss,
                                   reinterpret_cast<uint32_t*>(keys), bound_keys, slist, kSlist, err);
   const uint32_t t = bd.t, hmax = bd.hmax;
   const int n_tc = bd.n_list;
   const int n_list = min(n_tc, ss.cap_tiles);
   const uint32_t* list = n_list <= kSlist ? slist : ss.tlist + (size_t)r * ss.cap_tiles;
   const int target = min(ss.cap, kFinalSmemKeys);
-  int n_c = append_listed<T>(r, W_t, V, n_tiles, n_list, list, t, target, z, lse, cum, bias, ss,
-                             keys);
+  int n_c = append_listed<T>(V, n_tiles, n_list, list, t, target, z, rows, keys);
   if (n_c > target && n_c >= W_next && n_tc <= ss.cap_tiles) {
     uint32_t lo = t;
-    n_c = narrow_bound<T>(r, W_t, V, n_tiles, n_list, list, W_next, target, z, lse, cum, bias, ss,
+    n_c = narrow_bound<T>(V, n_tiles, n_list, list, W_next, target, z, rows,
                           reinterpret_cast<uint32_t*>(keys), t, hmax, &lo)
-              ? append_listed<T>(r, W_t, V, n_tiles, n_list, list, lo, target, z, lse, cum, bias,
-                                 ss, keys)
+              ? append_listed<T>(V, n_tiles, n_list, list, lo, target, z, rows, keys)
               : -1;
   }
   if (n_c < W_next || n_c > target || n_tc > ss.cap_tiles) {
@@ -591,11 +589,9 @@ __global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
   uint64_t prefix = 0;
   if (W_next < n_c)
     prefix = radix_kth<uint64_t>(n_c, (unsigned)W_next, [&](int i) { return keys[i]; }, hist, sh);
-  int P = 1;
-  while (P < W_next) P <<= 1;
-  for (int i = threadIdx.x; i < P; i += blockDim.x) win[i] = 0;
   if (threadIdx.x == 0) sh[3] = 0;
   __syncthreads();
+  // the keys >= prefix are exactly the W_next best (keys are unique)
   for (int i = threadIdx.x; i < n_c; i += blockDim.x) {
     const uint64_t key = keys[i];
     if (key >= prefix) {
@@ -605,7 +601,15 @@ __global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
   }
   __syncthreads();
   const size_t o = (size_t)r * W_next;
-  sort_and_emit(win, P, W_next, V, parents + o, tokens + o, cum_next + o);
+  if (W_next <= kRankMax) {
+    rank_and_emit(win, W_next, V, parents + o, tokens + o, cum_next + o);
+  } else {
+    int P = 1;
+    while (P < W_next) P <<= 1;
+    for (int i = W_next + threadIdx.x; i < P; i += blockDim.x) win[i] = 0;  // below every key
+    __syncthreads();
+    sort_and_emit(win, P, W_next, V, parents + o, tokens + o, cum_next + o);
+  }
 }
 
 // ---- fallback stage 1: per-row local top-K (rows of flagged requests only)
@@ -731,12 +735,14 @@ int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, 
   // bound, filter and exact top-W of each request in one block
   const int n_h = W_t * n_tiles;
   const int bound_keys = n_h <= 2 * kFinalSmemKeys ? n_h : 0;  // 32-bit keys in the key area
-  const size_t fused_smem = (size_t)kFinalSmemKeys * 8;
+  const int rows_on_chip = W_t <= kSmemRows ? 1 : 0;
+  const size_t fused_smem = (size_t)kFinalSmemKeys * 8 + (rows_on_chip ? (size_t)W_t * 16 : 0);
   GDN_CUDA(cudaFuncSetAttribute(select_fused_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)fused_smem));
   select_fused_kernel<T><<<R, kFinalThreads, fused_smem, s>>>(W_t, V, n_tiles, W_next, hint, z, lse,
-                                                              cum, bias, ss, bound_keys, parents,
-                                                              tokens, cum_next, err);
+                                                              cum, bias, ss, bound_keys,
+                                                              rows_on_chip, parents, tokens,
+                                                              cum_next, err);
   GDN_LAUNCH_CHECK();
   // exact fallback for requests whose buffer was short or overflowed
   const size_t row_smem = (size_t)V * 8;
