@@ -184,7 +184,8 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents,
                  const gdnbeam_dumps* dumps, gdnbeam_stream_t stream);
 
 /* Global top-W_next over the W_t x V candidates of every request (OneLA §1.1;
- * RecoGEM §4.3 two-stage exact selection). Score of candidate (b, v):
+ * RecoGEM §4.3 exact selection: the result is the exact top-W_next, whatever
+ * path computes it). Score of candidate (b, v):
  *   s = fl32(cum'_b + fl32(z_bv - lse_b)),  cum'_b = fl32(cum_b + bias_b)
  * in IEEE fp32 without contraction; order by s descending, then flat index
  * b*V + v ascending. t = -1 selects from the prefill row (W_t must be 1).
@@ -221,7 +222,7 @@ int gdnbeam_device_status(int clear);
 
 /* Name of the kernel variant the context uses for each stage
  * ("tc" = tcgen05 tensor cores, "simt" = CUDA cores), as a static string such
- * as "proj=tc replay=tc logits=tc select=radix". */
+ * as "proj=tc replay=tc logits=tc select=bound". */
 const char* gdnbeam_variant(const gdnbeam_ctx* ctx);
 
 const char* gdnbeam_strerror(int status);
@@ -233,7 +234,7 @@ enum {
   GDNBEAM_STAGE_PROJECT = 2,  /* q, k, v, alpha, beta projections */
   GDNBEAM_STAGE_REPLAY = 3,   /* fused shared-context replay */
   GDNBEAM_STAGE_LOGITS = 4,   /* codebook logits and log-normaliser */
-  GDNBEAM_STAGE_SELECT = 5,   /* two-stage top-W selection */
+  GDNBEAM_STAGE_SELECT = 5,   /* exact global top-W selection */
   GDNBEAM_STAGE_PREFILL = 6,  /* prefill recurrence */
   GDNBEAM_NSTAGES = 7
 };
