@@ -1,6 +1,8 @@
-"""Host-side figures the benchmark reports: the operator-sweep shapes and
-the algorithmic bytes of one replay call."""
+"""Host-side figures the benchmark reports: the operator-sweep shapes, the
+algorithmic bytes of one replay call, and the reference arm's JSON line."""
+import json
 import os
+import subprocess
 import sys
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -44,3 +46,34 @@ def test_replay_bytes_with_a_residual_stream():
     plain = bench.replay_bytes(32, 1024, 8, 8, 128, 128, 1, 2)
     resid = bench.replay_bytes(32, 1024, 8, 8, 128, 128, 1, 2, residual=True)
     assert resid - plain == 32 * 1024 * 8 * 128 * (10 - 4)
+
+
+def _reference_run(env_extra):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                           "--steps", "1", "--warmup", "1"], cwd=ROOT, env=env,
+                          capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_the_contract_line():
+    # the oracle timed on the host cores, on the same workload description
+    # as the CUDA arm's line
+    run = _reference_run({"RANK": "0", "WORLD_SIZE": "1"})
+    assert run.returncode == 0, run.stderr[-2000:]
+    line = json.loads(run.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == bench.UNIT and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT,
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    wl = synth.WORKLOADS["batched_r64_w512"]
+    cfg = dict(line["config"])
+    assert cfg.pop("sample")
+    assert cfg == bench.workload_config(wl)
+
+
+def test_reference_arm_prints_nothing_on_other_ranks():
+    run = _reference_run({"RANK": "1", "WORLD_SIZE": "2"})
+    assert run.returncode == 0, run.stderr[-2000:]
+    assert run.stdout.strip() == ""
