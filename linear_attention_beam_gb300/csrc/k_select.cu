@@ -39,8 +39,8 @@ namespace gdnbeam {
 namespace {
 
 constexpr int kTile = 256;           // codes per hint tile (the logits GEMM tile width)
-constexpr int kFinalThreads = 1024;
-constexpr int kFinalSmemKeys = 16384; // candidates a final block keeps on chip
+constexpr int kFinalThreads = 1024;   // threads of a request's selection block
+constexpr int kFinalSmemKeys = 16384; // candidates a selection block keeps on chip
 constexpr int kRowThreads = 512;
 constexpr int kReqThreads = 1024;
 constexpr int kMaxSort = 4096;
@@ -189,7 +189,7 @@ struct SelScratch {
   uint64_t* pre;    // [R*W_t][K] fallback precut keys
   float2* hint;     // [R*W_t][n_tiles] tile maxima computed here when not supplied
   uint32_t* tlist;  // [R][cap_tiles] (row, tile) pairs whose maximum reaches the bound, b * n_tiles + tile
-  float* cut;       // [R*W_t] per row the smallest stored logit whose score reaches the bound
+  float* cut;       // [R*W_t] rows' cutoff logits, when the rows do not fit on chip
   int cap;          // candidates a request may keep on chip before the bound is narrowed
   int cap_tiles;
 };
