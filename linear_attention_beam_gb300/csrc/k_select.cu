@@ -401,13 +401,17 @@ template <> struct Codes8<float> {
 // Visits the listed tiles of a request (list: n_list entries, on chip or in
 // global memory) with the whole block, one warp per tile, several tiles per
 // warp at a time so their loads overlap. Each lane compares its eight codes
-// with the row's cutoff and calls f(o, flat) for every code that reaches it,
-// with the code's score key and flat index; lanes do this independently (f
-// must not use warp collectives), since a listed tile holds only a few such
-// codes.
-template <typename T, typename F>
+// with the row's cutoff. A tile with few codes reaching it (the usual case)
+// has each lane call f(o, flat) for each of its codes, with the code's score
+// key and flat index, independently of the other lanes. A tile dense with
+// them (scores dominated by the row's parent) has every lane of the warp call
+// dense(hits, o, flat0) together, with its hit mask and the hits' keys.
+constexpr int kDenseHits = 32;
+
+template <typename T, typename F, typename D>
 __device__ __forceinline__ void for_listed_codes(int V, int n_tiles, int n_list, const uint32_t* list,
-                                                 const T* __restrict__ z, const Rows& rows, F&& f) {
+                                                 const T* __restrict__ z, const Rows& rows, F&& f,
+                                                 D&& dense) {
   constexpr int EPL = kTile / 32;
   constexpr int U = sizeof(T) == 2 ? 6 : 3;  // tiles in flight per warp
   const int lane = threadIdx.x & 31;
@@ -434,6 +438,14 @@ __device__ __forceinline__ void for_listed_codes(int V, int n_tiles, int n_list,
       for (int e = 0; e < EPL; ++e)
         if (zc[u].at(e) >= rp.z) hits |= 1u << e;  // NaN never compares true
       const uint32_t flat0 = (uint32_t)b * (uint32_t)V + (uint32_t)(tile * kTile + lane * EPL);
+      // warp-uniform: the same tile in every lane
+      if (__reduce_add_sync(0xffffffffu, (unsigned)__popc(hits)) > (unsigned)kDenseHits) {
+        uint32_t o[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = (hits >> e) & 1u ? orderable(score(rp.x, zc[u].at(e), rp.y)) : 0u;
+        dense(hits, o, flat0);
+        continue;
+      }
       while (hits) {
         const int e = __ffs(hits) - 1;
         hits &= hits - 1u;
@@ -450,14 +462,37 @@ template <typename T>
 __device__ int append_listed(int V, int n_tiles, int n_list, const uint32_t* list, uint32_t lo,
                              int target, const T* __restrict__ z, const Rows& rows, uint64_t* keys) {
   __shared__ unsigned s_cnt;
+  const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) s_cnt = 0u;
   __syncthreads();
-  for_listed_codes<T>(V, n_tiles, n_list, list, z, rows, [&](uint32_t o, uint32_t flat) {
-    if (o >= lo) {
-      const unsigned pos = atomicAdd(&s_cnt, 1u);
-      if (pos < (unsigned)target) keys[pos] = make_key(o, flat);
-    }
-  });
+  auto put = [&](unsigned pos, uint32_t o, uint32_t flat) {
+    if (pos < (unsigned)target) keys[pos] = make_key(o, flat);
+  };
+  for_listed_codes<T>(
+      V, n_tiles, n_list, list, z, rows,
+      [&](uint32_t o, uint32_t flat) {
+        if (o >= lo) put(atomicAdd(&s_cnt, 1u), o, flat);
+      },
+      [&](unsigned hits, const uint32_t (&o)[kTile / 32], uint32_t flat0) {
+        // one atomic per warp: the lanes' places from a scan of their counts
+        unsigned keep = 0;
+#pragma unroll
+        for (int e = 0; e < kTile / 32; ++e)
+          if (((hits >> e) & 1u) && o[e] >= lo) keep |= 1u << e;
+        const unsigned mine = (unsigned)__popc(keep);
+        unsigned incl = mine;
+#pragma unroll
+        for (int q = 1; q < 32; q <<= 1) {
+          const unsigned y = __shfl_up_sync(0xffffffffu, incl, q);
+          if (lane >= q) incl += y;
+        }
+        unsigned pos = 0;
+        if (lane == 31 && incl) pos = atomicAdd(&s_cnt, incl);
+        pos = __shfl_sync(0xffffffffu, pos, 31) + incl - mine;
+#pragma unroll
+        for (int e = 0; e < kTile / 32; ++e)
+          if ((keep >> e) & 1u) put(pos++, o[e], flat0 + (uint32_t)e);
+      });
   __syncthreads();
   return (int)s_cnt;
 }
@@ -485,10 +520,23 @@ __device__ bool narrow_bound(int V, int n_tiles, int n_list, const uint32_t* lis
     for (int i = threadIdx.x; i < kRefineBins; i += blockDim.x) bins[i] = 0u;
     if (threadIdx.x == 0) s_above = 0u;
     __syncthreads();
-    for_listed_codes<T>(V, n_tiles, n_list, list, z, rows, [&](uint32_t o, uint32_t) {
-      if (o > hi) atomicAdd(&s_above, 1u);
-      else if (o >= lo) atomicAdd(&bins[(o >> shift) - base], 1u);
-    });
+    for_listed_codes<T>(
+        V, n_tiles, n_list, list, z, rows,
+        [&](uint32_t o, uint32_t) {
+          if (o > hi) atomicAdd(&s_above, 1u);
+          else if (o >= lo) atomicAdd(&bins[(o >> shift) - base], 1u);
+        },
+        [&](unsigned hits, const uint32_t (&o)[kTile / 32], uint32_t) {
+          unsigned over = 0;
+#pragma unroll
+          for (int e = 0; e < kTile / 32; ++e) {
+            if (!((hits >> e) & 1u)) continue;
+            if (o[e] > hi) ++over;
+            else if (o[e] >= lo) atomicAdd(&bins[(o[e] >> shift) - base], 1u);
+          }
+          over = __reduce_add_sync(0xffffffffu, over);
+          if (lane == 0 && over) atomicAdd(&s_above, over);
+        });
     __syncthreads();
     if (threadIdx.x < 32) {
       // highest bin d whose count from the top of the window reaches the
