@@ -489,3 +489,19 @@ def test_gqa_value_heads_share_their_group_key():
     S2 = oracle.prefill(wl, p2, prompt)[0]
     np.testing.assert_array_equal(S1[:, :2], S2[:, :2])
     assert np.abs(S1[:, 2:] - S2[:, 2:]).max() > 1e-6
+
+
+def test_layer_feature_is_the_normalised_stream_or_the_outputs():
+    # the codebook head reads RMSNorm(x) of the residual stream on stacked
+    # layers (unit root-mean-square, no gain, direction kept) and concat_h o
+    # unchanged on a single layer
+    rng = np.random.default_rng(21)
+    # (row scales >= 1, where the norm's eps of 1e-6 moves the result < 1e-6)
+    x = rng.standard_normal((4, 96)) * np.array([[1.0], [3.0], [7.0], [300.0]])
+    f = oracle.layer_feature(synth.DEEP, x)
+    rms = np.sqrt((f ** 2).mean(axis=-1))
+    np.testing.assert_allclose(rms, 1.0, rtol=1e-6)
+    ratio = f / x
+    np.testing.assert_allclose(ratio, ratio[:, :1] * np.ones_like(ratio), rtol=1e-12)
+    assert np.all(ratio > 0)
+    np.testing.assert_array_equal(oracle.layer_feature(synth.SINGLE, x), x)
