@@ -25,6 +25,13 @@
  *   - Decode call t (0 <= t <= T-2) runs on the beams kept by selection t
  *     and feeds selection t+1; selection 0 reads the prefill row. A beam's
  *     slot at depth j is its ancestor's row index at decode call j.
+ *   - gdnbeam_step, gdnbeam_select and gdnbeam_get_paths only enqueue kernels
+ *     on the given stream, with every size and pointer fixed at the call; none
+ *     of them synchronises or allocates. A sequence of them (one decode step)
+ *     can therefore be captured on a non-default stream into a CUDA graph and
+ *     replayed, on the same buffers, with stage timing off (gdnbeam_timing):
+ *     a replay stores the same bits as the calls. The context's call-order
+ *     checks run at capture, not at replay.
  */
 #ifndef GDNBEAM_H_
 #define GDNBEAM_H_
