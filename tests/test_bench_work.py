@@ -77,3 +77,30 @@ def test_reference_arm_prints_nothing_on_other_ranks():
     run = _reference_run({"RANK": "1", "WORLD_SIZE": "2"})
     assert run.returncode == 0, run.stderr[-2000:]
     assert run.stdout.strip() == ""
+
+
+def test_gemm_and_selection_work_of_a_metric_decode_call():
+    # 64 requests x 512 beams: the projection GEMM is 32768 x 2048 x 6176
+    # (q, k, v of 16 heads of 128, and 2 x 16 gate logits) = 829 GFLOP, the
+    # codebook logits 32768 x 2048 x 8192 = 1.10 TFLOP; the selection reads the
+    # 32 tile statistics of each row (8 B each), each row's lse and cumulative
+    # score, and W_next = 512 listed tiles of 256 bf16 logits per request
+    wl = synth.WORKLOADS["batched_r64_w512"]
+    w = bench.stage_work(wl, 1)
+    n = 64 * 512
+    assert w["project"] == 2.0 * n * 2048 * 6176
+    assert abs(w["project"] / 829e9 - 1) < 2e-3
+    assert w["logits"] == 2.0 * n * 2048 * 8192
+    assert abs(w["logits"] / 1.0995e12 - 1) < 1e-4
+    assert w["select"] == n * 32 * 8 + n * 8 + 64 * 512 * 256 * 2
+    assert abs(w["select"] / 25.4e6 - 1) < 1e-2
+
+
+def test_stacked_layers_multiply_the_projection_work():
+    # four layers of 8 heads (d_model 1024): one projection GEMM per layer,
+    # one codebook head
+    wl = synth.WORKLOADS["deep4_w1024"]
+    w = bench.stage_work(wl, 0)
+    n = 32 * 1024
+    assert w["project"] == 4 * 2.0 * n * 1024 * (3 * 8 * 128 + 2 * 8)
+    assert w["logits"] == 2.0 * n * 1024 * 4096
