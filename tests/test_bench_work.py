@@ -104,3 +104,20 @@ def test_stacked_layers_multiply_the_projection_work():
     n = 32 * 1024
     assert w["project"] == 4 * 2.0 * n * 1024 * (3 * 8 * 128 + 2 * 8)
     assert w["logits"] == 2.0 * n * 1024 * 4096
+
+
+def test_clock_summary_takes_the_loaded_samples():
+    # idle samples (low power) around the timed region do not set the median;
+    # any throttle reason seen in any sample is reported
+    rows = [
+        ["0", "2070", "2070", "120.5", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"],
+        ["0", "1800", "2070", "1390.1", "0x4", "Not Active", "Not Active", "Not Active", "Active"],
+        ["0", "1850", "2070", "1385.0", "0x4", "Not Active", "Not Active", "Not Active", "Active"],
+        ["0", "1900", "2070", "1200.0", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"],
+        ["0", "2070", "2070", "[N/A]", "0x0", "Not Active", "Not Active", "Not Active", "Not Active"],
+    ]
+    c = bench.summarize_clock_rows(rows)
+    assert c["sm_mhz"] == 1850.0 and c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"] and c["samples"] == 5 and c["samples_under_load"] == 3
+    idle = bench.summarize_clock_rows([["0", "345", "2070", "[N/A]"] + ["Not Active"] * 5])
+    assert idle["sm_mhz"] == 345.0 and idle["samples_under_load"] == 0
