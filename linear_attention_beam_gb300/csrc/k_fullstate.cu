@@ -177,7 +177,6 @@ __global__ void __launch_bounds__(256, 2) replayssm_step_kernel(ReplaySsmArgs a)
   const int i = tid / TPR, part = tid % TPR, c0 = part * NCOL;
   const int H = a.H, dv = a.d_v;
   const int hk = h / (H / a.Hk);  // the key head this value head reads
-  constexpr int t = TD;
   const T* srow_g = (const T*)a.sctx_store + (size_t)r * a.sctx_rstride + (size_t)h * dv * DK;
   const uint32_t sbar = tc::smem_u32(&bar), stile = tc::smem_u32(tile);
   if (kTile) {
