@@ -365,7 +365,8 @@ int gdnbeam_select_topw(int R, int W_t, int W_next, int V, int dtype, const void
  *   - The first call on each device looks up the area's device address with
  *     that device current; make that first call before any stream capture.
  *   - All calls share the one area, and its contents persist between calls;
- *     every call resets the counters it relies on before use. Calls whose
+ *     every call writes each request's state in the area before reading it
+ *     (a leftover value can cost time, never change a result). Calls whose
  *     work overlaps on the GPU (other streams, other host threads) race on
  *     the area: order them on one stream or synchronise between them.
  * Arguments, outputs and errors are those of gdnbeam_select_topw. */
