@@ -25,7 +25,11 @@ def _worker(rank, world, port, out):
     units = 1000.0 * (rank + 1)          # uneven work per rank
     ms = 10.0 if rank == 0 else 40.0     # rank 1 is the slowest
     rate, max_ms = bench.job_rate(units, ms, dist)
-    out[rank] = (rate, max_ms)
+    # the graph timing runs on every rank or on none: rank 1's failed
+    # capture makes both fall back
+    both = bench.all_ranks_agree(True, dist)
+    one_failed = bench.all_ranks_agree(rank != 1, dist)
+    out[rank] = (rate, max_ms, both, one_failed)
     dist.barrier()
     dist.destroy_process_group()
 
@@ -42,12 +46,14 @@ def test_two_gloo_ranks_aggregate_like_the_bench():
         p.join(timeout=120)
         assert p.exitcode == 0
     for r in range(2):
-        rate, max_ms = out[r]
+        rate, max_ms, both, one_failed = out[r]
         assert max_ms == 40.0
         assert rate == pytest.approx(3000.0 / 0.040)
+        assert both is True and one_failed is False
 
 
 def test_single_process_rate():
     import bench
     rate, ms = bench.job_rate(98304.0, 6.5)
     assert rate == pytest.approx(98304 / 0.0065)
+    assert bench.all_ranks_agree(True) and not bench.all_ranks_agree(False)
