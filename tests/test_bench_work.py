@@ -121,3 +121,31 @@ def test_clock_summary_takes_the_loaded_samples():
     assert c["reasons"] == ["sw_power_cap"] and c["samples"] == 5 and c["samples_under_load"] == 3
     idle = bench.summarize_clock_rows([["0", "345", "2070", "[N/A]"] + ["Not Active"] * 5])
     assert idle["sm_mhz"] == 345.0 and idle["samples_under_load"] == 0
+
+
+def _ours_run(args, env_extra):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                          env=env, capture_output=True, text=True, timeout=300)
+
+
+def test_more_than_one_gpu_is_refused_before_any_gpu_work():
+    # the GEMMs' multicast tile loads run on one GPU only: a torchrun launch
+    # (WORLD_SIZE > 1) or --gpus > 1 exits with a reason and does no work
+    for args, env in ((["--steps", "1"], {"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"}),
+                      (["--gpus", "2", "--steps", "1"], {"WORLD_SIZE": "1"}),
+                      (["--stage", "logits", "--gpus", "4"], {})):
+        run = _ours_run(args, env)
+        assert run.returncode == 2, (args, run.stderr[-2000:])
+        line = json.loads(run.stdout.strip().splitlines()[-1])
+        assert line["metric"] == bench.METRIC and "one GPU" in line["unavailable"]
+        assert "one GPU" in run.stderr
+    other = _ours_run(["--steps", "1"], {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert other.returncode == 2 and other.stdout.strip() == ""
+
+
+def test_one_gpu_run_is_not_refused():
+    ns = type("A", (), {"gpus": 1})
+    assert bench.multi_gpu_refusal(ns, {"WORLD_SIZE": "1"}) is None
+    assert bench.multi_gpu_refusal(ns, {}) is None
+    assert bench.multi_gpu_refusal(ns, {"WORLD_SIZE": "2"}) is not None
