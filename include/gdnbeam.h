@@ -214,10 +214,30 @@ int gdnbeam_get_paths(gdnbeam_ctx* ctx, int W_final, const int32_t* parents,
  * by all beams, so its width is amortised over the beam width. */
 int gdnbeam_read_sctx(gdnbeam_ctx* ctx, float* out, gdnbeam_stream_t stream);
 
-/* Marks every request's state as released: records stay where they are
- * (nothing moves, OneLA §2.1/§2.4); a new prefill is required before the next
- * step. Host only. */
-int gdnbeam_reset(gdnbeam_ctx* ctx);
+/* Releases requests' contexts (OneLA §2.1: S_ctx is the one persistent state
+ * of a request; §2.4: records stay in their slots until the request ends,
+ * nothing moves). request_mask (host) is [R] int32: requests with a non-zero
+ * entry are released; NULL releases every request. Decoding restarts at
+ * t = 0 and gdnbeam_step returns GDNBEAM_ESTATE until every request holds a
+ * context again: gdnbeam_prefill_state (all requests) or
+ * gdnbeam_prefill_requests (some). Requests not released keep their S_ctx
+ * and the root rows the caller holds for them. Host only; no CUDA call. */
+int gdnbeam_reset(gdnbeam_ctx* ctx, const int32_t* request_mask);
+
+/* Prefill of some requests only (OneLA §1.1, §2.1), the others keeping their
+ * S_ctx: for i < count, request request_ids[i] (host array, distinct ids in
+ * [0, R)) gets the context of prompt row i.
+ *   prompts     [count][L] int32 token ids, 1 <= L <= L_max
+ *   root_logits [R][V] storage and root_lse [R] fp32: only the listed
+ *               requests' rows are written.
+ * The listed requests then hold a context again (see gdnbeam_reset); their
+ * S_ctx and root rows equal those a full gdnbeam_prefill_state with the same
+ * prompt rows would give. Each request runs as its own pass through the same
+ * kernels, in order on the stream. Errors as gdnbeam_prefill_state;
+ * GDNBEAM_EINVAL for an id out of range or listed twice (nothing launched). */
+int gdnbeam_prefill_requests(gdnbeam_ctx* ctx, const int32_t* request_ids, int count,
+                             const int32_t* prompts, int L, void* root_logits, float* root_lse,
+                             gdnbeam_stream_t stream);
 
 /* Synchronises the stream, then returns GDNBEAM_EDEVICE if the device error
  * word is set (and clears it), GDNBEAM_ECUDA on a CUDA error, else 0. */

@@ -75,7 +75,8 @@ _SIGS = {
     "gdnbeam_select": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _S]),
     "gdnbeam_get_paths": (_I, [_P, _I, _P, _P, _P, _S]),
     "gdnbeam_read_sctx": (_I, [_P, _P, _S]),
-    "gdnbeam_reset": (_I, [_P]),
+    "gdnbeam_reset": (_I, [_P, _P]),
+    "gdnbeam_prefill_requests": (_I, [_P, _P, _I, _P, _I, _P, _P, _S]),
     "gdnbeam_status": (_I, [_P, _S]),
     "gdnbeam_device_status": (_I, [_I]),
     "gdnbeam_variant": (C.c_char_p, [_P]),

@@ -20,18 +20,22 @@ namespace {
 
 __device__ unsigned int g_dev_error_word;
 
+// Device address of the error word per device, resolved once with that
+// device current (atomic: concurrent first calls store the same value).
 constexpr int kMaxDevices = 64;
-unsigned* g_err_ptr[kMaxDevices] = {nullptr};
+std::atomic<unsigned*> g_err_ptr[kMaxDevices] = {};
 
 unsigned* err_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_err_ptr[dev]) {
+  unsigned* e = g_err_ptr[dev].load(std::memory_order_relaxed);
+  if (!e) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_dev_error_word) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = (unsigned*)p;
+    e = (unsigned*)p;
+    g_err_ptr[dev].store(e, std::memory_order_relaxed);
   }
-  return g_err_ptr[dev];
+  return e;
 }
 
 inline size_t elem_size(int dtype) { return dtype == GDNBEAM_BF16 ? 2 : 4; }
@@ -100,8 +104,10 @@ struct gdnbeam_ctx {
   // prefill buffers for R*L_max rows
   void *pf_u, *pf_q, *pf_k, *pf_v, *pf_feat;
   float *pf_x, *pf_alpha, *pf_beta;
-  // sequencing
+  // sequencing: prefilled is set while every request holds a prefilled
+  // context (live[r]); a per-request reset clears some of them
   int prefilled;
+  std::vector<unsigned char> live;
   int last_step;
   int W_hist[GDNBEAM_MAX_T];
   // per-stage timing
@@ -331,6 +337,7 @@ int gdnbeam_create(const gdnbeam_config* cfg, const gdnbeam_weights* w, void* wo
     snprintf(x->variant, sizeof(x->variant), "proj=%s replay=%s logits=%s select=bound",
              tc ? "tc" : "simt", x->tc_replay ? "tc" : "simt", tc ? "tc" : "simt");
   x->prefilled = 0;
+  x->live.assign(cfg->R, 0);
   x->last_step = -1;
   *out = x;
   return GDNBEAM_OK;
@@ -340,25 +347,33 @@ void gdnbeam_destroy(gdnbeam_ctx* ctx) { delete ctx; }
 
 const char* gdnbeam_variant(const gdnbeam_ctx* ctx) { return ctx ? ctx->variant : ""; }
 
-int gdnbeam_reset(gdnbeam_ctx* ctx) {
+int gdnbeam_reset(gdnbeam_ctx* ctx, const int32_t* request_mask) {
   if (!ctx) return GDNBEAM_EINVAL;
+  const int R = ctx->c.R;
+  for (int r = 0; r < R; ++r)
+    if (!request_mask || request_mask[r]) ctx->live[r] = 0;
   ctx->prefilled = 0;
   ctx->last_step = -1;
   return GDNBEAM_OK;
 }
 
-int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* root_logits,
-                          float* root_lse, gdnbeam_stream_t stream) {
-  if (!ctx || !prompt || !root_logits || !root_lse) return GDNBEAM_EINVAL;
-  const gdnbeam_config& c = ctx->c;
-  if (L < 1 || L > c.L_max) return GDNBEAM_EINVAL;
-  cudaStream_t s = (cudaStream_t)stream;
+}  // extern "C"
+
+namespace {
+
+// Prefill of cp.R requests whose prompts are packed [cp.R][L] at prompt:
+// S_ctx of request i goes to sctx_base + i * (layers*H*d_v*d_k), its root
+// row's logits and lse to root_logits / root_lse row i, and (baselines) the
+// storage copy of S_ctx to sctx_store_base. cp is the context's
+// configuration with R set to the requests of this pass.
+int prefill_pass(gdnbeam_ctx* ctx, const gdnbeam_config& c, const int32_t* prompt, int L,
+                 float* sctx_base, void* sctx_store_base, void* root_logits, float* root_lse,
+                 cudaStream_t s) {
   unsigned* err = err_ptr();
   const int n = c.R * L;
   const size_t es = elem_size(c.dtype);
   const int Np = n_proj(c);
   const long long rstride = (long long)c.layers * c.H * c.d_v * c.d_k;
-  ctx->prefilled = 0;
   int ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
   int st = launch_gather_rows(c.dtype, n, c.d_model, prompt, c.V, ctx->w.E, ctx->pf_u,
                               c.residual ? ctx->pf_x : nullptr, err, s);
@@ -372,7 +387,7 @@ int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* 
       if (st) return st;
     }
     const char* Wp = (const char*)ctx->w.W_proj + (size_t)layer * Np * c.d_model * es;
-    float* sc = (float*)ctx->sctx + (size_t)layer * c.H * c.d_v * c.d_k;
+    float* sc = sctx_base + (size_t)layer * c.H * c.d_v * c.d_k;
     if (ctx->tc_gemm && tc_prefill_supported(c, c.residual ? ctx->pf_x : nullptr)) {
       // The chunked prefill reads the query only at each request's last
       // token: the projection over all prompt rows skips the query columns,
@@ -407,8 +422,7 @@ int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* 
     if (st) return st;
   }
   if (c.state_path) {  // the baselines read S_ctx in the storage type
-    st = launch_to_storage(c.dtype, (size_t)c.R * c.layers * c.H * c.d_v * c.d_k,
-                           (const float*)ctx->sctx, ctx->sctx_store, s);
+    st = launch_to_storage(c.dtype, (size_t)c.R * rstride, sctx_base, sctx_store_base, s);
     if (st) return st;
   }
   if (c.residual) {
@@ -419,12 +433,70 @@ int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* 
   ev = ctx->tic(GDNBEAM_STAGE_LOGITS, s);
   st = logits_any(c, ctx->tc_gemm, c.R, ctx->pf_feat, ctx->w.W_o, root_logits, root_lse,
                   ctx->gemm, ctx->gemm_bytes, ctx->tstats, nullptr, s);
+  ctx->toc(ev, s);
+  return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdnbeam_prefill_state(gdnbeam_ctx* ctx, const int32_t* prompt, int L, void* root_logits,
+                          float* root_lse, gdnbeam_stream_t stream) {
+  if (!ctx || !prompt || !root_logits || !root_lse) return GDNBEAM_EINVAL;
+  const gdnbeam_config& c = ctx->c;
+  if (L < 1 || L > c.L_max) return GDNBEAM_EINVAL;
+  ctx->prefilled = 0;
+  ctx->live.assign(c.R, 0);
+  ctx->last_logits = nullptr;
+  int st = prefill_pass(ctx, c, prompt, L, (float*)ctx->sctx, ctx->sctx_store, root_logits,
+                        root_lse, (cudaStream_t)stream);
+  if (st) return st;
   ctx->last_logits = root_logits;
   ctx->last_rows = c.R;
-  ctx->toc(ev, s);
-  if (st) return st;
+  ctx->live.assign(c.R, 1);
   ctx->prefilled = 1;
   ctx->last_step = -1;
+  return GDNBEAM_OK;
+}
+
+int gdnbeam_prefill_requests(gdnbeam_ctx* ctx, const int32_t* request_ids, int count,
+                             const int32_t* prompts, int L, void* root_logits, float* root_lse,
+                             gdnbeam_stream_t stream) {
+  if (!ctx || count < 0) return GDNBEAM_EINVAL;
+  const gdnbeam_config& c = ctx->c;
+  if (count == 0) return GDNBEAM_OK;
+  if (!request_ids || !prompts || !root_logits || !root_lse) return GDNBEAM_EINVAL;
+  if (L < 1 || L > c.L_max || count > c.R) return GDNBEAM_EINVAL;
+  std::vector<unsigned char> seen(c.R, 0);
+  for (int i = 0; i < count; ++i) {
+    const int r = request_ids[i];
+    if (r < 0 || r >= c.R || seen[r]) return GDNBEAM_EINVAL;
+    seen[r] = 1;
+  }
+  const size_t es = elem_size(c.dtype);
+  const size_t rstride = (size_t)c.layers * c.H * c.d_v * c.d_k;
+  gdnbeam_config one = c;
+  one.R = 1;
+  // The root rows written here are not the rows a selection would find the
+  // logits stage's tile maxima for: the selection computes its own.
+  ctx->last_logits = nullptr;
+  ctx->last_rows = 0;
+  ctx->last_step = -1;
+  for (int i = 0; i < count; ++i) {
+    const int r = request_ids[i];
+    ctx->live[r] = 0;
+    ctx->prefilled = 0;
+    int st = prefill_pass(ctx, one, prompts + (size_t)i * L, L, (float*)ctx->sctx + r * rstride,
+                          ctx->sctx_store ? (char*)ctx->sctx_store + r * rstride * es : nullptr,
+                          (char*)root_logits + (size_t)r * c.V * es, root_lse + r,
+                          (cudaStream_t)stream);
+    if (st) return st;
+    ctx->live[r] = 1;
+  }
+  bool all = true;
+  for (int r = 0; r < c.R; ++r) all = all && ctx->live[r];
+  ctx->prefilled = all ? 1 : 0;
   return GDNBEAM_OK;
 }
 

@@ -31,6 +31,8 @@
 //
 // Ancestry (OneLA §2.4 eq. 9): each child copies its parent's slot list and
 // appends the parent's row as the slot of the previous depth.
+#include <atomic>
+
 #include "common.cuh"
 #include "launchers.h"
 
@@ -809,11 +811,16 @@ int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, 
 }  // namespace
 
 int sm_count() {
-  static int sms[64] = {0};
+  static std::atomic<int> sms[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
-  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  return sms[dev] > 0 ? sms[dev] : 132;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 132;
+    sms[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
 }
 
 size_t select_scratch_bytes(int R, int W_t, int W_next, int V) {

@@ -7,6 +7,8 @@
 // a fixed scratch area inside the library itself, a file-scope device array
 // that exists on every GPU where the library is loaded, for the life of the
 // process. The selection it runs is the same as gdnbeam_select_topw's.
+#include <atomic>
+
 #include "common.cuh"
 #include "launchers.h"
 
@@ -19,19 +21,21 @@ static __device__ __align__(256) unsigned char g_select_scratch[kStaticSelectByt
 
 // Device address of g_select_scratch on each device, resolved on the first
 // call made with that device current. The host-side name of the array is not
-// a device address; only this resolved pointer is handed to kernels.
+// a device address; only this resolved pointer is handed to kernels. Host
+// threads making their first call at once may both resolve it; they store
+// the same value, and the atomic makes that well defined.
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+std::atomic<void*> g_scratch_addr[kMaxDevices] = {};
 
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDNBEAM_ECUDA;
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
+  void* p = g_scratch_addr[dev].load(std::memory_order_relaxed);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess || !p) return GDNBEAM_ECUDA;
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(p, std::memory_order_relaxed);
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return GDNBEAM_OK;
 }
 

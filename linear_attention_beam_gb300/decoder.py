@@ -152,8 +152,24 @@ class BeamDecoder:
     def status(self, stream=None) -> int:
         return self.lib.gdnbeam_status(self.ctx, stream_handle(stream))
 
-    def reset(self):
-        check(self.lib.gdnbeam_reset(self.ctx), "reset")
+    def reset(self, requests: Optional[Sequence[int]] = None):
+        """Releases the listed requests' contexts (all when None)."""
+        mask = None
+        if requests is not None:
+            m = np.zeros(self.cfg.R, dtype=np.int32)
+            m[list(requests)] = 1
+            mask = m.ctypes.data_as(C.POINTER(C.c_int32))
+        check(self.lib.gdnbeam_reset(self.ctx, mask), "reset")
+
+    def prefill_requests(self, requests: Sequence[int], prompts: torch.Tensor, stream=None):
+        """Prefills only the listed requests (prompt row i for requests[i])
+        into their slots; the others keep their contexts and root rows."""
+        ids = np.ascontiguousarray(np.asarray(requests, dtype=np.int32))
+        count, L = prompts.shape
+        check(self.lib.gdnbeam_prefill_requests(
+            self.ctx, ids.ctypes.data_as(C.POINTER(C.c_int32)), count, ptr(prompts), L,
+            ptr(self.root_logits), ptr(self.root_lse), stream_handle(stream)), "prefill_requests")
+        return self.root_logits, self.root_lse
 
     # ---------------------------------------------------------------- loop
     def decode(self, W: Sequence[int], bias: Optional[torch.Tensor] = None, forced=None,

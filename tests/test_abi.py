@@ -157,7 +157,7 @@ def test_call_sequence_is_enforced_on_the_host():
     assert lib.gdnbeam_select(h, -1, 2, 8, FAKE_WS, FAKE_WS, None, None, FAKE_WS, FAKE_WS, FAKE_WS, None) == gb.EINVAL
     assert lib.gdnbeam_select(h, 0, 8, 9, FAKE_WS, FAKE_WS, None, None, FAKE_WS, FAKE_WS, FAKE_WS, None) == gb.EINVAL
     assert lib.gdnbeam_select(h, 5, 8, 8, FAKE_WS, FAKE_WS, None, None, FAKE_WS, FAKE_WS, FAKE_WS, None) == gb.EINVAL
-    assert lib.gdnbeam_reset(h) == 0
+    assert lib.gdnbeam_reset(h, None) == 0
     assert "select=" in lib.gdnbeam_variant(h).decode()
     lib.gdnbeam_destroy(h)
 
@@ -184,4 +184,27 @@ def test_hot_path_uses_tensor_core_kernels():
     lib.gdnbeam_destroy(h)
     lib, h, _ = make_ctx(synth.TINY)
     assert "proj=simt" in lib.gdnbeam_variant(h).decode()
+    lib.gdnbeam_destroy(h)
+
+
+def test_per_request_reset_and_prefill_argument_checks():
+    # three requests: releasing one blocks decoding until it is prefilled
+    # again; bad request lists are refused before anything is launched
+    wl = synth.TINY.with_(R=3)
+    lib, h, _ = make_ctx(wl)
+    i32 = lambda *v: (C.c_int32 * len(v))(*v)
+    mask = i32(0, 1, 0)
+    assert lib.gdnbeam_reset(h, mask) == 0
+    assert lib.gdnbeam_step(h, 0, 8, None, FAKE_WS, FAKE_WS, FAKE_WS, None, None) == gb.ESTATE
+    assert lib.gdnbeam_read_sctx(h, FAKE_WS, None) == gb.ESTATE
+    pr = lambda ids, n, L=8: lib.gdnbeam_prefill_requests(h, ids, n, FAKE_WS, L, FAKE_WS, FAKE_WS, None)
+    assert pr(i32(1), 0) == 0                 # nothing to do
+    assert pr(i32(3), 1) == gb.EINVAL         # id out of range
+    assert pr(i32(-1), 1) == gb.EINVAL
+    assert pr(i32(1, 1), 2) == gb.EINVAL      # listed twice
+    assert pr(i32(0, 1, 2, 0), 4) == gb.EINVAL  # more ids than requests
+    assert pr(i32(1), 1, L=33) == gb.EINVAL   # L > L_max
+    assert pr(None, 1) == gb.EINVAL
+    assert lib.gdnbeam_prefill_requests(h, i32(1), 1, None, 8, FAKE_WS, FAKE_WS, None) == gb.EINVAL
+    assert lib.gdnbeam_reset(None, None) == gb.EINVAL
     lib.gdnbeam_destroy(h)

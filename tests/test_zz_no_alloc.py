@@ -69,3 +69,33 @@ def test_noalloc_selection_refuses_oversized_calls():
     st = lib.gdnbeam_select_topw_noalloc(R, W_t, W_next, V, gb.BF16, gb.ptr(z), gb.ptr(f), None, None,
                                          gb.ptr(i), gb.ptr(i), gb.ptr(f), None)
     assert st == gb.EWORKSPACE
+
+
+@pytest.mark.parametrize("dtype", [gb.BF16, gb.F32])
+def test_noalloc_selection_after_the_exact_fallback(dtype):
+    # all-equal logits overflow the on-chip candidate buffer and take the
+    # two-stage exact path, which leaves its flags in the shared area; the
+    # next call, on ordinary inputs, must not be steered by them
+    lib = gb.load()
+    R, W_t, W_next, V = 2, 64, 5, 100
+    scratch = torch.empty(lib.gdnbeam_select_scratch_bytes(R, W_t, W_next, V), dtype=torch.uint8, device=DEV)
+    td = torch.bfloat16 if dtype == gb.BF16 else torch.float32
+    ties = (torch.zeros(R * W_t, V, dtype=td, device=DEV), torch.zeros(R * W_t, device=DEV),
+            torch.zeros(R * W_t, device=DEV), None)
+    for call, (z, lse, cum, b) in enumerate([ties, _inputs(7, R, W_t, V, dtype), ties]):
+        ref = _outputs(R, W_next)
+        got = _outputs(R, W_next)
+        assert lib.gdnbeam_select_topw(R, W_t, W_next, V, dtype, gb.ptr(z), gb.ptr(lse), gb.ptr(cum), gb.ptr(b),
+                                       gb.ptr(ref[0]), gb.ptr(ref[1]), gb.ptr(ref[2]), gb.ptr(scratch),
+                                       scratch.numel(), None) == 0
+        assert lib.gdnbeam_select_topw_noalloc(R, W_t, W_next, V, dtype, gb.ptr(z), gb.ptr(lse), gb.ptr(cum),
+                                               gb.ptr(b), gb.ptr(got[0]), gb.ptr(got[1]), gb.ptr(got[2]),
+                                               None) == 0
+        torch.cuda.synchronize()
+        assert lib.gdnbeam_device_status(1) == 0
+        for a, c in zip(ref, got):
+            np.testing.assert_array_equal(a.cpu().numpy(), c.cpu().numpy())
+        if call != 1:  # every candidate ties: the lowest flat indices win
+            for r in range(R):
+                np.testing.assert_array_equal(got[0][r].cpu().numpy(), [0] * 5)
+                np.testing.assert_array_equal(got[1][r].cpu().numpy(), [0, 1, 2, 3, 4])
