@@ -410,11 +410,18 @@ int gdnbeam_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int3
  *   q, k [R*L][H_k*d_k], v [R*L][H*d_v] storage; alpha, beta [R*L][H] fp32;
  *   sctx_out [R][H][d_v][d_k] fp32 (request stride sctx_rstride elements);
  *   o_last [R][H*d_v] storage output at the last position (or NULL);
- *   x_inout optional fp32 [R*L][H*d_v]: o of every position is added to it. */
+ *   x_inout optional fp32 [R*L][H*d_v]: o of every position is added to it.
+ * bf16 storage with d_k = d_v = 128 runs the chunked tensor-core form (OneLA
+ * §2.1 prefill, 64-token chunks); with x_inout it also needs scratch of
+ * gdnbeam_prefill_scan_scratch_bytes(cfg, L, 1) bytes (every chunk's start
+ * state and every token's record, fp32), else GDNBEAM_EWORKSPACE. Other
+ * shapes run the recurrence on CUDA cores and need no scratch (may be NULL). */
+size_t gdnbeam_prefill_scan_scratch_bytes(const gdnbeam_config* cfg, int L, int with_residual);
 int gdnbeam_prefill_scan(const gdnbeam_config* cfg, int L, const void* q, const void* k,
                          const void* v, const float* alpha, const float* beta,
                          float* sctx_out, long long sctx_rstride, void* o_last,
-                         float* x_inout, gdnbeam_stream_t stream);
+                         float* x_inout, void* scratch, size_t scratch_bytes,
+                         gdnbeam_stream_t stream);
 
 #ifdef __cplusplus
 }

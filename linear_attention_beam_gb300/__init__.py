@@ -96,7 +96,9 @@ _SIGS = {
     "gdnbeam_select_noalloc_max_bytes": (_SZ, []),
     "gdnbeam_select_topw_noalloc": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _S]),
     "gdnbeam_ancestry": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S]),
-    "gdnbeam_prefill_scan": (_I, [C.POINTER(Config), _I, _P, _P, _P, _P, _P, _P, _LL, _P, _P, _S]),
+    "gdnbeam_prefill_scan_scratch_bytes": (_SZ, [C.POINTER(Config), _I, _I]),
+    "gdnbeam_prefill_scan": (_I, [C.POINTER(Config), _I, _P, _P, _P, _P, _P, _P, _LL, _P, _P, _P, _SZ,
+                                  _S]),
     "gdnbeam_fullstate_step": (_I, [C.POINTER(Config), _I, _I, _I, _P, _LL, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _P, _P, _S]),
     "gdnbeam_replayssm_step": (_I, [C.POINTER(Config), _I, _I, _P, _LL, _P, _P, _P, _P, _P,

@@ -104,6 +104,8 @@ struct gdnbeam_ctx {
   // prefill buffers for R*L_max rows
   void *pf_u, *pf_q, *pf_k, *pf_v, *pf_feat;
   float *pf_x, *pf_alpha, *pf_beta;
+  void* pf_scr;  // stacked layers on the chunked prefill: chunk states and records
+  size_t pf_scr_bytes;
   // sequencing: prefilled is set while every request holds a prefilled
   // context (live[r]); a per-request reset clears some of them
   int prefilled;
@@ -215,6 +217,9 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
   char* p_pfa = take(pf_rows * c.H * sizeof(float));
   char* p_pfb = take(pf_rows * c.H * sizeof(float));
   char* p_pff = take((size_t)c.R * feat_dim(c) * es);
+  const size_t pscr_b =
+      (c.residual && tc_gemm && tc_prefill_supported(c)) ? prefill_out_scratch_bytes(c, c.L_max) : 0;
+  char* p_pscr = take(pscr_b);
   if (x) {
     x->sctx = p_sctx; x->gtr_k = p_gk; x->gtr_delta = p_gd; x->gtr_alpha = (float*)p_ga;
     x->anc[0] = (int32_t*)p_anc0; x->anc[1] = (int32_t*)p_anc1;
@@ -225,6 +230,7 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
     x->states[0] = p_st0; x->states[1] = p_st1; x->sctx_store = p_sst;
     x->pf_u = p_pfu; x->pf_x = (float*)p_pfx; x->pf_q = p_pfq; x->pf_k = p_pfk;
     x->pf_v = p_pfv; x->pf_alpha = (float*)p_pfa; x->pf_beta = (float*)p_pfb; x->pf_feat = p_pff;
+    x->pf_scr = p_pscr; x->pf_scr_bytes = pscr_b;
   }
   if (fp) {
     fp->sctx_bytes = sctx_b;
@@ -388,7 +394,7 @@ int prefill_pass(gdnbeam_ctx* ctx, const gdnbeam_config& c, const int32_t* promp
     }
     const char* Wp = (const char*)ctx->w.W_proj + (size_t)layer * Np * c.d_model * es;
     float* sc = sctx_base + (size_t)layer * c.H * c.d_v * c.d_k;
-    if (ctx->tc_gemm && tc_prefill_supported(c, c.residual ? ctx->pf_x : nullptr)) {
+    if (ctx->tc_gemm && tc_prefill_supported(c) && !c.residual) {
       // The chunked prefill reads the query only at each request's last
       // token: the projection over all prompt rows skips the query columns,
       // and a second one forms the last rows' queries (into rows 0 .. R-1
@@ -415,9 +421,11 @@ int prefill_pass(gdnbeam_ctx* ctx, const gdnbeam_config& c, const int32_t* promp
     ctx->toc(ev, s);
     if (st) return st;
     ev = ctx->tic(GDNBEAM_STAGE_PREFILL, s);
+    // (stacked layers with tensor cores: the chunked prefill, every
+    // position's o added to the stream through pf_scr)
     st = launch_prefill_scan(c, L, ctx->pf_q, ctx->pf_k, ctx->pf_v, ctx->pf_alpha, ctx->pf_beta,
                              sc, rstride, c.residual ? nullptr : ctx->pf_feat,
-                             c.residual ? ctx->pf_x : nullptr, s);
+                             c.residual ? ctx->pf_x : nullptr, s, ctx->pf_scr, ctx->pf_scr_bytes);
     ctx->toc(ev, s);
     if (st) return st;
   }
@@ -860,15 +868,21 @@ int gdnbeam_ancestry(int R, int t, int T, int V, int W_prev, int W_t, const int3
                          sid_out, err_ptr(), (cudaStream_t)stream);
 }
 
+size_t gdnbeam_prefill_scan_scratch_bytes(const gdnbeam_config* cfg, int L, int with_residual) {
+  if (validate(cfg) || L < 1 || !with_residual) return 0;
+  return tc_prefill_supported(*cfg) ? prefill_out_scratch_bytes(*cfg, L) : 0;
+}
+
 int gdnbeam_prefill_scan(const gdnbeam_config* cfg, int L, const void* q, const void* k,
                          const void* v, const float* alpha, const float* beta, float* sctx_out,
-                         long long sctx_rstride, void* o_last, float* x_inout,
-                         gdnbeam_stream_t stream) {
+                         long long sctx_rstride, void* o_last, float* x_inout, void* scratch,
+                         size_t scratch_bytes, gdnbeam_stream_t stream) {
   int st = validate(cfg);
   if (st) return st;
   if (L < 1 || !q || !k || !v || !alpha || !beta || !sctx_out) return GDNBEAM_EINVAL;
+  if (x_inout && scratch_bytes < gdnbeam_prefill_scan_scratch_bytes(cfg, L, 1)) return GDNBEAM_EWORKSPACE;
   return launch_prefill_scan(*cfg, L, q, k, v, alpha, beta, sctx_out, sctx_rstride, o_last,
-                             x_inout, (cudaStream_t)stream);
+                             x_inout, (cudaStream_t)stream, scratch, scratch_bytes);
 }
 
 }  // extern "C"

@@ -259,14 +259,25 @@ int dispatch_dk(const gdnbeam_config& c, int L, const void* q, const void* k, co
 
 int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const void* k,
                         const void* v, const float* alpha, const float* beta, float* sctx,
-                        long long rs, void* o_last, float* x, cudaStream_t s) {
+                        long long rs, void* o_last, float* x, cudaStream_t s, void* scratch,
+                        size_t scratch_bytes) {
   if (L <= 0) return GDNBEAM_EINVAL;
   if (c.d_v > 128 && c.d_v % 128 != 0) return GDNBEAM_EUNSUPPORTED;
-  if (tc_prefill_supported(c, x)) {
+  const size_t out_bytes = x ? prefill_out_scratch_bytes(c, L) : 0;
+  if (tc_prefill_supported(c) && (!x || (scratch && scratch_bytes >= out_bytes))) {
     const long long qw = (long long)key_heads(c) * c.d_k;
     // (bf16 queries: two bytes each)
-    return launch_prefill_tc(c, L, (const char*)q + (size_t)(L - 1) * qw * 2,
-                             (long long)L * qw, k, v, alpha, beta, sctx, rs, o_last, s);
+    const char* q_last = (const char*)q + (size_t)(L - 1) * qw * 2;
+    if (!x)
+      return launch_prefill_tc(c, L, q_last, (long long)L * qw, k, v, alpha, beta, sctx, rs, o_last, s);
+    // stacked layers: the chain leaves every chunk's start state and every
+    // token's record in scratch, then every position's o joins the stream
+    float* dl = (float*)scratch;
+    float* s0 = dl + (size_t)c.R * L * c.H * c.d_v;
+    int st = launch_prefill_tc(c, L, q_last, (long long)L * qw, k, v, alpha, beta, sctx, rs, o_last,
+                               s, s0, dl);
+    if (st) return st;
+    return launch_prefill_out_tc(c, L, q, k, alpha, s0, dl, x, s);
   }
   if (c.dtype == GDNBEAM_BF16)
     return dispatch_dk<__nv_bfloat16>(c, L, q, k, v, alpha, beta, sctx, rs, o_last, x, s);

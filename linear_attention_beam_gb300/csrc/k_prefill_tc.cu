@@ -87,6 +87,10 @@ struct PrefillTcParams {
   float* sctx;                // S_ctx of head h of request r at sctx + r*rstride + h*128*128
   long long rstride;
   __nv_bfloat16* o_last;      // [R][H*128] or null
+  // stacked layers: every chunk's start state and every token's record, for
+  // the all-position outputs (k_prefill_out_tc.cu)
+  float* s0_out;              // [R*H][n_chunks][128 v][128 k] (chunk 0 not written)
+  float* delta_out;           // [R*L][H*128]
   unsigned* err;
 };
 
@@ -117,6 +121,7 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = bf2_bits(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
 }
 
+template <bool kAllOut>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, PrefillTcParams p) {
@@ -328,6 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               split2(__uint_as_float(x[u][2 * e]), __uint_as_float(x[u][2 * e + 1]), hi[e], lo[e]);
             tc::tmem_st16(lb + cSAHI + 16 * (q + u), hi);
             tc::tmem_st16(lb + cSALO + 16 * (q + u), lo);
+            if (kAllOut) {  // the chunk's start state, row v
+              float4* dst = reinterpret_cast<float4*>(
+                  p.s0_out + (((size_t)blockIdx.x * n_chunks + c) * DH + v) * DH + 32 * (q + u));
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                dst[e] = make_float4(__uint_as_float(x[u][4 * e]), __uint_as_float(x[u][4 * e + 1]),
+                                     __uint_as_float(x[u][4 * e + 2]), __uint_as_float(x[u][4 * e + 3]));
+            }
           }
         }
       }
@@ -393,6 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld32_nowait(lb + cZD, d[0]);
         tc::tmem_ld32_nowait(lb + cZD + 32, d[1]);
         tc::tmem_wait_ld();
+        if (kAllOut) {  // the chunk's records, value row v
+          const int n_tok = min(CH, p.L - c * CH);
+          float* dst = p.delta_out + ((size_t)r * p.L + (size_t)c * CH) * p.H * DH + (size_t)h * DH + v;
+#pragma unroll
+          for (int i = 0; i < CH; ++i)
+            if (i < n_tok) dst[(size_t)i * p.H * DH] = __uint_as_float(d[i >> 5][i & 31]);
+        }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t hi[16], lo[16];
@@ -656,34 +676,50 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// [R][L][width] bf16 rows as a 3-D map with a [64 columns][128 rows] box,
-// 128-byte swizzled; rows past L read as zeros.
-bool prompt_map(CUtensorMap* map, const void* ptr, int R, int L, int width) {
+}  // namespace
+
+// [R][L][width] bf16 rows as a 3-D map with a [64 columns][box_rows rows]
+// box, 128-byte swizzled; rows past L read as zeros.
+bool prefill_rows_map(CUtensorMap* map, const void* ptr, int R, int L, int width, int box_rows) {
   EncodeTiledFn fn = encode_tiled();
-  if (!fn || ((uintptr_t)ptr & 15) != 0) return false;
+  if (!fn || ((uintptr_t)ptr & 15) != 0 || (width * 2) % 16 != 0) return false;
   cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)L, (cuuint64_t)R};
   cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)L * width * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)PAIR, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
+// The fp32 residual stream [R][L][width] as a 3-D map with [128 columns][64
+// rows] boxes, unswizzled; rows past L read as zeros.
+bool prefill_stream_map(CUtensorMap* map, const float* x, int R, int L, int width) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn || ((uintptr_t)x & 15) != 0 || (width * 4) % 16 != 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)L, (cuuint64_t)R};
+  cuuint64_t strides[2] = {(cuuint64_t)width * 4, (cuuint64_t)L * width * 4};
+  cuuint32_t box[3] = {128, 64, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(x), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
-bool tc_prefill_supported(const gdnbeam_config& c, const float* x_inout) {
-  return c.dtype == GDNBEAM_BF16 && c.d_k == DH && c.d_v == DH && x_inout == nullptr;
+bool tc_prefill_supported(const gdnbeam_config& c) {
+  return c.dtype == GDNBEAM_BF16 && c.d_k == DH && c.d_v == DH;
 }
 
 int launch_prefill_tc(const gdnbeam_config& c, int L, const void* q_last, long long q_last_ld,
                       const void* k, const void* v, const float* alpha, const float* beta,
-                      float* sctx, long long rstride, void* o_last, cudaStream_t s) {
+                      float* sctx, long long rstride, void* o_last, cudaStream_t s,
+                      float* s0_out, float* delta_out) {
   if (L <= 0) return GDNBEAM_EINVAL;
   const int Hk = key_heads(c);
   if ((long long)c.R * L > 0x7FFFFFFFLL) return GDNBEAM_EUNSUPPORTED;
+  if ((s0_out == nullptr) != (delta_out == nullptr)) return GDNBEAM_EINVAL;
   CUtensorMap mk, mv;
-  if (!prompt_map(&mk, k, c.R, L, Hk * DH) || !prompt_map(&mv, v, c.R, L, c.H * DH))
+  if (!prefill_rows_map(&mk, k, c.R, L, Hk * DH, PAIR) || !prefill_rows_map(&mv, v, c.R, L, c.H * DH, PAIR))
     return GDNBEAM_ECUDA;
   PrefillTcParams p{};
   p.R = c.R; p.H = c.H; p.Hk = Hk; p.L = L;
@@ -693,10 +729,17 @@ int launch_prefill_tc(const gdnbeam_config& c, int L, const void* q_last, long l
   p.q_last_ld = q_last_ld;
   p.sctx = sctx; p.rstride = rstride;
   p.o_last = reinterpret_cast<__nv_bfloat16*>(o_last);
+  p.s0_out = s0_out; p.delta_out = delta_out;
   p.err = error_word();
-  GDN_CUDA(cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kDynSmem));
-  prefill_tc_kernel<<<c.R * c.H, kThreads, kDynSmem, s>>>(mk, mv, p);
+  if (s0_out) {
+    GDN_CUDA(cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kDynSmem));
+    prefill_tc_kernel<true><<<c.R * c.H, kThreads, kDynSmem, s>>>(mk, mv, p);
+  } else {
+    GDN_CUDA(cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kDynSmem));
+    prefill_tc_kernel<false><<<c.R * c.H, kThreads, kDynSmem, s>>>(mk, mv, p);
+  }
   GDN_LAUNCH_CHECK();
   return GDNBEAM_OK;
 }

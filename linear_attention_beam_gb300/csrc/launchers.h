@@ -2,6 +2,7 @@
 // Each returns a GDNBEAM_* status; all take the device error word pointer.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -116,17 +117,37 @@ int launch_replayssm(int dtype, const ReplaySsmArgs& a, cudaStream_t s);
 // dst[i] = storage(src[i]) for n elements (S_ctx copy for the FullState path).
 int launch_to_storage(int dtype, size_t n, const float* src, void* dst, cudaStream_t s);
 
-// Chunked tensor-core prefill (bf16, d_k = d_v = 128, no residual stream):
-// S_ctx and o at the last token, as launch_prefill_scan.
-bool tc_prefill_supported(const gdnbeam_config& c, const float* x_inout);
+// Chunked tensor-core prefill (bf16, d_k = d_v = 128): S_ctx and o at the
+// last token, as launch_prefill_scan.
+bool tc_prefill_supported(const gdnbeam_config& c);
+// [R][L][width] bf16 rows as a 3-D TMA map, [64 columns][box_rows rows]
+// boxes, 128-byte swizzled, rows past L read as zeros.
+bool prefill_rows_map(CUtensorMap* map, const void* ptr, int R, int L, int width, int box_rows);
+// The fp32 residual stream [R][L][width] as a 3-D TMA map with [128 columns]
+// [64 rows] boxes, unswizzled, rows past L read as zeros.
+bool prefill_stream_map(CUtensorMap* map, const float* x, int R, int L, int width);
 // q_last: each request's query row at its last prompt token, q_last_ld
-// elements apart.
+// elements apart. s0_out, delta_out (both or neither): every 64-token
+// chunk's start state [R*H][2*ceil(L/128)][128][128] and every token's
+// record [R*L][H*128], fp32, for launch_prefill_out_tc.
 int launch_prefill_tc(const gdnbeam_config& c, int L, const void* q_last, long long q_last_ld,
                       const void* k, const void* v, const float* alpha, const float* beta,
-                      float* sctx, long long rstride, void* o_last, cudaStream_t s);
+                      float* sctx, long long rstride, void* o_last, cudaStream_t s,
+                      float* s0_out = nullptr, float* delta_out = nullptr);
+// Stacked layers: adds o of every prompt position to the residual stream x
+// [R*L][H*128] from the chunk states and records launch_prefill_tc left in
+// scratch (prefill_out_scratch_bytes: the records, then the chunk states).
+size_t prefill_out_scratch_bytes(const gdnbeam_config& c, int L);
+int launch_prefill_out_tc(const gdnbeam_config& c, int L, const void* q, const void* k,
+                          const float* alpha, const float* s0, const float* delta, float* x,
+                          cudaStream_t s);
+// Prefill over L tokens of every request: the chunked tensor-core kernels
+// when the shape allows (with a residual stream x_inout only when scratch
+// holds prefill_out_scratch_bytes), else the recurrent CUDA-core scan.
 int launch_prefill_scan(const gdnbeam_config& c, int L, const void* q, const void* k,
                         const void* v, const float* alpha, const float* beta, float* sctx,
-                        long long sctx_rstride, void* o_last, float* x_inout, cudaStream_t s);
+                        long long sctx_rstride, void* o_last, float* x_inout, cudaStream_t s,
+                        void* scratch = nullptr, size_t scratch_bytes = 0);
 
 // Selection scratch and launch. hint (may be NULL): per (row, 256-code tile)
 // the maximum logit in .x, as the logits stages leave it; NULL computes it.

@@ -336,6 +336,18 @@ def test_prefill_chunked_tensor_cores(H, Hk, R, L, a_lo, a_hi):
     _prefill_scan_op("bf16", 128, 128, H, Hk, R, L, False, a_lo, a_hi)
 
 
+@pytest.mark.parametrize("H,Hk,R,L,a_lo,a_hi", [
+    (2, 2, 1, 1, 0.3, 1.0), (2, 2, 2, 64, 0.3, 1.0), (2, 1, 1, 65, 0.3, 1.0),
+    (4, 2, 2, 129, 0.3, 1.0), (2, 2, 1, 300, 0.01, 0.3), (1, 1, 1, 1000, 0.9, 1.0),
+    (2, 2, 3, 257, 0.5, 1.0)])
+def test_prefill_chunked_all_positions(H, Hk, R, L, a_lo, a_hi):
+    # stacked layers: the chunked tcgen05 prefill also adds o of every prompt
+    # position to the residual stream (chunk states and records from the
+    # chain, all positions' outputs from the parallel kernel); checked
+    # against the oracle's recurrence at every position
+    _prefill_scan_op("bf16", 128, 128, H, Hk, R, L, True, a_lo, a_hi)
+
+
 def _prefill_scan_op(dtype, dk, dv, H, Hk, R, L, resid, a_lo=0.3, a_hi=1.0):
     wl = synth.tiny_workload(d=dk, d_v=dv, V=5, H=H, R=R, dtype=dtype, H_k=Hk)
     rng = np.random.default_rng(L + dk + dv)
@@ -351,9 +363,14 @@ def _prefill_scan_op(dtype, dk, dv, H, Hk, R, L, resid, a_lo=0.3, a_hi=1.0):
     sc = torch.empty(R, H, dv, dk, dtype=torch.float32, device=DEV)
     ol = torch.empty(R, H * dv, dtype=td, device=DEV)
     xd = to_dev(x0.reshape(R * L, H * dv)) if resid else None
-    st = lib.gdnbeam_prefill_scan(C.byref(cfg), L, gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
-                                  gb.ptr(to_dev(v.reshape(-1), td)), gb.ptr(to_dev(a.reshape(-1))),
-                                  gb.ptr(to_dev(b.reshape(-1))), gb.ptr(sc), H * dv * dk, gb.ptr(ol), gb.ptr(xd), None)
+    sb = lib.gdnbeam_prefill_scan_scratch_bytes(C.byref(cfg), L, int(resid))
+    scr = torch.empty(max(sb, 1), dtype=torch.uint8, device=DEV)
+    args = (C.byref(cfg), L, gb.ptr(to_dev(q.reshape(-1), td)), gb.ptr(to_dev(k.reshape(-1), td)),
+            gb.ptr(to_dev(v.reshape(-1), td)), gb.ptr(to_dev(a.reshape(-1))),
+            gb.ptr(to_dev(b.reshape(-1))), gb.ptr(sc), H * dv * dk, gb.ptr(ol), gb.ptr(xd))
+    if sb:  # the chunked form with a residual stream needs its scratch
+        assert lib.gdnbeam_prefill_scan(*args, gb.ptr(scr), sb - 1, None) == gb.EWORKSPACE
+    st = lib.gdnbeam_prefill_scan(*args, gb.ptr(scr), sb, None)
     assert st == 0
     g = H // Hk
     for r in range(R):
@@ -361,8 +378,9 @@ def _prefill_scan_op(dtype, dk, dv, H, Hk, R, L, resid, a_lo=0.3, a_hi=1.0):
         S, o = oracle.prefill_scan(qe, ke, v[r], a[r], b[r])
         assert maxrel(host(sc[r]), S) <= _tol(wl), "S_ctx"
         _check_stored(host(ol[r]).reshape(H, dv), o[-1], wl, "o_last")
-        if resid:
-            assert maxrel(host(xd).reshape(R, L, H * dv)[r], x0[r] + o.reshape(L, H * dv)) <= _tol(wl)
+        if resid:  # what was added to the stream is o of every position
+            added = host(xd).reshape(R, L, H * dv)[r].astype(np.float64) - x0[r]
+            assert maxrel(added, o.reshape(L, H * dv)) <= _tol(wl), "o at every position"
 
 
 # ------------------------------------------------------------------ tensor-core GEMMs
