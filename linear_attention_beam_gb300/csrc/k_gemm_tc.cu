@@ -18,11 +18,16 @@
 //               producers of both CTAs and each finished tile to the epilogue;
 //   warps 2-5   read the accumulator rows out of TMEM (lane = tile row) and
 //   (2-9)       run the fused epilogue while the next tile accumulates into
-//               the other TMEM buffer.
+//               the other TMEM buffer. Each epilogue warp writes its bf16
+//               outputs 32 rows x 64 columns at a time into its own
+//               128-byte-swizzled staging buffer and stores the box by TMA,
+//               so global writes go out as whole rows, not one 16-byte piece
+//               of 32 different rows per instruction.
 // Every mbarrier wait is bounded in time; on a time-out the kernel raises
 // GDNBEAM_DERR_TIMEOUT, all roles leave their loops, in-flight copies and
 // MMAs are drained (again with a bound) and TMEM is freed.
 #include <cuda.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "launchers.h"
@@ -39,7 +44,6 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kNumBars = 2 * STAGES + 4 + 1;
-constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + 1024 + kNumBars * 8 + 16;
 
 enum { EPI_LOGITS = 0, EPI_PROJ = 1 };
 
@@ -50,7 +54,18 @@ enum { EPI_LOGITS = 0, EPI_PROJ = 1 };
 template <int EPI> struct Epi {
   static constexpr int kWarps = EPI == EPI_LOGITS ? 8 : 4;
   static constexpr int kThreads = 64 + 32 * kWarps;
+  // one epilogue warp's staging box: 32 rows x 32 bf16 (64-byte rows) for the
+  // logits, whose eight warps must fit beside the operand ring; 32 rows x 64
+  // bf16 (128-byte rows) for the projections
+  static constexpr int kBoxCols = EPI == EPI_LOGITS ? 32 : 64;
+  static constexpr int kStgBytes = 32 * kBoxCols * 2;
+  // operand ring, the epilogue warps' staging boxes, barriers
+  static constexpr size_t kSmemBytes =
+      (size_t)STAGES * STAGE_BYTES + (size_t)kWarps * kStgBytes + 1024 + kNumBars * 8 + 16;
 };
+// dynamic plus static shared memory (the logits pair partials, 2 KiB) per block
+static_assert(Epi<EPI_LOGITS>::kSmemBytes + 2048 <= 232448, "shared memory of the logits GEMM");
+static_assert(Epi<EPI_PROJ>::kSmemBytes + 2048 <= 232448, "shared memory of the projection GEMM");
 
 struct EpiArgs {
   int M, N, K;
@@ -67,8 +82,26 @@ struct EpiArgs {
   float *dq, *dk, *dv, *da, *db;
 };
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32]) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) d4[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+}
+
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+  return (uint32_t)row * 128u + ((uint32_t)(((col >> 3) ^ (row & 7)) & 7) << 4) +
+         (uint32_t)(col & 7) * 2u;
+}
+
+// 64-byte swizzle of a [rows][32 bf16] box: the 16-byte piece c of row r sits
+// at piece c ^ ((r >> 1) & 3) of the row (address bits 4-5 XOR bits 7-8).
+__device__ __forceinline__ uint32_t sw64_off(int row, int piece) {
+  return (uint32_t)row * 64u + ((uint32_t)((piece ^ (row >> 1)) & 3) << 4);
+}
+
+// 32 fp32 values of this lane's row as bf16 into a 32-column staging box
+// (row = lane; 64-byte swizzle).
+__device__ __forceinline__ void stage_bf16x32_sw64(uint8_t* stg, int lane, const float (&v)[32]) {
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
     uint32_t p[4];
@@ -77,57 +110,94 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
       __nv_bfloat162 h = __floats2bfloat162_rn(v[w * 8 + 2 * j], v[w * 8 + 2 * j + 1]);
       p[j] = *reinterpret_cast<uint32_t*>(&h);
     }
-    d4[w] = make_uint4(p[0], p[1], p[2], p[3]);
+    *reinterpret_cast<uint4*>(stg + sw64_off(lane, w)) = make_uint4(p[0], p[1], p[2], p[3]);
   }
 }
 
-__device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32]) {
-  float4* d4 = reinterpret_cast<float4*>(dst);
+// 32 fp32 values of this lane's row as bf16 into columns col0 .. col0+31 of
+// a 64-column staging box (row = lane; 128-byte swizzle).
+__device__ __forceinline__ void stage_bf16x32(uint8_t* stg, int lane, int col0, const float (&v)[32]) {
 #pragma unroll
-  for (int w = 0; w < 8; ++w) d4[w] = make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+  for (int w = 0; w < 4; ++w) {
+    uint32_t p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[w * 8 + 2 * j], v[w * 8 + 2 * j + 1]);
+      p[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(stg + sw128_off(lane, col0 + 8 * w)) = make_uint4(p[0], p[1], p[2], p[3]);
+  }
+}
+
+// Waits until this warp's previous box store has read its staging buffer.
+__device__ __forceinline__ void staging_free(int lane) {
+  if (lane == 0) tc::bulk_wait_read<0>();
+  __syncwarp();
+}
+
+// Sends the warp's staged box to (x, y) of the map.
+__device__ __forceinline__ void staging_store(const CUtensorMap* map, int x, int y, uint32_t stg_s,
+                                              int lane) {
+  tc::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tc::tma_store_2d(map, x, y, stg_s);
+    tc::bulk_commit();
+  }
 }
 
 // Logits epilogue for one tile row and one half of the tile's columns: bf16
-// z, optional fp32 dump, and the half row's (max, sum exp), returned.
-__device__ __forceinline__ float2 epi_logits(const EpiArgs& ea, uint32_t taddr, int m, int n0,
-                                             int half) {
+// z (staged, stored by TMA in boxes of 32 columns), optional fp32 dump, and
+// the half row's (max, sum exp), returned. y0: first row of the warp's 32.
+__device__ __forceinline__ float2 epi_logits(const EpiArgs& ea, const CUtensorMap* tmz, uint32_t taddr,
+                                             uint8_t* stg, uint32_t stg_s, int lane, int m, int y0,
+                                             int n0, int half) {
   float run_max = -INFINITY, run_sum = 0.0f;
   const bool row_ok = m < ea.M;
 #pragma unroll 1
   for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
+    const int n = n0 + c * 32;
+    if (n >= ea.N) break;  // warp-uniform
+    staging_free(lane);
     float v[32];
     tc::tmem_ld32(taddr + c * 32, v);
-    const int n = n0 + c * 32;
-    if (!row_ok || n >= ea.N) continue;
-    const size_t off = (size_t)m * ea.N + n;
-    if (n + 32 <= ea.N) {
-      store_bf16x32(ea.z + off, v);
-      if (ea.z_dump) store_f32x32(ea.z_dump + off, v);
-    } else {
-      for (int j = 0; j < 32 && n + j < ea.N; ++j) {
-        ea.z[off + j] = __float2bfloat16_rn(v[j]);
-        if (ea.z_dump) ea.z_dump[off + j] = v[j];
+    stage_bf16x32_sw64(stg, lane, v);
+    staging_store(tmz, n, y0, stg_s, lane);  // rows past M, columns past N are not written
+    {
+      if (!row_ok) continue;
+      if (ea.z_dump) {
+        const size_t off = (size_t)m * ea.N + n;
+        if (n + 32 <= ea.N) {
+          store_f32x32(ea.z_dump + off, v);
+        } else {
+          for (int j = 0; j < 32 && n + j < ea.N; ++j) ea.z_dump[off + j] = v[j];
+        }
       }
+      const int cnt = min(32, ea.N - n);
+      float cm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < cnt) cm = fmaxf(cm, v[j]);
+      const float nm = fmaxf(run_max, cm);
+      float sm = run_sum * expf(run_max - nm);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < cnt) sm += expf(v[j] - nm);
+      run_sum = sm;
+      run_max = nm;
     }
-    const int cnt = min(32, ea.N - n);
-    float cm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < cnt) cm = fmaxf(cm, v[j]);
-    const float nm = fmaxf(run_max, cm);
-    float s = run_sum * expf(run_max - nm);
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < cnt) s += expf(v[j] - nm);
-    run_sum = s;
-    run_max = nm;
   }
   return make_float2(run_max, run_sum);
 }
 
 // Projection epilogue for one tile row and one of the tile's two heads
-// (head width 128).
-__device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int m, int n0, int g) {
+// (head width 128): q and k L2-normalised per head, v as is (bf16, staged
+// and stored by TMA in boxes of 64 columns), the gates in fp32. y0: first
+// row of the warp's 32; tmq, tmk, tmv: the outputs' maps.
+__device__ __forceinline__ void epi_proj(const EpiArgs& ea, const CUtensorMap* tmq,
+                                         const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                         uint32_t taddr, uint8_t* stg, uint32_t stg_s, int lane,
+                                         int m, int y0, int n0, int g) {
   const int H = ea.H, Hk = ea.Hk, D = 128;
   const bool row_ok = m < ea.M;
   const int q_end = Hk * D, k_end = 2 * Hk * D, v_end = k_end + H * D;
@@ -147,31 +217,38 @@ __device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int 
         for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
       }
       const float inv = 1.0f / sqrtf(ss + 1e-6f);
-      __nv_bfloat16* dst = is_q ? ea.q : ea.k;
       float* dmp = is_q ? ea.dq : ea.dk;
       const size_t off = (size_t)m * Hk * D + (size_t)head * D;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tc::tmem_ld32(ta + c * 32, v);
+      for (int bx = 0; bx < 2; ++bx) {
+        staging_free(lane);
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * bx + cc;
+          float v[32];
+          tc::tmem_ld32(ta + c * 32, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= inv;
-        if (row_ok) {
-          store_bf16x32(dst + off + c * 32, v);
-          if (dmp) store_f32x32(dmp + off + c * 32, v);
+          for (int j = 0; j < 32; ++j) v[j] *= inv;
+          stage_bf16x32(stg, lane, 32 * cc, v);
+          if (row_ok && dmp) store_f32x32(dmp + off + c * 32, v);
         }
+        staging_store(is_q ? tmq : tmk, head * D + bx * 64, y0, stg_s, lane);
       }
     } else if (col0 < v_end) {
       const int head = (col0 - k_end) / D;
       const size_t off = (size_t)m * H * D + (size_t)head * D;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tc::tmem_ld32(ta + c * 32, v);
-        if (row_ok) {
-          store_bf16x32(ea.v + off + c * 32, v);
-          if (ea.dv) store_f32x32(ea.dv + off + c * 32, v);
+      for (int bx = 0; bx < 2; ++bx) {
+        staging_free(lane);
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * bx + cc;
+          float v[32];
+          tc::tmem_ld32(ta + c * 32, v);
+          stage_bf16x32(stg, lane, 32 * cc, v);
+          if (row_ok && ea.dv) store_f32x32(ea.dv + off + c * 32, v);
         }
+        staging_store(tmv, head * D + bx * 64, y0, stg_s, lane);
       }
     } else {
       // gate columns: H decay-gate logits, then H write-gate logits
@@ -201,18 +278,21 @@ __device__ __forceinline__ void epi_proj(const EpiArgs& ea, uint32_t taddr, int 
 template <int EPI>
 __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   EpiArgs ea) {
+                   const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
+                   const __grid_constant__ CUtensorMap tmC2, EpiArgs ea) {
+  // output maps: logits z (C0); projections q (C0), k (C1), v (C2)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+  const uint32_t stg0 = base + STAGES * STAGE_BYTES;  // epilogue warps' staging boxes
+  const uint32_t bar0 = stg0 + Epi<EPI>::kWarps * Epi<EPI>::kStgBytes;
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
   auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + kNumBars * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 - base) + kNumBars * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto sA = [&](int s) { return base + (uint32_t)s * STAGE_BYTES; };
   auto sB = [&](int s) { return base + (uint32_t)s * STAGE_BYTES + A_BYTES; };
@@ -321,6 +401,8 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThr
     const int half = (warp - 2) >> 2;
     const int pair_bar = 1 + lane_grp;
     const int row = lane_grp * 32 + lane;
+    const uint32_t stg_s = stg0 + (uint32_t)(warp - 2) * Epi<EPI>::kStgBytes;
+    uint8_t* stg = gbase + (stg_s - base);
     __shared__ float2 s_half[2][4][32];  // the second half's row partials, per accumulator
     int i = 0;
     for (int tile = cid; tile < num_tiles; tile += n_clusters, ++i) {
@@ -339,8 +421,9 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThr
       const int m_tile = 2 * (tile / n_tiles) + rank, n_tile = tile % n_tiles;
       const uint32_t taddr = tmem_base + ((uint32_t)(lane_grp * 32) << 16) + (uint32_t)(acc * BN);
       const int m = m_tile * BM + row;
+      const int y0 = m_tile * BM + lane_grp * 32;
       if (EPI == EPI_LOGITS) {
-        const float2 pr = epi_logits(ea, taddr, m, n_tile * BN, half);
+        const float2 pr = epi_logits(ea, &tmC0, taddr, stg, stg_s, lane, m, y0, n_tile * BN, half);
         if (half) s_half[acc][lane_grp][lane] = pr;
         tc::named_sync(pair_bar, 64);
         if (!half && m < ea.M) {
@@ -352,12 +435,16 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThr
           ea.part[(size_t)m * n_tiles + n_tile] = make_float2(nm, sum);
         }
       } else {
-        for (int g = 0; g < BN / 128; ++g) epi_proj(ea, taddr, m, n_tile * BN, g);
+        for (int g = 0; g < BN / 128; ++g)
+          epi_proj(ea, &tmC0, &tmC1, &tmC2, taddr, stg, stg_s, lane, m, y0, n_tile * BN, g);
       }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tempty(acc));
     }
+    // the warp's box stores have finished before the CTA leaves
+    if (lane == 0) tc::bulk_wait_all();
+    __syncwarp();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -425,6 +512,23 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int box_row
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output map of a GEMM epilogue: row-major bf16 [rows][cols] with a box of
+// box_cols (64: 128-byte swizzle; 32: 64-byte swizzle) x 32 rows, one
+// epilogue warp's staging box.
+bool make_store_map(CUtensorMap* map, const void* ptr, int rows, int cols, int box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !ptr || ((uintptr_t)ptr & 15) != 0 || (cols * 2) % 16 != 0) return false;
+  if (box_cols != 32 && box_cols != 64) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms() {
   static int sms[64] = {0};
   int dev = 0;
@@ -444,7 +548,7 @@ int max_clusters() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CLUSTER * (num_sms() / CLUSTER), 1, 1);
     cfg.blockDim = dim3(Epi<EPI>::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = Epi<EPI>::kSmemBytes;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = CLUSTER;
@@ -460,9 +564,11 @@ int max_clusters() {
   return cached[dev][EPI];
 }
 
+// out[i]: the epilogue's output maps (see tc_gemm_kernel); unused ones are
+// left zeroed and never referenced.
 template <int EPI>
-int launch_gemm(const void* A, const void* B, const EpiArgs& ea, cudaStream_t s,
-                long long lda = 0) {
+int launch_gemm(const void* A, const void* B, const EpiArgs& ea, const CUtensorMap (&out)[3],
+                cudaStream_t s, long long lda = 0) {
   if (ea.M <= 0) return GDNBEAM_OK;
   CUtensorMap ta, tb;
   if (!make_map(&ta, A, ea.M, ea.K, BM, lda) || !make_map(&tb, B, ea.N, ea.K, BN / 2))
@@ -470,14 +576,15 @@ int launch_gemm(const void* A, const void* B, const EpiArgs& ea, cudaStream_t s,
   static bool attr_set[2] = {false, false};
   if (!attr_set[EPI]) {
     GDN_CUDA(cudaFuncSetAttribute(tc_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kSmemBytes));
+                                  (int)Epi<EPI>::kSmemBytes));
     attr_set[EPI] = true;
   }
   const int pair_tiles = ((ea.M + BM - 1) / BM + 1) / 2 * ((ea.N + BN - 1) / BN);
   int clusters = max_clusters<EPI>();
   if (clusters <= 0) return GDNBEAM_ECUDA;
   if (clusters > pair_tiles) clusters = pair_tiles;
-  tc_gemm_kernel<EPI><<<CLUSTER * clusters, Epi<EPI>::kThreads, kSmemBytes, s>>>(ta, tb, ea);
+  tc_gemm_kernel<EPI><<<CLUSTER * clusters, Epi<EPI>::kThreads, Epi<EPI>::kSmemBytes, s>>>(
+      ta, tb, out[0], out[1], out[2], ea);
   GDN_LAUNCH_CHECK();
   return GDNBEAM_OK;
 }
@@ -520,7 +627,17 @@ int launch_tc_project(const gdnbeam_config& c, int n, const void* u, const void*
   if (d) {
     ea.dq = d->q; ea.dk = d->k; ea.dv = d->v; ea.da = d->alpha; ea.db = d->beta;
   }
-  return launch_gemm<EPI_PROJ>(u, W_proj, ea, s, ldu);
+  CUtensorMap out[3];
+  memset(out, 0, sizeof(out));
+  const int kw = key_heads(c) * c.d_k;
+  // the maps of the outputs this call writes
+  const bool want_q = cols != PROJ_NO_Q, want_kv = cols != PROJ_Q_ONLY;
+  constexpr int bc = Epi<EPI_PROJ>::kBoxCols;
+  if ((want_q && !make_store_map(&out[0], q, n, kw, bc)) ||
+      (want_kv && (!make_store_map(&out[1], k, n, kw, bc) ||
+                   !make_store_map(&out[2], v, n, c.H * c.d_v, bc))))
+    return GDNBEAM_ECUDA;
+  return launch_gemm<EPI_PROJ>(u, W_proj, ea, out, s, ldu);
 }
 
 size_t tc_logits_scratch_bytes(const gdnbeam_config& c, int n) {
@@ -536,7 +653,10 @@ int launch_tc_logits(const gdnbeam_config& c, int n, const void* feat, const voi
   ea.z = (__nv_bfloat16*)z;
   ea.z_dump = d ? d->logits : nullptr;
   ea.part = (float2*)scratch;
-  int st = launch_gemm<EPI_LOGITS>(feat, W_o, ea, s);
+  CUtensorMap out[3];
+  memset(out, 0, sizeof(out));
+  if (!make_store_map(&out[0], z, n, c.V, Epi<EPI_LOGITS>::kBoxCols)) return GDNBEAM_ECUDA;
+  int st = launch_gemm<EPI_LOGITS>(feat, W_o, ea, out, s);
   if (st) return st;
   const int n_tiles = (c.V + BN - 1) / BN;
   lse_reduce_kernel<<<(n + 7) / 8, 256, 0, s>>>(n, n_tiles, (const float2*)scratch, lse);

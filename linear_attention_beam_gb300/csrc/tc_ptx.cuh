@@ -353,6 +353,15 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int 
       "r"(x), "r"(y), "r"(z), "r"(src)
       : "memory");
 }
+// 2-D tile store from shared memory (x innermost, in elements); parts of
+// the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          (uint64_t)map),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
