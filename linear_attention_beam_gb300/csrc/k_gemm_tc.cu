@@ -5,24 +5,28 @@
 //   * codebook logits Z = F . W_o^T, with the bf16 store of z and per-tile
 //     (max, sum exp) partials of the row log-normaliser fused in.
 //
-// Persistent CTAs in clusters of two, one CTA per SM, 192 (projections) or
-// 320 (logits) threads in three roles. The two CTAs of a cluster take vertically adjacent tiles (m, n) and
-// (m + 1, n) in lockstep and share the B tile: each loads its own A tile and
-// one 128-row half of B, multicast into both CTAs, so B leaves L2 once per
-// pair of tiles.
-//   warp 0      one thread issues TMA tile loads (A 128x64, B 2 x 128x64 bf16,
-//               128-byte swizzle) into a 4-stage shared-memory ring;
-//   warp 1      owns the TMEM allocation (2 x 256 fp32 columns) and one thread
-//               issues tcgen05.mma (M=128, N=256, K=16) into the accumulator
-//               of the current tile, committing each stage back to the
-//               producers of both CTAs and each finished tile to the epilogue;
-//   warps 2-5   read the accumulator rows out of TMEM (lane = tile row) and
-//   (2-9)       run the fused epilogue while the next tile accumulates into
-//               the other TMEM buffer. Each epilogue warp writes its bf16
-//               outputs 32 rows x 64 columns at a time into its own
-//               128-byte-swizzled staging buffer and stores the box by TMA,
-//               so global writes go out as whole rows, not one 16-byte piece
-//               of 32 different rows per instruction.
+// Persistent CTA pairs: clusters of two CTAs on two SMs, one CTA per SM,
+// run one MMA of M = 256 rows x N = 256 columns per tile
+// (tcgen05.mma.cta_group::2). Each CTA stages its own 128 rows of A and its
+// own half (128 rows) of the B tile, so a pipeline stage is 32 KB per SM
+// instead of 48 KB for a one-CTA 128 x 256 tile, B leaves L2 once per 256
+// rows, and the ring holds five or six stages. Roles, 192 (projections) or
+// 320 (logits) threads per CTA:
+//   warp 0      one thread per CTA issues the TMA loads of that CTA's A and
+//               B boxes (128 x 64 bf16, 128-byte swizzle); both CTAs' copies
+//               complete on the leader CTA's stage barrier;
+//   warp 1      allocates the pair's tensor memory (2 x 256 fp32 columns in
+//               each CTA); in the leader CTA one thread issues the pair MMAs
+//               (K = 16 each) and commits every stage back to both
+//               producers and every finished tile to both CTAs' epilogues;
+//   warps 2-5   read this CTA's 128 accumulator rows out of TMEM (lane = tile
+//   (2-9)       row) and run the fused epilogue while the next tile
+//               accumulates into the other TMEM buffer, then release the
+//               buffer on the leader's barrier. Each epilogue warp writes its
+//               bf16 outputs 32 rows at a time into its own 128- or 64-byte-
+//               swizzled staging boxes (two, used in turn) and stores each
+//               box by TMA, so global writes go out as whole rows and a box
+//               is refilled while the previous one is still being stored.
 // Every mbarrier wait is bounded in time; on a time-out the kernel raises
 // GDNBEAM_DERR_TIMEOUT, all roles leave their loops, in-flight copies and
 // MMAs are drained (again with a bound) and TMEM is freed.
@@ -37,13 +41,14 @@ namespace gdnbeam {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int CLUSTER = 2;  // CTAs sharing a B tile
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
+constexpr int BM = 128;  // accumulator rows per CTA; the pair's MMA has M = 2 * BM
+constexpr int BN = 256;  // columns per tile, the pair MMA's N
+constexpr int BK = 64;
+constexpr int CLUSTER = 2;                  // the CTA pair
+constexpr int A_BYTES = BM * BK * 2;        // this CTA's A rows
+constexpr int B_BYTES = (BN / 2) * BK * 2;  // this CTA's half of the B tile
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kNumBars = 2 * STAGES + 4 + 1;
 
 enum { EPI_LOGITS = 0, EPI_PROJ = 1 };
 
@@ -54,18 +59,30 @@ enum { EPI_LOGITS = 0, EPI_PROJ = 1 };
 template <int EPI> struct Epi {
   static constexpr int kWarps = EPI == EPI_LOGITS ? 8 : 4;
   static constexpr int kThreads = 64 + 32 * kWarps;
-  // one epilogue warp's staging box: 32 rows x 32 bf16 (64-byte rows) for the
-  // logits, whose eight warps must fit beside the operand ring; 32 rows x 64
-  // bf16 (128-byte rows) for the projections
+  static constexpr int kStages = EPI == EPI_LOGITS ? 5 : 6;  // operand ring depth
+  // one staging box: 32 rows x 32 bf16 (64-byte rows) for the logits, whose
+  // eight warps must fit beside the operand ring; 32 rows x 64 bf16
+  // (128-byte rows) for the projections. Two boxes per warp, used in turn.
   static constexpr int kBoxCols = EPI == EPI_LOGITS ? 32 : 64;
   static constexpr int kStgBytes = 32 * kBoxCols * 2;
-  // operand ring, the epilogue warps' staging boxes, barriers
-  static constexpr size_t kSmemBytes =
-      (size_t)STAGES * STAGE_BYTES + (size_t)kWarps * kStgBytes + 1024 + kNumBars * 8 + 16;
+  static constexpr int kStgBufs = 2;
+  // the logits pairs' half-row partials, per accumulator buffer
+  static constexpr int kHalfBytes = EPI == EPI_LOGITS ? 2 * 4 * 32 * 8 : 0;
+  static constexpr int kNumBars = 2 * kStages + 4 + 1;
+  // operand ring, staging boxes, partials, barriers, TMEM slot and abort flag
+  static constexpr size_t kSmemBytes = (size_t)kStages * STAGE_BYTES +
+                                       (size_t)kWarps * kStgBufs * kStgBytes + kHalfBytes + 1024 +
+                                       kNumBars * 8 + 16;
 };
-// dynamic plus static shared memory (the logits pair partials, 2 KiB) per block
-static_assert(Epi<EPI_LOGITS>::kSmemBytes + 2048 <= 232448, "shared memory of the logits GEMM");
-static_assert(Epi<EPI_PROJ>::kSmemBytes + 2048 <= 232448, "shared memory of the projection GEMM");
+static_assert(Epi<EPI_LOGITS>::kSmemBytes <= 232448, "shared memory of the logits GEMM");
+static_assert(Epi<EPI_PROJ>::kSmemBytes <= 232448, "shared memory of the projection GEMM");
+
+// MMA width for a column tile with n_here valid columns: the full BN, or the
+// valid columns rounded up to 32 so each CTA's half of B stays a multiple of
+// 16 rows. The epilogues never read past N.
+__host__ __device__ __forceinline__ int mma_cols(int n_here) {
+  return n_here >= BN ? BN : ((n_here + 31) & ~31);
+}
 
 struct EpiArgs {
   int M, N, K;
@@ -99,21 +116,6 @@ __device__ __forceinline__ uint32_t sw64_off(int row, int piece) {
   return (uint32_t)row * 64u + ((uint32_t)((piece ^ (row >> 1)) & 3) << 4);
 }
 
-// 32 fp32 values of this lane's row as bf16 into a 32-column staging box
-// (row = lane; 64-byte swizzle).
-__device__ __forceinline__ void stage_bf16x32_sw64(uint8_t* stg, int lane, const float (&v)[32]) {
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    uint32_t p[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(v[w * 8 + 2 * j], v[w * 8 + 2 * j + 1]);
-      p[j] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(stg + sw64_off(lane, w)) = make_uint4(p[0], p[1], p[2], p[3]);
-  }
-}
-
 // 32 fp32 values of this lane's row as bf16 into columns col0 .. col0+31 of
 // a 64-column staging box (row = lane; 128-byte swizzle).
 __device__ __forceinline__ void stage_bf16x32(uint8_t* stg, int lane, int col0, const float (&v)[32]) {
@@ -129,146 +131,220 @@ __device__ __forceinline__ void stage_bf16x32(uint8_t* stg, int lane, int col0, 
   }
 }
 
-// Waits until this warp's previous box store has read its staging buffer.
-__device__ __forceinline__ void staging_free(int lane) {
-  if (lane == 0) tc::bulk_wait_read<0>();
-  __syncwarp();
+// One epilogue warp's staging boxes in shared memory, filled and stored by
+// TMA in turn. acquire() waits until the box about to be filled has been
+// read by its previous store (the most recent store may still be reading
+// the other box); store() sends the filled box and moves to the next one.
+template <int EPI>
+struct Stager {
+  uint8_t* gen;  // generic address of box 0
+  uint32_t sa;   // shared-window address of box 0
+  int cur;
+  __device__ __forceinline__ uint8_t* acquire(int lane) {
+    if (lane == 0) tc::bulk_wait_read<Epi<EPI>::kStgBufs - 1>();
+    __syncwarp();
+    return gen + cur * Epi<EPI>::kStgBytes;
+  }
+  // Rows past the map's rows and columns past its columns are not written.
+  __device__ __forceinline__ void store(const CUtensorMap* map, int x, int y, int lane) {
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tc::tma_store_2d(map, x, y, sa + (uint32_t)(cur * Epi<EPI>::kStgBytes));
+      tc::bulk_commit();
+    }
+    cur = cur + 1 == Epi<EPI>::kStgBufs ? 0 : cur + 1;
+  }
+};
+
+// exp(x) for the row normaliser is evaluated as 2^(x log2 e) with the
+// hardware base-2 exponential (ex2.approx, relative error about 2^-22).
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Packed fp32 pairs (low word = first element).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
-// Sends the warp's staged box to (x, y) of the map.
-__device__ __forceinline__ void staging_store(const CUtensorMap* map, int x, int y, uint32_t stg_s,
-                                              int lane) {
-  tc::fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    tc::tma_store_2d(map, x, y, stg_s);
-    tc::bulk_commit();
+// 32 fp32 values (as bits) of this lane's row as bf16 into a 32-column
+// staging box (row = lane; 64-byte swizzle).
+__device__ __forceinline__ void stage_bf16x32_sw64(uint8_t* stg, int lane, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[w * 8 + 2 * j]),
+                                               __uint_as_float(r[w * 8 + 2 * j + 1]));
+      p[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(stg + sw64_off(lane, w)) = make_uint4(p[0], p[1], p[2], p[3]);
   }
 }
 
-// Logits epilogue for one tile row and one half of the tile's columns: bf16
-// z (staged, stored by TMA in boxes of 32 columns), optional fp32 dump, and
-// the half row's (max, sum exp), returned. y0: first row of the warp's 32.
-__device__ __forceinline__ float2 epi_logits(const EpiArgs& ea, const CUtensorMap* tmz, uint32_t taddr,
-                                             uint8_t* stg, uint32_t stg_s, int lane, int m, int y0,
-                                             int n0, int half) {
-  float run_max = -INFINITY, run_sum = 0.0f;
-  const bool row_ok = m < ea.M;
-#pragma unroll 1
-  for (int c = half * (BN / 64); c < (half + 1) * (BN / 64); ++c) {
-    const int n = n0 + c * 32;
-    if (n >= ea.N) break;  // warp-uniform
-    staging_free(lane);
-    float v[32];
-    tc::tmem_ld32(taddr + c * 32, v);
-    stage_bf16x32_sw64(stg, lane, v);
-    staging_store(tmz, n, y0, stg_s, lane);  // rows past M, columns past N are not written
-    {
-      if (!row_ok) continue;
-      if (ea.z_dump) {
-        const size_t off = (size_t)m * ea.N + n;
-        if (n + 32 <= ea.N) {
-          store_f32x32(ea.z_dump + off, v);
-        } else {
-          for (int j = 0; j < 32 && n + j < ea.N; ++j) ea.z_dump[off + j] = v[j];
-        }
-      }
-      const int cnt = min(32, ea.N - n);
-      float cm = -INFINITY;
+// Logits epilogue for one tile row and one half (128 columns) of the tile,
+// from accumulator values already in registers (r[c]: the half's columns
+// 32c .. 32c+31): bf16 z (staged, stored by TMA in boxes of 32 columns),
+// optional fp32 dump, and the half row's (max, sum exp), returned; an empty
+// half gives (-inf, 0). y0: first row of the warp's 32; nh: the half's
+// first column.
+__device__ __forceinline__ float2 epi_logits(const EpiArgs& ea, const CUtensorMap* tmz,
+                                             const uint32_t (&r)[4][32], Stager<EPI_LOGITS>& stg,
+                                             int lane, int m, int y0, int nh) {
+  const int cnt = ea.N - nh;  // valid columns of the half (all 128 except in a last tile)
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < cnt) cm = fmaxf(cm, v[j]);
-      const float nm = fmaxf(run_max, cm);
-      float sm = run_sum * expf(run_max - nm);
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < cnt) sm += expf(v[j] - nm);
-      run_sum = sm;
-      run_max = nm;
+  for (int c = 0; c < 4; ++c) {
+    if (c * 32 < cnt) {  // warp-uniform
+      uint8_t* box = stg.acquire(lane);
+      stage_bf16x32_sw64(box, lane, r[c]);
+      stg.store(tmz, nh + c * 32, y0, lane);
     }
   }
-  return make_float2(run_max, run_sum);
+  if (m >= ea.M || cnt <= 0) return make_float2(-INFINITY, 0.0f);
+  if (ea.z_dump) {
+    float* d = ea.z_dump + (size_t)m * ea.N + nh;
+    for (int c = 0; c < 4; ++c)
+      for (int j = 0; j < 32; ++j)
+        if (c * 32 + j < cnt) d[c * 32 + j] = __uint_as_float(r[c][j]);
+  }
+  float mx = -INFINITY;
+  if (cnt >= 128) {
+    // max by three-input compares; then sum 2^(log2e (v - max)) with packed
+    // fp32 pairs: one FMA and one add per two columns, one ex2 per column
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int j = 0; j < 32; j += 2)
+        mx = fmax3(mx, __uint_as_float(r[c][j]), __uint_as_float(r[c][j + 1]));
+    const float nb = -mx * kLog2e;
+    const uint64_t l2 = pack2(kLog2e, kLog2e), nb2 = pack2(nb, nb);
+    uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const uint64_t t = fma2(((uint64_t)r[c][j + 1] << 32) | r[c][j], l2, nb2);
+        acc[c] = add2(acc[c], pack2(ex2(__uint_as_float((uint32_t)t)),
+                                    ex2(__uint_as_float((uint32_t)(t >> 32)))));
+      }
+    const uint64_t a = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+    return make_float2(mx, __uint_as_float((uint32_t)a) + __uint_as_float((uint32_t)(a >> 32)));
+  }
+  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c * 32 + j < cnt) mx = fmaxf(mx, __uint_as_float(r[c][j]));
+    const float nb = -mx * kLog2e;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c * 32 + j < cnt) s[c] += ex2(fmaf(__uint_as_float(r[c][j]), kLog2e, nb));
+  }
+  return make_float2(mx, (s[0] + s[1]) + (s[2] + s[3]));
 }
 
 // Projection epilogue for one tile row and one of the tile's two heads
 // (head width 128): q and k L2-normalised per head, v as is (bf16, staged
 // and stored by TMA in boxes of 64 columns), the gates in fp32. y0: first
-// row of the warp's 32; tmq, tmk, tmv: the outputs' maps.
+// row of the warp's 32; tmq, tmk, tmv: the outputs' maps. (Holding the
+// head's 128 accumulator values in registers to read TMEM once measured
+// slower than reading q and k twice.)
 __device__ __forceinline__ void epi_proj(const EpiArgs& ea, const CUtensorMap* tmq,
                                          const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                         uint32_t taddr, uint8_t* stg, uint32_t stg_s, int lane,
+                                         uint32_t taddr, Stager<EPI_PROJ>& stg, int lane,
                                          int m, int y0, int n0, int g) {
   const int H = ea.H, Hk = ea.Hk, D = 128;
   const bool row_ok = m < ea.M;
   const int q_end = Hk * D, k_end = 2 * Hk * D, v_end = k_end + H * D;
-  {
-    if (n0 + g * D >= ea.N) return;
-    const int col0 = n0 + g * D + ea.col_off;  // column of the full projection
-    const uint32_t ta = taddr + g * D;
-    if (col0 < k_end) {
-      const bool is_q = col0 < q_end;
-      const int head = (is_q ? col0 : col0 - q_end) / D;
-      float ss = 0.0f;
+  if (n0 + g * D >= ea.N) return;
+  const int col0 = n0 + g * D + ea.col_off;  // column of the full projection
+  const uint32_t ta = taddr + g * D;
+  if (col0 < k_end) {
+    const bool is_q = col0 < q_end;
+    const int head = (is_q ? col0 : col0 - q_end) / D;
+    float ss = 0.0f;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 4; ++c) {
+      float v[32];
+      tc::tmem_ld32(ta + c * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+    }
+    const float inv = 1.0f / sqrtf(ss + 1e-6f);
+    float* dmp = is_q ? ea.dq : ea.dk;
+    const size_t off = (size_t)m * Hk * D + (size_t)head * D;
+#pragma unroll 1
+    for (int bx = 0; bx < 2; ++bx) {
+      uint8_t* box = stg.acquire(lane);
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * bx + cc;
         float v[32];
         tc::tmem_ld32(ta + c * 32, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ss = fmaf(v[j], v[j], ss);
+        for (int j = 0; j < 32; ++j) v[j] *= inv;
+        stage_bf16x32(box, lane, 32 * cc, v);
+        if (row_ok && dmp) store_f32x32(dmp + off + c * 32, v);
       }
-      const float inv = 1.0f / sqrtf(ss + 1e-6f);
-      float* dmp = is_q ? ea.dq : ea.dk;
-      const size_t off = (size_t)m * Hk * D + (size_t)head * D;
+      stg.store(is_q ? tmq : tmk, head * D + bx * 64, y0, lane);
+    }
+  } else if (col0 < v_end) {
+    const int head = (col0 - k_end) / D;
+    const size_t off = (size_t)m * H * D + (size_t)head * D;
 #pragma unroll 1
-      for (int bx = 0; bx < 2; ++bx) {
-        staging_free(lane);
+    for (int bx = 0; bx < 2; ++bx) {
+      uint8_t* box = stg.acquire(lane);
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * bx + cc;
-          float v[32];
-          tc::tmem_ld32(ta + c * 32, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= inv;
-          stage_bf16x32(stg, lane, 32 * cc, v);
-          if (row_ok && dmp) store_f32x32(dmp + off + c * 32, v);
-        }
-        staging_store(is_q ? tmq : tmk, head * D + bx * 64, y0, stg_s, lane);
-      }
-    } else if (col0 < v_end) {
-      const int head = (col0 - k_end) / D;
-      const size_t off = (size_t)m * H * D + (size_t)head * D;
-#pragma unroll 1
-      for (int bx = 0; bx < 2; ++bx) {
-        staging_free(lane);
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * bx + cc;
-          float v[32];
-          tc::tmem_ld32(ta + c * 32, v);
-          stage_bf16x32(stg, lane, 32 * cc, v);
-          if (row_ok && ea.dv) store_f32x32(ea.dv + off + c * 32, v);
-        }
-        staging_store(tmv, head * D + bx * 64, y0, stg_s, lane);
-      }
-    } else {
-      // gate columns: H decay-gate logits, then H write-gate logits
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * bx + cc;
         float v[32];
         tc::tmem_ld32(ta + c * 32, v);
-        if (!row_ok) continue;
+        stage_bf16x32(box, lane, 32 * cc, v);
+        if (row_ok && ea.dv) store_f32x32(ea.dv + off + c * 32, v);
+      }
+      stg.store(tmv, head * D + bx * 64, y0, lane);
+    }
+  } else {
+    // gate columns: H decay-gate logits, then H write-gate logits
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float v[32];
+      tc::tmem_ld32(ta + c * 32, v);
+      if (!row_ok) continue;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int idx = c * 32 + j;
-          if (idx < H) {
-            const float a = decay_gate(v[j]);
-            ea.alpha[(size_t)m * H + idx] = a;
-            if (ea.da) ea.da[(size_t)m * H + idx] = a;
-          } else if (idx < 2 * H) {
-            const float b = write_gate(v[j]);
-            ea.beta[(size_t)m * H + idx - H] = b;
-            if (ea.db) ea.db[(size_t)m * H + idx - H] = b;
-          }
+      for (int j = 0; j < 32; ++j) {
+        const int idx = c * 32 + j;
+        if (idx < H) {
+          const float a = decay_gate(v[j]);
+          ea.alpha[(size_t)m * H + idx] = a;
+          if (ea.da) ea.da[(size_t)m * H + idx] = a;
+        } else if (idx < 2 * H) {
+          const float b = write_gate(v[j]);
+          ea.beta[(size_t)m * H + idx - H] = b;
+          if (ea.db) ea.db[(size_t)m * H + idx - H] = b;
         }
       }
     }
@@ -281,40 +357,47 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThr
                    const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                    const __grid_constant__ CUtensorMap tmC2, EpiArgs ea) {
   // output maps: logits z (C0); projections q (C0), k (C1), v (C2)
+  using E = Epi<EPI>;
+  constexpr int S = E::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
+  // both CTAs of the pair lay out their shared memory identically: the
+  // pair MMA reads the peer's operands at the leader's offsets
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t stg0 = base + STAGES * STAGE_BYTES;  // epilogue warps' staging boxes
-  const uint32_t bar0 = stg0 + Epi<EPI>::kWarps * Epi<EPI>::kStgBytes;
-  auto full = [&](int s) { return bar0 + 8u * s; };
-  auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 - base) + kNumBars * 8);
+  const uint32_t stg0 = base + S * STAGE_BYTES;  // epilogue warps' staging boxes
+  const uint32_t half0 = stg0 + E::kWarps * E::kStgBufs * E::kStgBytes;
+  const uint32_t bar0 = half0 + E::kHalfBytes;
+  auto full = [&](int s_) { return bar0 + 8u * s_; };
+  auto empty = [&](int s_) { return bar0 + 8u * (S + s_); };
+  auto tfull = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (bar0 - base) + E::kNumBars * 8);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  auto sA = [&](int s) { return base + (uint32_t)s * STAGE_BYTES; };
-  auto sB = [&](int s) { return base + (uint32_t)s * STAGE_BYTES + A_BYTES; };
+  auto sA = [&](int s_) { return base + (uint32_t)s_ * STAGE_BYTES; };
+  auto sB = [&](int s_) { return base + (uint32_t)s_ * STAGE_BYTES + A_BYTES; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tiles = (ea.M + BM - 1) / BM, n_tiles = (ea.N + BN - 1) / BN;
-  // pair tiles: rows 2 mp and 2 mp + 1 (the second may lie past M: its A
-  // box reads zeros and its rows are not stored) against one B tile
-  const int num_tiles = ((m_tiles + 1) / 2) * n_tiles;
+  // a tile is 2 * BM rows (this CTA's BM of them start at row
+  // (2 * tile_row + rank) * BM; rows past M read zeros and are not stored)
+  // by BN columns
+  const int m_tiles = (ea.M + 2 * BM - 1) / (2 * BM), n_tiles = (ea.N + BN - 1) / BN;
+  const int num_tiles = m_tiles * n_tiles;
   const int k_blocks = (ea.K + BK - 1) / BK;
-  const int rank = (int)tc::cluster_ctarank();
+  const uint32_t rank = tc::cluster_ctarank();
+  const bool leader = rank == 0;
   const int cid = blockIdx.x / CLUSTER, n_clusters = gridDim.x / CLUSTER;
-  const uint16_t both = (uint16_t)((1u << CLUSTER) - 1u);
+  constexpr uint16_t kBoth = (uint16_t)((1u << CLUSTER) - 1u);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      tc::mbar_init(full(s), 1);
-      tc::mbar_init(empty(s), CLUSTER);  // the MMA commits of both CTAs
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(full(i), 1);   // leader: its producer's arrival + both CTAs' bytes
+      tc::mbar_init(empty(i), 1);  // the leader's MMA commit
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull(a), 1);
-      tc::mbar_init(tempty(a), Epi<EPI>::kWarps);
+      tc::mbar_init(tempty(a), CLUSTER * E::kWarps);  // leader: both CTAs' epilogue warps
     }
     tc::mbar_init(drain_bar, 1);
     *abort = 0;
@@ -324,86 +407,91 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThr
     tc::tma_prefetch(&tmA);
     tc::tma_prefetch(&tmB);
   }
-  if (warp == 1) tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+  if (warp == 1) tc::tmem_alloc_pair(tc::smem_u32(tmem_slot), kTmemCols);
   tc::fence_before_sync();
   __syncthreads();
-  // the peer's barriers are initialised before any copy or commit reaches them
+  // the peer's barriers are initialised before any copy, commit or arrival
+  // reaches them
   tc::cluster_sync();
   tc::fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
-      int s = 0;
+      int st = 0;
       uint32_t ph = 0;
-      uint32_t issued_phase[STAGES];
-      bool issued[STAGES];
-      for (int i = 0; i < STAGES; ++i) issued[i] = false;
+      int n_issued = 0;  // stage loads issued so far
       bool ok = true;
       for (int tile = cid; tile < num_tiles && ok; tile += n_clusters) {
-        const int m0 = (2 * (tile / n_tiles) + rank) * BM, n0 = (tile % n_tiles) * BN;
+        const int m0 = (2 * (tile / n_tiles) + (int)rank) * BM;
+        const int n0 = (tile % n_tiles) * BN;
+        // this CTA's half of the tile's B rows
+        const int nb = n0 + (int)rank * (mma_cols(ea.N - n0) / 2);
         for (int kb = 0; kb < k_blocks; ++kb) {
-          // the stage is free in both CTAs (the peer's half of B lands here too)
-          if (!tc::mbar_wait(empty(s), ph ^ 1u, abort, ea.err)) { ok = false; break; }
-          tc::mbar_arrive_expect_tx(full(s), STAGE_BYTES);
-          tc::tma_load_2d(sA(s), &tmA, kb * BK, m0, full(s));
-          tc::tma_load_2d_mc(sB(s) + rank * (BN / 2) * 128, &tmB, kb * BK, n0 + rank * (BN / 2),
-                             full(s), both);
-          issued[s] = true;
-          issued_phase[s] = ph;
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+          // the leader's MMAs have finished reading this stage in both CTAs
+          if (!tc::mbar_wait(empty(st), ph ^ 1u, abort, ea.err)) { ok = false; break; }
+          const uint32_t bar = tc::mapa_shared(full(st), 0);
+          if (leader) tc::mbar_arrive_expect_tx(full(st), CLUSTER * STAGE_BYTES);
+          tc::tma_load_2d_pair(sA(st), &tmA, kb * BK, m0, bar);
+          tc::tma_load_2d_pair(sB(st), &tmB, kb * BK, nb, bar);
+          ++n_issued;
+          if (++st == S) { st = 0; ph ^= 1u; }
         }
       }
-      // every copy this thread started has landed before the CTA can exit
-      for (int i = 0; i < STAGES; ++i)
-        if (issued[i]) tc::mbar_wait_drain(full(i), issued_phase[i]);
+      // every copy of the pair has landed before the CTAs can exit: both
+      // CTAs' copies complete on the leader's stage barriers, which its
+      // producer drains (the two producers issue the same stages)
+      // (the q-th load went to stage q % S in phase (q / S) & 1)
+      if (leader)
+        for (int q = max(0, n_issued - S); q < n_issued; ++q)
+          tc::mbar_wait_drain(full(q % S), (uint32_t)(q / S) & 1u);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_full = tc::idesc_bf16_f32(BM, BN);
-      int s = 0;
+    if (lane == 0 && leader) {
+      int st = 0;
       uint32_t ph = 0;
       bool ok = true;
       int i = 0;
       for (int tile = cid; tile < num_tiles && ok; tile += n_clusters, ++i) {
         // a last column tile narrower than BN runs MMAs only as wide as its
-        // columns (rounded up to 16); the epilogues never read past N
-        const int n_here = ea.N - (tile % n_tiles) * BN;
-        const uint32_t idesc =
-            n_here >= BN ? idesc_full : tc::idesc_bf16_f32(BM, (n_here + 15) & ~15);
+        // columns (rounded up to 32); the epilogues never read past N
+        const int nm = mma_cols(ea.N - (tile % n_tiles) * BN);
+        const uint32_t idesc = tc::idesc_bf16_f32(2 * BM, nm);
         const int acc = i & 1;
         const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+        // both CTAs' epilogues have drained this accumulator buffer
         if (!tc::mbar_wait(tempty(acc), aph ^ 1u, abort, ea.err)) break;
         tc::fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!tc::mbar_wait(full(s), ph, abort, ea.err)) { ok = false; break; }
+          if (!tc::mbar_wait(full(st), ph, abort, ea.err)) { ok = false; break; }
           tc::fence_after_sync();
-          const uint64_t ad = tc::sw128_desc(sA(s)), bd = tc::sw128_desc(sB(s));
+          const uint64_t ad = tc::sw128_desc(sA(st)), bd = tc::sw128_desc(sB(st));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            tc::mma_bf16(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0);
-          tc::mma_commit_mc(empty(s), both);
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+            tc::mma_bf16_pair(d_tmem, ad + 2u * kk, bd + 2u * kk, idesc, (kb | kk) != 0);
+          tc::mma_commit_pair_mc(empty(st), kBoth);
+          if (++st == S) { st = 0; ph ^= 1u; }
         }
-        if (ok) tc::mma_commit(tfull(acc));
+        if (ok) tc::mma_commit_pair_mc(tfull(acc), kBoth);
       }
       // every MMA this thread issued has finished before TMEM is released
-      tc::mma_commit(drain_bar);
+      tc::mma_commit_pair(drain_bar);
       tc::mbar_wait_drain(drain_bar, 0);
     }
   } else {
     // one or two warps per TMEM lane group (lanes 32*lane_grp .. +31); with
     // two, each takes half the tile's columns and the pair meets at named
     // barrier 1 + lane_grp
-    constexpr bool kPairs = Epi<EPI>::kWarps == 8;
+    constexpr bool kPairs = E::kWarps == 8;
     const int lane_grp = warp & 3;
     const int half = (warp - 2) >> 2;
     const int pair_bar = 1 + lane_grp;
     const int row = lane_grp * 32 + lane;
-    const uint32_t stg_s = stg0 + (uint32_t)(warp - 2) * Epi<EPI>::kStgBytes;
-    uint8_t* stg = gbase + (stg_s - base);
-    __shared__ float2 s_half[2][4][32];  // the second half's row partials, per accumulator
+    const uint32_t stg_s = stg0 + (uint32_t)((warp - 2) * E::kStgBufs * E::kStgBytes);
+    Stager<EPI> stg{gbase + (stg_s - base), stg_s, 0};
+    // the second half's row partials, per accumulator buffer
+    float2* s_half = reinterpret_cast<float2*>(gbase + (half0 - base));
     int i = 0;
     for (int tile = cid; tile < num_tiles; tile += n_clusters, ++i) {
       const int acc = i & 1;
@@ -418,17 +506,27 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThr
         if (!got) break;
       }
       tc::fence_after_sync();
-      const int m_tile = 2 * (tile / n_tiles) + rank, n_tile = tile % n_tiles;
+      const int m_tile = 2 * (tile / n_tiles) + (int)rank, n_tile = tile % n_tiles;
       const uint32_t taddr = tmem_base + ((uint32_t)(lane_grp * 32) << 16) + (uint32_t)(acc * BN);
       const int m = m_tile * BM + row;
       const int y0 = m_tile * BM + lane_grp * 32;
-      if (EPI == EPI_LOGITS) {
-        const float2 pr = epi_logits(ea, &tmC0, taddr, stg, stg_s, lane, m, y0, n_tile * BN, half);
-        if (half) s_half[acc][lane_grp][lane] = pr;
+      if constexpr (EPI == EPI_LOGITS) {
+        // this warp's half row into registers, then the accumulator buffer
+        // goes back to the MMA before the math and the stores
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32_nowait(taddr + (uint32_t)(half * 128 + c * 32), r[c]);
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_remote(tc::mapa_shared(tempty(acc), 0));
+        const float2 pr = epi_logits(ea, &tmC0, r, stg, lane, m, y0, n_tile * BN + half * 128);
+        float2* sh = s_half + (acc * 4 + lane_grp) * 32;
+        if (half) sh[lane] = pr;
         tc::named_sync(pair_bar, 64);
         if (!half && m < ea.M) {
           // merge the halves' (max, sum exp); an empty half has max -inf
-          const float2 q = s_half[acc][lane_grp][lane];
+          const float2 q = sh[lane];
           const float nm = fmaxf(pr.x, q.x);
           const float sum = (pr.x == -INFINITY ? 0.0f : pr.y * expf(pr.x - nm)) +
                             (q.x == -INFINITY ? 0.0f : q.y * expf(q.x - nm));
@@ -436,11 +534,12 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThr
         }
       } else {
         for (int g = 0; g < BN / 128; ++g)
-          epi_proj(ea, &tmC0, &tmC1, &tmC2, taddr, stg, stg_s, lane, m, y0, n_tile * BN, g);
+          epi_proj(ea, &tmC0, &tmC1, &tmC2, taddr, stg, lane, m, y0, n_tile * BN, g);
+        // this warp's TMEM reads are done: release the buffer on the leader
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_remote(tc::mapa_shared(tempty(acc), 0));
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tempty(acc));
     }
     // the warp's box stores have finished before the CTA leaves
     if (lane == 0) tc::bulk_wait_all();
@@ -448,12 +547,12 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(Epi<EPI>::kThr
   }
   tc::fence_before_sync();
   __syncthreads();
-  // neither CTA leaves while the other may still multicast into it or
-  // arrive on its barriers
+  // neither CTA leaves while the leader may still write the peer's TMEM,
+  // signal its barriers or read its shared memory
   tc::cluster_sync();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem_base, kTmemCols);
+    tc::tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -579,7 +678,7 @@ int launch_gemm(const void* A, const void* B, const EpiArgs& ea, const CUtensorM
                                   (int)Epi<EPI>::kSmemBytes));
     attr_set[EPI] = true;
   }
-  const int pair_tiles = ((ea.M + BM - 1) / BM + 1) / 2 * ((ea.N + BN - 1) / BN);
+  const int pair_tiles = (ea.M + 2 * BM - 1) / (2 * BM) * ((ea.N + BN - 1) / BN);
   int clusters = max_clusters<EPI>();
   if (clusters <= 0) return GDNBEAM_ECUDA;
   if (clusters > pair_tiles) clusters = pair_tiles;

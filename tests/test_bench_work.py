@@ -130,7 +130,7 @@ def _ours_run(args, env_extra):
 
 
 def test_more_than_one_gpu_is_refused_before_any_gpu_work():
-    # the GEMMs' multicast tile loads run on one GPU only: a torchrun launch
+    # the decode runs on one GPU (replicas are not built): a torchrun launch
     # (WORLD_SIZE > 1) or --gpus > 1 exits with a reason and does no work
     for args, env in ((["--steps", "1"], {"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"}),
                       (["--gpus", "2", "--steps", "1"], {"WORLD_SIZE": "1"}),

@@ -392,8 +392,11 @@ def test_project_op_tensor_cores(H, d_model, n):
     test_project_op("bf16", 128, H, d_model, n)
 
 
-@pytest.mark.parametrize("F,V,n", [(2048, 8192, 300), (1024, 4096, 129), (256, 1000, 1), (2048, 8192, 512)])
+@pytest.mark.parametrize("F,V,n", [(2048, 8192, 300), (1024, 4096, 129), (256, 1000, 1), (2048, 8192, 512),
+                                   (2048, 8232, 700), (1024, 520, 257)])
 def test_logits_op_tensor_cores(F, V, n):
+    # ragged row tails around the 256-row pair tiles; last column tiles of
+    # full width, 232 columns, and 40 or 8 columns (narrowed MMAs)
     test_logits_op("bf16", F, V, n)
 
 
