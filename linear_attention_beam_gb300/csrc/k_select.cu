@@ -167,22 +167,128 @@ __device__ void sort_and_emit(uint64_t* win, int P, int W_next, int V, int32_t* 
   }
 }
 
-// Writes the W_next unique keys of win[] in descending order: each key goes
-// to its rank, the number of keys above it. W_next^2 comparisons: used up to
-// kRankMax keys, a bitonic sort above.
-constexpr int kRankMax = 512;
-__device__ void rank_and_emit(const uint64_t* win, int W_next, int V, int32_t* parents,
-                              int32_t* tokens, float* cum_next) {
+// Writes the W_next (<= kOrderMax) unique keys of win[] in descending order.
+// Each warp sorts runs of 32 keys in registers (a bitonic network over
+// shuffles) and writes them back; then each key's rank is its place in its
+// run plus, for every other run, the count of that run's keys above it (a
+// binary search in the sorted run). win must have room for the last run's
+// padding up to a multiple of 32.
+constexpr int kOrderMax = 1024;
+__device__ void order_and_emit(uint64_t* win, int W_next, int V, int32_t* parents,
+                               int32_t* tokens, float* cum_next) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  const int runs = (W_next + 31) >> 5;
+  for (int run = warp; run < runs; run += n_warps) {
+    const int i = run * 32 + lane;
+    uint64_t v = i < W_next ? win[i] : 0ull;  // padding sorts below every key
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+        // blocks of k lanes alternate direction; the whole run ends descending
+        const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+        v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+      }
+    }
+    win[i] = v;
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i < W_next; i += blockDim.x) {
     const uint64_t key = win[i];
-    int rank = 0;
-#pragma unroll 8
-    for (int j = 0; j < W_next; ++j) rank += win[j] > key ? 1 : 0;
+    const int mine = i >> 5;
+    int rank = i & 31;
+    for (int b = 0; b < runs; ++b) {
+      if (b == mine) continue;
+      const uint64_t* rb = win + 32 * b;
+      int pos = 0;
+#pragma unroll
+      for (int st = 16; st > 0; st >>= 1)
+        if (rb[pos + st - 1] > key) pos += st;
+      if (rb[pos] > key) ++pos;
+      rank += pos;
+    }
     const uint32_t flat = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFu);
     parents[rank] = (int32_t)(flat / (uint32_t)V);
     tokens[rank] = (int32_t)(flat % (uint32_t)V);
     cum_next[rank] = from_orderable((uint32_t)(key >> 32));
   }
+}
+
+__device__ __forceinline__ int high_bit(uint32_t x) { return 31 - __clz(x); }
+__device__ __forceinline__ int high_bit(uint64_t x) { return 63 - __clzll(x); }
+
+// Block-wide search for the K-th largest of n keys (read through get()),
+// all of which lie in [lo, hi]. Each round histograms the keys inside the
+// window on the 8 bits below the highest bit where its ends differ, keeps
+// the bin that holds the K-th largest and narrows the window to it, until
+// that bin is taken whole or holds a single value. Returns prefix such that
+// the keys >= prefix are the K largest, ties at the K-th value all
+// included. bins: kBins words of shared memory; sh: 4 words. Starting from
+// the keys' own range skips the leading bits they all share, where fixed
+// digits put nearly every key into one bucket.
+constexpr int kBins = 256;
+template <typename Key, typename Get>
+__device__ Key radix_window(int n, unsigned K, Key lo, Key hi, Get get, unsigned* bins,
+                            unsigned* sh) {
+  unsigned remaining = K;  // rank of the target among the window's keys
+  const int lane = threadIdx.x & 31;
+  while (lo < hi) {
+    const int p = high_bit(lo ^ hi);
+    const int shift = p >= 7 ? p - 7 : 0;
+    const Key base = lo >> shift;  // (hi >> shift) - base < kBins
+    for (int i = threadIdx.x; i < kBins; i += blockDim.x) bins[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const Key key = get(i);
+      if (key >= lo && key <= hi) atomicAdd(&bins[(unsigned)((key >> shift) - base)], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // the highest bin d whose count from the top of the window reaches
+      // `remaining`; lane l owns bins 255 - 8l - k, k = 0..7
+      unsigned cnt[8], tot = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        cnt[k] = bins[kBins - 1 - 8 * lane - k];
+        tot += cnt[k];
+      }
+      unsigned incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned excl = incl - tot;
+      const unsigned hit = __ballot_sync(0xffffffffu, excl < remaining && incl >= remaining);
+      if (hit == 0u && lane == 0) sh[2] = 0xFFFFFFFFu;  // fewer keys than K in the window
+      if (hit != 0u && lane == __ffs(hit) - 1) {
+        unsigned acc = excl;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (acc + cnt[k] >= remaining) {
+            sh[0] = (unsigned)(kBins - 1 - 8 * lane - k);
+            sh[1] = remaining - acc;  // rank of the target within the bin
+            sh[2] = cnt[k];
+            break;
+          }
+          acc += cnt[k];
+        }
+      }
+    }
+    __syncthreads();
+    const unsigned d = sh[0], rem = sh[1], c = sh[2];
+    __syncthreads();  // everyone has read sh before the next round writes it
+    if (c == 0xFFFFFFFFu) return lo;
+    const Key blo = (base + (Key)d) << shift;
+    const Key bhi = ((base + (Key)d + 1) << shift) - 1;  // wraps to the top at the last bin
+    const Key nlo = blo > lo ? blo : lo;
+    if (c == rem) return nlo;  // the whole bin is taken
+    lo = nlo;
+    hi = bhi < hi ? bhi : hi;
+    remaining = rem;
+  }
+  return lo;
 }
 
 struct SelScratch {
@@ -291,16 +397,13 @@ template <typename T>
 __device__ Bound bound_phase(int r, int W_t, int n_tiles, int W_next,
                             const float2* __restrict__ hint, const Rows& rows,
                             const SelScratch& ss, uint32_t* hkeys, int smem_keys, uint32_t* slist,
-                            int slist_cap, unsigned* err) {
-  __shared__ unsigned hist[256];
-  __shared__ unsigned sh[3];
+                            int slist_cap, unsigned* bins, unsigned* err) {
+  __shared__ unsigned sh[4];
   __shared__ int s_cnt;
-  __shared__ unsigned s_max;
+  __shared__ uint32_t s_wlo[32], s_whi[32];
   const int n_h = W_t * n_tiles;
-  if (threadIdx.x == 0) {
-    s_cnt = 0;
-    s_max = 0u;
-  }
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) s_cnt = 0;
   // the rows' parameters; a row whose lse or cumulative score is not finite
   // is flagged
   for (int b = threadIdx.x; b < W_t; b += blockDim.x) {
@@ -314,20 +417,67 @@ __device__ Bound bound_phase(int r, int W_t, int n_tiles, int W_next,
     const int b = i / n_tiles;
     const float4 rp = rows.get(b);
     const float zm = hint[(rows.base + b) * n_tiles + (i % n_tiles)].x;
-    const float zs = St<T>::to_f(St<T>::from_f(zm));  // stored value of the tile's top element
+    const float zs = St<T>::to_f(St<T>::from_f(zm));
     return orderable(score(rp.x, zs, rp.y));
   };
+  // the hint keys (kept on chip when they fit) and the block's smallest and
+  // largest, which bound the search below
+  // Each thread issues eight hint loads before it uses any: the hints are
+  // mostly not in L2 (the logits were written after them), and eight misses
+  // in flight per thread instead of one cut this pass by more than half.
   const bool on_chip = n_h <= smem_keys;
-  uint32_t t = 0u;  // too few hints for a bound: keep every tile
-  if (on_chip) {
-    for (int i = threadIdx.x; i < n_h; i += blockDim.x) hkeys[i] = key_of(i);
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  const float2* hreq = hint + rows.base * n_tiles;
+  for (int i0 = threadIdx.x; i0 < n_h; i0 += 8 * blockDim.x) {
+    float zm[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      zm[u] = i < n_h ? hreq[i].x : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < n_h) {
+        const float4 rp = rows.get(i / n_tiles);
+        const float zs = St<T>::to_f(St<T>::from_f(zm[u]));  // stored value of the tile's top element
+        const uint32_t key = orderable(score(rp.x, zs, rp.y));
+        if (on_chip) hkeys[i] = key;
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+      }
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  if (lane == 0) {
+    s_wlo[threadIdx.x >> 5] = kmin;
+    s_whi[threadIdx.x >> 5] = kmax;
   }
   __syncthreads();
+  uint32_t klo = 0xFFFFFFFFu, khi = 0u;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+    klo = min(klo, s_wlo[w]);
+    khi = max(khi, s_whi[w]);
+  }
+  uint32_t t = 0u;  // too few hints for a bound: keep every tile
   if (W_next <= n_h) {
     if (on_chip)
-      t = radix_kth<uint32_t>(n_h, (unsigned)W_next, [&](int i) { return hkeys[i]; }, hist, sh);
+      t = radix_window<uint32_t>(n_h, (unsigned)W_next, klo, khi, [&](int i) { return hkeys[i]; },
+                                 bins, sh);
     else
-      t = radix_kth<uint32_t>(n_h, (unsigned)W_next, key_of, hist, sh);
+      t = radix_window<uint32_t>(n_h, (unsigned)W_next, klo, khi, key_of, bins, sh);
+  }
+  // the tiles whose hint reaches t
+  uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
+  for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
+    if ((on_chip ? hkeys[i] : key_of(i)) >= t) {
+      const int pos = atomicAdd(&s_cnt, 1);
+      if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
+      if (pos < slist_cap) slist[pos] = (uint32_t)i;  // the on-chip copy, when it fits
+    }
   }
   // each row's cutoff: the smallest stored value whose score reaches t, by
   // bisection over the storage keys (scores are monotone in the stored
@@ -342,21 +492,8 @@ __device__ Bound bound_phase(int r, int W_t, int n_tiles, int W_next,
     }
     rows.set_cut(b, SKey<T>::value(lo));
   }
-  uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
-  unsigned my_max = 0u;
-  for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
-    const uint32_t key = on_chip ? hkeys[i] : key_of(i);
-    my_max = max(my_max, key);
-    if (key >= t) {
-      const int pos = atomicAdd(&s_cnt, 1);
-      if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
-      if (pos < slist_cap) slist[pos] = (uint32_t)i;  // the on-chip copy, when it fits
-    }
-  }
-  for (int o = 16; o > 0; o >>= 1) my_max = max(my_max, __shfl_xor_sync(0xffffffffu, my_max, o));
-  if ((threadIdx.x & 31) == 0) atomicMax(&s_max, my_max);
-  __syncthreads();  // the list, the cutoffs and the counters are complete
-  return Bound{t, s_max, s_cnt};
+  __syncthreads();  // the list, the cutoffs and the counter are complete
+  return Bound{t, khi, s_cnt};
 }
 
 // Eight stored codes as loaded: one 16-byte word of bf16, two of fp32.
@@ -603,7 +740,6 @@ __global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
   // first the bound's hint keys (32-bit), then the candidates' keys (64-bit);
   // after them the rows' parameters when they fit
   extern __shared__ uint64_t keys[];
-  __shared__ unsigned hist[256];
   __shared__ unsigned sh[4];
   __shared__ uint64_t win[kMaxSort];
   const int r = blockIdx.x;
@@ -613,19 +749,24 @@ __global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
   constexpr int kSlist = 2 * kMaxSort;
   const Rows rows{rows_on_chip ? reinterpret_cast<float4*>(keys + kFinalSmemKeys) : nullptr, lse, cum,
                   bias, ss.cut, (size_t)r * W_t};
+  // the radix bins share the sort window too: the bound's search ends
+  // before the tile list is written there, and the top-W search before the
+  // window is filled
+  unsigned* bins = reinterpret_cast<unsigned*>(win);
   const Bound bd = bound_phase<T>(r, W_t, n_tiles, W_next, hint, rows, ss,
-                                  reinterpret_cast<uint32_t*>(keys), bound_keys, slist, kSlist, err);
+                                  reinterpret_cast<uint32_t*>(keys), bound_keys, slist, kSlist,
+                                  bins, err);
   const uint32_t t = bd.t, hmax = bd.hmax;
   const int n_tc = bd.n_list;
   const int n_list = min(n_tc, ss.cap_tiles);
   const uint32_t* list = n_list <= kSlist ? slist : ss.tlist + (size_t)r * ss.cap_tiles;
   const int target = min(ss.cap, kFinalSmemKeys);
   int n_c = append_listed<T>(V, n_tiles, n_list, list, t, target, z, rows, keys);
+  uint32_t lo_key = t;
   if (n_c > target && n_c >= W_next && n_tc <= ss.cap_tiles) {
-    uint32_t lo = t;
     n_c = narrow_bound<T>(V, n_tiles, n_list, list, W_next, target, z, rows,
-                          reinterpret_cast<uint32_t*>(keys), t, hmax, &lo)
-              ? append_listed<T>(V, n_tiles, n_list, list, lo, target, z, rows, keys)
+                          reinterpret_cast<uint32_t*>(keys), t, hmax, &lo_key)
+              ? append_listed<T>(V, n_tiles, n_list, list, lo_key, target, z, rows, keys)
               : -1;
   }
   if (n_c < W_next || n_c > target || n_tc > ss.cap_tiles) {
@@ -636,23 +777,33 @@ __global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
     return;
   }
   if (threadIdx.x == 0) ss.fb_flag[r] = 0;
+  // every kept key has a score key of at least lo_key (the bound, raised if
+  // narrowed) and at most the largest hint key
   uint64_t prefix = 0;
   if (W_next < n_c)
-    prefix = radix_kth<uint64_t>(n_c, (unsigned)W_next, [&](int i) { return keys[i]; }, hist, sh);
+    prefix = radix_window<uint64_t>(n_c, (unsigned)W_next, (uint64_t)lo_key << 32,
+                                    ((uint64_t)hmax << 32) | 0xFFFFFFFFull,
+                                    [&](int i) { return keys[i]; }, bins, sh);
   if (threadIdx.x == 0) sh[3] = 0;
   __syncthreads();
-  // the keys >= prefix are exactly the W_next best (keys are unique)
-  for (int i = threadIdx.x; i < n_c; i += blockDim.x) {
-    const uint64_t key = keys[i];
-    if (key >= prefix) {
-      unsigned idx = atomicAdd(&sh[3], 1u);
-      if (idx < (unsigned)W_next) win[idx] = key;
-    }
+  // the keys >= prefix are exactly the W_next best (keys are unique); they
+  // go to the window a warp at a time
+  const int lane = threadIdx.x & 31;
+  for (int i0 = threadIdx.x & ~31; i0 < n_c; i0 += blockDim.x) {
+    const int i = i0 + lane;
+    const uint64_t key = i < n_c ? keys[i] : 0ull;
+    const bool keep = i < n_c && key >= prefix;
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    if (m == 0u) continue;
+    unsigned pos = 0;
+    if (lane == 0) pos = atomicAdd(&sh[3], (unsigned)__popc(m));
+    pos = __shfl_sync(0xffffffffu, pos, 0) + (unsigned)__popc(m & ((1u << lane) - 1u));
+    if (keep && pos < (unsigned)W_next) win[pos] = key;
   }
   __syncthreads();
   const size_t o = (size_t)r * W_next;
-  if (W_next <= kRankMax) {
-    rank_and_emit(win, W_next, V, parents + o, tokens + o, cum_next + o);
+  if (W_next <= kOrderMax) {
+    order_and_emit(win, W_next, V, parents + o, tokens + o, cum_next + o);
   } else {
     int P = 1;
     while (P < W_next) P <<= 1;
