@@ -77,6 +77,7 @@ class BeamDecoder:
         self.root_logits = torch.empty(R_, V, dtype=self.tdtype, device=dev)
         self.root_lse = torch.empty(R_, dtype=torch.float32, device=dev)
         self.sid = torch.empty(R_, W, T, dtype=torch.int32, device=dev)
+        self._serve = {}  # per served shape: its buffers and captured graph
 
     @classmethod
     def for_workload(cls, wl, weights, L_max: Optional[int] = None, device="cuda",
@@ -214,6 +215,93 @@ class BeamDecoder:
         ft = forced[1][T - 1] if forced is not None else tokens[T - 1]
         sid = self.get_paths(W[T - 1], fp_ if T > 1 else None, ft, stream=stream)
         return DecodeResult(parents, tokens, cums, sid, logits_k, lse_k, dumps_k)
+
+    # ---------------------------------------------------------------- serving
+    def serve(self, prompts, W: Sequence[int], bias: Optional[torch.Tensor] = None, *,
+              graph: bool = True):
+        """One batch of requests end to end: prompts (host int32 [R, L]) go to
+        the device, then prefill, the root selection, the T-1 decode calls and
+        their selections, and the SID paths [R, W[-1], T] and final cumulative
+        scores [R, W[-1]] come back to host memory. W and bias as in decode.
+
+        Returns (sid, cum) as pinned host tensors owned by the decoder and
+        overwritten by the next call of the same shape; the call returns once
+        they hold the results, after checking the device error word.
+
+        With graph=True the sequence, its two host copies included, is
+        captured into a CUDA graph the first time a (prompt length, W, bias)
+        shape is served (after one ordinary run of it) and replayed from then
+        on: one graph launch instead of some thirty kernel launches, with the
+        gaps between dependent kernels gone. Prompts and bias are first copied
+        into the buffers the captured work reads."""
+        c = self.cfg
+        W = tuple(int(w) for w in W)
+        prompts = torch.as_tensor(prompts)
+        if prompts.device.type != "cpu" or prompts.dim() != 2 or prompts.shape[0] != c.R:
+            raise ValueError("prompts: host tensor [R, L]")
+        if len(W) != c.T or max(W) > c.W_max:
+            raise ValueError("W: one width per selection, at most W_max")
+        key = (int(prompts.shape[1]), W, bias is not None)
+        st = self._serve.get(key)
+        fresh = st is None
+        if fresh:
+            st = self._serve_buffers(key[0], W, bias is not None)
+            self._serve[key] = st
+        st["h_prompt"].copy_(prompts)
+        stream = st["stream"]
+        with torch.cuda.stream(stream):
+            if bias is not None:
+                for t in range(c.T - 1):
+                    st["bias"][t].copy_(bias[t, :, :W[t]], non_blocking=True)
+            if not graph:
+                self._serve_run(st, W, stream)
+            elif fresh or st["graph"] is None:
+                # one ordinary run (first-use set-up, the results of this
+                # call), then the capture
+                self._serve_run(st, W, stream)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    self._serve_run(st, W, stream)
+                st["graph"] = g
+            else:
+                st["graph"].replay()
+        check(self.status(stream), "serve")
+        return st["h_sid"], st["h_cum"]
+
+    def _serve_buffers(self, L: int, W: Sequence[int], with_bias: bool):
+        c = self.cfg
+        dev = self.device
+        T, R = c.T, c.R
+        i32 = dict(dtype=torch.int32, device=dev)
+        return {
+            "h_prompt": torch.empty(R, L, dtype=torch.int32).pin_memory(),
+            "d_prompt": torch.empty(R, L, **i32),
+            "sel": [(torch.empty(R, W[s], **i32), torch.empty(R, W[s], **i32),
+                     torch.empty(R, W[s], dtype=torch.float32, device=dev)) for s in range(T)],
+            "bias": ([torch.empty(R, W[t], dtype=torch.float32, device=dev) for t in range(T - 1)]
+                     if with_bias else None),
+            "d_sid": torch.empty(R, W[T - 1], T, **i32),
+            "h_sid": torch.empty(R, W[T - 1], T, dtype=torch.int32).pin_memory(),
+            "h_cum": torch.empty(R, W[T - 1], dtype=torch.float32).pin_memory(),
+            "stream": torch.cuda.Stream(dev),
+            "graph": None,
+        }
+
+    def _serve_run(self, st, W: Sequence[int], stream):
+        T = self.cfg.T
+        st["d_prompt"].copy_(st["h_prompt"], non_blocking=True)
+        self.prefill(st["d_prompt"], stream=stream)
+        par, tok, cum = self.select(-1, 1, W[0], self.root_logits, self.root_lse, out=st["sel"][0],
+                                    stream=stream)
+        for t in range(T - 1):
+            lg, ls = self.step(t, W[t], par if t else None, tok, stream=stream)
+            b = st["bias"][t] if st["bias"] is not None else None
+            par, tok, cum = self.select(t, W[t], W[t + 1], lg, ls, cum, b, out=st["sel"][t + 1],
+                                        stream=stream)
+        sid = self.get_paths(W[T - 1], par if T > 1 else None, tok, sid=st["d_sid"], stream=stream)
+        st["h_sid"].copy_(sid, non_blocking=True)
+        st["h_cum"].copy_(cum, non_blocking=True)
 
     def _forced_cum(self, t, forced):
         # under a forced lineage the cumulative scores of the forced beams are

@@ -68,3 +68,34 @@ def test_graph_replay_matches_eager_calls(name):
     replayed = [x for o in outs[1:] for x in o] + [sid]
     for a, b in zip(eager, replayed):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_serve_graph_matches_decode(name):
+    # BeamDecoder.serve captures a whole batch (prompt upload, prefill, root
+    # selection, decode calls, selections, paths and scores download) once per
+    # shape and replays it: two batches of different prompts, served one
+    # after the other, give bit for bit what an ordinary decode of each gives
+    wl = CASES[name]
+    p = synth.make_params(wl)
+    dec = decoder_for(wl, p)
+    bias = synth.make_bias(wl)
+    bias_dev = to_dev(bias) if bias is not None else None
+    rng = np.random.default_rng(5)
+    batches = [synth.make_prompt(wl), rng.integers(0, wl.V, size=(wl.R, wl.L)).astype(np.int32)]
+    expect = []
+    for prompts in batches:
+        dec.prefill(to_dev(prompts, torch.int32))
+        res = dec.decode(wl.W, bias=bias_dev)
+        torch.cuda.synchronize()
+        assert dec.status() == 0
+        expect.append((res.sid.cpu().clone(), res.cum[-1].cpu().clone()))
+    for rep in range(2):  # first use (ordinary run, then capture), then replays
+        for prompts, (sid_e, cum_e) in zip(batches, expect):
+            sid, cum = dec.serve(torch.as_tensor(prompts), wl.W, bias_dev)
+            assert torch.equal(sid, sid_e), (rep, "sid")
+            assert torch.equal(cum.view(torch.int32), cum_e.view(torch.int32)), (rep, "cum")
+    # the same batches served as ordinary calls
+    for prompts, (sid_e, cum_e) in zip(batches, expect):
+        sid, cum = dec.serve(torch.as_tensor(prompts), wl.W, bias_dev, graph=False)
+        assert torch.equal(sid, sid_e) and torch.equal(cum.view(torch.int32), cum_e.view(torch.int32))
