@@ -35,6 +35,7 @@
 
 #include "common.cuh"
 #include "launchers.h"
+#include "tc_ptx.cuh"
 
 namespace gdnbeam {
 
@@ -71,6 +72,33 @@ template <> struct SKey<float> {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
   }
 };
+
+// The block of a request's cluster that filters listed tile i (the tile's
+// index in the request's hint array): a multiplicative hash of i spread over
+// `parts` blocks, so tiles of one code range do not all go to one block.
+__device__ __forceinline__ int tile_owner(uint32_t i, int parts) {
+  return (int)(((uint64_t)(i * 0x9E3779B1u) * (uint32_t)parts) >> 32);
+}
+
+// Blocks in this block's cluster (1 without a cluster launch).
+__device__ __forceinline__ uint32_t cluster_nctas() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+// Loads from the same shared-memory location in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t ld_cluster_u32(const void* p, uint32_t rank) {
+  uint32_t v;
+  const uint32_t a = tc::mapa_shared(tc::smem_u32(p), rank);
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_cluster_u64(const void* p, uint32_t rank) {
+  uint64_t v;
+  const uint32_t a = tc::mapa_shared(tc::smem_u32(p), rank);
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ float cum_prime(const float* cum, const float* bias, size_t row) {
   float cp = cum ? cum[row] : 0.0f;
@@ -369,7 +397,8 @@ __global__ void tile_max_kernel(int n, int V, int n_tiles, const T* __restrict__
 // in every thread); hkeys holds smem_keys 32-bit keys.
 struct Bound {
   uint32_t t, hmax;
-  int n_list;
+  int n_list;  // tiles reaching the bound
+  int n_own;   // of them, this block's share (tile_owner == part)
 };
 
 // Per-row parameters of a request: cum' and lse, and the row's cutoff logit
@@ -397,13 +426,16 @@ template <typename T>
 __device__ Bound bound_phase(int r, int W_t, int n_tiles, int W_next,
                             const float2* __restrict__ hint, const Rows& rows,
                             const SelScratch& ss, uint32_t* hkeys, int smem_keys, uint32_t* slist,
-                            int slist_cap, unsigned* bins, unsigned* err) {
+                            int slist_cap, unsigned* bins, int part, int parts, unsigned* err) {
   __shared__ unsigned sh[4];
-  __shared__ int s_cnt;
+  __shared__ int s_cnt, s_own;
   __shared__ uint32_t s_wlo[32], s_whi[32];
   const int n_h = W_t * n_tiles;
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) s_cnt = 0;
+  if (threadIdx.x == 0) {
+    s_cnt = 0;
+    s_own = 0;
+  }
   // the rows' parameters; a row whose lse or cumulative score is not finite
   // is flagged
   for (int b = threadIdx.x; b < W_t; b += blockDim.x) {
@@ -470,13 +502,36 @@ __device__ Bound bound_phase(int r, int W_t, int n_tiles, int W_next,
     else
       t = radix_window<uint32_t>(n_h, (unsigned)W_next, klo, khi, key_of, bins, sh);
   }
-  // the tiles whose hint reaches t
+  // the tiles whose hint reaches t: all of them to the request's list in
+  // global memory (written by block part 0 alone), this block's share to its
+  // on-chip list (every tile when parts = 1)
   uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
-  for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
-    if ((on_chip ? hkeys[i] : key_of(i)) >= t) {
-      const int pos = atomicAdd(&s_cnt, 1);
-      if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
-      if (pos < slist_cap) slist[pos] = (uint32_t)i;  // the on-chip copy, when it fits
+  if (parts == 1) {
+    for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
+      if ((on_chip ? hkeys[i] : key_of(i)) >= t) {
+        const int pos = atomicAdd(&s_cnt, 1);
+        if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
+        if (pos < slist_cap) slist[pos] = (uint32_t)i;  // the on-chip copy, when it fits
+      }
+    }
+  } else {
+    int mine = 0;  // listed tiles this thread saw (the other blocks count them too)
+    for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
+      if ((on_chip ? hkeys[i] : key_of(i)) >= t) {
+        ++mine;
+        if (part == 0) {
+          const int pos = atomicAdd(&s_cnt, 1);
+          if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
+        }
+        if (tile_owner((uint32_t)i, parts) == part) {
+          const int q = atomicAdd(&s_own, 1);
+          if (q < slist_cap) slist[q] = (uint32_t)i;
+        }
+      }
+    }
+    if (part != 0) {
+      for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+      if (lane == 0 && mine) atomicAdd(&s_cnt, mine);
     }
   }
   // each row's cutoff: the smallest stored value whose score reaches t, by
@@ -492,8 +547,8 @@ __device__ Bound bound_phase(int r, int W_t, int n_tiles, int W_next,
     }
     rows.set_cut(b, SKey<T>::value(lo));
   }
-  __syncthreads();  // the list, the cutoffs and the counter are complete
-  return Bound{t, khi, s_cnt};
+  __syncthreads();  // the list, the cutoffs and the counters are complete
+  return Bound{t, khi, s_cnt, s_own};
 }
 
 // Eight stored codes as loaded: one 16-byte word of bf16, two of fp32.
@@ -550,7 +605,7 @@ constexpr int kDenseHits = 32;
 template <typename T, typename F, typename D>
 __device__ __forceinline__ void for_listed_codes(int V, int n_tiles, int n_list, const uint32_t* list,
                                                  const T* __restrict__ z, const Rows& rows, F&& f,
-                                                 D&& dense) {
+                                                 D&& dense, int part = 0, int parts = 1) {
   constexpr int EPL = kTile / 32;
   constexpr int U = sizeof(T) == 2 ? 6 : 3;  // tiles in flight per warp
   const int lane = threadIdx.x & 31;
@@ -559,7 +614,12 @@ __device__ __forceinline__ void for_listed_codes(int V, int n_tiles, int n_list,
   for (int j0 = (threadIdx.x >> 5) * U; j0 < n_list; j0 += warps * U) {
     uint32_t ids[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) ids[u] = j0 + u < n_list ? list[j0 + u] : 0xFFFFFFFFu;
+    for (int u = 0; u < U; ++u) {
+      ids[u] = j0 + u < n_list ? list[j0 + u] : 0xFFFFFFFFu;
+      // with parts > 1, only tiles whose id falls in this block's share
+      if (parts > 1 && ids[u] != 0xFFFFFFFFu && tile_owner(ids[u], parts) != part)
+        ids[u] = 0xFFFFFFFFu;
+    }
     Codes8<T> zc[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -599,7 +659,8 @@ __device__ __forceinline__ void for_listed_codes(int V, int n_tiles, int n_list,
 // past target are counted, not written).
 template <typename T>
 __device__ int append_listed(int V, int n_tiles, int n_list, const uint32_t* list, uint32_t lo,
-                             int target, const T* __restrict__ z, const Rows& rows, uint64_t* keys) {
+                             int target, const T* __restrict__ z, const Rows& rows, uint64_t* keys,
+                             int part = 0, int parts = 1) {
   __shared__ unsigned s_cnt;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) s_cnt = 0u;
@@ -631,7 +692,8 @@ __device__ int append_listed(int V, int n_tiles, int n_list, const uint32_t* lis
 #pragma unroll
         for (int e = 0; e < kTile / 32; ++e)
           if ((keep >> e) & 1u) put(pos++, o[e], flat0 + (uint32_t)e);
-      });
+      },
+      part, parts);
   __syncthreads();
   return (int)s_cnt;
 }
@@ -742,7 +804,15 @@ __global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
   extern __shared__ uint64_t keys[];
   __shared__ unsigned sh[4];
   __shared__ uint64_t win[kMaxSort];
-  const int r = blockIdx.x;
+  __shared__ int s_nloc;
+  // A request runs on one block, or on a cluster of csize blocks when
+  // requests are fewer than the SMs: every block computes the same bound,
+  // each filters its share of the listed tiles (tile_owner), and the
+  // first block gathers the others' candidates from their shared memory and
+  // finishes the selection alone.
+  const int csize = (int)cluster_nctas();
+  const int rank = (int)tc::cluster_ctarank();
+  const int r = blockIdx.x / csize;
   // the tile list is kept on chip in the sort window (idle until the end)
   // when it fits
   uint32_t* slist = reinterpret_cast<uint32_t*>(win);
@@ -755,13 +825,44 @@ __global__ void __launch_bounds__(kFinalThreads) select_fused_kernel(
   unsigned* bins = reinterpret_cast<unsigned*>(win);
   const Bound bd = bound_phase<T>(r, W_t, n_tiles, W_next, hint, rows, ss,
                                   reinterpret_cast<uint32_t*>(keys), bound_keys, slist, kSlist,
-                                  bins, err);
+                                  bins, rank, csize, err);
   const uint32_t t = bd.t, hmax = bd.hmax;
   const int n_tc = bd.n_list;
   const int n_list = min(n_tc, ss.cap_tiles);
-  const uint32_t* list = n_list <= kSlist ? slist : ss.tlist + (size_t)r * ss.cap_tiles;
+  // the whole list: on chip with one block per request when it fits, else
+  // the copy in global memory
+  const uint32_t* full = ss.tlist + (size_t)r * ss.cap_tiles;
+  const bool on_chip_list = n_list <= kSlist;  // the same in every block of the cluster
+  const uint32_t* list = on_chip_list && csize == 1 ? slist : full;
   const int target = min(ss.cap, kFinalSmemKeys);
-  int n_c = append_listed<T>(V, n_tiles, n_list, list, t, target, z, rows, keys);
+  int n_c;
+  if (csize == 1) {
+    n_c = append_listed<T>(V, n_tiles, n_list, list, t, target, z, rows, keys);
+  } else {
+    // this block's share: its on-chip list, or the global list (written by
+    // block 0, complete once the cluster has met) with the other tiles skipped
+    if (!on_chip_list) tc::cluster_sync();
+    n_c = on_chip_list
+              ? append_listed<T>(V, n_tiles, bd.n_own, slist, t, target, z, rows, keys)
+              : append_listed<T>(V, n_tiles, n_list, full, t, target, z, rows, keys, rank, csize);
+    if (threadIdx.x == 0) s_nloc = n_c;
+    tc::cluster_sync();  // every block's candidates are in its shared memory
+    if (rank == 0) {
+      int total = n_c;
+      for (int q = 1; q < csize; ++q) total += (int)ld_cluster_u32(&s_nloc, q);
+      if (total <= target) {
+        int off = n_c;
+        for (int q = 1; q < csize; ++q) {
+          const int nq = (int)ld_cluster_u32(&s_nloc, q);
+          for (int i = threadIdx.x; i < nq; i += blockDim.x) keys[off + i] = ld_cluster_u64(&keys[i], q);
+          off += nq;
+        }
+      }
+      n_c = total;  // above target: narrowed below over the whole list
+    }
+    tc::cluster_sync();  // block 0 has read the others' candidates
+    if (rank != 0) return;
+  }
   uint32_t lo_key = t;
   if (n_c > target && n_c >= W_next && n_tc <= ss.cap_tiles) {
     n_c = narrow_bound<T>(V, n_tiles, n_list, list, W_next, target, z, rows,
@@ -940,10 +1041,26 @@ int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, 
   const size_t fused_smem = (size_t)kFinalSmemKeys * 8 + (rows_on_chip ? (size_t)W_t * 16 : 0);
   GDN_CUDA(cudaFuncSetAttribute(select_fused_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)fused_smem));
-  select_fused_kernel<T><<<R, kFinalThreads, fused_smem, s>>>(W_t, V, n_tiles, W_next, hint, z, lse,
-                                                              cum, bias, ss, bound_keys,
-                                                              rows_on_chip, parents, tokens,
-                                                              cum_next, err);
+  // a cluster of blocks per request while requests are fewer than the SMs
+  int csize = 1;
+  while (csize < 4 && (long long)R * csize * 2 <= sm_count()) csize *= 2;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(R * csize), 1, 1);
+    cfg.blockDim = dim3(kFinalThreads, 1, 1);
+    cfg.dynamicSmemBytes = fused_smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)csize;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    GDN_CUDA(cudaLaunchKernelEx(&cfg, select_fused_kernel<T>, W_t, V, n_tiles, W_next, hint, z, lse,
+                                cum, bias, ss, bound_keys, rows_on_chip, parents, tokens, cum_next,
+                                err));
+  }
   GDN_LAUNCH_CHECK();
   // exact fallback for requests whose buffer was short or overflowed
   const size_t row_smem = (size_t)V * 8;
