@@ -704,6 +704,7 @@ int launch_tc_project(const gdnbeam_config& c, int n, const void* u, const void*
   EpiArgs ea{};
   ea.M = n;
   ea.K = c.d_model;
+  ea.err = error_word();
   // the projection columns computed: all, all but the queries, or only them
   if (cols == PROJ_ALL) {
     ea.N = n_full;
@@ -748,6 +749,7 @@ int launch_tc_logits(const gdnbeam_config& c, int n, const void* feat, const voi
   EpiArgs ea{};
   ea.M = n;
   ea.N = c.V;
+  ea.err = error_word();
   ea.K = c.residual ? c.d_model : c.H * c.d_v;
   ea.z = (__nv_bfloat16*)z;
   ea.z_dump = d ? d->logits : nullptr;

@@ -27,31 +27,49 @@ __global__ void gather_rows_kernel(int n, int d_model, const int32_t* __restrict
   }
 }
 
-// Same, 16 bytes per thread: chunk c of the output is row c / cpr, piece
-// c % cpr (cpr 16-byte pieces per row).
+// Same, one warp per row, 16-byte pieces: the row's token is read once (the
+// warp's next row's token is fetched while this row is copied) and each
+// lane issues up to kGatherU piece loads before storing any, so a warp keeps
+// a whole 4 KB bf16 row in flight. cpr: 16-byte pieces per row.
+constexpr int kGatherU = 8;
 template <typename T>
-__global__ void gather_rows_vec_kernel(long long chunks, int cpr, const int32_t* __restrict__ tokens,
-                                       int V, const uint4* __restrict__ E, uint4* __restrict__ u,
+__global__ void gather_rows_vec_kernel(int n, int cpr, const int32_t* __restrict__ tokens, int V,
+                                       const uint4* __restrict__ E, uint4* __restrict__ u,
                                        float4* __restrict__ x, unsigned* err) {
   constexpr int EPC = 16 / (int)sizeof(T);
-  for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < chunks;
-       c += (long long)gridDim.x * blockDim.x) {
-    const long long m = c / cpr;
-    const int piece = (int)(c - m * cpr);
-    const int tok = __ldg(tokens + m);
+  const int lane = threadIdx.x & 31;
+  const int step = gridDim.x * (blockDim.x >> 5);
+  int m = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int tok = m < n ? __ldg(tokens + m) : 0;
+  for (; m < n; m += step) {
+    const int next = m + step < n ? __ldg(tokens + m + step) : 0;
     const bool ok = tok >= 0 && tok < V;
-    if (!ok && piece == 0) raise_error(err, GDNBEAM_DERR_TOKEN);
-    const uint4 val = ok ? __ldg(E + (size_t)tok * cpr + piece) : make_uint4(0u, 0u, 0u, 0u);
-    u[c] = val;
-    if (x) {
-      const T* e = reinterpret_cast<const T*>(&val);
-      float f[EPC];
+    if (!ok && lane == 0) raise_error(err, GDNBEAM_DERR_TOKEN);
+    const uint4* src = E + (size_t)(ok ? tok : 0) * cpr;
+    uint4* dst = u + (size_t)m * cpr;
+    for (int p0 = 0; p0 < cpr; p0 += 32 * kGatherU) {
+      uint4 val[kGatherU];
 #pragma unroll
-      for (int i = 0; i < EPC; ++i) f[i] = St<T>::to_f(e[i]);
+      for (int i = 0; i < kGatherU; ++i) {
+        const int p = p0 + 32 * i + lane;
+        val[i] = ok && p < cpr ? __ldg(src + p) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-      for (int i = 0; i < EPC / 4; ++i)
-        x[c * (EPC / 4) + i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+      for (int i = 0; i < kGatherU; ++i) {
+        const int p = p0 + 32 * i + lane;
+        if (p >= cpr) continue;
+        dst[p] = val[i];
+        if (x) {
+          const T* e = reinterpret_cast<const T*>(&val[i]);
+          float4* xr = x + ((size_t)m * cpr + p) * (EPC / 4);
+#pragma unroll
+          for (int j = 0; j < EPC / 4; ++j)
+            xr[j] = make_float4(St<T>::to_f(e[4 * j]), St<T>::to_f(e[4 * j + 1]),
+                                St<T>::to_f(e[4 * j + 2]), St<T>::to_f(e[4 * j + 3]));
+        }
+      }
     }
+    tok = next;
   }
 }
 
@@ -62,14 +80,14 @@ int launch_gather_rows(int dtype, int n, int d_model, const int32_t* tokens, int
   if ((d_model * esz) % 16 == 0 && ((uintptr_t)E & 15) == 0 && ((uintptr_t)u & 15) == 0 &&
       ((uintptr_t)x & 15) == 0) {
     const int cpr = d_model * esz / 16;
-    const long long chunks = (long long)n * cpr;
-    const long long want = (chunks + 255) / 256;
-    const int blocks = (int)(want < 16 * sm_count() ? want : 16 * sm_count());
+    // eight rows (warps) per block, at most eight blocks per SM
+    const long long want = ((long long)n + 7) / 8;
+    const int blocks = (int)(want < 8 * sm_count() ? want : 8 * sm_count());
     if (dtype == GDNBEAM_BF16)
       gather_rows_vec_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
-          chunks, cpr, tokens, V, (const uint4*)E, (uint4*)u, (float4*)x, err);
+          n, cpr, tokens, V, (const uint4*)E, (uint4*)u, (float4*)x, err);
     else
-      gather_rows_vec_kernel<float><<<blocks, 256, 0, s>>>(chunks, cpr, tokens, V, (const uint4*)E,
+      gather_rows_vec_kernel<float><<<blocks, 256, 0, s>>>(n, cpr, tokens, V, (const uint4*)E,
                                                            (uint4*)u, (float4*)x, err);
     GDN_LAUNCH_CHECK();
     return GDNBEAM_OK;

@@ -282,12 +282,30 @@ def test_step_before_prefill_is_rejected():
     assert ei.value.status == gb.ESTATE
 
 
-def test_bad_token_sets_device_error():
-    wl = synth.TINY
+@pytest.mark.parametrize("wl", [synth.TINY, synth.GQA.with_(name="gqa_r1", R=1, L=64)],
+                         ids=["tiny_f32", "gqa_bf16"])
+def test_bad_token_sets_device_error(wl):
+    # a token outside [0, V) is reported through the status word, whether
+    # the embedding rows are copied out (CUDA-core path) or gathered by the
+    # tensor-core projection's own loads
     dec = decoder_for(wl, synth.make_params(wl))
     dec.prefill(_i32(synth.make_prompt(wl)))
-    tok = _i32(np.full((1, 8), 99))  # V = 16
-    dec.step(0, 8, None, tok)
+    assert dec.status() == 0
+    W = wl.W[0]
+    tok = np.zeros((wl.R, W), dtype=np.int32)
+    tok[0, W // 2] = wl.V + 3
+    dec.step(0, W, None, _i32(tok))
+    assert dec.status() == gb.EDEVICE
+    assert device_status_clear() == 0
+
+
+def test_bad_prompt_token_sets_device_error():
+    # the chunked prefill's projections gather the prompt rows themselves
+    wl = synth.GQA.with_(name="gqa_r1", R=1, L=64)
+    dec = decoder_for(wl, synth.make_params(wl))
+    prompt = synth.make_prompt(wl)
+    prompt[0, wl.L - 1] = -1  # the last token: read by both prefill projections
+    dec.prefill(_i32(prompt))
     assert dec.status() == gb.EDEVICE
     assert device_status_clear() == 0
 
