@@ -243,6 +243,23 @@ size_t carve(const gdnbeam_config& c, bool tc_gemm, char* base, gdnbeam_ctx* x,
   return off;
 }
 
+// Embedding rows of n tokens: u = E[tok] without a residual stream; with
+// one, x = E[tok] (fp32) and, when the fused pass supports the width, u =
+// the first layer's RMS-normalised rows in the same pass (*normed set).
+int embed_rows(const gdnbeam_config& c, int n, const int32_t* tok, const void* E, void* u,
+               float* x, unsigned* err, cudaStream_t s, bool* normed) {
+  *normed = false;
+  if (c.residual) {
+    const int st = launch_gather_norm_rows(c.dtype, n, c.d_model, tok, c.V, E, x, u, err, s);
+    if (st != GDNBEAM_EINVAL) {
+      *normed = st == GDNBEAM_OK;
+      return st;
+    }
+  }
+  return launch_gather_rows(c.dtype, n, c.d_model, tok, c.V, E, u, c.residual ? x : nullptr, err,
+                            s);
+}
+
 int project_any(const gdnbeam_config& c, bool tc, int n, const void* u, const void* Wp, void* q,
                 void* k, void* v, float* alpha, float* beta, void* scratch, size_t scratch_bytes,
                 const gdnbeam_dumps* d, cudaStream_t s) {
@@ -381,12 +398,12 @@ int prefill_pass(gdnbeam_ctx* ctx, const gdnbeam_config& c, const int32_t* promp
   const int Np = n_proj(c);
   const long long rstride = (long long)c.layers * c.H * c.d_v * c.d_k;
   int ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
-  int st = launch_gather_rows(c.dtype, n, c.d_model, prompt, c.V, ctx->w.E, ctx->pf_u,
-                              c.residual ? ctx->pf_x : nullptr, err, s);
+  bool normed = false;  // pf_u already holds layer 0's normalised rows
+  int st = embed_rows(c, n, prompt, ctx->w.E, ctx->pf_u, ctx->pf_x, err, s, &normed);
   ctx->toc(ev, s);
   if (st) return st;
   for (int layer = 0; layer < c.layers; ++layer) {
-    if (c.residual) {
+    if (c.residual && !(layer == 0 && normed)) {
       ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
       st = launch_rmsnorm_rows(c.dtype, n, c.d_model, ctx->pf_x, c.d_model, ctx->pf_u, s);
       ctx->toc(ev, s);
@@ -530,12 +547,12 @@ int gdnbeam_step(gdnbeam_ctx* ctx, int t, int W_t, const int32_t* parents, const
   ctx->toc(ev, s);
   if (st) return st;
   ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
-  st = launch_gather_rows(c.dtype, n, c.d_model, tokens, c.V, ctx->w.E, ctx->u,
-                          c.residual ? ctx->x : nullptr, err, s);
+  bool normed = false;  // u already holds layer 0's normalised rows
+  st = embed_rows(c, n, tokens, ctx->w.E, ctx->u, ctx->x, err, s, &normed);
   ctx->toc(ev, s);
   if (st) return st;
   for (int layer = 0; layer < c.layers; ++layer) {
-    if (c.residual) {
+    if (c.residual && !(layer == 0 && normed)) {
       ev = ctx->tic(GDNBEAM_STAGE_EMBED, s);
       st = launch_rmsnorm_rows(c.dtype, n, c.d_model, ctx->x, c.d_model, ctx->u, s);
       ctx->toc(ev, s);

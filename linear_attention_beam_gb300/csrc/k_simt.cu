@@ -161,6 +161,81 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_vec_kernel(int n, int nv, co
   }
 }
 
+// Embedding rows into a residual stream and its first RMS norm in one pass:
+// x[m] = E[tok[m]] (fp32) and u[m] = x[m] / rms(x[m]) in the storage type,
+// one warp per row held in registers, with the chunk-to-lane layout and the
+// arithmetic of rmsnorm_rows_vec_kernel (lane l holds 4-element chunks
+// l + 32k, k < nv; d = 128 nv). A token outside [0, V) gives a zero row and
+// is reported.
+template <typename T>
+__global__ void __launch_bounds__(256) gather_norm_rows_kernel(int n, int nv,
+                                                               const int32_t* __restrict__ tokens,
+                                                               int V, const T* __restrict__ E,
+                                                               float* __restrict__ x,
+                                                               T* __restrict__ u, unsigned* err) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= n) return;
+  const int d = nv * 128;
+  const int tok = __ldg(tokens + warp);
+  const bool ok = tok >= 0 && tok < V;
+  if (!ok && lane == 0) raise_error(err, GDNBEAM_DERR_TOKEN);
+  const T* src = E + (size_t)(ok ? tok : 0) * d;
+  float4 v[kNormMaxVec];
+  float ss = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kNormMaxVec; ++k) {
+    if (k < nv) {
+      const int c = 4 * (lane + 32 * k);
+      if constexpr (sizeof(T) == 2) {
+        const uint2 w = ok ? __ldg(reinterpret_cast<const uint2*>(src + c)) : make_uint2(0u, 0u);
+        v[k] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+      } else {
+        v[k] = ok ? __ldg(reinterpret_cast<const float4*>(src + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      reinterpret_cast<float4*>(x + (size_t)warp * d)[lane + 32 * k] = v[k];
+      ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv = 1.0f / sqrtf(ss / (float)d + 1e-6f);
+#pragma unroll
+  for (int k = 0; k < kNormMaxVec; ++k) {
+    if (k < nv) {
+      const size_t c = (size_t)warp * d + 4 * (lane + 32 * k);
+      if constexpr (sizeof(T) == 2) {
+        const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[k].x * inv)) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[k].y * inv)) << 16);
+        const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[k].z * inv)) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[k].w * inv)) << 16);
+        *reinterpret_cast<uint2*>(u + c) = make_uint2(lo, hi);
+      } else {
+        *reinterpret_cast<float4*>(u + c) =
+            make_float4(v[k].x * inv, v[k].y * inv, v[k].z * inv, v[k].w * inv);
+      }
+    }
+  }
+}
+
+int launch_gather_norm_rows(int dtype, int n, int d, const int32_t* tokens, int V, const void* E,
+                            float* x, void* u, unsigned* err, cudaStream_t s) {
+  if (n <= 0) return GDNBEAM_OK;
+  const int esz = dtype == GDNBEAM_BF16 ? 2 : 4;
+  if (d % 128 != 0 || d > 128 * kNormMaxVec || ((uintptr_t)E & (4 * esz - 1)) != 0 ||
+      ((uintptr_t)x & 15) != 0 || ((uintptr_t)u & (4 * esz - 1)) != 0)
+    return GDNBEAM_EINVAL;
+  const int blocks = (n + 7) / 8;
+  if (dtype == GDNBEAM_BF16)
+    gather_norm_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+        n, d / 128, tokens, V, (const __nv_bfloat16*)E, x, (__nv_bfloat16*)u, err);
+  else
+    gather_norm_rows_kernel<float><<<blocks, 256, 0, s>>>(n, d / 128, tokens, V, (const float*)E,
+                                                          x, (float*)u, err);
+  GDN_LAUNCH_CHECK();
+  return GDNBEAM_OK;
+}
+
 int launch_rmsnorm_rows(int dtype, int n, int d, const float* x, long long xs, void* u,
                         cudaStream_t s) {
   if (n <= 0) return GDNBEAM_OK;

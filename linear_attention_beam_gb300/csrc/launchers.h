@@ -13,6 +13,12 @@ namespace gdnbeam {
 // ---- CUDA-core kernels (any supported shape, fp32 or bf16 storage) -------
 
 // u[m] = E[tokens[m]] (storage copy); if x != NULL also x[m] = fp32(E[...]).
+// Rows of E into a residual stream plus its first RMS norm, one pass:
+// x[m] = E[tok[m]] as fp32, u[m] = x[m] / rms(x[m]) (unit gain, eps 1e-6).
+// GDNBEAM_EINVAL (nothing launched) unless d is a multiple of 128 up to 2048
+// and the rows are vector-aligned.
+int launch_gather_norm_rows(int dtype, int n, int d, const int32_t* tokens, int V, const void* E,
+                            float* x, void* u, unsigned* err, cudaStream_t s);
 int launch_gather_rows(int dtype, int n, int d_model, const int32_t* tokens, int V,
                        const void* E, void* u, float* x, unsigned* err, cudaStream_t s);
 

@@ -102,6 +102,14 @@ SMALL = {
                                     d_model=96, L=24, seed=12),
     "wide_v256": synth.Workload("wide_v256", R=1, layers=1, H=4, d_k=128, d_v=256, d_model=512,
                                 V=1024, T=3, W=(64, 64, 64), L=96, dtype="bf16", seed=13, H_k=2),
+    # stacked layers with a residual stream: the embedding rows and the first
+    # layer's RMS norm in one pass (d_model a multiple of 128), or as a gather
+    # then a norm (d_model = 96); and one request of the four-layer bf16 model
+    "resid_f32": synth.tiny_workload(d=16, H=8, layers=3, residual=True, V=24, T=3, W=(8, 12, 10),
+                                     d_model=128, L=40, seed=5),
+    "resid96_f32": synth.tiny_workload(d=16, H=6, layers=3, residual=True, V=24, T=3, W=(8, 12, 10),
+                                       d_model=96, L=40, seed=6),
+    "deep_r1": synth.DEEP.with_(name="deep_r1", R=1, W=(32, 64, 64, 64), L=130),
 }
 
 
