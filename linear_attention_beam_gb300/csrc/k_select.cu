@@ -76,6 +76,11 @@ template <> struct SKey<float> {
 // The block of a request's cluster that filters listed tile i (the tile's
 // index in the request's hint array): a multiplicative hash of i spread over
 // `parts` blocks, so tiles of one code range do not all go to one block.
+// A listed (row b, tile) pair is stored as b << tile_bits(n_tiles) | tile,
+// so the filter splits it with a shift and a mask.
+__device__ __forceinline__ int tile_bits(int n_tiles) {
+  return n_tiles > 1 ? 32 - __clz(n_tiles - 1) : 0;
+}
 __device__ __forceinline__ int tile_owner(uint32_t i, int parts) {
   return (int)(((uint64_t)(i * 0x9E3779B1u) * (uint32_t)parts) >> 32);
 }
@@ -324,7 +329,7 @@ struct SelScratch {
   int* fb_any;      // [1] some request needs the fallback (reset by the fallback's last kernel)
   uint64_t* pre;    // [R*W_t][K] fallback precut keys
   float2* hint;     // [R*W_t][n_tiles] tile maxima computed here when not supplied
-  uint32_t* tlist;  // [R][cap_tiles] (row, tile) pairs whose maximum reaches the bound, b * n_tiles + tile
+  uint32_t* tlist;  // [R][cap_tiles] (row, tile) pairs whose maximum reaches the bound, b << tile_bits | tile
   float* cut;       // [R*W_t] rows' cutoff logits, when the rows do not fit on chip
   int cap;          // candidates a request may keep on chip before the bound is narrowed
   int cap_tiles;
@@ -506,26 +511,38 @@ __device__ Bound bound_phase(int r, int W_t, int n_tiles, int W_next,
   // global memory (written by block part 0 alone), this block's share to its
   // on-chip list (every tile when parts = 1)
   uint32_t* list = ss.tlist + (size_t)r * ss.cap_tiles;
+  // thread i's (row, tile) = (i / n_tiles, i % n_tiles), stepped along
+  // with i (one division per thread)
+  const int tb = tile_bits(n_tiles);
+  const int db = (int)blockDim.x / n_tiles, dt = (int)blockDim.x % n_tiles;
+  int cb = (int)threadIdx.x / n_tiles, ct = (int)threadIdx.x % n_tiles;
+  auto step_bt = [&]() {
+    cb += db;
+    ct += dt;
+    if (ct >= n_tiles) { ct -= n_tiles; ++cb; }
+  };
   if (parts == 1) {
-    for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
+    for (int i = threadIdx.x; i < n_h; i += blockDim.x, step_bt()) {
       if ((on_chip ? hkeys[i] : key_of(i)) >= t) {
+        const uint32_t e = ((uint32_t)cb << tb) | (uint32_t)ct;
         const int pos = atomicAdd(&s_cnt, 1);
-        if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
-        if (pos < slist_cap) slist[pos] = (uint32_t)i;  // the on-chip copy, when it fits
+        if (pos < ss.cap_tiles) list[pos] = e;
+        if (pos < slist_cap) slist[pos] = e;  // the on-chip copy, when it fits
       }
     }
   } else {
     int mine = 0;  // listed tiles this thread saw (the other blocks count them too)
-    for (int i = threadIdx.x; i < n_h; i += blockDim.x) {
+    for (int i = threadIdx.x; i < n_h; i += blockDim.x, step_bt()) {
       if ((on_chip ? hkeys[i] : key_of(i)) >= t) {
+        const uint32_t e = ((uint32_t)cb << tb) | (uint32_t)ct;
         ++mine;
         if (part == 0) {
           const int pos = atomicAdd(&s_cnt, 1);
-          if (pos < ss.cap_tiles) list[pos] = (uint32_t)i;
+          if (pos < ss.cap_tiles) list[pos] = e;
         }
-        if (tile_owner((uint32_t)i, parts) == part) {
+        if (tile_owner(e, parts) == part) {
           const int q = atomicAdd(&s_own, 1);
-          if (q < slist_cap) slist[q] = (uint32_t)i;
+          if (q < slist_cap) slist[q] = e;
         }
       }
     }
@@ -611,6 +628,8 @@ __device__ __forceinline__ void for_listed_codes(int V, int n_tiles, int n_list,
   const int lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const bool vec = (V % 8) == 0 && ((uintptr_t)z & 15) == 0;
+  const int tb = tile_bits(n_tiles);
+  const uint32_t tmask = (1u << tb) - 1u;
   for (int j0 = (threadIdx.x >> 5) * U; j0 < n_list; j0 += warps * U) {
     uint32_t ids[U];
 #pragma unroll
@@ -624,13 +643,13 @@ __device__ __forceinline__ void for_listed_codes(int V, int n_tiles, int n_list,
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (ids[u] == 0xFFFFFFFFu) continue;
-      const int b = (int)(ids[u] / (uint32_t)n_tiles), tile = (int)(ids[u] % (uint32_t)n_tiles);
+      const int b = (int)(ids[u] >> tb), tile = (int)(ids[u] & tmask);
       zc[u].load(z + (rows.base + b) * (size_t)V, tile * kTile + lane * EPL, V, vec);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if (ids[u] == 0xFFFFFFFFu) continue;
-      const int b = (int)(ids[u] / (uint32_t)n_tiles), tile = (int)(ids[u] % (uint32_t)n_tiles);
+      const int b = (int)(ids[u] >> tb), tile = (int)(ids[u] & tmask);
       const float4 rp = rows.get(b);
       unsigned hits = 0;
 #pragma unroll
@@ -1066,7 +1085,7 @@ int run_select(int R, int W_t, int W_next, int V, const T* z, const float* lse, 
   const size_t row_smem = (size_t)V * 8;
   GDN_CUDA(cudaFuncSetAttribute(select_rowcut_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)row_smem));
-  const int rc_grid = n < 4 * sm_count() ? n : 4 * sm_count();
+  const int rc_grid = n < sm_count() ? n : sm_count();  // one wave: cheap when it exits at once
   select_rowcut_kernel<T><<<rc_grid, kRowThreads, row_smem, s>>>(n, W_t, V, K, z, lse, cum, bias,
                                                                  ss, err);
   GDN_LAUNCH_CHECK();
