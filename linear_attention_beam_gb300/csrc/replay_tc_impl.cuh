@@ -168,6 +168,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int rec_off = B_BYTES + V_BYTES;
   constexpr int kEpi0 = 2, kRec0 = 2 + kEpiWarps, kScal0 = kRec0 + 2;  // first warp of each role
 
+  // Epilogue warps: their S_ctx row (vb * 128 + i_row, K half hb) in batches
+  // of 32 values; the first batches are requested before anything else (the
+  // barrier and TMEM set-up, the table), so those latencies overlap.
+  const bool epi_warp = warp >= kEpi0 && warp < kEpi0 + kEpiWarps;
+  const int e_hb = (warp - kEpi0) >> 2, e_row = (warp & 3) * 32 + lane;
+  const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * p.dv * DK +
+                   (size_t)(vb * VR + e_row) * DK + e_hb * (DK / 2);
+  constexpr int kBatches = DK / 64;
+  constexpr int kEarly = kBatches < 2 ? kBatches : 2;
+  float4 xe[kEarly][8];
+  if (epi_warp) {
+#pragma unroll
+    for (int bt = 0; bt < kEarly; ++bt)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) xe[bt][c] = __ldg(reinterpret_cast<const float4*>(S) + bt * 8 + c);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       tc::mbar_init(full(s), TD > 0 ? 3 : 1);  // the producer and the record loaders
@@ -195,22 +211,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem_base = s_tmem;
 
-  // Epilogue warps: their S_ctx row (vb * 128 + i_row, K half hb) in batches
-  // of 32 values; the first batches are loaded before the table is built,
-  // so the two latencies overlap.
-  const bool epi_warp = warp >= kEpi0 && warp < kEpi0 + kEpiWarps;
-  const int e_hb = (warp - kEpi0) >> 2, e_row = (warp & 3) * 32 + lane;
-  const float* S = p.sctx + (size_t)r * p.sctx_rstride + (size_t)h * p.dv * DK +
-                   (size_t)(vb * VR + e_row) * DK + e_hb * (DK / 2);
-  constexpr int kBatches = DK / 64;
-  constexpr int kEarly = kBatches < 2 ? kBatches : 2;
-  float4 xe[kEarly][8];
-  if (epi_warp) {
-#pragma unroll
-    for (int bt = 0; bt < kEarly; ++bt)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) xe[bt][c] = __ldg(reinterpret_cast<const float4*>(S) + bt * 8 + c);
-  }
   // The block's table, built by every thread (one beam each at W = 512):
   // gates, ancestor slots and decays of every beam. The slot loads go out
   // together before the dependent decay loads.
