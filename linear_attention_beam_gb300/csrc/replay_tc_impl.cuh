@@ -39,6 +39,13 @@
 #include <cuda.h>
 #include <string.h>
 
+#include <algorithm>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
 #include "common.cuh"
 #include "launchers.h"
 #include "tc_ptx.cuh"
@@ -79,6 +86,7 @@ struct RecMaps {
 struct TcReplayParams {
   int R, H, Hk, dv, t, W_t, n_tiles, stages, stage_bytes;
   int tiles_per_block;  // beam tiles of one block; blockIdx.z picks the range
+  int first_tiles;      // > 0: two blocks per triple, tiles [0, first_tiles) and the rest
   const float* sctx;
   long long sctx_rstride;
   const float *alpha, *beta;
@@ -142,8 +150,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   // this block's beam tiles: tile0 .. tile0 + nt - 1, beams bb .. bb + nbeams - 1
-  const int tile0 = blockIdx.z * p.tiles_per_block;
-  const int nt = min(p.tiles_per_block, p.n_tiles - tile0);
+  int tile0, nt;
+  if (p.first_tiles > 0) {
+    tile0 = blockIdx.z == 0 ? 0 : p.first_tiles;
+    nt = blockIdx.z == 0 ? p.first_tiles : p.n_tiles - p.first_tiles;
+  } else {
+    tile0 = blockIdx.z * p.tiles_per_block;
+    nt = min(p.tiles_per_block, p.n_tiles - tile0);
+  }
   const int bb = tile0 * NB;
   const int nbeams = min(nt * NB, p.W_t - bb);
   // the table holds this block's beams, indexed from bb
@@ -661,6 +675,54 @@ inline bool rows_map(CUtensorMap* map, const void* ptr, long long rows, int cols
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Makespan, in tile times, of `base` blocks of each size sizes[0..n) run in
+// launch order (every block of the first size before any of the next, as
+// grid z is the slowest index), each on the SM that frees first, one block
+// per SM; a block costs its tiles plus a prologue of about three tiles.
+inline long long list_schedule(long long base, const int* sizes, int n, int sms) {
+  std::vector<long long> h((size_t)sms, 0);  // SM free times, a min-heap
+  long long mk = 0;
+  for (int z = 0; z < n; ++z)
+    for (long long b = 0; b < base; ++b) {
+      std::pop_heap(h.begin(), h.end(), std::greater<long long>());
+      h.back() += sizes[z] + 3;
+      mk = std::max(mk, h.back());
+      std::push_heap(h.begin(), h.end(), std::greater<long long>());
+    }
+  return mk;
+}
+
+// When the uniform split leaves a short grid's last wave part full, each
+// triple's tiles may go in two unequal blocks instead: all the large ones
+// first, then the small ones fill the SMs that free early. Returns the size
+// of the first block, or 0 when no such split beats `tpb`-tile blocks.
+// (Decided once per grid shape.)
+inline int two_piece_split(long long base, int n_tiles, int tpb, int sms) {
+  static std::mutex mu;
+  static std::map<std::tuple<long long, int, int, int>, int> memo;
+  const auto key = std::make_tuple(base, n_tiles, tpb, sms);
+  std::lock_guard<std::mutex> lock(mu);
+  const auto it = memo.find(key);
+  if (it != memo.end()) return it->second;
+  int best = 0;
+  if (sms > 0 && base < 4LL * sms && n_tiles >= 4) {
+    const int ns = (n_tiles + tpb - 1) / tpb;
+    std::vector<int> uni((size_t)ns, tpb);
+    uni.back() = n_tiles - tpb * (ns - 1);
+    long long best_cost = list_schedule(base, uni.data(), ns, sms);
+    for (int first = (n_tiles + 1) / 2; first < n_tiles; ++first) {
+      const int sizes[2] = {first, n_tiles - first};
+      const long long c = list_schedule(base, sizes, 2, sms);
+      if (c < best_cost) {
+        best_cost = c;
+        best = first;
+      }
+    }
+  }
+  memo[key] = best;
+  return best;
+}
+
 // Launches the kernel for key width DK (the caller checked the shape).
 template <int DK>
 int launch_tc_replay_dk(const ReplayArgs& a, cudaStream_t s) {
@@ -686,8 +748,11 @@ int launch_tc_replay_dk(const ReplayArgs& a, cudaStream_t s) {
         p.tiles_per_block = tpb;
       }
     }
+    p.first_tiles = two_piece_split(base, p.n_tiles, p.tiles_per_block, (int)sms);
+    if (p.first_tiles > 0) p.tiles_per_block = p.first_tiles;  // the larger block
   }
-  const int nsplit = (p.n_tiles + p.tiles_per_block - 1) / p.tiles_per_block;
+  const int nsplit =
+      p.first_tiles > 0 ? 2 : (p.n_tiles + p.tiles_per_block - 1) / p.tiles_per_block;
   p.stage_bytes = B_BYTES + V_BYTES + a.t * REC_BYTES;
   const size_t table = (size_t)p.tiles_per_block * NB * (8 + 8 * a.t);
   const int static_bytes = 2 * OUT_BYTES + 10 * 1024;  // output tiles, scalar buffers, barriers

@@ -260,7 +260,9 @@ def test_decode_full_size_sampled(name):
             calls[r].append(d)
             pars = [x[r] for x in lin_par]
             h = oracle.ancestry_slots(pars, t)
-            beams = sorted({0, 1, W_t // 3, W_t // 2, W_t - 1})
+            # (W_t - 65, W_t - 64: the boundary when a request's beams are
+            # split over two unequal blocks in the replay)
+            beams = sorted({0, 1, W_t // 3, W_t // 2, max(W_t - 65, 0), max(W_t - 64, 0), W_t - 1})
             _check_stages(name, wl, p, sctx_h[r], calls[r], h, t, beams)
             # end to end against an fp64 single-path decode (derived bound)
             for bb in sorted({0, W_t // 2, W_t - 1}):
