@@ -198,6 +198,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 8; ++c) xe[bt][c] = __ldg(reinterpret_cast<const float4*>(S) + bt * 8 + c);
   }
+  // so are this thread's first beam's ancestor slots and gates (the table
+  // below)
+  int sl0[TD > 0 ? TD : 1];
+  float2 ab0 = make_float2(0.0f, 0.0f);
+  if ((int)threadIdx.x < nbeams) {
+    const size_t row = (size_t)r * p.W_t + bb + threadIdx.x;
+#pragma unroll
+    for (int j = 0; j < t; ++j) sl0[j] = p.anc[row * p.anc_stride + j];
+    ab0 = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       tc::mbar_init(full(s), TD > 0 ? 3 : 1);  // the producer and the record loaders
@@ -231,9 +241,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int b = threadIdx.x; b < nbeams; b += kThreads) {
     const size_t row = (size_t)r * p.W_t + bb + b;
     int sl[TD > 0 ? TD : 1];
+    if (b == (int)threadIdx.x) {  // requested at the top
 #pragma unroll
-    for (int j = 0; j < t; ++j) sl[j] = p.anc[row * p.anc_stride + j];
-    tab_ab[b] = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
+      for (int j = 0; j < t; ++j) sl[j] = sl0[j];
+      tab_ab[b] = ab0;
+    } else {
+#pragma unroll
+      for (int j = 0; j < t; ++j) sl[j] = p.anc[row * p.anc_stride + j];
+      tab_ab[b] = make_float2(p.alpha[row * p.H + h], p.beta[row * p.H + h]);
+    }
 #pragma unroll
     for (int j = 0; j < t; ++j) {
       float a = -1.0f;  // marks a slot outside its depth: the record is skipped
