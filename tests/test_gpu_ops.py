@@ -141,7 +141,11 @@ def test_ancestry_op_matches_walk():
     ("bf16", 128, 2, 2, 300, 0, False), ("bf16", 32, 1, 1, 5, 5, False),
     ("bf16", 128, 4, 3, 64, 3, False), ("bf16", 128, 1, 1, 1, 1, False),
     ("bf16", 128, 2, 1, 96, 5, False), ("bf16", 128, 2, 2, 40, 1, True),
-    ("bf16", 128, 3, 2, 512, 2, False), ("bf16", 128, 2, 2, 70, 4, False)])
+    ("bf16", 128, 3, 2, 512, 2, False), ("bf16", 128, 2, 2, 70, 4, False),
+    # 96 (request, head) pairs of 8 beam tiles on 152 SMs: each pair's tiles
+    # go in two unequal blocks (6 + 2); ragged and residual variants
+    ("bf16", 128, 16, 6, 256, 2, False), ("bf16", 128, 16, 6, 250, 3, False),
+    ("bf16", 128, 16, 6, 250, 1, True)])
 def test_replay_op(dtype, d, H, R, W_t, t, resid):
     _replay_op(dtype, d, H, R, W_t, t, resid, H)
 
